@@ -1,0 +1,421 @@
+"""Benchmark: decode-attention KV tokens/s and achieved HBM GB/s on one GB300.
+
+Default workload: the hybrid 6-layer decode step (batch 256, 32 query heads,
+lognormal lengths with median 4096 clipped to [256, 32768], layers 0-4 local
+with window 1024, layer 5 global, buffer map {0,0,1,1,2,3}, page size 16).
+One step = cai_kv_append of the current token into each of the 4 buffers,
+then cai_mqa_decode for each of the 6 layers (split-KV decode + LSE combine).
+Inputs are resident in HBM when the timed region starts; the KV read per step
+(~0.77 GB) is larger than L2, and the KV loads carry an L2 evict-first hint.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cai|reference] [--config 1..5]
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention KV tokens/s and achieved HBM GB/s (% of peak) per GB300"
+UNIT = "KV tokens/s"
+BYTES_PER_TOKEN = 2 * 128 + 8  # int8 K + int8 V + two fp32 scales
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cai", choices=["cai", "reference"])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 5])
+    ap.add_argument("--sigma", type=float, default=1.0)
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (testing only)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- work accounting
+
+def layer_work(w, layer):
+    """Attended tokens, pages and algorithmic HBM bytes of one decode launch."""
+    W = w.layer_windows[layer]
+    P = w.page_size
+    L = np.asarray(w.ctx_len, dtype=np.int64)
+    lo = np.maximum(0, L - W) if W > 0 else np.zeros_like(L)
+    tokens = L - lo
+    pages = np.where(tokens > 0, (L - 1) // P - lo // P + 1, 0)
+    q_out = w.batch * w.num_q_heads * 128 * (2 + 4) + w.batch * 4
+    bytes_ = int(tokens.sum()) * BYTES_PER_TOKEN + int(pages.sum()) * 4 + q_out
+    return int(tokens.sum()), int(pages.sum()), bytes_
+
+
+def append_bytes(w):
+    # fp32 K and V rows read + int8 codes and scales written, per buffer
+    return w.num_buffers * w.batch * w.n_new * (2 * 128 * 4 + BYTES_PER_TOKEN + 4)
+
+
+def step_work(w):
+    toks, byts = 0, 0
+    for layer in range(len(w.layer_windows)):
+        t, _, b = layer_work(w, layer)
+        toks += t
+        byts += b
+    return toks, byts
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- peaks and profiles
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profiled_traffic(workload_tag: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it matches the current kernel."""
+    path = os.path.join(ROOT, "profiles", "decode_dram_traffic.txt")
+    src = os.path.join(ROOT, "int8_mqa_decode_gb300", "csrc", "decode.cu")
+    if not os.path.exists(path):
+        return None
+    info = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            info[k.strip()] = v.strip()
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if info.get("decode_cu_sha256") != sha or info.get("workload") != workload_tag:
+        return None
+    try:
+        return float(info["dram_bytes_per_decode_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+def cpu_oracle(w, seconds: float):
+    """Time the oracle (as it stands) on host cores over a bounded sample of the workload's sequences."""
+    import oracle
+    import synth
+    from concurrent.futures import ThreadPoolExecutor
+
+    order = np.argsort(w.ctx_len)
+    picks = [int(order[0]), int(order[-1])] + [int(i) for i in order[1:-1:max(1, len(order) // 14)]]
+    picks = list(dict.fromkeys(picks))
+    # Inputs (codes, scales, queries) prepared untimed, like resident device inputs.
+    prepared = []
+    for b in picks:
+        L = int(w.ctx_len[b])
+        kv = {buf: oracle.seq_kv(w.seed, buf, b, L) for buf in range(w.num_buffers)}
+        for layer in range(len(w.layer_windows)):
+            qb = synth.q_rows(w.seed, synth.stream_q(layer), b, w.num_q_heads)
+            W = w.layer_windows[layer]
+            tokens = min(L, W) if W > 0 else L
+            prepared.append((qb, kv[w.layer_to_buffer[layer]], L, W, tokens))
+    cores = os.cpu_count() or 1
+
+    def one(item):
+        qb, (kc, ks, vc, vs), L, W, _ = item
+        oracle.decode_seq(qb, kc, ks, vc, vs, L, W, w.softmax_scale)
+
+    done_tokens, t0 = 0, time.perf_counter()
+    with ThreadPoolExecutor(cores) as ex:
+        while True:
+            list(ex.map(one, prepared))
+            done_tokens += sum(p[4] for p in prepared)
+            if time.perf_counter() - t0 >= seconds:
+                break
+    dt = time.perf_counter() - t0
+    return {"value": done_tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(picks)} sequences (shortest, longest and evenly spaced by length) x "
+                      f"{len(w.layer_windows)} layers, repeated for {dt:.1f} s; float64 C oracle, "
+                      f"{cores} threads over (sequence, layer)"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world):
+    import torch
+    import harness
+    import int8_mqa_decode_gb300 as cai
+    import synth
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    import __graft_entry__
+    __graft_entry__.build()
+    seed = (1000 + args.config) + 100 * rank
+    w = synth.workload(args.config, seed=seed, sigma=args.sigma, batch=args.batch)
+    cache = harness.PagedCache(w)
+    cache.fill()
+    nl = len(w.layer_windows)
+    qs = [cache.decode_q(layer) for layer in range(nl)]
+    outs = [torch.empty(w.batch, w.num_q_heads, 128, device="cuda") for _ in range(nl)]
+    wss = [cache.workspace(layer, args.num_splits) for layer in range(nl)]
+    step_kv = [cache.step_kv(buf) for buf in range(w.num_buffers)]
+    stream = torch.cuda.current_stream()
+    n_events = nl
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n_events)] for _ in range(args.steps)]
+
+    def step(record=None):
+        for buf, pool in enumerate(cache.pools):
+            k, v, start = step_kv[buf]
+            cai.cai_kv_append(pool, k, v, cache.table, start)
+        for layer in range(nl):
+            if record is not None:
+                record[2 * layer].record(stream)
+            cai.cai_mqa_decode(cache.pools, w.layer_to_buffer, layer, qs[layer], cache.table, cache.ctx_len,
+                               w.layer_windows[layer], w.softmax_scale, args.num_splits, wss[layer], outs[layer])
+            if record is not None:
+                record[2 * layer + 1].record(stream)
+
+    launches_per_step = w.num_buffers + sum(
+        1 + (1 if cai.cai_mqa_decode_workspace_size(w.batch, w.num_q_heads, cache.max_pages_per_seq, w.page_size,
+                                                    w.layer_windows[layer], args.num_splits) > 0 else 0)
+        for layer in range(nl))
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for s in range(args.steps):
+            step(ev[s])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    ms_total = t_start.elapsed_time(t_end)
+    decode_ms = sum(ev[s][2 * l].elapsed_time(ev[s][2 * l + 1]) for s in range(args.steps) for l in range(nl))
+    ms_max = allreduce_max(ms_total, world)
+
+    toks_step, bytes_step = step_work(w)
+    value = world * toks_step * args.steps / (ms_max * 1e-3)
+    peak, peak_kind = measured_peaks()
+    achieved = bytes_step * args.steps / (decode_ms * 1e-3) / 1e9
+    tag = f"config{args.config}-B{w.batch}-seed{seed}"
+    traffic = profiled_traffic(tag)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 KV, fp16 MMA / fp32 accumulate",
+        "data": "synthetic (seeded Irwin-Hall normals, lengths and permuted block tables)",
+        "config": {"workload": w.name, "global_batch": w.batch * world, "seq_len": "lognormal" if args.config == 3
+                   else "uniform", "kv_tokens_per_step": toks_step, "num_splits": args.num_splits or "auto",
+                   "l2": "KV read per step larger than L2 (129 MB); KV loads are L2 evict-first",
+                   "parallelism": f"replicas x{world} (independent sequences per GPU)"},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "cai_mqa_decode (split-KV decode + LSE combine), 6 launches per step",
+                     "algorithmic_bytes_per_step": bytes_step},
+        "hbm_gbs_step": bytes_step * args.steps / (ms_max * 1e-3) / 1e9,
+        "queries_per_s": world * w.batch * args.steps / (ms_max * 1e-3),
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_oracle(w, args.cpu_seconds)
+    return result
+
+
+def run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world):
+    """Same step through the public API with inputs in pinned host memory: H2D + step + D2H, timed."""
+    import torch
+    import int8_mqa_decode_gb300 as cai
+
+    nl = len(w.layer_windows)
+    h_q = [q.cpu().pin_memory() for q in qs]
+    h_kv = [(k.cpu().pin_memory(), v.cpu().pin_memory(), s.cpu().pin_memory()) for k, v, s in step_kv]
+    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    d_q = [torch.empty_like(q) for q in qs]
+    d_kv = [(torch.empty_like(k), torch.empty_like(v), torch.empty_like(s)) for k, v, s in step_kv]
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in h_q) + sum(
+        sum(t.numel() * t.element_size() for t in kv) for kv in h_kv)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def step():
+        for (hk, hv, hs), (dk, dv, ds) in zip(h_kv, d_kv):
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            ds.copy_(hs, non_blocking=True)
+        for hq, dq in zip(h_q, d_q):
+            dq.copy_(hq, non_blocking=True)
+        for buf, pool in enumerate(cache.pools):
+            dk, dv, ds = d_kv[buf]
+            cai.cai_kv_append(pool, dk, dv, cache.table, ds)
+        for layer in range(nl):
+            cai.cai_mqa_decode(cache.pools, w.layer_to_buffer, layer, d_q[layer], cache.table, cache.ctx_len,
+                               w.layer_windows[layer], w.softmax_scale, args.num_splits, wss[layer], outs[layer])
+            h_out[layer].copy_(outs[layer], non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = allreduce_max(e0.elapsed_time(e1), world)
+    return {"value": world * toks_step * args.steps / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
+
+
+# ----------------------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args):
+    import synth
+
+    w = synth.workload(args.config, sigma=args.sigma, batch=args.batch)
+    per_step = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle(w, per_step / 4)
+    vals, t0 = [], time.perf_counter()
+    last = None
+    for _ in range(args.steps):
+        last = cpu_oracle(w, per_step)
+        vals.append(last["value"])
+    dt = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / max(1, args.steps) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "global_batch": w.batch, "sample": last["sample"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": last["cores"], "kind": "oracle",
+                             "sample": last["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse()
+    rank, world = dist_init()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    res = run_gpu(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,151 @@
+/*
+ * cai.h - C ABI of the int8 MQA paged decode library (libcai.so).
+ *
+ * What the library computes comes from the pages it was written from:
+ *  - "Character.AI: inference optimization", 03 Model architecture, technique
+ *    table: Multi-Query Attention in every attention layer (all query heads
+ *    read one K/V head); hybrid attention where most layers are local with a
+ *    horizon of 1024 and one layer in six is global; KV shared by
+ *    neighbouring layers.
+ *  - same page, 05 Quantization and cost: the attention KV cache is int8.
+ *  - same page, 04 Cache between turns, and the Red Hat page "Como funciona a
+ *    inferencia de IA", section "3. Cache de prefixo": the KV of a cached
+ *    prefix is reused and only new tokens are processed.
+ *  - Red Hat page, section "1. PagedAttention": the cache is cut into
+ *    fixed-size blocks placed anywhere in memory, with a per-request table of
+ *    block ids.
+ *  - Red Hat page, "Por que o cache KV existe": K and V are computed once for
+ *    each new token and stored; the new token's query is compared with the
+ *    keys of all tokens so far and the values are summed with those weights.
+ *
+ * Conventions for every call:
+ *  - All pointers to tensors are DEVICE pointers unless marked "host".  The
+ *    caller owns all memory; the library allocates nothing.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Host-side validation failures return a status and
+ *    launch nothing.  Problems only the device can see (a block-table entry
+ *    outside the pool, a length beyond the table) set bits in `*err_flag`
+ *    (atomic OR; nullable) and the affected work is skipped: outputs of
+ *    affected rows are then unspecified, but no out-of-bounds access happens.
+ *  - The library keeps no global state apart from a per-device attribute
+ *    cache; calls on different streams are independent.
+ *  - head_dim is 128.  Queries are bf16 and must be within the fp16 range
+ *    (|q| <= 65504): the tensor-core path runs in fp16 with fp32 accumulation.
+ *    K/V inputs must be finite.
+ */
+#ifndef CAI_H_
+#define CAI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum cai_status {
+  CAI_OK = 0,
+  CAI_ERR_INVALID_ARG = 1, /* null pointer, negative size, misaligned pointer, index out of range */
+  CAI_ERR_UNSUPPORTED = 2, /* head_dim, page_size or head count outside what the kernels implement */
+  CAI_ERR_WORKSPACE = 3,   /* workspace missing or smaller than cai_mqa_decode_workspace_size() */
+  CAI_ERR_CUDA = 4         /* a CUDA runtime call or a launch failed */
+} cai_status;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define CAI_DEVERR_PAGE 1   /* a needed block-table entry is outside [0, num_pages) */
+#define CAI_DEVERR_LENGTH 2 /* a length or position is negative or beyond max_pages_per_seq * page_size */
+#define CAI_DEVERR_TIMEOUT 4 /* a bounded wait inside a kernel gave up; that launch's outputs are unspecified */
+
+/* One KV buffer: a pool of fixed-size pages (PagedAttention blocks).
+ * Page layout (bytes), for P = page_size and d = head_dim:
+ *   [0,        P*d)        K codes, int8 [P][d]
+ *   [P*d,      2*P*d)      V codes, int8 [P][d]
+ *   [2*P*d,    2*P*d+4*P)  K scales, fp32 [P]
+ *   [2*P*d+4P, 2*P*d+8*P)  V scales, fp32 [P]
+ * Token at position p of a sequence lives in page block_table[p / P], slot p % P.
+ * `pages` must be 16-byte aligned; it holds num_pages * cai_page_bytes(P, d) bytes. */
+typedef struct cai_kv_pool {
+  void* pages;
+  int32_t num_pages;
+  int32_t page_size; /* 16, 32 or 64 tokens */
+  int32_t head_dim;  /* 128 */
+} cai_kv_pool;
+
+/* Bytes of one page: page_size * (2*head_dim + 8).  0 for non-positive arguments. */
+size_t cai_page_bytes(int32_t page_size, int32_t head_dim);
+
+/* Quantize new tokens to int8 and write them into their pages.
+ * Int8 KV cache ("Character.AI: inference optimization", 05), written once per
+ * new token (Red Hat page, "Por que o cache KV existe").  For each token and
+ * separately for K and V: s = max_i |x_i| / 127 (fp32, IEEE division),
+ * code_i = clamp(round_half_even(x_i / s), -127, 127); s = 0 and codes 0 when
+ * the vector is all zeros.  Results are bit-exact.
+ *   pool        host pointer to the pool description
+ *   k_new,v_new fp32 [batch][n_new][head_dim], 16-byte aligned
+ *   block_table int32 [batch][max_pages_per_seq]; entries for the written positions must be valid pages
+ *   start_pos   int32 [batch]: token i of sequence b goes to position start_pos[b] + i
+ *   err_flag    int32, nullable
+ * Positions outside [0, max_pages_per_seq * page_size) set CAI_DEVERR_LENGTH; bad
+ * page ids set CAI_DEVERR_PAGE; such tokens are not written.  No other byte of the
+ * pool changes (K and V of past tokens never change). */
+cai_status cai_kv_append(const cai_kv_pool* pool, const float* k_new, const float* v_new, int32_t batch,
+                         int32_t n_new, const int32_t* block_table, int32_t max_pages_per_seq,
+                         const int32_t* start_pos, int32_t* err_flag, void* stream);
+
+/* Bytes of workspace cai_mqa_decode needs for these arguments (0 when no split is needed).
+ * Arguments as for cai_mqa_decode. */
+size_t cai_mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_pages_per_seq,
+                                     int32_t page_size, int32_t window, int32_t num_splits);
+
+/* One decode step of one layer: MQA attention of one query token per sequence
+ * over its int8 paged KV.
+ *   pools, num_pools       host array of KV buffers
+ *   layer_to_pool          host int32 [num_layers]: buffer read by each layer (layers may share one)
+ *   layer                  the layer to run
+ *   q                      bf16 bits [batch][num_q_heads][head_dim], 16-byte aligned
+ *   num_q_heads            1..64 query heads, all sharing the single K/V head
+ *   block_table            int32 [batch][max_pages_per_seq]
+ *   ctx_len                int32 [batch]: cached tokens INCLUDING the current one (append first)
+ *   window                 0 = global; W > 0 = local: only the last W positions
+ *                          [max(0, L-W), L) are attended, pages wholly before them are never read
+ *   softmax_scale          logit = softmax_scale * <q, k>
+ *   num_splits             0 = automatic; otherwise the attended span is cut into at most
+ *                          this many chunks (1..64) processed by separate CTAs and merged
+ *                          with their log-sum-exp
+ *   workspace              device scratch of at least cai_mqa_decode_workspace_size() bytes
+ *                          (nullable when that is 0), 256-byte aligned
+ *   out                    fp32 [batch][num_q_heads][head_dim]
+ *   lse_out                fp32 [batch][num_q_heads] natural-log log-sum-exp of the logits, nullable
+ * A sequence with nothing to attend (L = 0) gets out = 0 and lse = -inf. */
+cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int32_t* layer_to_pool,
+                          int32_t num_layers, int32_t layer, const uint16_t* q, int32_t batch,
+                          int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
+                          const int32_t* ctx_len, int32_t window, float softmax_scale, int32_t num_splits,
+                          void* workspace, size_t workspace_bytes, float* out, float* lse_out,
+                          int32_t* err_flag, void* stream);
+
+/* Attention for a chunk of new tokens appended on top of a reused prefix.
+ * Prefix caching (Red Hat page, "3. Cache de prefixo") and the cross-turn
+ * cache ("Character.AI: inference optimization", 04): the prefix K/V is read
+ * from the int8 cache, not recomputed.  The chunk's own K/V must already be
+ * appended (cai_kv_append with start_pos = prefix_len), so prefix and chunk
+ * keys are read from the same int8 pages.  New token i of sequence b sits at
+ * position p0 + i (p0 = prefix_len[b]) and attends keys [lo, p0 + i] with
+ * lo = 0 (window 0) or max(0, p0 + i + 1 - window).
+ *   q       bf16 bits [batch][n_new][num_q_heads][head_dim], 16-byte aligned
+ *   num_q_heads  a power of two from 1 to 128
+ *   out     fp32 [batch][n_new][num_q_heads][head_dim]
+ *   lse_out fp32 [batch][n_new][num_q_heads], nullable */
+cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int32_t batch, int32_t n_new,
+                                 int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
+                                 const int32_t* prefix_len, int32_t window, float softmax_scale, float* out,
+                                 float* lse_out, int32_t* err_flag, void* stream);
+
+/* Static description of a status code. */
+const char* cai_status_string(cai_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CAI_H_ */

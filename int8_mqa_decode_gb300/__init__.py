@@ -1,0 +1,194 @@
+"""Python binding of libcai, the int8 MQA paged-KV decode library (include/cai.h).
+
+Argument marshalling only: each function checks tensor devices, dtypes,
+shapes and contiguity, turns them into pointers and sizes, and calls the C
+entry point of the same name on the current CUDA stream.  Every step of the
+computation runs in the CUDA kernels behind libcai.so; there is no CPU or
+eager fallback.  If the compiled library is missing, importing the binding's
+functions raises ``CaiUnavailable``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+__all__ = [
+    "CaiError", "CaiUnavailable", "KVPool", "library_path", "load", "cai_page_bytes", "cai_status_string",
+    "cai_kv_append", "cai_mqa_decode_workspace_size", "cai_mqa_decode", "cai_mqa_prefill_chunk",
+    "CAI_DEVERR_PAGE", "CAI_DEVERR_LENGTH", "CAI_DEVERR_TIMEOUT", "HEAD_DIM",
+]
+
+HEAD_DIM = 128
+CAI_OK, CAI_ERR_INVALID_ARG, CAI_ERR_UNSUPPORTED, CAI_ERR_WORKSPACE, CAI_ERR_CUDA = range(5)
+CAI_DEVERR_PAGE, CAI_DEVERR_LENGTH, CAI_DEVERR_TIMEOUT = 1, 2, 4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+
+
+class CaiUnavailable(RuntimeError):
+    """The compiled CUDA library (libcai.so) is not there or does not load."""
+
+
+class CaiError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {cai_status_string(status)} (status {status})")
+        self.status = status
+
+
+class cai_kv_pool(ctypes.Structure):
+    _fields_ = [("pages", ctypes.c_void_p), ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libcai.so")
+
+
+def load():
+    """Load libcai.so (built by ``build.py``); raise CaiUnavailable if it cannot be loaded."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise CaiUnavailable(f"{path} is missing: build it with `python -m int8_mqa_decode_gb300.build`")
+    try:
+        lib = ctypes.CDLL(path)
+    except OSError as e:  # pragma: no cover - depends on the machine
+        raise CaiUnavailable(f"cannot load {path}: {e}") from e
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    pool_p = ctypes.POINTER(cai_kv_pool)
+    lib.cai_page_bytes.argtypes = [i32, i32]
+    lib.cai_page_bytes.restype = sz
+    lib.cai_status_string.argtypes = [ctypes.c_int]
+    lib.cai_status_string.restype = ctypes.c_char_p
+    lib.cai_kv_append.argtypes = [pool_p, vp, vp, i32, i32, vp, i32, vp, vp, vp]
+    lib.cai_kv_append.restype = ctypes.c_int
+    lib.cai_mqa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.cai_mqa_decode_workspace_size.restype = sz
+    lib.cai_mqa_decode.argtypes = [pool_p, i32, vp, i32, i32, vp, i32, i32, vp, i32, vp, i32, ctypes.c_float, i32,
+                                   vp, sz, vp, vp, vp, vp]
+    lib.cai_mqa_decode.restype = ctypes.c_int
+    lib.cai_mqa_prefill_chunk.argtypes = [pool_p, vp, i32, i32, i32, vp, i32, vp, i32, ctypes.c_float, vp, vp, vp,
+                                          vp]
+    lib.cai_mqa_prefill_chunk.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def cai_status_string(status: int) -> str:
+    return load().cai_status_string(int(status)).decode()
+
+
+def cai_page_bytes(page_size: int, head_dim: int = HEAD_DIM) -> int:
+    return int(load().cai_page_bytes(page_size, head_dim))
+
+
+def _check(status: int, where: str) -> None:
+    if status != CAI_OK:
+        raise CaiError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor], name: str, dtype=None, shape=None) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr()
+
+
+class KVPool:
+    """One KV buffer: ``num_pages`` pages of ``page_size`` tokens in one uint8 CUDA tensor.
+
+    Page layout: K codes int8 [P][128], V codes int8 [P][128], K scales fp32 [P],
+    V scales fp32 [P].  ``pages`` may also be given (any uint8 CUDA tensor of the
+    right size, e.g. a view into a larger arena).
+    """
+
+    def __init__(self, num_pages: int, page_size: int, head_dim: int = HEAD_DIM, device=None,
+                 pages: Optional[torch.Tensor] = None):
+        nbytes = num_pages * cai_page_bytes(page_size, head_dim)
+        if pages is None:
+            pages = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+        if pages.dtype != torch.uint8 or pages.numel() != nbytes or not pages.is_cuda:
+            raise ValueError("pages must be a uint8 CUDA tensor of num_pages * page_bytes bytes")
+        self.pages = pages
+        self.num_pages, self.page_size, self.head_dim = num_pages, page_size, head_dim
+        self.struct = cai_kv_pool(pages.data_ptr(), num_pages, page_size, head_dim)
+
+
+def cai_kv_append(pool: KVPool, k_new: torch.Tensor, v_new: torch.Tensor, block_table: torch.Tensor,
+                  start_pos: torch.Tensor, err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Quantize k_new/v_new fp32 [batch][n_new][128] to int8 and write them at start_pos[b] + i."""
+    batch, n_new = (k_new.shape[0], k_new.shape[1]) if k_new.dim() == 3 else (0, 0)
+    shape = (batch, n_new, pool.head_dim)
+    st = load().cai_kv_append(
+        ctypes.byref(pool.struct), _ptr(k_new, "k_new", torch.float32, shape), _ptr(v_new, "v_new", torch.float32, shape),
+        batch, n_new, _ptr(block_table, "block_table", torch.int32), block_table.shape[-1],
+        _ptr(start_pos, "start_pos", torch.int32, (batch,)), _ptr(err_flag, "err_flag", torch.int32), _stream(stream))
+    _check(st, "cai_kv_append")
+
+
+def cai_mqa_decode_workspace_size(batch: int, num_q_heads: int, max_pages_per_seq: int, page_size: int,
+                                  window: int, num_splits: int = 0) -> int:
+    return int(load().cai_mqa_decode_workspace_size(batch, num_q_heads, max_pages_per_seq, page_size, window,
+                                                     num_splits))
+
+
+def _pool_array(pools: Sequence[KVPool]):
+    arr = (cai_kv_pool * len(pools))()
+    for i, p in enumerate(pools):
+        arr[i] = p.struct
+    return arr
+
+
+def cai_mqa_decode(pools: Sequence[KVPool], layer_to_pool: Sequence[int], layer: int, q: torch.Tensor,
+                   block_table: torch.Tensor, ctx_len: torch.Tensor, window: int, softmax_scale: float,
+                   num_splits: int, workspace: Optional[torch.Tensor], out: torch.Tensor,
+                   lse_out: Optional[torch.Tensor] = None, err_flag: Optional[torch.Tensor] = None,
+                   stream=None) -> None:
+    """One decode step of one layer: q bf16 [batch][Hq][128] -> out fp32 [batch][Hq][128]."""
+    batch, hq = q.shape[0], q.shape[1]
+    l2p = (ctypes.c_int32 * len(layer_to_pool))(*layer_to_pool)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().cai_mqa_decode(
+        _pool_array(pools), len(pools), l2p, len(layer_to_pool), layer,
+        _ptr(q, "q", (torch.bfloat16, torch.int16), (batch, hq, HEAD_DIM)), batch, hq,
+        _ptr(block_table, "block_table", torch.int32), block_table.shape[-1],
+        _ptr(ctx_len, "ctx_len", torch.int32, (batch,)), window, float(softmax_scale), num_splits,
+        _ptr(workspace, "workspace"), ws_bytes, _ptr(out, "out", torch.float32, (batch, hq, HEAD_DIM)),
+        _ptr(lse_out, "lse_out", torch.float32, (batch, hq)), _ptr(err_flag, "err_flag", torch.int32),
+        _stream(stream))
+    _check(st, "cai_mqa_decode")
+
+
+def cai_mqa_prefill_chunk(pool: KVPool, q: torch.Tensor, block_table: torch.Tensor, prefix_len: torch.Tensor,
+                          window: int, softmax_scale: float, out: torch.Tensor,
+                          lse_out: Optional[torch.Tensor] = None, err_flag: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
+    """Attention of n_new appended tokens on a reused prefix: q bf16 [batch][n_new][Hq][128]."""
+    batch, n_new, hq = q.shape[0], q.shape[1], q.shape[2]
+    st = load().cai_mqa_prefill_chunk(
+        ctypes.byref(pool.struct), _ptr(q, "q", (torch.bfloat16, torch.int16), (batch, n_new, hq, HEAD_DIM)), batch,
+        n_new, hq, _ptr(block_table, "block_table", torch.int32), block_table.shape[-1],
+        _ptr(prefix_len, "prefix_len", torch.int32, (batch,)), window, float(softmax_scale),
+        _ptr(out, "out", torch.float32, (batch, n_new, hq, HEAD_DIM)),
+        _ptr(lse_out, "lse_out", torch.float32, (batch, n_new, hq)), _ptr(err_flag, "err_flag", torch.int32),
+        _stream(stream))
+    _check(st, "cai_mqa_prefill_chunk")

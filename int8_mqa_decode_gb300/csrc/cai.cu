@@ -1,0 +1,175 @@
+// Host side of the C ABI: argument validation, split planning and launches.
+// Everything here is plain bookkeeping; all arithmetic on the data runs in
+// the kernels.
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace cai {
+
+static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+static inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static inline bool page_size_ok(int32_t P) { return P == 16 || P == 32 || P == 64; }
+
+// Split plan.  The attended span of a sequence is at most `span` tokens (the
+// window, or the block-table capacity for a global layer).  Chunks are
+// multiples of the 64-token decode tile.  Automatic choice: about 16 chunks
+// per maximal span, between 256 and 4096 tokens, never more than 64 splits.
+DecodePlan plan_decode(int32_t max_pages_per_seq, int32_t page_size, int32_t window, int32_t num_splits) {
+  const int64_t cap = (int64_t)max_pages_per_seq * page_size;
+  const int64_t span = window > 0 ? (window < cap ? window : cap) : cap;
+  int64_t chunk;
+  if (num_splits > 0) {
+    chunk = round_up(ceil_div(span, num_splits), kDecodeTile);
+  } else {
+    chunk = round_up(ceil_div(span, 16), kDecodeTile);
+    if (chunk < 256) chunk = 256;
+    if (chunk > 4096) chunk = 4096;
+    const int64_t min_chunk = round_up(ceil_div(span, kMaxSplits), kDecodeTile);
+    if (chunk < min_chunk) chunk = min_chunk;
+  }
+  if (chunk < kDecodeTile) chunk = kDecodeTile;
+  // A window that does not start on a chunk boundary can touch one extra chunk.
+  int64_t splits = ceil_div(span, chunk) + (window > 0 ? 1 : 0);
+  if (splits < 1) splits = 1;
+  DecodePlan p;
+  p.chunk = (int32_t)chunk;
+  p.max_splits = (int32_t)splits;
+  return p;
+}
+
+static size_t workspace_bytes_for(int32_t batch, int32_t num_q_heads, const DecodePlan& plan) {
+  if (plan.max_splits <= 1) return 0;
+  const size_t rows = (size_t)batch * plan.max_splits * num_q_heads;
+  const size_t o_bytes = (size_t)round_up((int64_t)(rows * kHeadDim * sizeof(float)), 256);
+  return o_bytes + (size_t)round_up((int64_t)(rows * sizeof(float)), 256);
+}
+
+}  // namespace cai
+
+using namespace cai;
+
+extern "C" {
+
+size_t cai_page_bytes(int32_t page_size, int32_t head_dim) {
+  if (page_size <= 0 || head_dim <= 0) return 0;
+  return (size_t)page_size * (2 * (size_t)head_dim + 8);
+}
+
+const char* cai_status_string(cai_status status) {
+  switch (status) {
+    case CAI_OK: return "ok";
+    case CAI_ERR_INVALID_ARG: return "invalid argument";
+    case CAI_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CAI_ERR_WORKSPACE: return "workspace missing or too small";
+    case CAI_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+static cai_status check_pool(const cai_kv_pool* pool) {
+  if (!pool || !pool->pages || pool->num_pages <= 0) return CAI_ERR_INVALID_ARG;
+  if (!aligned16(pool->pages)) return CAI_ERR_INVALID_ARG;
+  if (pool->head_dim != kHeadDim || !page_size_ok(pool->page_size)) return CAI_ERR_UNSUPPORTED;
+  return CAI_OK;
+}
+
+cai_status cai_kv_append(const cai_kv_pool* pool, const float* k_new, const float* v_new, int32_t batch,
+                         int32_t n_new, const int32_t* block_table, int32_t max_pages_per_seq,
+                         const int32_t* start_pos, int32_t* err_flag, void* stream) {
+  cai_status st = check_pool(pool);
+  if (st != CAI_OK) return st;
+  if (batch < 0 || n_new < 0 || max_pages_per_seq <= 0) return CAI_ERR_INVALID_ARG;
+  if ((int64_t)max_pages_per_seq * pool->page_size > (1ll << 30)) return CAI_ERR_UNSUPPORTED;
+  if (batch == 0 || n_new == 0) return CAI_OK;
+  if ((int64_t)batch * n_new > (1ll << 30)) return CAI_ERR_UNSUPPORTED;
+  if (!k_new || !v_new || !block_table || !start_pos) return CAI_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return CAI_ERR_INVALID_ARG;
+  AppendParams p;
+  p.pages = static_cast<uint8_t*>(pool->pages);
+  p.num_pages = pool->num_pages;
+  p.page_size = pool->page_size;
+  p.max_pages = max_pages_per_seq;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.batch = batch;
+  p.n_new = n_new;
+  p.table = block_table;
+  p.start_pos = start_pos;
+  p.err = err_flag;
+  return launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CAI_OK : CAI_ERR_CUDA;
+}
+
+size_t cai_mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_pages_per_seq,
+                                     int32_t page_size, int32_t window, int32_t num_splits) {
+  if (batch <= 0 || num_q_heads <= 0 || max_pages_per_seq <= 0 || !page_size_ok(page_size) || window < 0 ||
+      num_splits < 0 || num_splits > kMaxSplits)
+    return 0;
+  return workspace_bytes_for(batch, num_q_heads, plan_decode(max_pages_per_seq, page_size, window, num_splits));
+}
+
+cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int32_t* layer_to_pool,
+                          int32_t num_layers, int32_t layer, const uint16_t* q, int32_t batch,
+                          int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
+                          const int32_t* ctx_len, int32_t window, float softmax_scale, int32_t num_splits,
+                          void* workspace, size_t workspace_bytes, float* out, float* lse_out,
+                          int32_t* err_flag, void* stream) {
+  if (!pools || num_pools <= 0 || !layer_to_pool || num_layers <= 0 || layer < 0 || layer >= num_layers)
+    return CAI_ERR_INVALID_ARG;
+  const int32_t buf = layer_to_pool[layer];
+  if (buf < 0 || buf >= num_pools) return CAI_ERR_INVALID_ARG;
+  const cai_kv_pool* pool = &pools[buf];
+  cai_status st = check_pool(pool);
+  if (st != CAI_OK) return st;
+  if (batch < 0 || max_pages_per_seq <= 0 || window < 0 || num_splits < 0 || num_splits > kMaxSplits ||
+      !std::isfinite(softmax_scale))
+    return CAI_ERR_INVALID_ARG;
+  if (num_q_heads < 1 || num_q_heads > kDecodeRows) return CAI_ERR_UNSUPPORTED;
+  if ((int64_t)max_pages_per_seq * pool->page_size > (1ll << 30) || batch > 65535) return CAI_ERR_UNSUPPORTED;
+  if (batch == 0) return CAI_OK;
+  if (!q || !block_table || !ctx_len || !out) return CAI_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return CAI_ERR_INVALID_ARG;
+
+  const DecodePlan plan = plan_decode(max_pages_per_seq, pool->page_size, window, num_splits);
+  const size_t need = workspace_bytes_for(batch, num_q_heads, plan);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CAI_ERR_WORKSPACE;
+
+  DecodeParams p;
+  p.pages = static_cast<const uint8_t*>(pool->pages);
+  p.num_pages = pool->num_pages;
+  p.table = block_table;
+  p.max_pages = max_pages_per_seq;
+  p.ctx_len = ctx_len;
+  p.q = q;
+  p.batch = batch;
+  p.num_heads = num_q_heads;
+  p.window = window;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.plan = plan;
+  p.out = out;
+  p.lse_out = lse_out;
+  p.ws_o = nullptr;
+  p.ws_lse = nullptr;
+  if (need > 0) {
+    const size_t rows = (size_t)batch * plan.max_splits * num_q_heads;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        (size_t)round_up((int64_t)(rows * kHeadDim * sizeof(float)), 256));
+  }
+  p.err = err_flag;
+  return launch_decode(p, pool->page_size, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CAI_OK
+                                                                                                : CAI_ERR_CUDA;
+}
+
+cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int32_t batch, int32_t n_new,
+                                 int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
+                                 const int32_t* prefix_len, int32_t window, float softmax_scale, float* out,
+                                 float* lse_out, int32_t* err_flag, void* stream) {
+  (void)pool; (void)q; (void)batch; (void)n_new; (void)num_q_heads; (void)block_table; (void)max_pages_per_seq;
+  (void)prefix_len; (void)window; (void)softmax_scale; (void)out; (void)lse_out; (void)err_flag; (void)stream;
+  return CAI_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// Shared definitions of the CUDA side of libcai: launch parameter blocks,
+// constants and the split plan.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "cai.h"
+
+namespace cai {
+
+constexpr int kHeadDim = 128;
+constexpr int kMaxSplits = 64;
+constexpr int kDecodeTile = 64;        // tokens per decode tile (one MMA N)
+constexpr int kDecodeRows = 64;        // MMA M for decode: query heads padded to 64
+constexpr int kDecodeStages = 3;       // raw page stages in flight per CTA
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Bytes of one page for head_dim 128: P * (2*128 + 8).
+__host__ __device__ constexpr int page_bytes(int P) { return P * (2 * kHeadDim + 8); }
+
+struct AppendParams {
+  uint8_t* pages;
+  int32_t num_pages, page_size, max_pages;
+  const float* k_new;
+  const float* v_new;
+  int32_t batch, n_new;
+  const int32_t* table;
+  const int32_t* start_pos;
+  int32_t* err;
+};
+
+// Work split of one decode launch.  The attended span [lo, hi) of every
+// sequence is cut at absolute multiples of `chunk` tokens; split j of
+// sequence b covers chunk number (lo / chunk) + j.
+struct DecodePlan {
+  int32_t chunk;       // tokens per split, a multiple of kDecodeTile
+  int32_t max_splits;  // grid.x: upper bound of splits per sequence
+};
+
+struct DecodeParams {
+  const uint8_t* pages;
+  int32_t num_pages;
+  const int32_t* table;
+  int32_t max_pages;
+  const int32_t* ctx_len;
+  const uint16_t* q;  // bf16 bits [B][Hq][128]
+  int32_t batch, num_heads, window;
+  float scale_log2;   // softmax_scale * log2(e)
+  DecodePlan plan;
+  float* out;         // [B][Hq][128]
+  float* lse_out;     // [B][Hq] natural log, nullable
+  float* ws_o;        // [B][max_splits][Hq][128] partial outputs (normalised)
+  float* ws_lse;      // [B][max_splits][Hq] partial lse, log2 units
+  int32_t* err;
+};
+
+// Attended range and split bookkeeping shared by the decode and combine kernels.
+struct SeqSplits {
+  int32_t lo, hi;      // attended positions [lo, hi)
+  int32_t first_chunk; // chunk index of split 0
+  int32_t nsplit;      // number of non-empty splits (0 if nothing to attend)
+  bool valid;          // length within the block table
+};
+
+__host__ __device__ inline SeqSplits seq_splits(int32_t L, int32_t window, int32_t max_tokens, int32_t chunk) {
+  SeqSplits s;
+  s.valid = (L >= 0 && L <= max_tokens);
+  if (!s.valid) L = 0;
+  s.hi = L;
+  s.lo = (window > 0 && L > window) ? L - window : 0;
+  if (s.hi <= s.lo) {
+    s.first_chunk = 0;
+    s.nsplit = 0;
+    return s;
+  }
+  s.first_chunk = s.lo / chunk;
+  s.nsplit = (s.hi - 1) / chunk - s.first_chunk + 1;
+  return s;
+}
+
+// Host side: the split plan for a launch (also used by the workspace query).
+DecodePlan plan_decode(int32_t max_pages_per_seq, int32_t page_size, int32_t window, int32_t num_splits);
+
+// Kernel launchers (return cudaGetLastError()).
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int page_size, cudaStream_t stream);
+
+}  // namespace cai

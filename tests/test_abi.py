@@ -1,0 +1,116 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and its host-side validation answers with status codes
+before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import int8_mqa_decode_gb300 as cai
+from int8_mqa_decode_gb300 import build as cai_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails before any launch
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cai_build.build()
+    return cai.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "cai.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cai_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"cai_kv_append", "cai_mqa_decode", "cai_mqa_prefill_chunk", "cai_mqa_decode_workspace_size",
+            "cai_status_string", "cai_page_bytes"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_page_bytes_and_status_strings(lib):
+    assert cai.cai_page_bytes(16) == 16 * 264 == 4224
+    assert cai.cai_page_bytes(64) == 16896
+    assert cai.cai_page_bytes(0) == 0
+    assert cai.cai_status_string(0) == "ok"
+    assert "workspace" in cai.cai_status_string(3)
+
+
+def test_workspace_size_plan(lib):
+    # One split needs no workspace; the local layer of 1024 positions splits into 256-token chunks (+1 straddle).
+    assert cai.cai_mqa_decode_workspace_size(4, 8, 32, 16, 0, 1) == 0
+    ws = cai.cai_mqa_decode_workspace_size(256, 32, 2048, 16, 1024, 0)
+    rows = 256 * 5 * 32
+    assert ws == ((rows * 128 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    assert cai.cai_mqa_decode_workspace_size(4, 8, 32, 24, 0, 0) == 0  # unsupported page size
+    assert cai.cai_mqa_decode_workspace_size(4, 8, 32, 16, 0, 65) == 0  # too many splits
+
+
+def _pool(num_pages=8, page_size=16, head_dim=128, pages=FAKE):
+    return cai.cai_kv_pool(pages, num_pages, page_size, head_dim)
+
+
+def test_append_validation(lib):
+    pool = _pool()
+    ok_args = dict(k=FAKE, v=FAKE, batch=2, n_new=1, table=FAKE, maxp=4, start=FAKE)
+
+    def call(pool, **kw):
+        a = dict(ok_args, **kw)
+        return lib.cai_kv_append(ctypes.byref(pool), a["k"], a["v"], a["batch"], a["n_new"], a["table"], a["maxp"],
+                                 a["start"], None, None)
+
+    assert lib.cai_kv_append(None, FAKE, FAKE, 1, 1, FAKE, 4, FAKE, None, None) == 1
+    assert call(_pool(head_dim=64)) == 2
+    assert call(_pool(page_size=24)) == 2
+    assert call(_pool(page_size=128)) == 2
+    assert call(_pool(pages=FAKE + 4)) == 1     # misaligned pool
+    assert call(pool, k=FAKE + 8) == 1          # misaligned input
+    assert call(pool, table=None) == 1
+    assert call(pool, batch=-1) == 1
+    assert call(pool, batch=0) == 0             # nothing to do, nothing launched
+    assert call(pool, n_new=0) == 0
+
+
+def test_decode_validation(lib):
+    pools = (cai.cai_kv_pool * 2)(_pool(), _pool())
+    l2p = (ctypes.c_int32 * 3)(0, 0, 1)
+
+    def call(**kw):
+        a = dict(pools=pools, npools=2, l2p=l2p, nlayers=3, layer=0, q=FAKE, batch=2, hq=8, table=FAKE, maxp=64,
+                 ctx=FAKE, window=0, scale=0.088, splits=1, ws=None, ws_bytes=0, out=FAKE)
+        a.update(kw)
+        return lib.cai_mqa_decode(a["pools"], a["npools"], a["l2p"], a["nlayers"], a["layer"], a["q"], a["batch"],
+                                  a["hq"], a["table"], a["maxp"], a["ctx"], a["window"], a["scale"], a["splits"],
+                                  a["ws"], a["ws_bytes"], a["out"], None, None, None)
+
+    assert call(layer=3) == 1
+    assert call(layer=2, l2p=(ctypes.c_int32 * 3)(0, 0, 2)) == 1  # buffer index out of range
+    assert call(hq=0) == 2
+    assert call(hq=65) == 2
+    assert call(q=FAKE + 2) == 1
+    assert call(out=None) == 1
+    assert call(window=-1) == 1
+    assert call(splits=65) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(batch=0) == 0
+    # 64 pages of 16 tokens in 4 splits need a workspace; every call here fails before any launch.
+    assert call(splits=4) == 3
+    assert call(splits=4, ws=FAKE, ws_bytes=16) == 3
+    bad = (cai.cai_kv_pool * 1)(_pool(head_dim=96))
+    assert call(pools=bad, npools=1, l2p=(ctypes.c_int32 * 1)(0), nlayers=1) == 2
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    pool = cai.KVPool.__new__(cai.KVPool)
+    pool.struct = _pool()
+    pool.head_dim = 128
+    x = torch.zeros(1, 1, 128)
+    with pytest.raises(ValueError):
+        cai.cai_kv_append(pool, x, x, torch.zeros(1, 4, dtype=torch.int32), torch.zeros(1, dtype=torch.int32))

@@ -1,0 +1,256 @@
+"""GPU parity of the append and decode path against the oracle.
+
+Append: the whole pool, byte for byte (codes, scales and every untouched
+byte).  Decode: outputs and log-sum-exp within 2e-3 absolute of the float64
+oracle, over the pages' workload shapes (shrunk where the oracle needs it),
+every split count, page size, head count and window edge.
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import harness  # noqa: E402
+import int8_mqa_decode_gb300 as cai  # noqa: E402
+import oracle  # noqa: E402
+import synth  # noqa: E402
+
+ATOL = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from int8_mqa_decode_gb300 import build
+    build.build()
+    import synth.gpu
+    synth.gpu.build()
+
+
+def make_workload(B, Hq, P, lengths, windows=(0,), l2b=(0,), seed=5, n_new=1):
+    L = np.asarray(lengths, dtype=np.int64)
+    assert len(L) == B
+    return synth.Workload("test", B, Hq, P, L, list(windows), list(l2b), n_new=n_new, seed=seed)
+
+
+def oracle_pool(w, cache, buf):
+    pool = oracle.pool_new(cache.num_pages, w.page_size, fill=0xA5)
+    for b in range(w.batch):
+        kc, ks, vc, vs = oracle.seq_kv(w.seed, buf, b, int(w.ctx_len[b]))
+        oracle.pool_write(pool, cache.table_np[b], 0, kc, ks, vc, vs, w.page_size)
+    return pool
+
+
+def run_decode(cache, layer, num_splits=0, with_lse=True):
+    w = cache.w
+    q = cache.decode_q(layer)
+    out = torch.full((w.batch, w.num_q_heads, 128), float("nan"), device="cuda")
+    lse = torch.full((w.batch, w.num_q_heads), float("nan"), device="cuda") if with_lse else None
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache.decode(layer, q, out, lse, num_splits=num_splits, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return out.cpu().numpy(), (lse.cpu().numpy() if with_lse else None)
+
+
+def oracle_decode(w, layer, b, heads=None):
+    L = int(w.ctx_len[b])
+    buf = w.layer_to_buffer[layer]
+    kc, ks, vc, vs = oracle.seq_kv(w.seed, buf, b, L)
+    qb = synth.q_rows(w.seed, synth.stream_q(layer), b, w.num_q_heads)
+    if heads is not None:
+        qb = qb[heads]
+    return oracle.decode_seq(qb, kc, ks, vc, vs, L, w.layer_windows[layer], w.softmax_scale)
+
+
+def check_layer(cache, layer, out, lse, seqs=None):
+    w = cache.w
+    seqs = range(w.batch) if seqs is None else seqs
+    worst = 0.0
+    for b in seqs:
+        o_ref, l_ref = oracle_decode(w, layer, b)
+        err = np.abs(out[b] - o_ref).max()
+        worst = max(worst, err)
+        assert err <= ATOL, (b, err)
+        if lse is not None:
+            assert np.abs(lse[b] - l_ref).max() <= ATOL, b
+    return worst
+
+
+# --------------------------------------------------------------------- append
+
+@pytest.mark.parametrize("P", [16, 32, 64])
+def test_append_bit_exact_whole_pool(P):
+    B = 5
+    L = synth.uniform_int(11, 1, B, 1, 700)
+    L[0] = 1
+    L[1] = P  # exactly one page
+    w = make_workload(B, 8, P, L, seed=11)
+    cache = harness.PagedCache(w, sentinel=0xA5, spare_pages=3)
+    cache.fill(upto=w.ctx_len)
+    torch.cuda.synchronize()
+    got = cache.pools[0].pages.cpu().numpy()
+    assert np.array_equal(got, oracle_pool(w, cache, 0))
+
+
+def test_append_chunk_across_page_boundaries_and_errors():
+    P = 16
+    w = make_workload(3, 8, P, [100, 37, 64], seed=12, n_new=29)
+    cache = harness.PagedCache(w, sentinel=0xA5)
+    cache.fill()                      # positions [0, L - 29)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache.append_step(err=err)        # 29 tokens per sequence, crossing page boundaries
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(cache.pools[0].pages.cpu().numpy(), oracle_pool(w, cache, 0))
+    # A position beyond the table and a bad page id: flagged, nothing written.
+    before = cache.pools[0].pages.clone()
+    k = torch.ones(1, 1, 128, device="cuda")
+    bad_start = torch.tensor([cache.max_pages_per_seq * P], dtype=torch.int32, device="cuda")
+    cai.cai_kv_append(cache.pools[0], k, k, cache.table[:1], bad_start, err_flag=err)
+    bad_table = torch.full((1, cache.max_pages_per_seq), cache.num_pages, dtype=torch.int32, device="cuda")
+    cai.cai_kv_append(cache.pools[0], k, k, bad_table, torch.zeros(1, dtype=torch.int32, device="cuda"), err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == cai.CAI_DEVERR_LENGTH | cai.CAI_DEVERR_PAGE
+    assert torch.equal(before, cache.pools[0].pages)
+
+
+def test_append_quantizer_edge_rows():
+    # Zero row, integer row with amax 127 (scale 1, exact halves -> ties to even), tiny and huge magnitudes.
+    P = 16
+    pool = cai.KVPool(2, P)
+    pool.pages.fill_(0)
+    x = torch.zeros(1, 4, 128, dtype=torch.float32)
+    x[0, 1, 0] = 127.0
+    x[0, 1, 1:10] = torch.tensor([0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 126.5, -126.5])
+    x[0, 2] = torch.linspace(-1e-30, 1e-30, 128)
+    x[0, 3] = torch.linspace(-3e38, 3e38, 128)
+    table = torch.tensor([[1, 0]], dtype=torch.int32, device="cuda")
+    cai.cai_kv_append(pool, x.cuda(), (-x).cuda().contiguous(), table, torch.zeros(1, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    ref = oracle.pool_new(2, P, fill=0)
+    kc, ks = oracle.quantize_rows(x[0].numpy())
+    vc, vs = oracle.quantize_rows((-x[0]).numpy())
+    oracle.pool_write(ref, np.array([1, 0]), 0, kc, ks, vc, vs, P)
+    assert np.array_equal(pool.pages.cpu().numpy(), ref)
+    assert list(kc[1, 1:10]) == [0, 2, 2, 4, 0, -2, -2, 126, -126]
+
+
+# --------------------------------------------------------------------- decode
+
+def build(w, **kw):
+    cache = harness.PagedCache(w, **kw)
+    cache.fill(upto=w.ctx_len)
+    return cache
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 2, 3, 8])
+def test_decode_tiny_global_config(num_splits):
+    w = synth.workload(1)  # B=4, Hq=8, L~U[64,512], P=16, permuted pages
+    cache = build(w)
+    out, lse = run_decode(cache, 0, num_splits)
+    check_layer(cache, 0, out, lse)
+
+
+@pytest.mark.parametrize("P", [16, 32, 64])
+@pytest.mark.parametrize("Hq", [1, 8, 17, 32, 64])
+def test_decode_heads_and_page_sizes(P, Hq):
+    L = [1, 2, 63, 64, 65, 200, 1000, 1500]
+    w = make_workload(len(L), Hq, P, L, seed=20 + P + Hq)
+    cache = build(w)
+    for splits in (1, 0):
+        out, lse = run_decode(cache, 0, splits)
+        check_layer(cache, 0, out, lse)
+
+
+@pytest.mark.parametrize("L", [1, 5, 1023, 1024, 1025, 1040, 2047, 3000])
+def test_decode_window_edges(L):
+    w = make_workload(2, 32, 16, [L, L + 17], windows=(1024,), seed=31)
+    cache = build(w)
+    for splits in (1, 4, 0):
+        out, lse = run_decode(cache, 0, splits)
+        check_layer(cache, 0, out, lse)
+
+
+def test_decode_local_config_shape():
+    w = synth.workload(2, batch=8)  # B shrunk from 64: L~U[1024,8192], W=1024, Hq=32, P=16
+    cache = build(w)
+    out, lse = run_decode(cache, 0, 0)
+    check_layer(cache, 0, out, lse)
+
+
+def test_decode_hybrid_six_layers_shared_buffers():
+    w = synth.workload(3, batch=6)  # lognormal lengths, map {0,0,1,1,2,3}, W=1024 x5 + global
+    cache = build(w)
+    outs = {}
+    for layer in range(6):
+        out, lse = run_decode(cache, layer, 0)
+        check_layer(cache, layer, out, lse)
+        outs[layer] = out
+    # Layers 0 and 1 share buffer 0 but have different queries; the same query through a shared
+    # map entry and through a private copy of the buffer gives identical bits.
+    q = cache.decode_q(0)
+    a = torch.empty(w.batch, w.num_q_heads, 128, device="cuda")
+    b_ = torch.empty_like(a)
+    copy = cai.KVPool(cache.num_pages, w.page_size, pages=cache.pools[0].pages.clone())
+    pools = [cache.pools[0], copy]
+    for l2p, dst in (([0, 0], a), ([0, 1], b_)):
+        cai.cai_mqa_decode(pools, l2p, 1, q, cache.table, cache.ctx_len, 1024, w.softmax_scale, 0,
+                           cache.workspace(0), dst)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b_)
+
+
+def test_decode_long_global_config_sampled():
+    # The long-context workload's shape at a reduced batch: Hq=64, P=64, L~U[16384,131072].
+    w = synth.workload(5, batch=6)
+    cache = build(w)
+    for splits in (0, 8, 32):
+        out, lse = run_decode(cache, 0, splits)
+        check_layer(cache, 0, out, lse, seqs=[0, int(np.argmax(w.ctx_len))])
+
+
+def test_decode_empty_and_invalid_lengths():
+    w = make_workload(3, 8, 16, [0, 40, 40], seed=41)
+    cache = build(w)
+    cache.ctx_len[2] = cache.max_pages_per_seq * 16 + 1  # beyond the table
+    q = cache.decode_q(0)
+    out = torch.full((3, 8, 128), float("nan"), device="cuda")
+    lse = torch.full((3, 8), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache.decode(0, q, out, lse, num_splits=0, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == cai.CAI_DEVERR_LENGTH
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    assert not o[0].any() and np.all(np.isneginf(l[0]))
+    ref, ref_l = oracle_decode(w, 0, 1)
+    assert np.abs(o[1] - ref).max() <= ATOL and np.abs(l[1] - ref_l).max() <= ATOL
+
+
+def test_decode_bad_page_id_sets_flag():
+    w = make_workload(2, 8, 16, [300, 300], seed=42)
+    cache = build(w)
+    cache.table[1, 3] = cache.num_pages + 5
+    q = cache.decode_q(0)
+    out = torch.empty(2, 8, 128, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache.decode(0, q, out, None, num_splits=1, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == cai.CAI_DEVERR_PAGE
+    ref, _ = oracle_decode(w, 0, 0)
+    assert np.abs(out[0].cpu().numpy() - ref).max() <= ATOL  # the other sequence is unaffected
+
+
+def test_decode_step_appends_then_attends():
+    # One full hybrid decode step: append the current token to each of the four buffers, then six layers.
+    w = synth.workload(3, batch=4)
+    cache = harness.PagedCache(w)
+    cache.fill()            # all but the current token
+    cache.append_step()     # the current token of each buffer
+    for layer in (0, 5):
+        out, lse = run_decode(cache, layer, 0)
+        check_layer(cache, layer, out, lse)
