@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ncu", action="store_true",
+                    help="open the CUDA profiler window around the timed steps only (for ncu --profile-from-start off)")
     return ap.parse_args()
 
 
@@ -138,6 +140,15 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def smi_index(device: int) -> int:
+    """nvidia-smi index of a CUDA device, honouring CUDA_VISIBLE_DEVICES when it lists numbers."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [p.strip() for p in vis.split(",") if p.strip()]
+    if device < len(parts) and parts[device].isdigit():
+        return int(parts[device])
+    return device
+
+
 # ----------------------------------------------------------------------------- peaks and profiles
 
 def measured_peaks():
@@ -170,43 +181,51 @@ def profiled_traffic(workload_tag: str):
 
 # ----------------------------------------------------------------------------- CPU oracle leg
 
-def cpu_oracle(w, seconds: float):
-    """Time the oracle (as it stands) on host cores over a bounded sample of the workload's sequences."""
-    import oracle
-    import synth
-    from concurrent.futures import ThreadPoolExecutor
+class CpuOracle:
+    """The oracle (as it stands) on host cores over a bounded sample of the workload's sequences."""
 
-    order = np.argsort(w.ctx_len)
-    picks = [int(order[0]), int(order[-1])] + [int(i) for i in order[1:-1:max(1, len(order) // 14)]]
-    picks = list(dict.fromkeys(picks))
-    # Inputs (codes, scales, queries) prepared untimed, like resident device inputs.
-    prepared = []
-    for b in picks:
-        L = int(w.ctx_len[b])
-        kv = {buf: oracle.seq_kv(w.seed, buf, b, L) for buf in range(w.num_buffers)}
-        for layer in range(len(w.layer_windows)):
-            qb = synth.q_rows(w.seed, synth.stream_q(layer), b, w.num_q_heads)
-            W = w.layer_windows[layer]
-            tokens = min(L, W) if W > 0 else L
-            prepared.append((qb, kv[w.layer_to_buffer[layer]], L, W, tokens))
-    cores = os.cpu_count() or 1
+    def __init__(self, w):
+        import oracle
+        import synth
 
-    def one(item):
-        qb, (kc, ks, vc, vs), L, W, _ = item
-        oracle.decode_seq(qb, kc, ks, vc, vs, L, W, w.softmax_scale)
+        self.w = w
+        order = np.argsort(w.ctx_len)
+        picks = [int(order[0]), int(order[-1])] + [int(i) for i in order[1:-1:max(1, len(order) // 14)]]
+        self.picks = list(dict.fromkeys(picks))
+        # Inputs (codes, scales, queries) prepared untimed, like resident device inputs.
+        self.items = []
+        for b in self.picks:
+            L = int(w.ctx_len[b])
+            kv = {buf: oracle.seq_kv(w.seed, buf, b, L) for buf in range(w.num_buffers)}
+            for layer in range(len(w.layer_windows)):
+                qb = synth.q_rows(w.seed, synth.stream_q(layer), b, w.num_q_heads)
+                W = w.layer_windows[layer]
+                tokens = min(L, W) if W > 0 else L
+                self.items.append((qb, kv[w.layer_to_buffer[layer]], L, W, tokens))
+        self.cores = os.cpu_count() or 1
 
-    done_tokens, t0 = 0, time.perf_counter()
-    with ThreadPoolExecutor(cores) as ex:
-        while True:
-            list(ex.map(one, prepared))
-            done_tokens += sum(p[4] for p in prepared)
-            if time.perf_counter() - t0 >= seconds:
-                break
-    dt = time.perf_counter() - t0
-    return {"value": done_tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{len(picks)} sequences (shortest, longest and evenly spaced by length) x "
-                      f"{len(w.layer_windows)} layers, repeated for {dt:.1f} s; float64 C oracle, "
-                      f"{cores} threads over (sequence, layer)"}
+    def run(self, seconds: float):
+        import oracle
+        from concurrent.futures import ThreadPoolExecutor
+
+        w = self.w
+
+        def one(item):
+            qb, (kc, ks, vc, vs), L, W, _ = item
+            oracle.decode_seq(qb, kc, ks, vc, vs, L, W, w.softmax_scale)
+
+        done_tokens, t0 = 0, time.perf_counter()
+        with ThreadPoolExecutor(self.cores) as ex:
+            while True:
+                list(ex.map(one, self.items))
+                done_tokens += sum(p[4] for p in self.items)
+                if time.perf_counter() - t0 >= seconds:
+                    break
+        dt = time.perf_counter() - t0
+        return {"value": done_tokens / dt, "unit": UNIT, "cores": self.cores, "kind": "oracle",
+                "sample": f"{len(self.picks)} sequences (shortest, longest and evenly spaced by length) x "
+                          f"{len(w.layer_windows)} layers of the same workload, repeated for {dt:.1f} s; float64 C "
+                          f"oracle, {self.cores} threads over (sequence, layer)"}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -256,13 +275,17 @@ def run_gpu(args, rank, world):
     barrier(world)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as clocks:
+    with ClockSampler(smi_index(torch.cuda.current_device())) as clocks:
         torch.cuda.synchronize()
+        if args.ncu:
+            torch.cuda.profiler.start()
         t_start.record(stream)
         for s in range(args.steps):
             step(ev[s])
         t_end.record(stream)
         torch.cuda.synchronize()
+        if args.ncu:
+            torch.cuda.profiler.stop()
     ms_total = t_start.elapsed_time(t_end)
     decode_ms = sum(ev[s][2 * l].elapsed_time(ev[s][2 * l + 1]) for s in range(args.steps) for l in range(nl))
     ms_max = allreduce_max(ms_total, world)
@@ -298,7 +321,7 @@ def run_gpu(args, rank, world):
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu:
-        result["cpu_baseline"] = cpu_oracle(w, args.cpu_seconds)
+        result["cpu_baseline"] = CpuOracle(w).run(args.cpu_seconds)
     return result
 
 
@@ -353,13 +376,14 @@ def run_reference(args):
     import synth
 
     w = synth.workload(args.config, sigma=args.sigma, batch=args.batch)
-    per_step = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    cpu = CpuOracle(w)
+    per_step = max(1.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        cpu_oracle(w, per_step / 4)
+        cpu.run(per_step / 2)
     vals, t0 = [], time.perf_counter()
     last = None
     for _ in range(args.steps):
-        last = cpu_oracle(w, per_step)
+        last = cpu.run(per_step)
         vals.append(last["value"])
     dt = time.perf_counter() - t0
     value = statistics.mean(vals)
