@@ -90,6 +90,20 @@ class PagedCache:
                                               w.layer_windows[layer], num_splits)
         return torch.empty(n, dtype=torch.uint8, device=self.device) if n else None
 
+    def prefill_workspace(self) -> torch.Tensor:
+        n = cai.cai_mqa_prefill_workspace_size(self.w.batch, self.max_pages_per_seq, self.w.page_size)
+        return torch.empty(n, dtype=torch.uint8, device=self.device)
+
+    def prefill(self, q: torch.Tensor, out: torch.Tensor, lse: torch.Tensor | None = None, workspace=None,
+                window: int | None = None, err=None) -> None:
+        """Attention of the step's n_new tokens (already appended) on the prefix ctx_len - n_new."""
+        w = self.w
+        if workspace is None:
+            workspace = self.prefill_workspace()
+        prefix = (self.ctx_len - w.n_new).to(torch.int32)
+        cai.cai_mqa_prefill_chunk(self.pools[0], q, self.table, prefix, w.layer_windows[0] if window is None else window,
+                                  w.softmax_scale, workspace, out, lse, err)
+
     def decode(self, layer: int, q: torch.Tensor, out: torch.Tensor, lse: torch.Tensor | None = None,
                num_splits: int = 0, workspace=None, err=None) -> None:
         w = self.w

@@ -124,6 +124,11 @@ cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int
                           void* workspace, size_t workspace_bytes, float* out, float* lse_out,
                           int32_t* err_flag, void* stream);
 
+/* Bytes of workspace cai_mqa_prefill_chunk needs: a contiguous 16-bit copy of
+ * the K and V codes and the scales of up to max_pages_per_seq * page_size keys
+ * per sequence (rounded up to 128).  Arguments as for cai_mqa_prefill_chunk. */
+size_t cai_mqa_prefill_workspace_size(int32_t batch, int32_t max_pages_per_seq, int32_t page_size);
+
 /* Attention for a chunk of new tokens appended on top of a reused prefix.
  * Prefix caching (Red Hat page, "3. Cache de prefixo") and the cross-turn
  * cache ("Character.AI: inference optimization", 04): the prefix K/V is read
@@ -132,14 +137,19 @@ cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int
  * keys are read from the same int8 pages.  New token i of sequence b sits at
  * position p0 + i (p0 = prefix_len[b]) and attends keys [lo, p0 + i] with
  * lo = 0 (window 0) or max(0, p0 + i + 1 - window).
- *   q       bf16 bits [batch][n_new][num_q_heads][head_dim], 16-byte aligned
- *   num_q_heads  a power of two from 1 to 128
- *   out     fp32 [batch][n_new][num_q_heads][head_dim]
- *   lse_out fp32 [batch][n_new][num_q_heads], nullable */
+ *   q           bf16 bits [batch][n_new][num_q_heads][head_dim], 16-byte aligned
+ *   num_q_heads a power of two from 1 to 128
+ *   block_table int32 [batch][max_pages_per_seq]; prefix_len int32 [batch]
+ *   workspace   device scratch of cai_mqa_prefill_workspace_size() bytes, 256-byte aligned
+ *   out         fp32 [batch][n_new][num_q_heads][head_dim]
+ *   lse_out     fp32 [batch][n_new][num_q_heads], natural log, nullable
+ * A sequence whose prefix_len + n_new exceeds the table sets CAI_DEVERR_LENGTH and
+ * gets out = 0, lse = -inf. */
 cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int32_t batch, int32_t n_new,
                                  int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
-                                 const int32_t* prefix_len, int32_t window, float softmax_scale, float* out,
-                                 float* lse_out, int32_t* err_flag, void* stream);
+                                 const int32_t* prefix_len, int32_t window, float softmax_scale, void* workspace,
+                                 size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
+                                 void* stream);
 
 /* Static description of a status code. */
 const char* cai_status_string(cai_status status);

@@ -17,7 +17,8 @@ import torch
 
 __all__ = [
     "CaiError", "CaiUnavailable", "KVPool", "library_path", "load", "cai_page_bytes", "cai_status_string",
-    "cai_kv_append", "cai_mqa_decode_workspace_size", "cai_mqa_decode", "cai_mqa_prefill_chunk",
+    "cai_kv_append", "cai_mqa_decode_workspace_size", "cai_mqa_decode", "cai_mqa_prefill_workspace_size",
+    "cai_mqa_prefill_chunk",
     "CAI_DEVERR_PAGE", "CAI_DEVERR_LENGTH", "CAI_DEVERR_TIMEOUT", "HEAD_DIM",
 ]
 
@@ -73,8 +74,10 @@ def load():
     lib.cai_mqa_decode.argtypes = [pool_p, i32, vp, i32, i32, vp, i32, i32, vp, i32, vp, i32, ctypes.c_float, i32,
                                    vp, sz, vp, vp, vp, vp]
     lib.cai_mqa_decode.restype = ctypes.c_int
-    lib.cai_mqa_prefill_chunk.argtypes = [pool_p, vp, i32, i32, i32, vp, i32, vp, i32, ctypes.c_float, vp, vp, vp,
-                                          vp]
+    lib.cai_mqa_prefill_workspace_size.argtypes = [i32, i32, i32]
+    lib.cai_mqa_prefill_workspace_size.restype = sz
+    lib.cai_mqa_prefill_chunk.argtypes = [pool_p, vp, i32, i32, i32, vp, i32, vp, i32, ctypes.c_float, vp, sz, vp, vp,
+                                          vp, vp]
     lib.cai_mqa_prefill_chunk.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -178,17 +181,22 @@ def cai_mqa_decode(pools: Sequence[KVPool], layer_to_pool: Sequence[int], layer:
     _check(st, "cai_mqa_decode")
 
 
+def cai_mqa_prefill_workspace_size(batch: int, max_pages_per_seq: int, page_size: int) -> int:
+    return int(load().cai_mqa_prefill_workspace_size(batch, max_pages_per_seq, page_size))
+
+
 def cai_mqa_prefill_chunk(pool: KVPool, q: torch.Tensor, block_table: torch.Tensor, prefix_len: torch.Tensor,
-                          window: int, softmax_scale: float, out: torch.Tensor,
+                          window: int, softmax_scale: float, workspace: torch.Tensor, out: torch.Tensor,
                           lse_out: Optional[torch.Tensor] = None, err_flag: Optional[torch.Tensor] = None,
                           stream=None) -> None:
     """Attention of n_new appended tokens on a reused prefix: q bf16 [batch][n_new][Hq][128]."""
     batch, n_new, hq = q.shape[0], q.shape[1], q.shape[2]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = load().cai_mqa_prefill_chunk(
         ctypes.byref(pool.struct), _ptr(q, "q", (torch.bfloat16, torch.int16), (batch, n_new, hq, HEAD_DIM)), batch,
         n_new, hq, _ptr(block_table, "block_table", torch.int32), block_table.shape[-1],
         _ptr(prefix_len, "prefix_len", torch.int32, (batch,)), window, float(softmax_scale),
-        _ptr(out, "out", torch.float32, (batch, n_new, hq, HEAD_DIM)),
+        _ptr(workspace, "workspace"), ws_bytes, _ptr(out, "out", torch.float32, (batch, n_new, hq, HEAD_DIM)),
         _ptr(lse_out, "lse_out", torch.float32, (batch, n_new, hq)), _ptr(err_flag, "err_flag", torch.int32),
         _stream(stream))
     _check(st, "cai_mqa_prefill_chunk")

@@ -163,13 +163,47 @@ cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int
                                                                                                 : CAI_ERR_CUDA;
 }
 
+size_t cai_mqa_prefill_workspace_size(int32_t batch, int32_t max_pages_per_seq, int32_t page_size) {
+  if (batch <= 0 || max_pages_per_seq <= 0 || !page_size_ok(page_size)) return 0;
+  return prefill_workspace_bytes(batch, max_pages_per_seq, page_size);
+}
+
 cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int32_t batch, int32_t n_new,
                                  int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
-                                 const int32_t* prefix_len, int32_t window, float softmax_scale, float* out,
-                                 float* lse_out, int32_t* err_flag, void* stream) {
-  (void)pool; (void)q; (void)batch; (void)n_new; (void)num_q_heads; (void)block_table; (void)max_pages_per_seq;
-  (void)prefix_len; (void)window; (void)softmax_scale; (void)out; (void)lse_out; (void)err_flag; (void)stream;
-  return CAI_ERR_UNSUPPORTED;
+                                 const int32_t* prefix_len, int32_t window, float softmax_scale, void* workspace,
+                                 size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
+                                 void* stream) {
+  cai_status st = check_pool(pool);
+  if (st != CAI_OK) return st;
+  if (batch < 0 || n_new < 0 || max_pages_per_seq <= 0 || window < 0 || !std::isfinite(softmax_scale))
+    return CAI_ERR_INVALID_ARG;
+  if (num_q_heads < 1 || num_q_heads > 128 || (num_q_heads & (num_q_heads - 1)) != 0) return CAI_ERR_UNSUPPORTED;
+  if ((int64_t)max_pages_per_seq * pool->page_size > (1ll << 24) || batch > 65535) return CAI_ERR_UNSUPPORTED;
+  if ((int64_t)n_new * num_q_heads > (1ll << 24)) return CAI_ERR_UNSUPPORTED;
+  if (batch == 0 || n_new == 0) return CAI_OK;
+  if (!q || !block_table || !prefix_len || !out) return CAI_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return CAI_ERR_INVALID_ARG;
+  const size_t need = prefill_workspace_bytes(batch, max_pages_per_seq, pool->page_size);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return CAI_ERR_WORKSPACE;
+  PrefillLaunch L;
+  L.pages = static_cast<const uint8_t*>(pool->pages);
+  L.num_pages = pool->num_pages;
+  L.page_size = pool->page_size;
+  L.max_pages = max_pages_per_seq;
+  L.table = block_table;
+  L.prefix_len = prefix_len;
+  L.q = q;
+  L.batch = batch;
+  L.n_new = n_new;
+  L.num_heads = num_q_heads;
+  L.window = window;
+  L.scale_log2 = softmax_scale * kLog2e;
+  L.workspace = workspace;
+  L.out = out;
+  L.lse_out = lse_out;
+  L.err = err_flag;
+  return launch_prefill(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CAI_OK : CAI_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -10,7 +10,7 @@ namespace cai {
 
 constexpr int kHeadDim = 128;
 constexpr int kMaxSplits = 64;
-constexpr int kDecodeTile = 64;        // tokens per decode tile (one MMA N)
+constexpr int kDecodeTile = 128;       // tokens per decode tile (MMA N of S, K of PV)
 constexpr int kDecodeRows = 64;        // MMA M for decode: query heads padded to 64
 constexpr int kDecodeStages = 3;       // raw page stages in flight per CTA
 constexpr float kLog2e = 1.4426950408889634f;
@@ -78,6 +78,23 @@ __host__ __device__ inline SeqSplits seq_splits(int32_t L, int32_t window, int32
   s.nsplit = (s.hi - 1) / chunk - s.first_chunk + 1;
   return s;
 }
+
+struct PrefillLaunch {
+  const uint8_t* pages;
+  int32_t num_pages, page_size, max_pages;
+  const int32_t* table;
+  const int32_t* prefix_len;
+  const uint16_t* q;
+  int32_t batch, n_new, num_heads, window;
+  float scale_log2;
+  void* workspace;
+  float* out;
+  float* lse_out;
+  int32_t* err;
+};
+
+size_t prefill_workspace_bytes(int32_t batch, int32_t max_pages_per_seq, int32_t page_size);
+cudaError_t launch_prefill(const PrefillLaunch& p, cudaStream_t stream);
 
 // Host side: the split plan for a launch (also used by the workspace query).
 DecodePlan plan_decode(int32_t max_pages_per_seq, int32_t page_size, int32_t window, int32_t num_splits);

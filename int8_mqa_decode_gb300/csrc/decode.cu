@@ -2,7 +2,7 @@
 // combine of the splits.
 //
 // What it computes (definition): for one query token per sequence and each
-// query head h, softmax over the attended positions of
+// query head h, softmax over the attended positions t of
 //   z_t = softmax_scale * <q_h, s_k[t] * k_code[t]>
 // and out_h = sum_t p_t * s_v[t] * v_code[t]  (Red Hat page, "Por que o cache
 // KV existe"), where every head reads the same single K/V head (Multi-Query
@@ -10,333 +10,461 @@
 // (hybrid attention, technique table of "Character.AI: inference
 // optimization", section 03).
 //
-// How (one CTA per (sequence, split); 4 warps; 2 CTAs per SM):
-//  * pages of a 64-token tile arrive by 1-D bulk copies (TMA engine) into a
-//    3-stage ring; one copy per page brings K codes, V codes and both scale
-//    rows, and serves all query heads;
-//  * all warps convert the int8 codes to fp16 (exact) into the canonical
-//    no-swizzle tcgen05 operand layouts (K: K-major; V: MN-major);
-//  * S = Q K^T runs on the tensor cores (tcgen05.mma kind::f16, M = 64 padded
-//    heads, N = 64 tokens, K = 128) into tensor memory; the per-token K scale
-//    and the softmax scale are applied in fp32 afterwards;
-//  * online softmax on S (two threads per head, one shuffle for the row max),
-//    with the reference max raised only when a logit exceeds it by 2^8 so that
-//    the output accumulator is rarely rescaled; P is scaled by the per-token V
-//    scale, rounded to fp16 and stored as the A operand of O += P V;
-//  * the split's partial output and log-sum-exp go to the workspace, or
-//    straight to `out` when the sequence has a single split.
+// How.  A persistent kernel, one CTA per SM, walks a static list of work
+// items (sequence, split) in 128-token tiles with five warp roles connected by
+// mbarriers:
+//  * producer (warp 0): one 1-D bulk copy (TMA engine) per page into a
+//    3-stage ring; a page carries K codes, V codes and both scale rows and is
+//    read once for all query heads.  Pages wholly outside the split (the part
+//    of a local layer before its window) are never read;
+//  * converters (warps 2-5): int8 codes -> fp16 (exact) into the canonical
+//    no-swizzle tcgen05 operand layouts in shared memory (K K-major, V
+//    MN-major), the per-token scales and mask into a small ring, and the
+//    item's query (bf16 -> fp16) into tensor memory;
+//  * MMA issuer (warp 1): S = Q K^T (tcgen05.mma kind::f16, M = 64 padded
+//    heads, N = 128 tokens, K = 128, A from tensor memory) into a double-
+//    buffered S, then O += P V (P from tensor memory, V from shared memory);
+//  * softmax (warps 6-9, two threads per head): applies the per-token K scale
+//    and softmax scale in fp32, keeps a reference maximum that is raised only
+//    when a logit exceeds it by 2^8 (so O is rarely rescaled), scales P by the
+//    per-token V scale, rounds it to fp16 into the S buffer it came from, and
+//    at the end of an item writes the normalised partial output and its
+//    log-sum-exp (or the final output when the sequence has one split).
 #include "common.cuh"
 #include "ptx.cuh"
 
 namespace cai {
 namespace {
 
-constexpr int T = kDecodeTile;                 // tokens per tile
-constexpr int NST = kDecodeStages;             // raw stages
-constexpr int kRawStageBytes = T * 264;        // 64 tokens of K, V and scales
-constexpr int kK16Bytes = T * kHeadDim * 2;    // fp16 K tile
-constexpr int kV16Bytes = T * kHeadDim * 2;    // fp16 V tile
-constexpr int kQ16Bytes = kDecodeRows * kHeadDim * 2;
-constexpr int kP16Bytes = kDecodeRows * T * 2;
+constexpr int T = kDecodeTile;                 // 128 tokens per tile
+constexpr int NST = kDecodeStages;             // raw page stages
+constexpr int kRawStageBytes = T * 264;        // K, V and scales of 128 tokens
+constexpr int kOp16Bytes = T * kHeadDim * 2;   // one fp16 operand tile (32 KB)
 constexpr int kOffRaw = 0;
-constexpr int kOffK16 = kOffRaw + NST * kRawStageBytes;
-constexpr int kOffV16 = kOffK16 + kK16Bytes;
-constexpr int kOffQ16 = kOffV16 + kV16Bytes;
-constexpr int kOffP16 = kOffQ16 + kQ16Bytes;
-constexpr int kOffKsc = kOffP16 + kP16Bytes;
-constexpr int kOffVsc = kOffKsc + T * 4;
-constexpr int kOffKbias = kOffVsc + T * 4;
-constexpr int kOffBars = kOffKbias + T * 4;     // full[NST], s_bar, pv_bar
-constexpr int kOffMisc = kOffBars + 8 * (NST + 2);
-constexpr int kSmemBytes = kOffMisc + 16 + 1024; // + alignment slack
-constexpr uint32_t kTmemCols = 256;             // S: cols [0, 64); O: cols [128, 256)
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 128;
-constexpr float kRescaleThreshold = 8.0f;       // log2 units: p <= 2^8 between rescales
+constexpr int kOffK16 = kOffRaw + NST * kRawStageBytes;  // K16[2]
+constexpr int kOffV16 = kOffK16 + 2 * kOp16Bytes;        // V16[1]
+constexpr int kOffScale = kOffV16 + kOp16Bytes;          // [2][3][T] floats: k scale, bias, v scale
+constexpr int kOffBars = kOffScale + 2 * 3 * T * 4;
+constexpr int kNumBars = 2 * NST + 2 + 1 + 2 + 2 + 1 + 1 + 1;
+constexpr int kOffMisc = kOffBars + 8 * kNumBars;        // tmem slot, abort flag, page_ok[NST]
+constexpr int kSmemBytes = kOffMisc + 64 + 1024;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColQ = 0;    // Q[2]: 64 columns each (128 fp16 channels as pairs)
+constexpr uint32_t kColS = 128;  // S[2]: 128 columns each; P (fp16 pairs) overwrites the first 64
+constexpr uint32_t kColO = 384;  // O: 128 columns
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: weights stay <= 2^8 between rescales
 
-// K-major no-swizzle operand tile with 128 columns (fp16): element (r, k) at
-// (r/8)*2048 + (k/8)*128 + (r%8)*16 + (k%8)*2.
-__device__ __forceinline__ uint32_t kmajor128_off(int r, int k8) { return (r >> 3) * 2048 + k8 * 128 + (r & 7) * 16; }
-// MN-major no-swizzle tile, T tokens along K, 128 channels along N: element (t, n)
-// at (n/8)*(T*16) + (t/8)*128 + (t%8)*16 + (n%8)*2.
+// K-major no-swizzle operand with 128 channels: element (t, k) at
+// (t/8)*2048 + (k/8)*128 + (t%8)*16 + (k%8)*2.
+__device__ __forceinline__ uint32_t kmajor_off(int t, int k8) { return (t >> 3) * 2048 + k8 * 128 + (t & 7) * 16; }
+// MN-major no-swizzle operand, T tokens along K and 128 channels along N:
+// element (t, n) at (n/8)*(T*16) + (t/8)*128 + (t%8)*16 + (n%8)*2.
 __device__ __forceinline__ uint32_t mnmajor_off(int t, int n8) { return n8 * (T * 16) + (t >> 3) * 128 + (t & 7) * 16; }
 
 __device__ __forceinline__ void set_err(int32_t* err, int bits) {
   if (err) atomicOr(err, bits);
 }
 
+// The static work list: items (sequence, split) in row-major order, taken
+// round-robin by the persistent CTAs.  Every role walks it identically.
+struct Item {
+  int b, split, start, end, tile0, ntiles;
+  bool direct;  // single split: write the final output
+  int kind;     // 0 = tiles to process, 1 = nothing to attend (split 0 writes zeros), 2 = skip
+  bool invalid;
+};
+
 template <int P>
-__global__ void __launch_bounds__(128, 2) decode_kernel(const DecodeParams p) {
+__device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
+  Item it;
+  it.b = idx / p.plan.max_splits;
+  it.split = idx - it.b * p.plan.max_splits;
+  const SeqSplits sp = seq_splits(p.ctx_len[it.b], p.window, p.max_pages * P, p.plan.chunk);
+  it.invalid = !sp.valid;
+  it.direct = sp.nsplit == 1;
+  it.ntiles = 0;
+  it.start = it.end = it.tile0 = 0;
+  if (sp.nsplit == 0) {
+    it.kind = it.split == 0 ? 1 : 2;
+    return it;
+  }
+  if (it.split >= sp.nsplit) {
+    it.kind = 2;
+    return it;
+  }
+  it.kind = 0;
+  const int chunk_idx = sp.first_chunk + it.split;
+  it.start = max(sp.lo, chunk_idx * p.plan.chunk);
+  it.end = min(sp.hi, (chunk_idx + 1) * p.plan.chunk);
+  it.tile0 = it.start / T;
+  it.ntiles = (it.end - 1) / T - it.tile0 + 1;
+  return it;
+}
+
+template <int P>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* raw = smem + kOffRaw;
   uint8_t* k16 = smem + kOffK16;
   uint8_t* v16 = smem + kOffV16;
-  uint8_t* q16 = smem + kOffQ16;
-  uint8_t* p16 = smem + kOffP16;
-  float* ksc = reinterpret_cast<float*>(smem + kOffKsc);
-  float* vsc = reinterpret_cast<float*>(smem + kOffVsc);
-  float* kbias = reinterpret_cast<float*>(smem + kOffKbias);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* s_bar = full + NST;
-  uint64_t* pv_bar = full + NST + 1;
+  float* scal = reinterpret_cast<float*>(smem + kOffScale);  // [2][3][T]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* raw_full = bars;              // [NST] producer -> converters (tx bytes)
+  uint64_t* raw_empty = bars + NST;       // [NST] converters -> producer (4 warps)
+  uint64_t* k_full = bars + 2 * NST;      // [2] converters -> MMA, softmax (4 warps)
+  uint64_t* v_full = k_full + 2;          // converters -> MMA (4 warps), one phase per tile
+  uint64_t* s_full = v_full + 1;          // [2] MMA commit after S
+  uint64_t* p_full = s_full + 2;          // [2] softmax -> MMA, converters (4 warps)
+  uint64_t* v_free = p_full + 2;          // MMA commit after PV, one phase per tile
+  uint64_t* o_full = v_free + 1;          // MMA commit after an item's last PV
+  uint64_t* o_empty = o_full + 1;         // softmax -> MMA after reading O (4 warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  uint32_t* page_ok = tmem_slot + 1;  // [NST] bit per page slot of the stage
-  int32_t* timeout = reinterpret_cast<int32_t*>(tmem_slot + 1 + NST);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kOffMisc + 4);
+  uint32_t* page_ok = reinterpret_cast<uint32_t*>(smem + kOffMisc + 8);  // [NST]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y, split = blockIdx.x;
   const int Hq = p.num_heads;
-  const int max_tokens = p.max_pages * P;
-  const SeqSplits sp = seq_splits(p.ctx_len[b], p.window, max_tokens, p.plan.chunk);
+  const int num_items = p.batch * p.plan.max_splits;
 
-  if (!sp.valid || sp.nsplit == 0) {
-    // Nothing to attend (or an invalid length): out = 0, lse = -inf, written by split 0.
-    if (split == 0) {
-      if (!sp.valid && tid == 0) set_err(p.err, CAI_DEVERR_LENGTH);
-      for (int e = tid; e < Hq * kHeadDim; e += blockDim.x) p.out[(int64_t)b * Hq * kHeadDim + e] = 0.0f;
-      if (p.lse_out)
-        for (int h = tid; h < Hq; h += blockDim.x) p.lse_out[(int64_t)b * Hq + h] = -INFINITY;
-    }
-    return;
-  }
-  if (split >= sp.nsplit) return;
-  const int chunk_idx = sp.first_chunk + split;
-  const int start = max(sp.lo, chunk_idx * p.plan.chunk);
-  const int end = min(sp.hi, (chunk_idx + 1) * p.plan.chunk);
-  const int tile0 = start / T;
-  const int ntiles = (end - 1) / T - tile0 + 1;
-  const bool direct = sp.nsplit == 1;
-  const int32_t* table = p.table + (int64_t)b * p.max_pages;
-
-  // ---- set-up: barriers, tensor memory, Q (bf16 -> fp16, padded rows = 0)
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
-    for (int s = 0; s < NST; ++s) mbar_init(&full[s], 1);
-    mbar_init(s_bar, 1);
-    mbar_init(pv_bar, 1);
-    *timeout = 0;
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], 4);
+    }
+    for (int c = 0; c < 2; ++c) {
+      mbar_init(&k_full[c], 4);
+      mbar_init(&s_full[c], 1);
+      mbar_init(&p_full[c], 4);
+    }
+    mbar_init(v_full, 4);
+    mbar_init(v_free, 1);
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, 4);
+    *abort_flag = 0;
     fence_barrier_init();
   }
-  {
-    const uint16_t* qb = p.q + (int64_t)b * Hq * kHeadDim;
-    for (int u = tid; u < kDecodeRows * 16; u += blockDim.x) {  // (row, 8-channel group)
-      const int r = u >> 4, k8 = u & 15;
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if (r < Hq) {
-        const uint4 src = *reinterpret_cast<const uint4*>(qb + r * kHeadDim + k8 * 8);
-        const uint32_t s4[4] = {src.x, src.y, src.z, src.w};
-        uint32_t d4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float lo = __uint_as_float(s4[e] << 16), hi = __uint_as_float(s4[e] & 0xFFFF0000u);
-          d4[e] = pack_f16x2(lo, hi);
-        }
-        w = make_uint4(d4[0], d4[1], d4[2], d4[3]);
-      }
-      *reinterpret_cast<uint4*>(q16 + kmajor128_off(r, k8)) = w;
-    }
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Issue the bulk copies of tile i into its stage (thread 0 only).
-  auto issue_tile = [&](int i) {
-    const int stage = i % NST;
-    const int tb = (tile0 + i) * T;
-    uint32_t bytes = 0, ok = 0;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t policy = policy_evict_first();
+      int g = 0;
+      for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
+        const Item it = make_item<P>(p, idx);
+        if (it.kind != 0) continue;
+        const int32_t* table = p.table + (int64_t)it.b * p.max_pages;
+        for (int t = 0; t < it.ntiles; ++t, ++g) {
+          const int s = g % NST;
+          if (g >= NST && !mbar_wait_abortable(&raw_empty[s], ((g / NST) - 1) & 1, abort_flag)) break;
+          const int tb = (it.tile0 + t) * T;
+          uint32_t ok = 0, bytes = 0;
 #pragma unroll
-    for (int ps = 0; ps < T / P; ++ps) {
-      const int t0 = tb + ps * P;
-      if (t0 + P <= start || t0 >= end) continue;  // page wholly outside the split
-      const int32_t pid = table[t0 / P];
-      if (pid < 0 || pid >= p.num_pages) {
-        set_err(p.err, CAI_DEVERR_PAGE);
+          for (int ps = 0; ps < T / P; ++ps) {
+            const int t0 = tb + ps * P;
+            if (t0 + P <= it.start || t0 >= it.end) continue;  // page wholly outside the split
+            const int32_t pid = table[t0 / P];
+            if (pid < 0 || pid >= p.num_pages) {
+              set_err(p.err, CAI_DEVERR_PAGE);
+              continue;
+            }
+            ok |= 1u << ps;
+            bytes += page_bytes(P);
+          }
+          page_ok[s] = ok;
+          mbar_arrive_expect_tx(&raw_full[s], bytes);
+#pragma unroll
+          for (int ps = 0; ps < T / P; ++ps) {
+            if (!(ok & (1u << ps))) continue;
+            const int32_t pid = table[(tb + ps * P) / P];
+            bulk_g2s_hint(raw + s * kRawStageBytes + ps * page_bytes(P), p.pages + (int64_t)pid * page_bytes(P),
+                          page_bytes(P), &raw_full[s], policy);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_f16_f32(kDecodeRows, T, 0, 0);
+      constexpr uint32_t idesc_o = idesc_f16_f32(kDecodeRows, kHeadDim, 0, 1);
+      const uint32_t k16a = smem_addr(k16), v16a = smem_addr(v16);
+      int g = 0, item_n = 0;
+      // The previous tile, whose PV is issued after the next S.
+      bool have_prev = false, prev_first = false, prev_last = false;
+      int prev_item_n = 0;
+      auto issue_pv = [&](int gp) {
+        const int c = gp & 1;
+        if (!mbar_wait_abortable(&p_full[c], (gp >> 1) & 1, abort_flag)) return;
+        if (!mbar_wait_abortable(v_full, gp & 1, abort_flag)) return;
+        if (prev_first && prev_item_n > 0 && !mbar_wait_abortable(o_empty, (prev_item_n - 1) & 1, abort_flag)) return;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < T / 16; ++ks)
+          mma_f16_ts(tmem + kColO, tmem + kColS + c * 128 + ks * 8, smem_desc(v16a + ks * 256, 128, T * 16),
+                     idesc_o, (!prev_first || ks > 0) ? 1u : 0u);
+        mma_commit(v_free);
+        if (prev_last) mma_commit(o_full);
+      };
+      for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
+        const Item it = make_item<P>(p, idx);
+        if (it.kind != 0) continue;
+        for (int t = 0; t < it.ntiles; ++t, ++g) {
+          const int c = g & 1;
+          if (!mbar_wait_abortable(&k_full[c], (g >> 1) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t qcol = kColQ + (item_n & 1) * 64;
+#pragma unroll
+          for (int ks = 0; ks < kHeadDim / 16; ++ks)
+            mma_f16_ts(tmem + kColS + c * 128, tmem + qcol + ks * 8, smem_desc(k16a + c * kOp16Bytes + ks * 256, 128, 2048),
+                       idesc_s, ks > 0 ? 1u : 0u);
+          mma_commit(&s_full[c]);
+          if (have_prev) issue_pv(g - 1);
+          have_prev = true;
+          prev_first = t == 0;
+          prev_last = t == it.ntiles - 1;
+          prev_item_n = item_n;
+        }
+        ++item_n;
+      }
+      if (have_prev && !*abort_flag) issue_pv(g - 1);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ converters
+    const int ctid = tid - 64;        // 0..127
+    const int quarter = warp & 3;     // TMEM lanes this warp may touch
+    int g = 0, item_n = 0;
+    for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
+      const Item it = make_item<P>(p, idx);
+      if (it.kind != 0) continue;
+      bool ok = true;
+      for (int t = 0; t < it.ntiles && ok; ++t, ++g) {
+        const int s = g % NST, c = g & 1;
+        const uint8_t* rs = raw + s * kRawStageBytes;
+        ok = mbar_wait_abortable(&raw_full[s], (g / NST) & 1, abort_flag);
+        if (ok && g >= 2) ok = mbar_wait_abortable(&s_full[c], ((g >> 1) - 1) & 1, abort_flag);  // K16[c] free
+        if (!ok) break;
+        // K: 1024 16-byte units per tile, 8 per thread; lanes rotated across chunks (conflict-free).
+#pragma unroll 4
+        for (int u8 = 0; u8 < 8; ++u8) {
+          const int unit = u8 * 16 + (ctid >> 3);
+          const int tt = (unit >> 3) * 8 + (ctid & 7);
+          const int ch = ((unit & 7) + (ctid & 7)) & 7;
+          const uint4 w = *reinterpret_cast<const uint4*>(rs + (tt / P) * page_bytes(P) + (tt % P) * kHeadDim + ch * 16);
+          uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
+          i8x4_to_f16x4(w.x, a0, a1);
+          i8x4_to_f16x4(w.y, a2, a3);
+          i8x4_to_f16x4(w.z, a4, a5);
+          i8x4_to_f16x4(w.w, a6, a7);
+          uint8_t* kd = k16 + c * kOp16Bytes;
+          *reinterpret_cast<uint4*>(kd + kmajor_off(tt, 2 * ch)) = make_uint4(a0, a1, a2, a3);
+          *reinterpret_cast<uint4*>(kd + kmajor_off(tt, 2 * ch + 1)) = make_uint4(a4, a5, a6, a7);
+        }
+        // Scales and mask of tile g into slot c: softmax of tile g-2 must be done with the slot.
+        if (g >= 2) ok = mbar_wait_abortable(&p_full[c], ((g >> 1) - 1) & 1, abort_flag);
+        if (!ok) break;
+        {
+          const int tt = ctid;
+          const int abs_t = (it.tile0 + t) * T + tt;
+          const bool valid = abs_t >= it.start && abs_t < it.end && ((page_ok[s] >> (tt / P)) & 1u);
+          const float* sc = reinterpret_cast<const float*>(rs + (tt / P) * page_bytes(P) + 2 * P * kHeadDim);
+          float* dst = scal + c * 3 * T;
+          dst[tt] = valid ? sc[tt % P] * p.scale_log2 : 0.0f;
+          dst[T + tt] = valid ? 0.0f : -INFINITY;
+          dst[2 * T + tt] = valid ? sc[P + tt % P] : 0.0f;
+        }
+        if (t == 0) {
+          // The item's query, bf16 -> fp16, into tensor memory Q[item_n & 1]: this warp's 16 rows.
+          const int r = quarter * 16 + (lane & 15);
+          const int half = lane >> 4;
+          uint32_t w[32];
+          if (r < Hq) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)it.b * Hq + r) * kHeadDim + half * 64);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const uint4 x = src[v];
+              const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[v * 4 + e] = pack_f16x2(__uint_as_float(xs[e] << 16), __uint_as_float(xs[e] & 0xFFFF0000u));
+            }
+          } else {
+#pragma unroll
+            for (int v = 0; v < 32; ++v) w[v] = 0;
+          }
+          tmem_st_16x32bx2_x32<32>(tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + (item_n & 1) * 64, w);
+          tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&k_full[c]);
+        // V: the single V16 buffer is free once PV of the previous tile is done.
+        if (g >= 1) ok = mbar_wait_abortable(v_free, (g - 1) & 1, abort_flag);
+        if (!ok) break;
+#pragma unroll 4
+        for (int u8 = 0; u8 < 8; ++u8) {
+          const int unit = u8 * 16 + (ctid >> 3);
+          const int tt = (unit >> 3) * 8 + (ctid & 7);
+          const int ch = ((unit & 7) + (ctid & 7)) & 7;
+          const uint4 w = *reinterpret_cast<const uint4*>(rs + (tt / P) * page_bytes(P) + P * kHeadDim +
+                                                          (tt % P) * kHeadDim + ch * 16);
+          uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
+          i8x4_to_f16x4(w.x, a0, a1);
+          i8x4_to_f16x4(w.y, a2, a3);
+          i8x4_to_f16x4(w.z, a4, a5);
+          i8x4_to_f16x4(w.w, a6, a7);
+          *reinterpret_cast<uint4*>(v16 + mnmajor_off(tt, 2 * ch)) = make_uint4(a0, a1, a2, a3);
+          *reinterpret_cast<uint4*>(v16 + mnmajor_off(tt, 2 * ch + 1)) = make_uint4(a4, a5, a6, a7);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&raw_empty[s]);
+          mbar_arrive(v_full);
+        }
+      }
+      if (!ok) break;
+      ++item_n;
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int quarter = warp & 3;
+    const int h = quarter * 16 + (lane & 15);  // head row
+    const int th = lane >> 4;                  // token half of each tile / channel half of O
+    const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
+    const bool warp_live = quarter * 16 < Hq;  // padded rows only: skip the arithmetic
+    int g = 0, item_n = 0;
+    for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
+      const Item it = make_item<P>(p, idx);
+      if (it.kind == 2) continue;
+      if (it.kind == 1) {
+        // Nothing to attend (L = 0) or an invalid length: out = 0, lse = -inf.
+        if (it.invalid && tid == 192) set_err(p.err, CAI_DEVERR_LENGTH);
+        if (h < Hq) {
+          float* dst = p.out + ((int64_t)it.b * Hq + h) * kHeadDim + th * 64;
+          for (int d = 0; d < 64; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (p.lse_out && th == 0) p.lse_out[(int64_t)it.b * Hq + h] = -INFINITY;
+        }
         continue;
       }
-      ok |= 1u << ps;
-      bytes += page_bytes(P);
-    }
-    page_ok[stage] = ok;
-    mbar_arrive_expect_tx(&full[stage], bytes);
+      float m_ref = -INFINITY, l_sum = 0.0f;
+      bool ok = true;
+      for (int t = 0; t < it.ntiles; ++t, ++g) {
+        const int c = g & 1;
+        ok = mbar_wait_abortable(&s_full[c], (g >> 1) & 1, abort_flag) &&
+             mbar_wait_abortable(&k_full[c], (g >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t scol = kColS + c * 128;
+        if (warp_live) {
+          uint32_t sr[64];
+          tmem_ld_16x32bx2_x64<64>(tmem + t_lane + scol, sr);
+          tmem_wait_ld();
+          const float* ksc = scal + c * 3 * T + th * 64;
+          const float* kbias = ksc + T;
+          const float* vsc = ksc + 2 * T;
+          float mx = -INFINITY;
 #pragma unroll
-    for (int ps = 0; ps < T / P; ++ps) {
-      if (!(ok & (1u << ps))) continue;
-      const int32_t pid = table[(tb + ps * P) / P];
-      bulk_g2s(raw + stage * kRawStageBytes + ps * page_bytes(P), p.pages + (int64_t)pid * page_bytes(P),
-               page_bytes(P), &full[stage]);
-    }
-  };
-
-  if (tid == 0)
-    for (int i = 0; i < NST && i < ntiles; ++i) issue_tile(i);
-
-  // Softmax state: this thread owns head row h, token half th of each tile.
-  const int h = warp * 16 + (lane & 15);
-  const int th = lane >> 4;
-  float m_ref = -INFINITY, l_sum = 0.0f;
-  const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
-  bool ok_all = true;
-
-  for (int i = 0; i < ntiles; ++i) {
-    const int stage = i % NST;
-    const uint8_t* rs = raw + stage * kRawStageBytes;
-    if (!mbar_wait(&full[stage], (i / NST) & 1)) ok_all = false;
-    if (i > 0 && !mbar_wait(pv_bar, (i - 1) & 1)) ok_all = false;
-
-    // ---- int8 -> fp16 conversion of K and V (rotated lane mapping: conflict-free)
+          for (int j = 0; j < 64; j += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(ksc + j);
+            const float4 bb = *reinterpret_cast<const float4*>(kbias + j);
+            float z0 = fmaf(__uint_as_float(sr[j]), a.x, bb.x), z1 = fmaf(__uint_as_float(sr[j + 1]), a.y, bb.y);
+            float z2 = fmaf(__uint_as_float(sr[j + 2]), a.z, bb.z), z3 = fmaf(__uint_as_float(sr[j + 3]), a.w, bb.w);
+            sr[j] = __float_as_uint(z0);
+            sr[j + 1] = __float_as_uint(z1);
+            sr[j + 2] = __float_as_uint(z2);
+            sr[j + 3] = __float_as_uint(z3);
+            mx = fmaxf(mx, fmaxf(fmaxf(z0, z1), fmaxf(z2, z3)));
+          }
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const bool raise = mx > m_ref + kRescaleThreshold;
+          const float alpha = raise ? ex2_approx(m_ref - mx) : 1.0f;
+          if (t > 0 && __any_sync(0xffffffffu, raise)) {
+            // O holds earlier tiles of this item: wait for the previous PV, then rescale.
+            ok = mbar_wait_abortable(v_free, (g - 1) & 1, abort_flag);
+            if (ok) {
+              tc_fence_after();
+              uint32_t o[64];
+              tmem_ld_16x32bx2_x64<64>(tmem + t_lane + kColO, o);
+              tmem_wait_ld();
 #pragma unroll
-    for (int it = 0; it < (T * 8) / 128; ++it) {
-      const int unit = it * 16 + (tid >> 3);  // 0 .. T-1 groups of 8 units
-      const int t = (unit >> 3) * 8 + (tid & 7);
-      const int c = ((unit & 7) + (tid & 7)) & 7;  // 16-byte chunk of the 128-byte row
-      const int ps = t / P, slot = t % P;
-      const uint8_t* pg = rs + ps * page_bytes(P);
-      const uint4 kw = *reinterpret_cast<const uint4*>(pg + slot * kHeadDim + c * 16);
-      const uint4 vw = *reinterpret_cast<const uint4*>(pg + P * kHeadDim + slot * kHeadDim + c * 16);
-      uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
-      i8x4_to_f16x4(kw.x, a0, a1);
-      i8x4_to_f16x4(kw.y, a2, a3);
-      i8x4_to_f16x4(kw.z, a4, a5);
-      i8x4_to_f16x4(kw.w, a6, a7);
-      *reinterpret_cast<uint4*>(k16 + kmajor128_off(t, 2 * c)) = make_uint4(a0, a1, a2, a3);
-      *reinterpret_cast<uint4*>(k16 + kmajor128_off(t, 2 * c + 1)) = make_uint4(a4, a5, a6, a7);
-      i8x4_to_f16x4(vw.x, a0, a1);
-      i8x4_to_f16x4(vw.y, a2, a3);
-      i8x4_to_f16x4(vw.z, a4, a5);
-      i8x4_to_f16x4(vw.w, a6, a7);
-      *reinterpret_cast<uint4*>(v16 + mnmajor_off(t, 2 * c)) = make_uint4(a0, a1, a2, a3);
-      *reinterpret_cast<uint4*>(v16 + mnmajor_off(t, 2 * c + 1)) = make_uint4(a4, a5, a6, a7);
-    }
-    if (tid < T) {
-      const int t = tid;
-      const int ps = t / P, slot = t % P;
-      const int abs_t = (tile0 + i) * T + t;
-      const bool valid = abs_t >= start && abs_t < end && ((page_ok[stage] >> ps) & 1u);
-      const float* sc = reinterpret_cast<const float*>(rs + ps * page_bytes(P) + 2 * P * kHeadDim);
-      ksc[t] = valid ? sc[slot] * p.scale_log2 : 0.0f;
-      kbias[t] = valid ? 0.0f : -INFINITY;
-      vsc[t] = valid ? sc[P + slot] : 0.0f;
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    if (tid == 0) {
-      if (i + NST < ntiles) issue_tile(i + NST);
-      constexpr uint32_t idesc = idesc_f16_f32(64, T, 0, 0);
-      const uint32_t qa = smem_addr(q16), ka = smem_addr(k16);
+              for (int j = 0; j < 64; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+              tmem_st_16x32bx2_x64<64>(tmem + t_lane + kColO, o);
+              tmem_wait_st();
+            }
+          }
+          if (raise) {
+            l_sum *= alpha;
+            m_ref = mx;
+          }
+          const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
+          uint32_t pw[32];
 #pragma unroll
-      for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        mma_f16_ss(tmem + kColS, smem_desc(qa + ks * 256, 128, 2048), smem_desc(ka + ks * 256, 128, 2048), idesc,
-                   ks > 0);
-      mma_commit(s_bar);
-    }
-    if (!mbar_wait(s_bar, i & 1)) ok_all = false;
-    tc_fence_after();
-
-    // ---- softmax on this thread's 32 logits
-    uint32_t sr[32];
-    tmem_ld_16x32bx2_x32<32>(tmem + t_lane + kColS, sr);
-    tmem_wait_ld();
-    float z[32];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int t = th * 32 + j;
-      z[j] = fmaf(__uint_as_float(sr[j]), ksc[t], kbias[t]);
-      mx = fmaxf(mx, z[j]);
-    }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    const bool raise = mx > m_ref + kRescaleThreshold;
-    const float alpha = raise ? ex2_approx(m_ref - mx) : 1.0f;  // m_ref = -inf -> 0
-    if (i > 0 && __any_sync(0xffffffffu, raise)) {
-      // Rescale this warp's rows of O (columns th*64 .. th*64+63).
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t o[32];
-        const uint32_t ta = tmem + t_lane + kColO + half * 32;
-        tmem_ld_16x32bx2_x32<64>(ta, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-        tmem_st_16x32bx2_x32<64>(ta, o);
+          for (int j = 0; j < 64; j += 4) {
+            const float4 vs = *reinterpret_cast<const float4*>(vsc + j);
+            const float e0 = ex2_approx(__uint_as_float(sr[j]) - m_use);
+            const float e1 = ex2_approx(__uint_as_float(sr[j + 1]) - m_use);
+            const float e2 = ex2_approx(__uint_as_float(sr[j + 2]) - m_use);
+            const float e3 = ex2_approx(__uint_as_float(sr[j + 3]) - m_use);
+            l_sum += (e0 + e1) + (e2 + e3);
+            pw[j / 2] = pack_f16x2(e0 * vs.x, e1 * vs.y);
+            pw[j / 2 + 1] = pack_f16x2(e2 * vs.z, e3 * vs.w);
+          }
+          tmem_st_16x32bx2_x32<32>(tmem + t_lane + scol, pw);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[c]);
+        if (!ok) break;
       }
-      tmem_wait_st();
-    }
-    if (raise) {
-      l_sum *= alpha;
-      m_ref = mx;
-    }
-    const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
-    uint32_t pw[16];
+      if (!ok) break;
+      // ---- end of item: normalise this thread's half row of O and write it.
+      ok = mbar_wait_abortable(o_full, item_n & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      if (warp_live) {
+        const float l_row = l_sum + __shfl_xor_sync(0xffffffffu, l_sum, 16);
+        const float inv = l_row > 0.0f ? 1.0f / l_row : 0.0f;
+        uint32_t o[64];
+        tmem_ld_16x32bx2_x64<64>(tmem + t_lane + kColO, o);
+        tmem_wait_ld();
+        if (h < Hq) {
+          float* dst = it.direct ? p.out + ((int64_t)it.b * Hq + h) * kHeadDim + th * 64
+                                 : p.ws_o + (((int64_t)it.b * p.plan.max_splits + it.split) * Hq + h) * kHeadDim +
+                                       th * 64;
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const int t = th * 32 + j;
-      const float p0 = ex2_approx(z[j] - m_use), p1 = ex2_approx(z[j + 1] - m_use);
-      l_sum += p0 + p1;
-      pw[j / 2] = pack_f16x2(p0 * vsc[t], p1 * vsc[t + 1]);
-    }
-    // P (fp16) as the K-major A operand: row h, tokens th*32 .. th*32+31.
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      *reinterpret_cast<uint4*>(p16 + (h >> 3) * (T * 16) + (th * 4 + c) * 128 + (h & 7) * 16) =
-          make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(64, kHeadDim, 0, 1);
-      const uint32_t pa = smem_addr(p16), va = smem_addr(v16);
-#pragma unroll
-      for (int ks = 0; ks < T / 16; ++ks)
-        mma_f16_ss(tmem + kColO, smem_desc(pa + ks * 256, 128, T * 16), smem_desc(va + ks * 256, 128, T * 16), idesc,
-                   (i > 0 || ks > 0) ? 1u : 0u);
-      mma_commit(pv_bar);
+          for (int j = 0; j < 64; j += 4)
+            *reinterpret_cast<float4*>(dst + j) =
+                make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
+                            __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+          if (th == 0) {
+            const float lse2 = l_row > 0.0f ? m_ref + __log2f(l_row) : -INFINITY;
+            if (it.direct) {
+              if (p.lse_out) p.lse_out[(int64_t)it.b * Hq + h] = lse2 * kLn2;
+            } else {
+              p.ws_lse[((int64_t)it.b * p.plan.max_splits + it.split) * Hq + h] = lse2;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty);
+      ++item_n;
     }
   }
-  if (!mbar_wait(pv_bar, (ntiles - 1) & 1)) ok_all = false;
-  tc_fence_after();
-  if (!ok_all) atomicOr(timeout, 1);
 
-  // ---- epilogue: normalise this thread's half row of O and write it.
-  const float l_row = l_sum + __shfl_xor_sync(0xffffffffu, l_sum, 16);
-  const float inv = l_row > 0.0f ? 1.0f / l_row : 0.0f;
-  const float lse2 = l_row > 0.0f ? m_ref + __log2f(l_row) : -INFINITY;
-  float* dst;
-  if (direct) {
-    dst = p.out + ((int64_t)b * Hq + h) * kHeadDim + th * 64;
-  } else {
-    dst = p.ws_o + (((int64_t)b * p.plan.max_splits + split) * Hq + h) * kHeadDim + th * 64;
-  }
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint32_t o[32];
-    tmem_ld_16x32bx2_x32<64>(tmem + t_lane + kColO + half * 32, o);
-    tmem_wait_ld();
-    if (h < Hq) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(dst + half * 32 + j) =
-            make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv, __uint_as_float(o[j + 2]) * inv,
-                        __uint_as_float(o[j + 3]) * inv);
-    }
-  }
-  if (h < Hq && th == 0) {
-    if (direct) {
-      if (p.lse_out) p.lse_out[(int64_t)b * Hq + h] = lse2 * kLn2;
-    } else {
-      p.ws_lse[((int64_t)b * p.plan.max_splits + split) * Hq + h] = lse2;
-    }
-  }
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *timeout) set_err(p.err, CAI_DEVERR_TIMEOUT);
+  if (tid == 0 && *abort_flag) set_err(p.err, CAI_DEVERR_TIMEOUT);
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -373,6 +501,18 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
   if (p.lse_out && lane == 0) p.lse_out[(int64_t)b * Hq + h] = wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 1;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
 template <int P>
 cudaError_t launch_decode_p(const DecodeParams& p, cudaStream_t stream) {
   static bool attr_set[64] = {};
@@ -383,8 +523,9 @@ cudaError_t launch_decode_p(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  dim3 grid(p.plan.max_splits, p.batch);
-  decode_kernel<P><<<grid, 128, kSmemBytes, stream>>>(p);
+  const int64_t items = (int64_t)p.batch * p.plan.max_splits;
+  const int grid = (int)(items < num_sms() ? items : num_sms());
+  decode_kernel<P><<<grid, kThreads, kSmemBytes, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.plan.max_splits <= 1) return e;
   const int64_t warps = (int64_t)p.batch * p.num_heads;
