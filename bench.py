@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cai", choices=["cai", "reference"])
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 5])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--sigma", type=float, default=1.0)
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (testing only)")
@@ -98,7 +98,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -228,7 +228,95 @@ class CpuOracle:
                           f"oracle, {self.cores} threads over (sequence, layer)"}
 
 
-# ----------------------------------------------------------------------------- GPU arm
+# ----------------------------------------------------------------------------- GPU arm: append-prefill
+
+def prefill_flops(w):
+    """4*d FLOPs per (query row, attended key) pair: QK^T and PV, causal within the chunk."""
+    prefix = np.asarray(w.ctx_len, dtype=np.int64) - w.n_new
+    pairs = 0
+    for p0 in prefix:
+        for i in range(w.n_new):
+            hi = int(p0) + i + 1
+            lo = max(0, hi - w.layer_windows[0]) if w.layer_windows[0] > 0 else 0
+            pairs += hi - lo
+    return 4 * 128 * w.num_q_heads * pairs, pairs
+
+
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["bf16_tflops_sustained"]), float(d["bf16_tflops"]), "measured"
+    return 1700.0, 1900.0, "fallback"
+
+
+def run_prefill(args, rank, world):
+    import torch
+    import harness
+    import int8_mqa_decode_gb300 as cai
+    import synth
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    import __graft_entry__
+    __graft_entry__.build()
+    seed = 1004 + 100 * rank
+    w = synth.workload(4, seed=seed, batch=args.batch)
+    cache = harness.PagedCache(w)
+    cache.fill()
+    q = cache.prefill_q()
+    out = torch.empty(w.batch, w.n_new, w.num_q_heads, 128, device="cuda")
+    ws = cache.prefill_workspace()
+    kvs = [cache.step_kv(0)]
+    prefix = (cache.ctx_len - w.n_new).to(torch.int32)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def step(rec=None):
+        k, v, start = kvs[0]
+        cai.cai_kv_append(cache.pools[0], k, v, cache.table, start)
+        if rec is not None:
+            rec[0].record(stream)
+        cai.cai_mqa_prefill_chunk(cache.pools[0], q, cache.table, prefix, 0, w.softmax_scale, ws, out)
+        if rec is not None:
+            rec[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(smi_index(torch.cuda.current_device())) as clocks:
+        torch.cuda.synchronize()
+        if args.ncu:
+            torch.cuda.profiler.start()
+        t0.record(stream)
+        for s in range(args.steps):
+            step(ev[s])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if args.ncu:
+            torch.cuda.profiler.stop()
+    ms = allreduce_max(t0.elapsed_time(t1), world)
+    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    flops, pairs = prefill_flops(w)
+    sustained, burst, kind = bf16_peak()
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    return {
+        "metric": "append-prefill attention TFLOP/s (KV-query pairs / s)", "value": world * flops * args.steps / (ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 KV, bf16/fp16 MMA / fp32 accumulate", "data": "synthetic",
+        "config": {"workload": w.name, "global_batch": w.batch * world, "kv_query_pairs_per_head": pairs,
+                   "flops_per_step": flops, "parallelism": f"replicas x{world}"},
+        "gpu_launches": 3 * args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
+                     "frac": achieved / sustained, "traffic": None, "peak_kind": kind + " bf16 sustained",
+                     "kernel": "cai_mqa_prefill_chunk (dequant pass + tcgen05 attention)"},
+        "clocks": clocks.summary(),
+    }
+
+
+# ----------------------------------------------------------------------------- GPU arm: decode
 
 def run_gpu(args, rank, world):
     import torch
@@ -433,7 +521,7 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return
-    res = run_gpu(args, rank, world)
+    res = run_prefill(args, rank, world) if args.config == 4 else run_gpu(args, rank, world)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
