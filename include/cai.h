@@ -124,6 +124,29 @@ cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int
                           void* workspace, size_t workspace_bytes, float* out, float* lse_out,
                           int32_t* err_flag, void* stream);
 
+/* Decode without any caller scratch.  The pages have no counterpart to this
+ * entry point: it exists for callers that cannot allocate device memory at
+ * the moment they decode -- a serving loop that forbids cudaMalloc after
+ * warm-up (an allocation can synchronise the device and stall other
+ * streams), a plug-in interface that passes only input and output buffers,
+ * or a framework that owns all device memory and lends none to its plug-ins.
+ * It computes exactly what cai_mqa_decode computes, with the same arguments
+ * minus the workspace: the split partials go to a scratch array built into
+ * the library, CAI_NO_ALLOC_SCRATCH_BYTES per GPU, held by every GPU that
+ * loads the library until the process exits.  A call whose plan needs more
+ * (cai_mqa_decode_workspace_size() above the limit) returns
+ * CAI_ERR_WORKSPACE and launches nothing: lower num_splits (1 needs none).
+ * The first call on a device looks up the array's device address on that
+ * device; make that first call before any stream capture.  All calls share
+ * the array and it keeps the last call's contents: calls whose kernels
+ * overlap on the GPU (unordered streams) race on it. */
+#define CAI_NO_ALLOC_SCRATCH_BYTES (32u << 20)
+cai_status cai_mqa_decode_no_alloc(const cai_kv_pool* pools, int32_t num_pools, const int32_t* layer_to_pool,
+                                   int32_t num_layers, int32_t layer, const uint16_t* q, int32_t batch,
+                                   int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
+                                   const int32_t* ctx_len, int32_t window, float softmax_scale, int32_t num_splits,
+                                   float* out, float* lse_out, int32_t* err_flag, void* stream);
+
 /* Bytes of workspace cai_mqa_prefill_chunk needs: a contiguous 16-bit copy of
  * the K and V codes and the scales of up to max_pages_per_seq * page_size keys
  * per sequence (rounded up to 128).  Arguments as for cai_mqa_prefill_chunk. */

@@ -17,7 +17,8 @@ import torch
 
 __all__ = [
     "CaiError", "CaiUnavailable", "KVPool", "library_path", "load", "cai_page_bytes", "cai_status_string",
-    "cai_kv_append", "cai_mqa_decode_workspace_size", "cai_mqa_decode", "cai_mqa_prefill_workspace_size",
+    "cai_kv_append", "cai_mqa_decode_workspace_size", "cai_mqa_decode", "cai_mqa_decode_no_alloc",
+    "cai_mqa_prefill_workspace_size",
     "cai_mqa_prefill_chunk",
     "CAI_DEVERR_PAGE", "CAI_DEVERR_LENGTH", "CAI_DEVERR_TIMEOUT", "HEAD_DIM",
 ]
@@ -74,6 +75,9 @@ def load():
     lib.cai_mqa_decode.argtypes = [pool_p, i32, vp, i32, i32, vp, i32, i32, vp, i32, vp, i32, ctypes.c_float, i32,
                                    vp, sz, vp, vp, vp, vp]
     lib.cai_mqa_decode.restype = ctypes.c_int
+    lib.cai_mqa_decode_no_alloc.argtypes = [pool_p, i32, vp, i32, i32, vp, i32, i32, vp, i32, vp, i32,
+                                            ctypes.c_float, i32, vp, vp, vp, vp]
+    lib.cai_mqa_decode_no_alloc.restype = ctypes.c_int
     lib.cai_mqa_prefill_workspace_size.argtypes = [i32, i32, i32]
     lib.cai_mqa_prefill_workspace_size.restype = sz
     lib.cai_mqa_prefill_chunk.argtypes = [pool_p, vp, i32, i32, i32, vp, i32, vp, i32, ctypes.c_float, vp, sz, vp, vp,
@@ -179,6 +183,23 @@ def cai_mqa_decode(pools: Sequence[KVPool], layer_to_pool: Sequence[int], layer:
         _ptr(lse_out, "lse_out", torch.float32, (batch, hq)), _ptr(err_flag, "err_flag", torch.int32),
         _stream(stream))
     _check(st, "cai_mqa_decode")
+
+
+def cai_mqa_decode_no_alloc(pools: Sequence[KVPool], layer_to_pool: Sequence[int], layer: int, q: torch.Tensor,
+                            block_table: torch.Tensor, ctx_len: torch.Tensor, window: int, softmax_scale: float,
+                            num_splits: int, out: torch.Tensor, lse_out: Optional[torch.Tensor] = None,
+                            err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """cai_mqa_decode for callers that cannot allocate: split partials live in the library's own scratch."""
+    batch, hq = q.shape[0], q.shape[1]
+    l2p = (ctypes.c_int32 * len(layer_to_pool))(*layer_to_pool)
+    st = load().cai_mqa_decode_no_alloc(
+        _pool_array(pools), len(pools), l2p, len(layer_to_pool), layer,
+        _ptr(q, "q", (torch.bfloat16, torch.int16), (batch, hq, HEAD_DIM)), batch, hq,
+        _ptr(block_table, "block_table", torch.int32), block_table.shape[-1],
+        _ptr(ctx_len, "ctx_len", torch.int32, (batch,)), window, float(softmax_scale), num_splits,
+        _ptr(out, "out", torch.float32, (batch, hq, HEAD_DIM)), _ptr(lse_out, "lse_out", torch.float32, (batch, hq)),
+        _ptr(err_flag, "err_flag", torch.int32), _stream(stream))
+    _check(st, "cai_mqa_decode_no_alloc")
 
 
 def cai_mqa_prefill_workspace_size(batch: int, max_pages_per_seq: int, page_size: int) -> int:
