@@ -88,7 +88,7 @@ class PagedCache:
         w = self.w
         n = cai.cai_mqa_decode_workspace_size(w.batch, w.num_q_heads, self.max_pages_per_seq, w.page_size,
                                               w.layer_windows[layer], num_splits)
-        return torch.empty(n, dtype=torch.uint8, device=self.device) if n else None
+        return torch.zeros(n, dtype=torch.uint8, device=self.device)  # the header must start at zero
 
     def prefill_workspace(self) -> torch.Tensor:
         n = cai.cai_mqa_prefill_workspace_size(self.w.batch, self.max_pages_per_seq, self.w.page_size)

@@ -92,8 +92,11 @@ cai_status cai_kv_append(const cai_kv_pool* pool, const float* k_new, const floa
                          int32_t n_new, const int32_t* block_table, int32_t max_pages_per_seq,
                          const int32_t* start_pos, int32_t* err_flag, void* stream);
 
-/* Bytes of workspace cai_mqa_decode needs for these arguments (0 when no split is needed).
- * Arguments as for cai_mqa_decode. */
+/* Bytes of workspace cai_mqa_decode needs for these arguments: a 256-byte
+ * header (the counters of the kernel's work queue) plus, when sequences are
+ * split, the partial outputs.  Arguments as for cai_mqa_decode.  The automatic
+ * split plan (num_splits = 0) depends on the SM count of the current device:
+ * query with the device that will run the call. */
 size_t cai_mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_pages_per_seq,
                                      int32_t page_size, int32_t window, int32_t num_splits);
 
@@ -109,11 +112,14 @@ size_t cai_mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t
  *   window                 0 = global; W > 0 = local: only the last W positions
  *                          [max(0, L-W), L) are attended, pages wholly before them are never read
  *   softmax_scale          logit = softmax_scale * <q, k>
- *   num_splits             0 = automatic; otherwise the attended span is cut into at most
- *                          this many chunks (1..64) processed by separate CTAs and merged
- *                          with their log-sum-exp
- *   workspace              device scratch of at least cai_mqa_decode_workspace_size() bytes
- *                          (nullable when that is 0), 256-byte aligned
+ *   num_splits             0 = automatic; otherwise the attended span of each sequence is cut
+ *                          into at most this many consecutive chunks (1..64), processed as
+ *                          separate work items and merged with their log-sum-exp
+ *   workspace              device scratch of at least cai_mqa_decode_workspace_size() bytes,
+ *                          256-byte aligned.  Its first 256 bytes must be zero before the first
+ *                          call that uses it; every call leaves them zero again (after a call
+ *                          that reported CAI_DEVERR_TIMEOUT, zero them before reuse).  Calls that
+ *                          share a workspace must not overlap on the GPU.
  *   out                    fp32 [batch][num_q_heads][head_dim]
  *   lse_out                fp32 [batch][num_q_heads] natural-log log-sum-exp of the logits, nullable
  * A sequence with nothing to attend (L = 0) gets out = 0 and lse = -inf. */
@@ -173,6 +179,46 @@ cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int
                                  const int32_t* prefix_len, int32_t window, float softmax_scale, void* workspace,
                                  size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
                                  void* stream);
+
+/* ---- Cross-turn KV cache in host memory ----------------------------------
+ * "Character.AI: inference optimization", 04 Cache between turns: the KV of
+ * every processed prefix and generated message is kept in host memory in an
+ * LRU cache with a tree structure, indexed by a rolling hash of the prefix
+ * tokens; a query retrieves the longest matching prefix.  Here the tree's
+ * edges are whole pages (page_size tokens, all KV buffers of a layer stack);
+ * matches are confirmed token by token, so hash collisions cannot return the
+ * wrong KV; eviction removes the least recently used leaf.  Restored pages are
+ * byte-identical to the stored ones.  The cache owns a host arena of
+ * capacity_pages * num_buffers * cai_page_bytes() bytes (pinned when a GPU is
+ * present).  Calls on one cache are serialised by a mutex. */
+typedef struct cai_host_cache cai_host_cache;
+
+/* NULL on bad arguments or when the arena cannot be allocated. */
+cai_host_cache* cai_host_cache_create(int32_t page_size, int32_t head_dim, int32_t num_buffers,
+                                      int64_t capacity_pages);
+void cai_host_cache_destroy(cai_host_cache* cache);
+
+/* Tokens of the longest cached prefix of tokens[0, n_tokens): a multiple of page_size
+ * (0 on a miss).  Marks the matched path as recently used. */
+int32_t cai_host_cache_match(cai_host_cache* cache, const int32_t* tokens, int32_t n_tokens);
+
+/* Copy the cached pages of tokens[0, n_tokens) (n_tokens a multiple of page_size, all
+ * cached) into pages block_table_row[0 .. n_tokens/page_size) of each of the num_buffers
+ * pools.  block_table_row and pools are host arrays; pools[i].pages may be device or
+ * host memory.  Device copies are asynchronous on `stream`. */
+cai_status cai_host_cache_restore(cai_host_cache* cache, const int32_t* tokens, int32_t n_tokens,
+                                  const cai_kv_pool* pools, const int32_t* block_table_row, void* stream);
+
+/* Keep the full pages of tokens[0, n_tokens) (a trailing partial page is ignored), read
+ * from pages block_table_row[...] of each pool; pages already cached are not copied
+ * again.  Evicts least recently used leaves when the arena is full; returns
+ * CAI_ERR_WORKSPACE if the path alone does not fit.  Returns after the copies are done. */
+cai_status cai_host_cache_store(cai_host_cache* cache, const int32_t* tokens, int32_t n_tokens,
+                                const cai_kv_pool* pools, const int32_t* block_table_row, void* stream);
+
+/* Counters: matches with at least one page, matches with none, pages held, evictions. */
+void cai_host_cache_stats(cai_host_cache* cache, int64_t* hits, int64_t* misses, int64_t* pages_cached,
+                          int64_t* evictions);
 
 /* Static description of a status code. */
 const char* cai_status_string(cai_status status);

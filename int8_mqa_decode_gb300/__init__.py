@@ -20,7 +20,9 @@ __all__ = [
     "cai_kv_append", "cai_mqa_decode_workspace_size", "cai_mqa_decode", "cai_mqa_decode_no_alloc",
     "cai_mqa_prefill_workspace_size",
     "cai_mqa_prefill_chunk",
-    "CAI_DEVERR_PAGE", "CAI_DEVERR_LENGTH", "CAI_DEVERR_TIMEOUT", "HEAD_DIM",
+    "CAI_DEVERR_PAGE", "CAI_DEVERR_LENGTH", "CAI_DEVERR_TIMEOUT", "HEAD_DIM", "cai_host_cache_create",
+    "cai_host_cache_destroy", "cai_host_cache_match", "cai_host_cache_restore", "cai_host_cache_store",
+    "cai_host_cache_stats",
 ]
 
 HEAD_DIM = 128
@@ -83,6 +85,19 @@ def load():
     lib.cai_mqa_prefill_chunk.argtypes = [pool_p, vp, i32, i32, i32, vp, i32, vp, i32, ctypes.c_float, vp, sz, vp, vp,
                                           vp, vp]
     lib.cai_mqa_prefill_chunk.restype = ctypes.c_int
+    lib.cai_host_cache_create.argtypes = [i32, i32, i32, ctypes.c_int64]
+    lib.cai_host_cache_create.restype = vp
+    lib.cai_host_cache_destroy.argtypes = [vp]
+    lib.cai_host_cache_destroy.restype = None
+    lib.cai_host_cache_match.argtypes = [vp, vp, i32]
+    lib.cai_host_cache_match.restype = i32
+    lib.cai_host_cache_restore.argtypes = [vp, vp, i32, pool_p, vp, vp]
+    lib.cai_host_cache_restore.restype = ctypes.c_int
+    lib.cai_host_cache_store.argtypes = [vp, vp, i32, pool_p, vp, vp]
+    lib.cai_host_cache_store.restype = ctypes.c_int
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    lib.cai_host_cache_stats.argtypes = [vp, i64p, i64p, i64p, i64p]
+    lib.cai_host_cache_stats.restype = None
     _lib = lib
     return lib
 
@@ -221,3 +236,56 @@ def cai_mqa_prefill_chunk(pool: KVPool, q: torch.Tensor, block_table: torch.Tens
         _ptr(lse_out, "lse_out", torch.float32, (batch, n_new, hq)), _ptr(err_flag, "err_flag", torch.int32),
         _stream(stream))
     _check(st, "cai_mqa_prefill_chunk")
+
+
+# ----------------------------------------------------------------------------- cross-turn host KV cache
+
+def _i32_host(a) -> "ctypes.Array":
+    import numpy as np
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def cai_host_cache_create(page_size: int, num_buffers: int, capacity_pages: int, head_dim: int = HEAD_DIM) -> int:
+    h = load().cai_host_cache_create(page_size, head_dim, num_buffers, capacity_pages)
+    if not h:
+        raise CaiError(CAI_ERR_INVALID_ARG, "cai_host_cache_create")
+    return h
+
+
+def cai_host_cache_destroy(cache: int) -> None:
+    load().cai_host_cache_destroy(cache)
+
+
+def cai_host_cache_match(cache: int, tokens) -> int:
+    keep, ptr = _i32_host(tokens)
+    return int(load().cai_host_cache_match(cache, ptr, len(keep)))
+
+
+def _pool_structs(pools):
+    arr = (cai_kv_pool * len(pools))()
+    for i, p in enumerate(pools):
+        arr[i] = p.struct if isinstance(p, KVPool) else p
+    return arr
+
+
+def cai_host_cache_restore(cache: int, tokens, n_tokens: int, pools, block_table_row, stream=None) -> None:
+    keep, ptr = _i32_host(tokens)
+    tkeep, tptr = _i32_host(block_table_row)
+    st = load().cai_host_cache_restore(cache, ptr, n_tokens, _pool_structs(pools), tptr,
+                                       _stream(stream) if torch.cuda.is_available() else None)
+    _check(st, "cai_host_cache_restore")
+
+
+def cai_host_cache_store(cache: int, tokens, pools, block_table_row, stream=None) -> None:
+    keep, ptr = _i32_host(tokens)
+    tkeep, tptr = _i32_host(block_table_row)
+    st = load().cai_host_cache_store(cache, ptr, len(keep), _pool_structs(pools), tptr,
+                                     _stream(stream) if torch.cuda.is_available() else None)
+    _check(st, "cai_host_cache_store")
+
+
+def cai_host_cache_stats(cache: int) -> dict:
+    v = [ctypes.c_int64() for _ in range(4)]
+    load().cai_host_cache_stats(cache, *[ctypes.byref(x) for x in v])
+    return dict(zip(("hits", "misses", "pages_cached", "evictions"), (x.value for x in v)))

@@ -15,24 +15,32 @@ static inline bool page_size_ok(int32_t P) { return P == 16 || P == 32 || P == 6
 
 // Split plan.  The attended span of a sequence is at most `span` tokens (the
 // window, or the block-table capacity for a global layer).  Chunks are
-// multiples of the 64-token decode tile.  Automatic choice: about 16 chunks
-// per maximal span, between 256 and 4096 tokens, never more than 64 splits.
-DecodePlan plan_decode(int32_t max_pages_per_seq, int32_t page_size, int32_t window, int32_t num_splits) {
+// multiples of the 128-token tile.  Automatic choice: about eight work items
+// per SM for the expected total work (half the capacity per sequence for a
+// global layer, the whole window for a local one), chunks of 512 to 16384
+// tokens, at most 64 splits; a local layer is not split when its batch alone
+// gives every SM a sequence (each extra split costs its partial's write and
+// read, about an eighth of a 1024-token window at 32 heads).
+DecodePlan plan_decode(int32_t batch, int32_t max_pages_per_seq, int32_t page_size, int32_t window,
+                       int32_t num_splits, int32_t sms) {
   const int64_t cap = (int64_t)max_pages_per_seq * page_size;
   const int64_t span = window > 0 ? (window < cap ? window : cap) : cap;
   int64_t chunk;
   if (num_splits > 0) {
     chunk = round_up(ceil_div(span, num_splits), kDecodeTile);
+  } else if (window > 0) {
+    const int64_t want = batch >= sms ? 1 : ceil_div(sms, batch);
+    chunk = round_up(ceil_div(span, want), kDecodeTile);
   } else {
-    chunk = round_up(ceil_div(span, 16), kDecodeTile);
-    if (chunk < 256) chunk = 256;
-    if (chunk > 4096) chunk = 4096;
-    const int64_t min_chunk = round_up(ceil_div(span, kMaxSplits), kDecodeTile);
-    if (chunk < min_chunk) chunk = min_chunk;
+    const int64_t expected = (int64_t)batch * ((span + 1) / 2);
+    chunk = round_up(ceil_div(expected, 8ll * sms), kDecodeTile);
+    if (chunk < 512) chunk = 512;
+    if (chunk > 16384) chunk = 16384;
   }
+  const int64_t min_chunk = round_up(ceil_div(span, kMaxSplits), kDecodeTile);
+  if (chunk < min_chunk) chunk = min_chunk;
   if (chunk < kDecodeTile) chunk = kDecodeTile;
-  // A window that does not start on a chunk boundary can touch one extra chunk.
-  int64_t splits = ceil_div(span, chunk) + (window > 0 ? 1 : 0);
+  int64_t splits = ceil_div(span, chunk);
   if (splits < 1) splits = 1;
   DecodePlan p;
   p.chunk = (int32_t)chunk;
@@ -41,10 +49,10 @@ DecodePlan plan_decode(int32_t max_pages_per_seq, int32_t page_size, int32_t win
 }
 
 static size_t workspace_bytes_for(int32_t batch, int32_t num_q_heads, const DecodePlan& plan) {
-  if (plan.max_splits <= 1) return 0;
+  if (plan.max_splits <= 1) return kWorkspaceHeader;
   const size_t rows = (size_t)batch * plan.max_splits * num_q_heads;
   const size_t o_bytes = (size_t)round_up((int64_t)(rows * kHeadDim * sizeof(float)), 256);
-  return o_bytes + (size_t)round_up((int64_t)(rows * sizeof(float)), 256);
+  return kWorkspaceHeader + o_bytes + (size_t)round_up((int64_t)(rows * sizeof(float)), 256);
 }
 
 }  // namespace cai
@@ -107,7 +115,8 @@ size_t cai_mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t
   if (batch <= 0 || num_q_heads <= 0 || max_pages_per_seq <= 0 || !page_size_ok(page_size) || window < 0 ||
       num_splits < 0 || num_splits > kMaxSplits)
     return 0;
-  return workspace_bytes_for(batch, num_q_heads, plan_decode(max_pages_per_seq, page_size, window, num_splits));
+  return workspace_bytes_for(batch, num_q_heads,
+                             plan_decode(batch, max_pages_per_seq, page_size, window, num_splits, num_sms()));
 }
 
 cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int32_t* layer_to_pool,
@@ -132,9 +141,10 @@ cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int
   if (!q || !block_table || !ctx_len || !out) return CAI_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out)) return CAI_ERR_INVALID_ARG;
 
-  const DecodePlan plan = plan_decode(max_pages_per_seq, pool->page_size, window, num_splits);
+  const DecodePlan plan = plan_decode(batch, max_pages_per_seq, pool->page_size, window, num_splits, num_sms());
   const size_t need = workspace_bytes_for(batch, num_q_heads, plan);
-  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CAI_ERR_WORKSPACE;
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return CAI_ERR_WORKSPACE;
 
   DecodeParams p;
   p.pages = static_cast<const uint8_t*>(pool->pages);
@@ -150,13 +160,14 @@ cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int
   p.plan = plan;
   p.out = out;
   p.lse_out = lse_out;
+  p.queue = static_cast<uint32_t*>(workspace);
   p.ws_o = nullptr;
   p.ws_lse = nullptr;
-  if (need > 0) {
+  if (plan.max_splits > 1) {
     const size_t rows = (size_t)batch * plan.max_splits * num_q_heads;
-    p.ws_o = static_cast<float*>(workspace);
-    p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                        (size_t)round_up((int64_t)(rows * kHeadDim * sizeof(float)), 256));
+    uint8_t* base = static_cast<uint8_t*>(workspace) + kWorkspaceHeader;
+    p.ws_o = reinterpret_cast<float*>(base);
+    p.ws_lse = reinterpret_cast<float*>(base + (size_t)round_up((int64_t)(rows * kHeadDim * sizeof(float)), 256));
   }
   p.err = err_flag;
   return launch_decode(p, pool->page_size, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CAI_OK

@@ -11,8 +11,10 @@ namespace cai {
 constexpr int kHeadDim = 128;
 constexpr int kMaxSplits = 64;
 constexpr int kDecodeTile = 128;       // tokens per decode tile (MMA N of S, K of PV)
+constexpr int kRawTokens = 64;         // tokens per raw page stage (half a tile)
 constexpr int kDecodeRows = 64;        // MMA M for decode: query heads padded to 64
-constexpr int kDecodeStages = 3;       // raw page stages in flight per CTA
+constexpr int kDecodeStages = 5;       // raw page stages (64 tokens each) per CTA
+constexpr int kWorkspaceHeader = 256;  // decode workspace: work-queue counters, kept zero between calls
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -31,11 +33,11 @@ struct AppendParams {
 };
 
 // Work split of one decode launch.  The attended span [lo, hi) of every
-// sequence is cut at absolute multiples of `chunk` tokens; split j of
-// sequence b covers chunk number (lo / chunk) + j.
+// sequence is cut into consecutive chunks of `chunk` tokens starting at lo:
+// split j covers [lo + j*chunk, min(hi, lo + (j+1)*chunk)).
 struct DecodePlan {
   int32_t chunk;       // tokens per split, a multiple of kDecodeTile
-  int32_t max_splits;  // grid.x: upper bound of splits per sequence
+  int32_t max_splits;  // upper bound of splits per sequence
 };
 
 struct DecodeParams {
@@ -52,13 +54,13 @@ struct DecodeParams {
   float* lse_out;     // [B][Hq] natural log, nullable
   float* ws_o;        // [B][max_splits][Hq][128] partial outputs (normalised)
   float* ws_lse;      // [B][max_splits][Hq] partial lse, log2 units
+  uint32_t* queue;    // [2]: next work item, CTAs finished (both zero between calls)
   int32_t* err;
 };
 
 // Attended range and split bookkeeping shared by the decode and combine kernels.
 struct SeqSplits {
   int32_t lo, hi;      // attended positions [lo, hi)
-  int32_t first_chunk; // chunk index of split 0
   int32_t nsplit;      // number of non-empty splits (0 if nothing to attend)
   bool valid;          // length within the block table
 };
@@ -69,13 +71,7 @@ __host__ __device__ inline SeqSplits seq_splits(int32_t L, int32_t window, int32
   if (!s.valid) L = 0;
   s.hi = L;
   s.lo = (window > 0 && L > window) ? L - window : 0;
-  if (s.hi <= s.lo) {
-    s.first_chunk = 0;
-    s.nsplit = 0;
-    return s;
-  }
-  s.first_chunk = s.lo / chunk;
-  s.nsplit = (s.hi - 1) / chunk - s.first_chunk + 1;
+  s.nsplit = s.hi > s.lo ? (s.hi - s.lo + chunk - 1) / chunk : 0;
   return s;
 }
 
@@ -97,7 +93,9 @@ size_t prefill_workspace_bytes(int32_t batch, int32_t max_pages_per_seq, int32_t
 cudaError_t launch_prefill(const PrefillLaunch& p, cudaStream_t stream);
 
 // Host side: the split plan for a launch (also used by the workspace query).
-DecodePlan plan_decode(int32_t max_pages_per_seq, int32_t page_size, int32_t window, int32_t num_splits);
+DecodePlan plan_decode(int32_t batch, int32_t max_pages_per_seq, int32_t page_size, int32_t window,
+                       int32_t num_splits, int32_t num_sms);
+int num_sms();
 
 // Kernel launchers (return cudaGetLastError()).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);

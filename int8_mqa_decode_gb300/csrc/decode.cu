@@ -36,24 +36,28 @@
 namespace cai {
 namespace {
 
-constexpr int T = kDecodeTile;                 // 128 tokens per tile
+constexpr int T = kDecodeTile;                 // 128 tokens per MMA tile
+constexpr int RT = kRawTokens;                 // 64 tokens per raw stage
 constexpr int NST = kDecodeStages;             // raw page stages
-constexpr int kRawStageBytes = T * 264;        // K, V and scales of 128 tokens
+constexpr int kRawStageBytes = RT * 264;       // K, V and scales of 64 tokens
 constexpr int kOp16Bytes = T * kHeadDim * 2;   // one fp16 operand tile (32 KB)
+constexpr int kRing = 8;                       // work items published ahead by the producer
 constexpr int kOffRaw = 0;
 constexpr int kOffK16 = kOffRaw + NST * kRawStageBytes;  // K16[2]
-constexpr int kOffV16 = kOffK16 + 2 * kOp16Bytes;        // V16[1]
-constexpr int kOffScale = kOffV16 + kOp16Bytes;          // [2][3][T] floats: k scale, bias, v scale
+constexpr int kOffV16 = kOffK16 + 2 * kOp16Bytes;        // V16[2]
+constexpr int kOffScale = kOffV16 + 2 * kOp16Bytes;      // [2][3][T] floats: k scale, bias, v scale
 constexpr int kOffBars = kOffScale + 2 * 3 * T * 4;
-constexpr int kNumBars = 2 * NST + 2 + 1 + 2 + 2 + 1 + 1 + 1;
-constexpr int kOffMisc = kOffBars + 8 * kNumBars;        // tmem slot, abort flag, page_ok[NST]
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;
+constexpr int kNumBars = 2 * NST + 2 * 2 /*k_full,v_full*/ + 2 * 2 /*s_full,p_full*/ + 2 /*v_free*/ + 2 /*o*/ +
+                         2 * kRing;
+constexpr int kOffMisc = kOffBars + 8 * kNumBars;        // tmem slot, abort flag, page_ok[NST], ring[kRing]
+constexpr int kSmemBytes = kOffMisc + 16 + 4 * NST + 4 * kRing + 1024;
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0;    // Q[2]: 64 columns each (128 fp16 channels as pairs)
 constexpr uint32_t kColS = 128;  // S[2]: 128 columns each; P (fp16 pairs) overwrites the first 64
 constexpr uint32_t kColO = 384;  // O: 128 columns
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: weights stay <= 2^8 between rescales
+constexpr int kItemReaders = 9;  // converter warps + MMA warp + softmax warps
 
 // K-major no-swizzle operand with 128 channels: element (t, k) at
 // (t/8)*2048 + (k/8)*128 + (t%8)*16 + (k%8)*2.
@@ -66,15 +70,16 @@ __device__ __forceinline__ void set_err(int32_t* err, int bits) {
   if (err) atomicOr(err, bits);
 }
 
-// The static work list: items (sequence, split) in row-major order, taken
-// round-robin by the persistent CTAs.  Every role walks it identically.
+// A work item: one split of one sequence.  kind 0 = tiles to process,
+// 1 = nothing to attend (split 0 writes out = 0, lse = -inf).
 struct Item {
   int b, split, start, end, tile0, ntiles;
   bool direct;  // single split: write the final output
-  int kind;     // 0 = tiles to process, 1 = nothing to attend (split 0 writes zeros), 2 = skip
+  int kind;
   bool invalid;
 };
 
+// kind 2 = an empty split, never published.
 template <int P>
 __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
   Item it;
@@ -94,9 +99,8 @@ __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
     return it;
   }
   it.kind = 0;
-  const int chunk_idx = sp.first_chunk + it.split;
-  it.start = max(sp.lo, chunk_idx * p.plan.chunk);
-  it.end = min(sp.hi, (chunk_idx + 1) * p.plan.chunk);
+  it.start = sp.lo + it.split * p.plan.chunk;
+  it.end = min(sp.hi, it.start + p.plan.chunk);
   it.tile0 = it.start / T;
   it.ntiles = (it.end - 1) / T - it.tile0 + 1;
   return it;
@@ -114,15 +118,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   uint64_t* raw_full = bars;              // [NST] producer -> converters (tx bytes)
   uint64_t* raw_empty = bars + NST;       // [NST] converters -> producer (4 warps)
   uint64_t* k_full = bars + 2 * NST;      // [2] converters -> MMA, softmax (4 warps)
-  uint64_t* v_full = k_full + 2;          // converters -> MMA (4 warps), one phase per tile
-  uint64_t* s_full = v_full + 1;          // [2] MMA commit after S
+  uint64_t* v_full = k_full + 2;          // [2] converters -> MMA (4 warps)
+  uint64_t* s_full = v_full + 2;          // [2] MMA commit after S
   uint64_t* p_full = s_full + 2;          // [2] softmax -> MMA, converters (4 warps)
-  uint64_t* v_free = p_full + 2;          // MMA commit after PV, one phase per tile
-  uint64_t* o_full = v_free + 1;          // MMA commit after an item's last PV
+  uint64_t* v_free = p_full + 2;          // [2] MMA commit after PV
+  uint64_t* o_full = v_free + 2;          // MMA commit after an item's last PV
   uint64_t* o_empty = o_full + 1;         // softmax -> MMA after reading O (4 warps)
+  uint64_t* item_full = o_empty + 1;      // [kRing] producer -> readers
+  uint64_t* item_empty = item_full + kRing;  // [kRing] readers -> producer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kOffMisc + 4);
-  uint32_t* page_ok = reinterpret_cast<uint32_t*>(smem + kOffMisc + 8);  // [NST]
+  uint32_t* page_ok = reinterpret_cast<uint32_t*>(smem + kOffMisc + 16);      // [NST]
+  volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(page_ok + NST);  // [kRing]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_heads;
@@ -136,13 +143,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     }
     for (int c = 0; c < 2; ++c) {
       mbar_init(&k_full[c], 4);
+      mbar_init(&v_full[c], 4);
       mbar_init(&s_full[c], 1);
       mbar_init(&p_full[c], 4);
+      mbar_init(&v_free[c], 1);
     }
-    mbar_init(v_full, 4);
-    mbar_init(v_free, 1);
     mbar_init(o_full, 1);
     mbar_init(o_empty, 4);
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(&item_full[r], 1);
+      mbar_init(&item_empty[r], kItemReaders);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -151,118 +162,191 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Item k of this CTA, as published by the producer (-1 = no more work).
+  auto next_item = [&](int k, bool arrive_lane0) -> int {
+    const int slot = k % kRing;
+    if (!mbar_wait_abortable(&item_full[slot], (k / kRing) & 1, abort_flag)) return -1;
+    const int idx = ring[slot];
+    __syncwarp();
+    if (arrive_lane0 && lane == 0) mbar_arrive(&item_empty[slot]);
+    return idx;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t policy = policy_evict_first();
-      int g = 0;
-      for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
-        const Item it = make_item<P>(p, idx);
+      int r = 0, k = 0;
+      while (true) {
+        int idx = (int)atomicAdd(&p.queue[0], 1u);
+        if (idx >= num_items) idx = -1;
+        Item it;
+        if (idx >= 0) {
+          it = make_item<P>(p, idx);
+          if (it.kind == 2) continue;  // empty split: nobody needs to hear of it
+        }
+        const int slot = k % kRing;
+        if (k >= kRing && !mbar_wait_abortable(&item_empty[slot], ((k / kRing) - 1) & 1, abort_flag)) break;
+        ring[slot] = idx;
+        mbar_arrive(&item_full[slot]);
+        ++k;
+        if (idx < 0) break;
         if (it.kind != 0) continue;
         const int32_t* table = p.table + (int64_t)it.b * p.max_pages;
-        for (int t = 0; t < it.ntiles; ++t, ++g) {
-          const int s = g % NST;
-          if (g >= NST && !mbar_wait_abortable(&raw_empty[s], ((g / NST) - 1) & 1, abort_flag)) break;
-          const int tb = (it.tile0 + t) * T;
-          uint32_t ok = 0, bytes = 0;
-#pragma unroll
-          for (int ps = 0; ps < T / P; ++ps) {
-            const int t0 = tb + ps * P;
-            if (t0 + P <= it.start || t0 >= it.end) continue;  // page wholly outside the split
-            const int32_t pid = table[t0 / P];
-            if (pid < 0 || pid >= p.num_pages) {
-              set_err(p.err, CAI_DEVERR_PAGE);
-              continue;
+        bool ok = true;
+        for (int t = 0; t < it.ntiles && ok; ++t) {
+          for (int hf = 0; hf < 2; ++hf, ++r) {
+            const int s = r % NST;
+            if (r >= NST && !mbar_wait_abortable(&raw_empty[s], ((r / NST) - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
             }
-            ok |= 1u << ps;
-            bytes += page_bytes(P);
-          }
-          page_ok[s] = ok;
-          mbar_arrive_expect_tx(&raw_full[s], bytes);
+            const int tb = (it.tile0 + t) * T + hf * RT;
+            uint32_t okm = 0, bytes = 0;
+            int32_t pid[RT / P];
 #pragma unroll
-          for (int ps = 0; ps < T / P; ++ps) {
-            if (!(ok & (1u << ps))) continue;
-            const int32_t pid = table[(tb + ps * P) / P];
-            bulk_g2s_hint(raw + s * kRawStageBytes + ps * page_bytes(P), p.pages + (int64_t)pid * page_bytes(P),
-                          page_bytes(P), &raw_full[s], policy);
+            for (int ps = 0; ps < RT / P; ++ps) {
+              const int t0 = tb + ps * P;
+              pid[ps] = -1;
+              if (t0 + P <= it.start || t0 >= it.end) continue;  // page wholly outside the split
+              pid[ps] = table[t0 / P];
+            }
+#pragma unroll
+            for (int ps = 0; ps < RT / P; ++ps) {
+              const int t0 = tb + ps * P;
+              if (t0 + P <= it.start || t0 >= it.end) continue;
+              if (pid[ps] < 0 || pid[ps] >= p.num_pages) {
+                set_err(p.err, CAI_DEVERR_PAGE);
+                continue;
+              }
+              okm |= 1u << ps;
+              bytes += page_bytes(P);
+            }
+            page_ok[s] = okm;
+            mbar_arrive_expect_tx(&raw_full[s], bytes);
+#pragma unroll
+            for (int ps = 0; ps < RT / P; ++ps) {
+              if (!(okm & (1u << ps))) continue;
+              bulk_g2s_hint(raw + s * kRawStageBytes + ps * page_bytes(P), p.pages + (int64_t)pid[ps] * page_bytes(P),
+                            page_bytes(P), &raw_full[s], policy);
+            }
           }
         }
+        if (!ok) break;
+      }
+      // The last CTA to finish fetching leaves the queue counters at zero for the next call.
+      if (atomicAdd(&p.queue[1], 1u) == gridDim.x - 1) {
+        atomicExch(&p.queue[0], 0u);
+        atomicExch(&p.queue[1], 0u);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16_f32(kDecodeRows, T, 0, 0);
-      constexpr uint32_t idesc_o = idesc_f16_f32(kDecodeRows, kHeadDim, 0, 1);
-      const uint32_t k16a = smem_addr(k16), v16a = smem_addr(v16);
-      int g = 0, item_n = 0;
-      // The previous tile, whose PV is issued after the next S.
-      bool have_prev = false, prev_first = false, prev_last = false;
-      int prev_item_n = 0;
-      auto issue_pv = [&](int gp) {
-        const int c = gp & 1;
-        if (!mbar_wait_abortable(&p_full[c], (gp >> 1) & 1, abort_flag)) return;
-        if (!mbar_wait_abortable(v_full, gp & 1, abort_flag)) return;
-        if (prev_first && prev_item_n > 0 && !mbar_wait_abortable(o_empty, (prev_item_n - 1) & 1, abort_flag)) return;
-        tc_fence_after();
+    constexpr uint32_t idesc_s = idesc_f16_f32(kDecodeRows, T, 0, 0);
+    constexpr uint32_t idesc_o = idesc_f16_f32(kDecodeRows, kHeadDim, 0, 1);
+    const uint32_t k16a = smem_addr(k16), v16a = smem_addr(v16);
+    int g = 0, item_n = 0, k = 0;
+    bool have_prev = false, prev_first = false, prev_last = false;
+    int prev_item_n = 0;
+    auto issue_pv = [&](int gp) {
+      const int c = gp & 1;
+      if (!mbar_wait_abortable(&p_full[c], (gp >> 1) & 1, abort_flag)) return;
+      if (!mbar_wait_abortable(&v_full[c], (gp >> 1) & 1, abort_flag)) return;
+      if (prev_first && prev_item_n > 0 && !mbar_wait_abortable(o_empty, (prev_item_n - 1) & 1, abort_flag)) return;
+      tc_fence_after();
+      if (lane == 0) {
 #pragma unroll
         for (int ks = 0; ks < T / 16; ++ks)
-          mma_f16_ts(tmem + kColO, tmem + kColS + c * 128 + ks * 8, smem_desc(v16a + ks * 256, 128, T * 16),
-                     idesc_o, (!prev_first || ks > 0) ? 1u : 0u);
-        mma_commit(v_free);
+          mma_f16_ts(tmem + kColO, tmem + kColS + c * 128 + ks * 8,
+                     smem_desc(v16a + c * kOp16Bytes + ks * 256, 128, T * 16), idesc_o,
+                     (!prev_first || ks > 0) ? 1u : 0u);
+        mma_commit(&v_free[c]);
         if (prev_last) mma_commit(o_full);
-      };
-      for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
-        const Item it = make_item<P>(p, idx);
-        if (it.kind != 0) continue;
-        for (int t = 0; t < it.ntiles; ++t, ++g) {
-          const int c = g & 1;
-          if (!mbar_wait_abortable(&k_full[c], (g >> 1) & 1, abort_flag)) break;
-          tc_fence_after();
+      }
+      __syncwarp();
+    };
+    while (true) {
+      const int idx = next_item(k++, true);
+      if (idx < 0) break;
+      const Item it = make_item<P>(p, idx);
+      if (it.kind != 0) continue;
+      bool ok = true;
+      for (int t = 0; t < it.ntiles; ++t, ++g) {
+        const int c = g & 1;
+        if (!mbar_wait_abortable(&k_full[c], (g >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
           const uint32_t qcol = kColQ + (item_n & 1) * 64;
 #pragma unroll
           for (int ks = 0; ks < kHeadDim / 16; ++ks)
-            mma_f16_ts(tmem + kColS + c * 128, tmem + qcol + ks * 8, smem_desc(k16a + c * kOp16Bytes + ks * 256, 128, 2048),
-                       idesc_s, ks > 0 ? 1u : 0u);
+            mma_f16_ts(tmem + kColS + c * 128, tmem + qcol + ks * 8,
+                       smem_desc(k16a + c * kOp16Bytes + ks * 256, 128, 2048), idesc_s, ks > 0 ? 1u : 0u);
           mma_commit(&s_full[c]);
-          if (have_prev) issue_pv(g - 1);
-          have_prev = true;
-          prev_first = t == 0;
-          prev_last = t == it.ntiles - 1;
-          prev_item_n = item_n;
         }
-        ++item_n;
+        __syncwarp();
+        if (have_prev) issue_pv(g - 1);
+        have_prev = true;
+        prev_first = t == 0;
+        prev_last = t == it.ntiles - 1;
+        prev_item_n = item_n;
       }
-      if (have_prev && !*abort_flag) issue_pv(g - 1);
+      if (!ok) break;
+      ++item_n;
     }
+    if (have_prev && !*abort_flag) issue_pv(g - 1);
   } else if (warp < 6) {
     // ------------------------------------------------------------ converters
     const int ctid = tid - 64;        // 0..127
     const int quarter = warp & 3;     // TMEM lanes this warp may touch
-    int g = 0, item_n = 0;
-    for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
+    int g = 0, item_n = 0, k = 0;
+    while (true) {
+      const int idx = next_item(k++, true);
+      if (idx < 0) break;
       const Item it = make_item<P>(p, idx);
       if (it.kind != 0) continue;
+      // The item's query rows for this warp, bf16 -> fp16 (loaded now, stored with the first tile).
+      const int qr = quarter * 16 + (lane & 15);
+      uint32_t qw[32];
+      if (qr < Hq) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)it.b * Hq + qr) * kHeadDim + (lane >> 4) * 64);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = src[v];
+          const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            qw[v * 4 + e] = pack_f16x2(__uint_as_float(xs[e] << 16), __uint_as_float(xs[e] & 0xFFFF0000u));
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < 32; ++v) qw[v] = 0;
+      }
       bool ok = true;
       for (int t = 0; t < it.ntiles && ok; ++t, ++g) {
-        const int s = g % NST, c = g & 1;
-        const uint8_t* rs = raw + s * kRawStageBytes;
-        ok = mbar_wait_abortable(&raw_full[s], (g / NST) & 1, abort_flag);
+        const int c = g & 1;
+        const int s0 = (2 * g) % NST, s1 = (2 * g + 1) % NST;
+        ok = mbar_wait_abortable(&raw_full[s0], ((2 * g) / NST) & 1, abort_flag) &&
+             mbar_wait_abortable(&raw_full[s1], ((2 * g + 1) / NST) & 1, abort_flag);
         if (ok && g >= 2) ok = mbar_wait_abortable(&s_full[c], ((g >> 1) - 1) & 1, abort_flag);  // K16[c] free
         if (!ok) break;
         // K: 1024 16-byte units per tile, 8 per thread; lanes rotated across chunks (conflict-free).
+        uint8_t* kd = k16 + c * kOp16Bytes;
 #pragma unroll 4
         for (int u8 = 0; u8 < 8; ++u8) {
           const int unit = u8 * 16 + (ctid >> 3);
           const int tt = (unit >> 3) * 8 + (ctid & 7);
           const int ch = ((unit & 7) + (ctid & 7)) & 7;
-          const uint4 w = *reinterpret_cast<const uint4*>(rs + (tt / P) * page_bytes(P) + (tt % P) * kHeadDim + ch * 16);
+          const uint8_t* rs = raw + (tt < RT ? s0 : s1) * kRawStageBytes;
+          const int tr = tt & (RT - 1);
+          const uint4 w = *reinterpret_cast<const uint4*>(rs + (tr / P) * page_bytes(P) + (tr % P) * kHeadDim + ch * 16);
           uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
           i8x4_to_f16x4(w.x, a0, a1);
           i8x4_to_f16x4(w.y, a2, a3);
           i8x4_to_f16x4(w.z, a4, a5);
           i8x4_to_f16x4(w.w, a6, a7);
-          uint8_t* kd = k16 + c * kOp16Bytes;
           *reinterpret_cast<uint4*>(kd + kmajor_off(tt, 2 * ch)) = make_uint4(a0, a1, a2, a3);
           *reinterpret_cast<uint4*>(kd + kmajor_off(tt, 2 * ch + 1)) = make_uint4(a4, a5, a6, a7);
         }
@@ -271,63 +355,53 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         if (!ok) break;
         {
           const int tt = ctid;
+          const int s = tt < RT ? s0 : s1;
+          const int tr = tt & (RT - 1);
           const int abs_t = (it.tile0 + t) * T + tt;
-          const bool valid = abs_t >= it.start && abs_t < it.end && ((page_ok[s] >> (tt / P)) & 1u);
-          const float* sc = reinterpret_cast<const float*>(rs + (tt / P) * page_bytes(P) + 2 * P * kHeadDim);
+          const bool valid = abs_t >= it.start && abs_t < it.end && ((page_ok[s] >> (tr / P)) & 1u);
+          const float* sc = reinterpret_cast<const float*>(raw + s * kRawStageBytes + (tr / P) * page_bytes(P) +
+                                                           2 * P * kHeadDim);
           float* dst = scal + c * 3 * T;
-          dst[tt] = valid ? sc[tt % P] * p.scale_log2 : 0.0f;
+          dst[tt] = valid ? sc[tr % P] * p.scale_log2 : 0.0f;
           dst[T + tt] = valid ? 0.0f : -INFINITY;
-          dst[2 * T + tt] = valid ? sc[P + tt % P] : 0.0f;
+          dst[2 * T + tt] = valid ? sc[P + tr % P] : 0.0f;
         }
         if (t == 0) {
-          // The item's query, bf16 -> fp16, into tensor memory Q[item_n & 1]: this warp's 16 rows.
-          const int r = quarter * 16 + (lane & 15);
-          const int half = lane >> 4;
-          uint32_t w[32];
-          if (r < Hq) {
-            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)it.b * Hq + r) * kHeadDim + half * 64);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const uint4 x = src[v];
-              const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                w[v * 4 + e] = pack_f16x2(__uint_as_float(xs[e] << 16), __uint_as_float(xs[e] & 0xFFFF0000u));
-            }
-          } else {
-#pragma unroll
-            for (int v = 0; v < 32; ++v) w[v] = 0;
-          }
-          tmem_st_16x32bx2_x32<32>(tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + (item_n & 1) * 64, w);
+          // Q[item_n & 1] was last read by the S of an item at least two tiles back: done (K16 wait above).
+          tmem_st_16x32bx2_x32<32>(tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + (item_n & 1) * 64, qw);
           tmem_wait_st();
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&k_full[c]);
-        // V: the single V16 buffer is free once PV of the previous tile is done.
-        if (g >= 1) ok = mbar_wait_abortable(v_free, (g - 1) & 1, abort_flag);
+        // V: buffer c is free once PV of tile g-2 is done.
+        if (g >= 2) ok = mbar_wait_abortable(&v_free[c], ((g >> 1) - 1) & 1, abort_flag);
         if (!ok) break;
+        uint8_t* vd = v16 + c * kOp16Bytes;
 #pragma unroll 4
         for (int u8 = 0; u8 < 8; ++u8) {
           const int unit = u8 * 16 + (ctid >> 3);
           const int tt = (unit >> 3) * 8 + (ctid & 7);
           const int ch = ((unit & 7) + (ctid & 7)) & 7;
-          const uint4 w = *reinterpret_cast<const uint4*>(rs + (tt / P) * page_bytes(P) + P * kHeadDim +
-                                                          (tt % P) * kHeadDim + ch * 16);
+          const uint8_t* rs = raw + (tt < RT ? s0 : s1) * kRawStageBytes;
+          const int tr = tt & (RT - 1);
+          const uint4 w = *reinterpret_cast<const uint4*>(rs + (tr / P) * page_bytes(P) + P * kHeadDim +
+                                                          (tr % P) * kHeadDim + ch * 16);
           uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
           i8x4_to_f16x4(w.x, a0, a1);
           i8x4_to_f16x4(w.y, a2, a3);
           i8x4_to_f16x4(w.z, a4, a5);
           i8x4_to_f16x4(w.w, a6, a7);
-          *reinterpret_cast<uint4*>(v16 + mnmajor_off(tt, 2 * ch)) = make_uint4(a0, a1, a2, a3);
-          *reinterpret_cast<uint4*>(v16 + mnmajor_off(tt, 2 * ch + 1)) = make_uint4(a4, a5, a6, a7);
+          *reinterpret_cast<uint4*>(vd + mnmajor_off(tt, 2 * ch)) = make_uint4(a0, a1, a2, a3);
+          *reinterpret_cast<uint4*>(vd + mnmajor_off(tt, 2 * ch + 1)) = make_uint4(a4, a5, a6, a7);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&raw_empty[s]);
-          mbar_arrive(v_full);
+          mbar_arrive(&raw_empty[s0]);
+          mbar_arrive(&raw_empty[s1]);
+          mbar_arrive(&v_full[c]);
         }
       }
       if (!ok) break;
@@ -340,10 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     const int th = lane >> 4;                  // token half of each tile / channel half of O
     const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
     const bool warp_live = quarter * 16 < Hq;  // padded rows only: skip the arithmetic
-    int g = 0, item_n = 0;
-    for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
+    int g = 0, item_n = 0, k = 0;
+    while (true) {
+      const int idx = next_item(k++, true);
+      if (idx < 0) break;
       const Item it = make_item<P>(p, idx);
-      if (it.kind == 2) continue;
       if (it.kind == 1) {
         // Nothing to attend (L = 0) or an invalid length: out = 0, lse = -inf.
         if (it.invalid && tid == 192) set_err(p.err, CAI_DEVERR_LENGTH);
@@ -354,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         }
         continue;
       }
+      if (it.kind != 0) continue;
       float m_ref = -INFINITY, l_sum = 0.0f;
       bool ok = true;
       for (int t = 0; t < it.ntiles; ++t, ++g) {
@@ -375,8 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           for (int j = 0; j < 64; j += 4) {
             const float4 a = *reinterpret_cast<const float4*>(ksc + j);
             const float4 bb = *reinterpret_cast<const float4*>(kbias + j);
-            float z0 = fmaf(__uint_as_float(sr[j]), a.x, bb.x), z1 = fmaf(__uint_as_float(sr[j + 1]), a.y, bb.y);
-            float z2 = fmaf(__uint_as_float(sr[j + 2]), a.z, bb.z), z3 = fmaf(__uint_as_float(sr[j + 3]), a.w, bb.w);
+            const float z0 = fmaf(__uint_as_float(sr[j]), a.x, bb.x), z1 = fmaf(__uint_as_float(sr[j + 1]), a.y, bb.y);
+            const float z2 = fmaf(__uint_as_float(sr[j + 2]), a.z, bb.z), z3 = fmaf(__uint_as_float(sr[j + 3]), a.w, bb.w);
             sr[j] = __float_as_uint(z0);
             sr[j + 1] = __float_as_uint(z1);
             sr[j + 2] = __float_as_uint(z2);
@@ -388,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           const float alpha = raise ? ex2_approx(m_ref - mx) : 1.0f;
           if (t > 0 && __any_sync(0xffffffffu, raise)) {
             // O holds earlier tiles of this item: wait for the previous PV, then rescale.
-            ok = mbar_wait_abortable(v_free, (g - 1) & 1, abort_flag);
+            ok = mbar_wait_abortable(&v_free[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag);
             if (ok) {
               tc_fence_after();
               uint32_t o[64];
@@ -427,8 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       }
       if (!ok) break;
       // ---- end of item: normalise this thread's half row of O and write it.
-      ok = mbar_wait_abortable(o_full, item_n & 1, abort_flag);
-      if (!ok) break;
+      if (!mbar_wait_abortable(o_full, item_n & 1, abort_flag)) break;
       tc_fence_after();
       if (warp_live) {
         const float l_row = l_sum + __shfl_xor_sync(0xffffffffu, l_sum, 16);
@@ -501,6 +576,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
   if (p.lse_out && lane == 0) p.lse_out[(int64_t)b * Hq + h] = wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
+}  // namespace
+
 int num_sms() {
   static int cached[64] = {};
   int dev = 0;
@@ -512,6 +589,8 @@ int num_sms() {
   if (dev < 64) cached[dev] = n;
   return n;
 }
+
+namespace {
 
 template <int P>
 cudaError_t launch_decode_p(const DecodeParams& p, cudaStream_t stream) {

@@ -43,11 +43,12 @@ def test_page_bytes_and_status_strings(lib):
 
 
 def test_workspace_size_plan(lib):
-    # One split needs no workspace; the local layer of 1024 positions splits into 256-token chunks (+1 straddle).
-    assert cai.cai_mqa_decode_workspace_size(4, 8, 32, 16, 0, 1) == 0
-    ws = cai.cai_mqa_decode_workspace_size(256, 32, 2048, 16, 1024, 0)
-    rows = 256 * 5 * 32
-    assert ws == ((rows * 128 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    # One split needs only the 256-byte work-queue header; a 1024-position window in 4 splits also
+    # needs [B][4][Hq] partial outputs and log-sum-exps.
+    assert cai.cai_mqa_decode_workspace_size(4, 8, 32, 16, 0, 1) == 256
+    ws = cai.cai_mqa_decode_workspace_size(256, 32, 2048, 16, 1024, 4)
+    rows = 256 * 4 * 32
+    assert ws == 256 + ((rows * 128 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
     assert cai.cai_mqa_decode_workspace_size(4, 8, 32, 24, 0, 0) == 0  # unsupported page size
     assert cai.cai_mqa_decode_workspace_size(4, 8, 32, 16, 0, 65) == 0  # too many splits
 
@@ -99,9 +100,10 @@ def test_decode_validation(lib):
     assert call(splits=65) == 1
     assert call(scale=float("nan")) == 1
     assert call(batch=0) == 0
-    # 64 pages of 16 tokens in 4 splits need a workspace; every call here fails before any launch.
-    assert call(splits=4) == 3
+    # Every decode needs a workspace (at least its 256-byte header); every call here fails before any launch.
+    assert call(splits=1) == 3
     assert call(splits=4, ws=FAKE, ws_bytes=16) == 3
+    assert call(splits=1, ws=FAKE + 16, ws_bytes=4096) == 3  # not 256-byte aligned
     bad = (cai.cai_kv_pool * 1)(_pool(head_dim=96))
     assert call(pools=bad, npools=1, l2p=(ctypes.c_int32 * 1)(0), nlayers=1) == 2
 
