@@ -49,15 +49,29 @@ constexpr int kOffScale = kOffV16 + 2 * kOp16Bytes;      // [2][3][T] floats: k 
 constexpr int kOffBars = kOffScale + 2 * 3 * T * 4;
 constexpr int kNumBars = 2 * NST + 2 * 2 /*k_full,v_full*/ + 2 * 2 /*s_full,p_full*/ + 2 /*v_free*/ + 2 /*o*/ +
                          2 * kRing;
-constexpr int kOffMisc = kOffBars + 8 * kNumBars;        // tmem slot, abort flag, page_ok[NST], ring[kRing]
-constexpr int kSmemBytes = kOffMisc + 16 + 4 * NST + 4 * kRing + 1024;
-constexpr int kThreads = 320;
+constexpr int kOffMisc = kOffBars + 8 * kNumBars;        // tmem slot, abort flag, tile_full[2], page_ok[NST]
+constexpr int kOffRing = kOffMisc + 64;                  // [kRing] published work items
+constexpr int kRingInts = 16;                            // one ring entry: fields + first tile's page ids
+constexpr int kSmemBytes = kOffRing + kRing * kRingInts * 4 + 1024;
+// Warp roles, aligned to warpgroups so each group can resize its register file:
+//   warpgroup 0: producer (warp 0), MMA issuer (warp 1), scheduler (warp 2), spare (warp 3)
+//   warpgroups 1-2: converters (warps 4..11)
+//   warpgroup 3: softmax (warps 12..15, one per TMEM lane quarter)
+constexpr int kThreads = 512;
+constexpr int kSchedWarp = 2;
+constexpr int kConvWarp0 = 4;
+constexpr int kConvWarps = 8;
+constexpr int kSoftWarp0 = kConvWarp0 + kConvWarps;
+// Registers per thread after the split (launched with 128): 4 warps x 64 + 8 x 112 + 4 x 176
+// = 128 * (64 + 2 * 112 + 176) = 59392 <= 512 * 128 = 65536.
+constexpr int kRegsCtl = 64, kRegsConv = 112, kRegsSoft = 176;
+constexpr int kNoPage = -2147483647 - 1;                 // a page the tile does not need
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0;    // Q[2]: 64 columns each (128 fp16 channels as pairs)
 constexpr uint32_t kColS = 128;  // S[2]: 128 columns each; P (fp16 pairs) overwrites the first 64
 constexpr uint32_t kColO = 384;  // O: 128 columns
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: weights stay <= 2^8 between rescales
-constexpr int kItemReaders = 9;  // converter warps + MMA warp + softmax warps
+constexpr int kItemReaders = 2 + kConvWarps + 4;  // producer, MMA warp, converter warps, softmax warps
 
 // K-major no-swizzle operand with 128 channels: element (t, k) at
 // (t/8)*2048 + (k/8)*128 + (t%8)*16 + (k%8)*2.
@@ -78,6 +92,33 @@ struct Item {
   int kind;
   bool invalid;
 };
+
+// Ring entry: [0] b, [1] split, [2] start, [3] end, [4] tile0, [5] ntiles,
+// [6] flags (bit 0 direct, bit 1 invalid, bit 2 kind 1, bit 3 end of work),
+// [8 .. 8 + T/P) page ids of the item's first tile (kNoPage where not needed).
+__device__ __forceinline__ Item ring_item(const volatile int32_t* e, bool& done) {
+  Item it;
+  it.b = e[0];
+  it.split = e[1];
+  it.start = e[2];
+  it.end = e[3];
+  it.tile0 = e[4];
+  it.ntiles = e[5];
+  const int f = e[6];
+  it.direct = f & 1;
+  it.invalid = (f >> 1) & 1;
+  it.kind = (f >> 2) & 1;
+  done = (f >> 3) & 1;
+  return it;
+}
+
+// Page id of page slot `ps` of tile `t` of an item, or kNoPage if the tile does not need it.
+template <int P>
+__device__ __forceinline__ int32_t tile_page(const DecodeParams& p, const Item& it, int t, int ps) {
+  const int t0 = (it.tile0 + t) * T + ps * P;
+  if (ps >= T / P || t0 + P <= it.start || t0 >= it.end) return (int32_t)kNoPage;
+  return p.table[(int64_t)it.b * p.max_pages + t0 / P];
+}
 
 // kind 2 = an empty split, never published.
 template <int P>
@@ -108,6 +149,7 @@ __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
 
 template <int P>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+  static_assert(kRegsCtl * 128 + kRegsConv * 256 + kRegsSoft * 128 <= 128 * kThreads, "register split");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* raw = smem + kOffRaw;
@@ -128,8 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   uint64_t* item_empty = item_full + kRing;  // [kRing] readers -> producer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kOffMisc + 4);
-  uint32_t* page_ok = reinterpret_cast<uint32_t*>(smem + kOffMisc + 16);      // [NST]
-  volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(page_ok + NST);  // [kRing]
+  int32_t* tile_full = reinterpret_cast<int32_t*>(smem + kOffMisc + 8);               // [2]
+  uint32_t* page_ok = reinterpret_cast<uint32_t*>(smem + kOffMisc + 16);             // [NST]
+  volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(smem + kOffRing);      // [kRing][kRingInts]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_heads;
@@ -139,11 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 4);
+      mbar_init(&raw_empty[s], kConvWarps);
     }
     for (int c = 0; c < 2; ++c) {
-      mbar_init(&k_full[c], 4);
-      mbar_init(&v_full[c], 4);
+      mbar_init(&k_full[c], kConvWarps);
+      mbar_init(&v_full[c], kConvWarps);
       mbar_init(&s_full[c], 1);
       mbar_init(&p_full[c], 4);
       mbar_init(&v_free[c], 1);
@@ -162,59 +205,106 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Item k of this CTA, as published by the producer (-1 = no more work).
-  auto next_item = [&](int k, bool arrive_lane0) -> int {
+  // Item k of this CTA as published by the scheduler warp; every reader warp
+  // waits for it, copies it and releases the slot.
+  auto next_item = [&](int k, bool& done, int32_t* first_ids = nullptr) -> Item {
     const int slot = k % kRing;
-    if (!mbar_wait_abortable(&item_full[slot], (k / kRing) & 1, abort_flag)) return -1;
-    const int idx = ring[slot];
+    Item it = {};
+    if (!mbar_wait_abortable(&item_full[slot], (k / kRing) & 1, abort_flag)) {
+      done = true;
+      return it;
+    }
+    it = ring_item(ring + slot * kRingInts, done);
+    if (first_ids) *first_ids = lane < T / P ? (int32_t)ring[slot * kRingInts + 8 + lane] : (int32_t)kNoPage;
     __syncwarp();
-    if (arrive_lane0 && lane == 0) mbar_arrive(&item_empty[slot]);
-    return idx;
+    if (lane == 0) mbar_arrive(&item_empty[slot]);
+    return it;
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t policy = policy_evict_first();
-      int r = 0, k = 0;
-      while (true) {
-        int idx = (int)atomicAdd(&p.queue[0], 1u);
-        if (idx >= num_items) idx = -1;
-        Item it;
-        if (idx >= 0) {
-          it = make_item<P>(p, idx);
-          if (it.kind == 2) continue;  // empty split: nobody needs to hear of it
+  if (warp < kConvWarp0) {
+   setmaxnreg_dec<kRegsCtl>();
+   if (warp == kSchedWarp) {
+    // ------------------------------------------------------------ scheduler
+    // Takes work items from the global queue, decodes them and publishes them,
+    // up to kRing ahead of the roles that consume them.
+    int k = 0;
+    while (true) {
+      int idx = 0;
+      if (lane == 0) idx = (int)atomicAdd(&p.queue[0], 1u);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      const bool done = idx >= num_items;
+      Item it = {};
+      int32_t id = (int32_t)kNoPage;
+      if (!done) {
+        it = make_item<P>(p, idx);
+        if (it.kind == 2) continue;  // an empty split: nobody needs to hear of it
+        if (it.kind == 0) {
+          id = tile_page<P>(p, it, 0, lane);
+          // Warm L2 with the item's block-table entries (32 ids per 128-byte line, one line per lane).
+          const int first = it.start / P, last = (it.end - 1) / P;
+          const int32_t* row = p.table + (int64_t)it.b * p.max_pages;
+          for (int pg = (first & ~31) + lane * 32; pg <= last; pg += 32 * 32) prefetch_l2(row + pg);
         }
-        const int slot = k % kRing;
-        if (k >= kRing && !mbar_wait_abortable(&item_empty[slot], ((k / kRing) - 1) & 1, abort_flag)) break;
-        ring[slot] = idx;
+      }
+      const int slot = k % kRing;
+      if (k >= kRing && !mbar_wait_abortable(&item_empty[slot], ((k / kRing) - 1) & 1, abort_flag)) break;
+      volatile int32_t* e = ring + slot * kRingInts;
+      if (lane < T / P) e[8 + lane] = id;
+      if (lane == 0) {
+        if (!done) {
+          e[0] = it.b;
+          e[1] = it.split;
+          e[2] = it.start;
+          e[3] = it.end;
+          e[4] = it.tile0;
+          e[5] = it.ntiles;
+          e[6] = (it.direct ? 1 : 0) | (it.invalid ? 2 : 0) | (it.kind == 1 ? 4 : 0);
+        } else {
+          e[6] = 8;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
         mbar_arrive(&item_full[slot]);
-        ++k;
-        if (idx < 0) break;
-        if (it.kind != 0) continue;
-        const int32_t* table = p.table + (int64_t)it.b * p.max_pages;
-        bool ok = true;
-        for (int t = 0; t < it.ntiles && ok; ++t) {
-          for (int hf = 0; hf < 2; ++hf, ++r) {
-            const int s = r % NST;
-            if (r >= NST && !mbar_wait_abortable(&raw_empty[s], ((r / NST) - 1) & 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            const int tb = (it.tile0 + t) * T + hf * RT;
+      }
+      ++k;
+      if (done) break;
+    }
+    // The last CTA to finish fetching leaves the queue counters at zero for the next call.
+    if (lane == 0 && atomicAdd(&p.queue[1], 1u) == gridDim.x - 1) {
+      atomicExch(&p.queue[0], 0u);
+      atomicExch(&p.queue[1], 0u);
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // Page ids are fetched one tile ahead by the warp's lanes (lane i: page slot i).
+    const uint64_t policy = policy_evict_first();
+    int r = 0, k = 0;
+    while (true) {
+      bool done = false;
+      int32_t ids = kNoPage;
+      const Item it = next_item(k++, done, &ids);
+      if (done || *abort_flag) break;
+      if (it.kind != 0) continue;
+      bool ok = true;
+      int32_t ids_n1 = (1 < it.ntiles) ? tile_page<P>(p, it, 1, lane) : (int32_t)kNoPage;
+      for (int t = 0; t < it.ntiles && ok; ++t) {
+        const int32_t ids_n2 = (t + 2 < it.ntiles) ? tile_page<P>(p, it, t + 2, lane) : (int32_t)kNoPage;
+        for (int hf = 0; hf < 2; ++hf, ++r) {
+          const int s = r % NST;
+          if (r >= NST && !mbar_wait_abortable(&raw_empty[s], ((r / NST) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          int32_t pid[RT / P];
+#pragma unroll
+          for (int ps = 0; ps < RT / P; ++ps) pid[ps] = __shfl_sync(0xffffffffu, ids, hf * (RT / P) + ps);
+          if (lane == 0) {
             uint32_t okm = 0, bytes = 0;
-            int32_t pid[RT / P];
 #pragma unroll
             for (int ps = 0; ps < RT / P; ++ps) {
-              const int t0 = tb + ps * P;
-              pid[ps] = -1;
-              if (t0 + P <= it.start || t0 >= it.end) continue;  // page wholly outside the split
-              pid[ps] = table[t0 / P];
-            }
-#pragma unroll
-            for (int ps = 0; ps < RT / P; ++ps) {
-              const int t0 = tb + ps * P;
-              if (t0 + P <= it.start || t0 >= it.end) continue;
+              if (pid[ps] == kNoPage) continue;
               if (pid[ps] < 0 || pid[ps] >= p.num_pages) {
                 set_err(p.err, CAI_DEVERR_PAGE);
                 continue;
@@ -227,18 +317,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 #pragma unroll
             for (int ps = 0; ps < RT / P; ++ps) {
               if (!(okm & (1u << ps))) continue;
-              bulk_g2s_hint(raw + s * kRawStageBytes + ps * page_bytes(P), p.pages + (int64_t)pid[ps] * page_bytes(P),
-                            page_bytes(P), &raw_full[s], policy);
+              bulk_g2s_hint(raw + s * kRawStageBytes + ps * page_bytes(P),
+                            p.pages + (int64_t)pid[ps] * page_bytes(P), page_bytes(P), &raw_full[s], policy);
             }
           }
+          __syncwarp();
         }
-        if (!ok) break;
+        ids = ids_n1;
+        ids_n1 = ids_n2;
       }
-      // The last CTA to finish fetching leaves the queue counters at zero for the next call.
-      if (atomicAdd(&p.queue[1], 1u) == gridDim.x - 1) {
-        atomicExch(&p.queue[0], 0u);
-        atomicExch(&p.queue[1], 0u);
-      }
+      if (!ok) break;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -266,9 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       __syncwarp();
     };
     while (true) {
-      const int idx = next_item(k++, true);
-      if (idx < 0) break;
-      const Item it = make_item<P>(p, idx);
+      bool done = false;
+      const Item it = next_item(k++, done);
+      if (done) break;
       if (it.kind != 0) continue;
       bool ok = true;
       for (int t = 0; t < it.ntiles; ++t, ++g) {
@@ -297,20 +385,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       ++item_n;
     }
     if (have_prev && !*abort_flag) issue_pv(g - 1);
-  } else if (warp < 6) {
+   }
+  } else if (warp < kSoftWarp0) {
+    setmaxnreg_dec<kRegsConv>();
     // ------------------------------------------------------------ converters
-    const int ctid = tid - 64;        // 0..127
-    const int quarter = warp & 3;     // TMEM lanes this warp may touch
+    const int ctid = tid - kConvWarp0 * 32;  // 0 .. 32*kConvWarps-1
+    const int quarter = warp & 3;            // TMEM lanes this warp may touch
+    const bool q_warp = warp < kConvWarp0 + 4;  // one warp per lane quarter stores the query
+    constexpr int kUnits = (T * 8) / (32 * kConvWarps);  // 16-byte units per thread per operand
     int g = 0, item_n = 0, k = 0;
     while (true) {
-      const int idx = next_item(k++, true);
-      if (idx < 0) break;
-      const Item it = make_item<P>(p, idx);
+      bool done = false;
+      const Item it = next_item(k++, done);
+      if (done) break;
       if (it.kind != 0) continue;
       // The item's query rows for this warp, bf16 -> fp16 (loaded now, stored with the first tile).
       const int qr = quarter * 16 + (lane & 15);
       uint32_t qw[32];
-      if (qr < Hq) {
+      if (q_warp && qr < Hq) {
         const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)it.b * Hq + qr) * kHeadDim + (lane >> 4) * 64);
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -332,28 +424,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
              mbar_wait_abortable(&raw_full[s1], ((2 * g + 1) / NST) & 1, abort_flag);
         if (ok && g >= 2) ok = mbar_wait_abortable(&s_full[c], ((g >> 1) - 1) & 1, abort_flag);  // K16[c] free
         if (!ok) break;
-        // K: 1024 16-byte units per tile, 8 per thread; lanes rotated across chunks (conflict-free).
-        uint8_t* kd = k16 + c * kOp16Bytes;
-#pragma unroll 4
-        for (int u8 = 0; u8 < 8; ++u8) {
-          const int unit = u8 * 16 + (ctid >> 3);
-          const int tt = (unit >> 3) * 8 + (ctid & 7);
-          const int ch = ((unit & 7) + (ctid & 7)) & 7;
-          const uint8_t* rs = raw + (tt < RT ? s0 : s1) * kRawStageBytes;
-          const int tr = tt & (RT - 1);
-          const uint4 w = *reinterpret_cast<const uint4*>(rs + (tr / P) * page_bytes(P) + (tr % P) * kHeadDim + ch * 16);
-          uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
-          i8x4_to_f16x4(w.x, a0, a1);
-          i8x4_to_f16x4(w.y, a2, a3);
-          i8x4_to_f16x4(w.z, a4, a5);
-          i8x4_to_f16x4(w.w, a6, a7);
-          *reinterpret_cast<uint4*>(kd + kmajor_off(tt, 2 * ch)) = make_uint4(a0, a1, a2, a3);
-          *reinterpret_cast<uint4*>(kd + kmajor_off(tt, 2 * ch + 1)) = make_uint4(a4, a5, a6, a7);
+        // K: 1024 16-byte units per tile; lanes rotated across chunks (conflict-free).  All loads first.
+        {
+          uint4 w[kUnits];
+          int tts[kUnits], chs[kUnits];
+#pragma unroll
+          for (int u = 0; u < kUnits; ++u) {
+            const int unit = u * (4 * kConvWarps) + (ctid >> 3);
+            const int tt = (unit >> 3) * 8 + (ctid & 7);
+            const int ch = ((unit & 7) + (ctid & 7)) & 7;
+            const int tr = tt & (RT - 1);
+            tts[u] = tt;
+            chs[u] = ch;
+            w[u] = *reinterpret_cast<const uint4*>(raw + (tt < RT ? s0 : s1) * kRawStageBytes + (tr / P) * page_bytes(P) +
+                                                   (tr % P) * kHeadDim + ch * 16);
+          }
+          uint8_t* kd = k16 + c * kOp16Bytes;
+#pragma unroll
+          for (int u = 0; u < kUnits; ++u) {
+            uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
+            i8x4_to_f16x4(w[u].x, a0, a1);
+            i8x4_to_f16x4(w[u].y, a2, a3);
+            i8x4_to_f16x4(w[u].z, a4, a5);
+            i8x4_to_f16x4(w[u].w, a6, a7);
+            *reinterpret_cast<uint4*>(kd + kmajor_off(tts[u], 2 * chs[u])) = make_uint4(a0, a1, a2, a3);
+            *reinterpret_cast<uint4*>(kd + kmajor_off(tts[u], 2 * chs[u] + 1)) = make_uint4(a4, a5, a6, a7);
+          }
         }
         // Scales and mask of tile g into slot c: softmax of tile g-2 must be done with the slot.
         if (g >= 2) ok = mbar_wait_abortable(&p_full[c], ((g >> 1) - 1) & 1, abort_flag);
         if (!ok) break;
-        {
+        if (ctid < T) {
           const int tt = ctid;
           const int s = tt < RT ? s0 : s1;
           const int tr = tt & (RT - 1);
@@ -365,8 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           dst[tt] = valid ? sc[tr % P] * p.scale_log2 : 0.0f;
           dst[T + tt] = valid ? 0.0f : -INFINITY;
           dst[2 * T + tt] = valid ? sc[P + tr % P] : 0.0f;
+          if (tt == 0) {
+            const int tb = (it.tile0 + t) * T;
+            const uint32_t all = (1u << (RT / P)) - 1u;
+            tile_full[c] = tb >= it.start && tb + T <= it.end && page_ok[s0] == all && page_ok[s1] == all;
+          }
         }
-        if (t == 0) {
+        if (t == 0 && q_warp) {
           // Q[item_n & 1] was last read by the S of an item at least two tiles back: done (K16 wait above).
           tmem_st_16x32bx2_x32<32>(tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + (item_n & 1) * 64, qw);
           tmem_wait_st();
@@ -378,23 +484,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         // V: buffer c is free once PV of tile g-2 is done.
         if (g >= 2) ok = mbar_wait_abortable(&v_free[c], ((g >> 1) - 1) & 1, abort_flag);
         if (!ok) break;
-        uint8_t* vd = v16 + c * kOp16Bytes;
-#pragma unroll 4
-        for (int u8 = 0; u8 < 8; ++u8) {
-          const int unit = u8 * 16 + (ctid >> 3);
-          const int tt = (unit >> 3) * 8 + (ctid & 7);
-          const int ch = ((unit & 7) + (ctid & 7)) & 7;
-          const uint8_t* rs = raw + (tt < RT ? s0 : s1) * kRawStageBytes;
-          const int tr = tt & (RT - 1);
-          const uint4 w = *reinterpret_cast<const uint4*>(rs + (tr / P) * page_bytes(P) + P * kHeadDim +
-                                                          (tr % P) * kHeadDim + ch * 16);
-          uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
-          i8x4_to_f16x4(w.x, a0, a1);
-          i8x4_to_f16x4(w.y, a2, a3);
-          i8x4_to_f16x4(w.z, a4, a5);
-          i8x4_to_f16x4(w.w, a6, a7);
-          *reinterpret_cast<uint4*>(vd + mnmajor_off(tt, 2 * ch)) = make_uint4(a0, a1, a2, a3);
-          *reinterpret_cast<uint4*>(vd + mnmajor_off(tt, 2 * ch + 1)) = make_uint4(a4, a5, a6, a7);
+        {
+          uint4 w[kUnits];
+          int tts[kUnits], chs[kUnits];
+#pragma unroll
+          for (int u = 0; u < kUnits; ++u) {
+            const int unit = u * (4 * kConvWarps) + (ctid >> 3);
+            const int tt = (unit >> 3) * 8 + (ctid & 7);
+            const int ch = ((unit & 7) + (ctid & 7)) & 7;
+            const int tr = tt & (RT - 1);
+            tts[u] = tt;
+            chs[u] = ch;
+            w[u] = *reinterpret_cast<const uint4*>(raw + (tt < RT ? s0 : s1) * kRawStageBytes + (tr / P) * page_bytes(P) +
+                                                   P * kHeadDim + (tr % P) * kHeadDim + ch * 16);
+          }
+          uint8_t* vd = v16 + c * kOp16Bytes;
+#pragma unroll
+          for (int u = 0; u < kUnits; ++u) {
+            uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
+            i8x4_to_f16x4(w[u].x, a0, a1);
+            i8x4_to_f16x4(w[u].y, a2, a3);
+            i8x4_to_f16x4(w[u].z, a4, a5);
+            i8x4_to_f16x4(w[u].w, a6, a7);
+            *reinterpret_cast<uint4*>(vd + mnmajor_off(tts[u], 2 * chs[u])) = make_uint4(a0, a1, a2, a3);
+            *reinterpret_cast<uint4*>(vd + mnmajor_off(tts[u], 2 * chs[u] + 1)) = make_uint4(a4, a5, a6, a7);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -408,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       ++item_n;
     }
   } else {
+    setmaxnreg_inc<kRegsSoft>();
     // ------------------------------------------------------------ softmax + epilogue
     const int quarter = warp & 3;
     const int h = quarter * 16 + (lane & 15);  // head row
@@ -416,12 +531,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     const bool warp_live = quarter * 16 < Hq;  // padded rows only: skip the arithmetic
     int g = 0, item_n = 0, k = 0;
     while (true) {
-      const int idx = next_item(k++, true);
-      if (idx < 0) break;
-      const Item it = make_item<P>(p, idx);
+      bool done = false;
+      const Item it = next_item(k++, done);
+      if (done) break;
       if (it.kind == 1) {
         // Nothing to attend (L = 0) or an invalid length: out = 0, lse = -inf.
-        if (it.invalid && tid == 192) set_err(p.err, CAI_DEVERR_LENGTH);
+        if (it.invalid && tid == kSoftWarp0 * 32) set_err(p.err, CAI_DEVERR_LENGTH);
         if (h < Hq) {
           float* dst = p.out + ((int64_t)it.b * Hq + h) * kHeadDim + th * 64;
           for (int d = 0; d < 64; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -429,7 +544,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         }
         continue;
       }
-      if (it.kind != 0) continue;
       float m_ref = -INFINITY, l_sum = 0.0f;
       bool ok = true;
       for (int t = 0; t < it.ntiles; ++t, ++g) {
@@ -446,19 +560,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           const float* ksc = scal + c * 3 * T + th * 64;
           const float* kbias = ksc + T;
           const float* vsc = ksc + 2 * T;
-          float mx = -INFINITY;
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (tile_full[c]) {
 #pragma unroll
-          for (int j = 0; j < 64; j += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(ksc + j);
-            const float4 bb = *reinterpret_cast<const float4*>(kbias + j);
-            const float z0 = fmaf(__uint_as_float(sr[j]), a.x, bb.x), z1 = fmaf(__uint_as_float(sr[j + 1]), a.y, bb.y);
-            const float z2 = fmaf(__uint_as_float(sr[j + 2]), a.z, bb.z), z3 = fmaf(__uint_as_float(sr[j + 3]), a.w, bb.w);
-            sr[j] = __float_as_uint(z0);
-            sr[j + 1] = __float_as_uint(z1);
-            sr[j + 2] = __float_as_uint(z2);
-            sr[j + 3] = __float_as_uint(z3);
-            mx = fmaxf(mx, fmaxf(fmaxf(z0, z1), fmaxf(z2, z3)));
+            for (int j = 0; j < 64; j += 4) {
+              const float4 a = *reinterpret_cast<const float4*>(ksc + j);
+              const float z0 = __uint_as_float(sr[j]) * a.x, z1 = __uint_as_float(sr[j + 1]) * a.y;
+              const float z2 = __uint_as_float(sr[j + 2]) * a.z, z3 = __uint_as_float(sr[j + 3]) * a.w;
+              sr[j] = __float_as_uint(z0);
+              sr[j + 1] = __float_as_uint(z1);
+              sr[j + 2] = __float_as_uint(z2);
+              sr[j + 3] = __float_as_uint(z3);
+              mx4[0] = fmaxf(mx4[0], z0);
+              mx4[1] = fmaxf(mx4[1], z1);
+              mx4[2] = fmaxf(mx4[2], z2);
+              mx4[3] = fmaxf(mx4[3], z3);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+              const float4 a = *reinterpret_cast<const float4*>(ksc + j);
+              const float4 bb = *reinterpret_cast<const float4*>(kbias + j);
+              const float z0 = fmaf(__uint_as_float(sr[j]), a.x, bb.x), z1 = fmaf(__uint_as_float(sr[j + 1]), a.y, bb.y);
+              const float z2 = fmaf(__uint_as_float(sr[j + 2]), a.z, bb.z), z3 = fmaf(__uint_as_float(sr[j + 3]), a.w, bb.w);
+              sr[j] = __float_as_uint(z0);
+              sr[j + 1] = __float_as_uint(z1);
+              sr[j + 2] = __float_as_uint(z2);
+              sr[j + 3] = __float_as_uint(z3);
+              mx4[0] = fmaxf(mx4[0], z0);
+              mx4[1] = fmaxf(mx4[1], z1);
+              mx4[2] = fmaxf(mx4[2], z2);
+              mx4[3] = fmaxf(mx4[3], z3);
+            }
           }
+          float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
           const bool raise = mx > m_ref + kRescaleThreshold;
           const float alpha = raise ? ex2_approx(m_ref - mx) : 1.0f;
@@ -482,6 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           }
           const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
           uint32_t pw[32];
+          float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int j = 0; j < 64; j += 4) {
             const float4 vs = *reinterpret_cast<const float4*>(vsc + j);
@@ -489,10 +625,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
             const float e1 = ex2_approx(__uint_as_float(sr[j + 1]) - m_use);
             const float e2 = ex2_approx(__uint_as_float(sr[j + 2]) - m_use);
             const float e3 = ex2_approx(__uint_as_float(sr[j + 3]) - m_use);
-            l_sum += (e0 + e1) + (e2 + e3);
+            l4[0] += e0;
+            l4[1] += e1;
+            l4[2] += e2;
+            l4[3] += e3;
             pw[j / 2] = pack_f16x2(e0 * vs.x, e1 * vs.y);
             pw[j / 2 + 1] = pack_f16x2(e2 * vs.z, e3 * vs.w);
           }
+          l_sum += (l4[0] + l4[1]) + (l4[2] + l4[3]);
           tmem_st_16x32bx2_x32<32>(tmem + t_lane + scol, pw);
           tmem_wait_st();
         }

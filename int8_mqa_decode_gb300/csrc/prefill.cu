@@ -33,18 +33,20 @@
 namespace cai {
 namespace {
 
-constexpr int kRows = 128;                 // query rows per CTA (MMA M)
+constexpr int kRows = 128;                 // query rows per q-tile (MMA M)
+constexpr int kQT = 2;                     // q-tiles per CTA sharing each K/V tile
 constexpr int kKeys = 128;                 // keys per tile (MMA N of S, K of PV)
 constexpr int kTileBytes = kKeys * kHeadDim * 2;  // 32 KB of 16-bit values
 constexpr int kStages = 2;
-constexpr int kOffQ = 0;
-constexpr int kOffStage = kOffQ + kRows * kHeadDim * 2;
+constexpr int kOffQ = 0;                                     // Q[kQT]
+constexpr int kOffStage = kOffQ + kQT * kRows * kHeadDim * 2;
 constexpr int kStageBytes = 2 * kTileBytes + 2 * kKeys * 4;  // K, V, K scales, V scales
-constexpr int kOffBars = kOffStage + kStages * kStageBytes;  // full[2], s_bar, pv_bar
-constexpr int kOffMisc = kOffBars + 8 * (kStages + 2);
+constexpr int kOffBars = kOffStage + kStages * kStageBytes;
+constexpr int kNumBars = 2 * kStages + 6 * kQT;
+constexpr int kOffMisc = kOffBars + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
+constexpr int kThreads = 320;              // producer, MMA, 2 x 4 softmax warps
+constexpr uint32_t kTmemCols = 512;        // per q-tile: S (128 columns, P over its first 64) + O (128)
 constexpr float kRescaleThreshold = 8.0f;
 
 struct PrefillParams {
@@ -53,12 +55,12 @@ struct PrefillParams {
   const int32_t* table;
   const int32_t* prefix_len;
   const uint16_t* q;  // bf16 [B][n_new][Hq][128]
-  int32_t batch, n_new, num_heads, log2_heads, window, kt_rows;
+  int32_t batch, n_new, num_heads, log2_heads, window, kt_rows, pairs;
   float scale_log2;
   uint16_t* kb;  // scratch bf16 [B][KT][128]
   uint16_t* vh;  // scratch fp16 [B][KT][128]
-  float* ks;     // scratch [B][KT]
-  float* vs;     // scratch [B][KT]
+  float* ks;     // scratch [B][KT]: K scale * softmax scale * log2(e)
+  float* vs;     // scratch [B][KT]: V scale
   float* out;
   float* lse_out;
   int32_t* err;
@@ -98,7 +100,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const PrefillParams p) {
       kw = reinterpret_cast<const uint32_t*>(pg + slot * kHeadDim)[lane];
       vw = reinterpret_cast<const uint32_t*>(pg + P * kHeadDim + slot * kHeadDim)[lane];
       const float* sc = reinterpret_cast<const float*>(pg + 2 * P * kHeadDim);
-      ksc = sc[slot];
+      ksc = sc[slot] * p.scale_log2;
       vsc = sc[P + slot];
     } else if (lane == 0 && p.err) {
       atomicOr(p.err, CAI_DEVERR_PAGE);
@@ -131,203 +133,325 @@ __device__ __forceinline__ void tma_load_rows128(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// One work item: a pair of q-tiles (256 consecutive (token, head) rows) of one sequence.
+struct PItem {
+  int b, row0, kt0, nkt;
+  bool ok;
+};
+
+__device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
+  PItem it;
+  it.b = idx / p.pairs;
+  it.row0 = (idx - it.b * p.pairs) * (kQT * kRows);
+  const int32_t p0 = p.prefix_len[it.b];
+  it.ok = seq_ok(p, p0);
+  if (!it.ok) {
+    it.kt0 = it.nkt = 0;
+    return it;
+  }
+  const int i0 = it.row0 >> p.log2_heads;
+  const int i_last = min((it.row0 + kQT * kRows - 1) >> p.log2_heads, p.n_new - 1);
+  const int kv_hi = p0 + i_last + 1;
+  const int kv_lo = p.window > 0 ? max(0, p0 + i0 + 1 - p.window) : 0;
+  it.kt0 = kv_lo / kKeys;
+  it.nkt = (kv_hi - 1) / kKeys - it.kt0 + 1;
+  return it;
+}
+
 // Operand tiles in shared memory: element (r, k) of a 128x128 16-bit tile at
 // (k/8)*2048 + r*16 + (k%8)*2 -- the order a [16 chunks][128 rows][8] TMA box
 // writes.  As a K-major operand: LBO = 2048 (next 8 k), SBO = 128 (next 8 rows).
 // As an MN-major operand (rows = K, k = N): LBO = 128, SBO = 2048.
-__global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillParams p,
-                                                         const __grid_constant__ CUtensorMap kmap,
-                                                         const __grid_constant__ CUtensorMap vmap) {
+//
+// Persistent CTAs, one per SM, each taking pairs of q-tiles in turn.  Roles:
+// warp 0 loads K/V tiles (TMA tensor copies) into a 2-stage ring; warp 1
+// issues the MMAs in the order S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) ...
+// so that each softmax group works on one tile while the tensor core runs the
+// other group's MMAs; warps 2-5 and 6-9 run the softmax of q-tile 0 and 1 (one
+// thread per row) and write the outputs.
+__global__ void __maxnreg__(200) prefill_kernel(const PrefillParams p,
+                                                              const __grid_constant__ CUtensorMap kmap,
+                                                              const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* qs = smem + kOffQ;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* s_bar = full + kStages;
-  uint64_t* pv_bar = full + kStages + 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* kv_full = bars;                    // [kStages] producer -> MMA, softmax (tx bytes)
+  uint64_t* kv_empty = bars + kStages;         // [kStages] MMA commit after both PVs of the tile
+  uint64_t* q_full = bars + 2 * kStages;       // [kQT] softmax group -> MMA (4 warps)
+  uint64_t* s_full = q_full + kQT;             // [kQT] MMA commit after S
+  uint64_t* p_full = s_full + kQT;             // [kQT] softmax -> MMA (4 warps)
+  uint64_t* pv_done = p_full + kQT;            // [kQT] MMA commit after PV
+  uint64_t* o_full = pv_done + kQT;            // [kQT] MMA commit after an item's last PV
+  uint64_t* o_empty = o_full + kQT;            // [kQT] softmax -> MMA after reading O (4 warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  int32_t* timeout = reinterpret_cast<int32_t*>(tmem_slot + 1);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kOffMisc + 4);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int b = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_heads;
-  const int row0 = blockIdx.x * kRows;  // first (token, head) row of this CTA within the sequence
-  const int i0 = row0 >> p.log2_heads;
-  const int32_t p0 = p.prefix_len[b];
-  const int my_i = (row0 + tid) >> p.log2_heads;
-  const int my_h = (row0 + tid) & (Hq - 1);
-  const bool my_row = my_i < p.n_new;
-  float* out_row = p.out + (((int64_t)b * p.n_new + my_i) * Hq + my_h) * kHeadDim;
-
-  if (!seq_ok(p, p0)) {  // flagged by the dequant pass; outputs defined as 0 / -inf
-    if (my_row) {
-      for (int d = 0; d < kHeadDim; d += 4) *reinterpret_cast<float4*>(out_row + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (p.lse_out) p.lse_out[((int64_t)b * p.n_new + my_i) * Hq + my_h] = -INFINITY;
-    }
-    return;
-  }
-  const int i_last = min(i0 + (kRows >> p.log2_heads), p.n_new) - 1;
-  const int kv_hi = p0 + i_last + 1;
-  const int kv_lo = p.window > 0 ? max(0, p0 + i0 + 1 - p.window) : 0;
-  const int kt0 = kv_lo / kKeys;
-  const int nkt = (kv_hi - 1) / kKeys - kt0 + 1;
-  const int64_t seq_row0 = (int64_t)b * p.kt_rows;
-
-  const int q_pos = p0 + my_i;
-  const int k_lo = p.window > 0 ? max(0, q_pos + 1 - p.window) : 0;
+  const int num_items = p.batch * p.pairs;
+  const int64_t total_rows = (int64_t)p.n_new * Hq;
 
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
-    mbar_init(s_bar, 1);
-    mbar_init(pv_bar, 1);
-    *timeout = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int q = 0; q < kQT; ++q) {
+      mbar_init(&q_full[q], 4);
+      mbar_init(&s_full[q], 1);
+      mbar_init(&p_full[q], 4);
+      mbar_init(&pv_done[q], 1);
+      mbar_init(&o_full[q], 1);
+      mbar_init(&o_empty[q], 4);
+    }
+    *abort_flag = 0;
     fence_barrier_init();
   }
-  // Q tile (bf16), rows beyond the chunk zero.
-  {
-    const uint16_t* qb = p.q + ((int64_t)b * p.n_new * Hq + row0) * kHeadDim;
-    const int rows_here = min(kRows, p.n_new * Hq - row0);
-    for (int u = tid; u < kRows * 16; u += blockDim.x) {
-      const int r = u >> 4, c = u & 15;
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if (r < rows_here) w = *reinterpret_cast<const uint4*>(qb + (int64_t)r * kHeadDim + c * 8);
-      *reinterpret_cast<uint4*>(qs + c * 2048 + r * 16) = w;
-    }
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
 
-  auto issue = [&](int j) {
-    const int stage = j % kStages;
-    uint8_t* st = smem + kOffStage + stage * kStageBytes;
-    const int kt = kt0 + j;
-    mbar_arrive_expect_tx(&full[stage], kStageBytes);
-    tma_load_rows128(st, &kmap, (int)(seq_row0 + (int64_t)kt * kKeys), &full[stage]);
-    tma_load_rows128(st + kTileBytes, &vmap, (int)(seq_row0 + (int64_t)kt * kKeys), &full[stage]);
-    bulk_g2s(st + 2 * kTileBytes, p.ks + seq_row0 + (int64_t)kt * kKeys, kKeys * 4, &full[stage]);
-    bulk_g2s(st + 2 * kTileBytes + kKeys * 4, p.vs + seq_row0 + (int64_t)kt * kKeys, kKeys * 4, &full[stage]);
-  };
-  if (tid == 0) {
-    issue(0);
-    if (nkt > 1) issue(1);
-  }
-
-  float m_ref = -INFINITY, l_sum = 0.0f;
-  bool ok_all = true;
-  for (int j = 0; j < nkt; ++j) {
-    const int stage = j % kStages;
-    uint8_t* st = smem + kOffStage + stage * kStageBytes;
-    const float* kscale = reinterpret_cast<const float*>(st + 2 * kTileBytes);
-    const float* vscale = kscale + kKeys;
-    if (!mbar_wait(&full[stage], (j / kStages) & 1)) ok_all = false;
-    if (tid == 0) {
-      tc_fence_after();
-      constexpr uint32_t idesc = idesc_bf16_f32(kRows, kKeys, 0, 0);
-      const uint32_t qa = smem_addr(qs), ka = smem_addr(st);
-#pragma unroll
-      for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        mma_f16_ss(tmem + kColS, smem_desc(qa + ks * 4096, 2048, 128), smem_desc(ka + ks * 4096, 2048, 128), idesc,
-                   ks > 0);
-      mma_commit(s_bar);
-    }
-    if (!mbar_wait(s_bar, j & 1)) ok_all = false;
-    if (j > 0 && !mbar_wait(pv_bar, (j - 1) & 1)) ok_all = false;
-    tc_fence_after();
-    if (tid == 0 && j > 0 && j + 1 < nkt) issue(j + 1);  // into the stage tile j-1 used
-
-    // ---- softmax of this thread's row over the 128 keys of the tile
-    const int key0 = (kt0 + j) * kKeys;
-    float z[kKeys];
-#pragma unroll
-    for (int c = 0; c < kKeys; c += 32) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(tmem + t_lane + kColS + c, r);
-      tmem_wait_ld();
-#pragma unroll
-      for (int e = 0; e < 32; ++e) z[c + e] = __uint_as_float(r[e]) * (kscale[c + e] * p.scale_log2);
-    }
-    const bool full_tile = key0 >= k_lo && key0 + kKeys - 1 <= q_pos;
-    if (!full_tile) {
-#pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        const int key = key0 + c;
-        if (key < k_lo || key > q_pos) z[c] = -INFINITY;
+  if (warp == 0) {
+    // ------------------------------------------------------------ K/V producer
+    if (lane == 0) {
+      int g = 0;
+      for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
+        const PItem it = prefill_item(p, idx);
+        const int64_t seq_row0 = (int64_t)it.b * p.kt_rows;
+        for (int j = 0; j < it.nkt; ++j, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages && !mbar_wait_abortable(&kv_empty[s], ((g / kStages) - 1) & 1, abort_flag)) break;
+          uint8_t* st = smem + kOffStage + s * kStageBytes;
+          const int64_t row = seq_row0 + (int64_t)(it.kt0 + j) * kKeys;
+          mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
+          tma_load_rows128(st, &kmap, (int)row, &kv_full[s]);
+          tma_load_rows128(st + kTileBytes, &vmap, (int)row, &kv_full[s]);
+          bulk_g2s(st + 2 * kTileBytes, p.ks + row, kKeys * 4, &kv_full[s]);
+          bulk_g2s(st + 2 * kTileBytes + kKeys * 4, p.vs + row, kKeys * 4, &kv_full[s]);
+        }
       }
     }
-    float mx = -INFINITY;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0, 0);
+      constexpr uint32_t idesc_o = idesc_f16_f32(kRows, kHeadDim, 0, 1);
+      const uint32_t qa0 = smem_addr(smem + kOffQ);
+      int g = 0, n = 0;
+      auto issue_s = [&](int q, int gg) {
+        const uint32_t ka = smem_addr(smem + kOffStage + (gg % kStages) * kStageBytes);
+        const uint32_t qa = qa0 + q * kRows * kHeadDim * 2;
 #pragma unroll
-    for (int c = 0; c < kKeys; ++c) mx = fmaxf(mx, z[c]);
-    const bool raise = mx > m_ref + kRescaleThreshold;
-    const float alpha = raise ? ex2_approx(m_ref - mx) : 1.0f;
-    if (j > 0 && __any_sync(0xffffffffu, raise)) {
+        for (int ks = 0; ks < kHeadDim / 16; ++ks)
+          mma_f16_ss(tmem + q * 256, smem_desc(qa + ks * 4096, 2048, 128), smem_desc(ka + ks * 4096, 2048, 128),
+                     idesc_s, ks > 0);
+        mma_commit(&s_full[q]);
+      };
+      auto issue_pv = [&](int q, int gg, bool first) {
+        const uint32_t va = smem_addr(smem + kOffStage + (gg % kStages) * kStageBytes + kTileBytes);
+#pragma unroll
+        for (int ks = 0; ks < kKeys / 16; ++ks)
+          mma_f16_ts(tmem + q * 256 + 128, tmem + q * 256 + ks * 8, smem_desc(va + ks * 256, 128, 2048), idesc_o,
+                     (!first || ks > 0) ? 1u : 0u);
+        mma_commit(&pv_done[q]);
+      };
+      for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
+        const PItem it = prefill_item(p, idx);
+        if (!it.ok) continue;  // no MMA work; the softmax groups write its zeros
+        bool ok = mbar_wait_abortable(&q_full[0], n & 1, abort_flag) && mbar_wait_abortable(&q_full[1], n & 1, abort_flag);
+        for (int j = 0; j < it.nkt && ok; ++j, ++g) {
+          const int s = g % kStages;
+          if (j == 0) {
+            if (!mbar_wait_abortable(&kv_full[s], (g / kStages) & 1, abort_flag)) break;
+            tc_fence_after();
+            issue_s(0, g);
+            issue_s(1, g);
+          }
+          const bool more = j + 1 < it.nkt;
+          for (int q = 0; q < kQT; ++q) {
+            if (!mbar_wait_abortable(&p_full[q], g & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (j == 0 && n > 0 && !mbar_wait_abortable(&o_empty[q], (n - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(q, g, j == 0);
+            if (q == kQT - 1) mma_commit(&kv_empty[s]);
+            if (!more) mma_commit(&o_full[q]);
+            if (more) {
+              if (q == 0 && !mbar_wait_abortable(&kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(q, g + 1);
+            }
+          }
+        }
+        if (!ok) break;
+        ++n;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax groups
+    const int q = (warp - 2) >> 2;          // q-tile of this group
+    const int quarter = warp & 3;           // TMEM lane quarter
+    const int r = quarter * 32 + lane;      // row within the q-tile
+    const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
+    const uint32_t scol = (uint32_t)q * 256, ocol = scol + 128;
+    uint8_t* qs = smem + kOffQ + q * kRows * kHeadDim * 2;
+    int g = 0, n = 0;
+    for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
+      const PItem it = prefill_item(p, idx);
+      const int64_t row = it.row0 + q * kRows + r;  // (token, head) row within the sequence
+      const bool my_row = row < total_rows;
+      const int my_i = (int)(row >> p.log2_heads), my_h = (int)(row & (Hq - 1));
+      float* out_row = p.out + (((int64_t)it.b * p.n_new + my_i) * Hq + my_h) * kHeadDim;
+      if (!it.ok) {  // flagged by the dequant pass; outputs defined as 0 / -inf
+        if (my_row) {
+          for (int d = 0; d < kHeadDim; d += 4)
+            *reinterpret_cast<float4*>(out_row + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (p.lse_out) p.lse_out[((int64_t)it.b * p.n_new + my_i) * Hq + my_h] = -INFINITY;
+        }
+        continue;  // no MMA work for this item
+      }
+      // This row's query (bf16), zero beyond the chunk.
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)it.b * total_rows + row) * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          *reinterpret_cast<uint4*>(qs + c * 2048 + r * 16) = my_row ? src[c] : make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[q]);
+      const int32_t p0 = p.prefix_len[it.b];
+      const int q_pos = p0 + my_i;
+      const int k_lo = p.window > 0 ? max(0, q_pos + 1 - p.window) : 0;
+      float m_ref = -INFINITY, l_sum = 0.0f;
+      bool ok = true;
+      for (int j = 0; j < it.nkt; ++j, ++g) {
+        const int s = g % kStages;
+        ok = mbar_wait_abortable(&s_full[q], g & 1, abort_flag) &&
+             mbar_wait_abortable(&kv_full[s], (g / kStages) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const float* kscale = reinterpret_cast<const float*>(smem + kOffStage + s * kStageBytes + 2 * kTileBytes);
+        const float* vscale = kscale + kKeys;
+        const int key0 = (it.kt0 + j) * kKeys;
+        float z[kKeys];
+#pragma unroll
+        for (int c = 0; c < kKeys; c += 32) {
+          uint32_t rr[32];
+          tmem_ld_32x32b_x32(tmem + t_lane + scol + c, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(kscale + c + e);
+            z[c + e] = __uint_as_float(rr[e]) * a.x;
+            z[c + e + 1] = __uint_as_float(rr[e + 1]) * a.y;
+            z[c + e + 2] = __uint_as_float(rr[e + 2]) * a.z;
+            z[c + e + 3] = __uint_as_float(rr[e + 3]) * a.w;
+          }
+        }
+        if (!(key0 >= k_lo && key0 + kKeys - 1 <= q_pos)) {
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) {
+            const int key = key0 + c;
+            if (key < k_lo || key > q_pos) z[c] = -INFINITY;
+          }
+        }
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kKeys; c += 4) {
+          mx4[0] = fmaxf(mx4[0], z[c]);
+          mx4[1] = fmaxf(mx4[1], z[c + 1]);
+          mx4[2] = fmaxf(mx4[2], z[c + 2]);
+          mx4[3] = fmaxf(mx4[3], z[c + 3]);
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const bool raise = mx > m_ref + kRescaleThreshold;
+        const float alpha = raise ? ex2_approx(m_ref - mx) : 1.0f;
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+          ok = mbar_wait_abortable(&pv_done[q], (g - 1) & 1, abort_flag);
+          if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < kHeadDim; c += 32) {
+              uint32_t o[32];
+              tmem_ld_32x32b_x32(tmem + t_lane + ocol + c, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st_32x32b_x32(tmem + t_lane + ocol + c, o);
+            }
+            tmem_wait_st();
+          }
+        }
+        if (raise) {
+          l_sum *= alpha;
+          m_ref = mx;
+        }
+        const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < kKeys; c += 64) {
+          uint32_t pw[32];
+#pragma unroll
+          for (int e = 0; e < 64; e += 4) {
+            const float4 vs = *reinterpret_cast<const float4*>(vscale + c + e);
+            const float e0 = ex2_approx(z[c + e] - m_use), e1 = ex2_approx(z[c + e + 1] - m_use);
+            const float e2 = ex2_approx(z[c + e + 2] - m_use), e3 = ex2_approx(z[c + e + 3] - m_use);
+            l4[0] += e0;
+            l4[1] += e1;
+            l4[2] += e2;
+            l4[3] += e3;
+            pw[e / 2] = pack_f16x2(e0 * vs.x, e1 * vs.y);
+            pw[e / 2 + 1] = pack_f16x2(e2 * vs.z, e3 * vs.w);
+          }
+          tmem_st_32x32b_x32(tmem + t_lane + scol + c / 2, pw);
+        }
+        l_sum += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[q]);
+        if (!ok) break;
+      }
+      if (!ok) break;
+      if (!mbar_wait_abortable(&o_full[q], n & 1, abort_flag)) break;
+      tc_fence_after();
+      const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
 #pragma unroll
       for (int c = 0; c < kHeadDim; c += 32) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(tmem + t_lane + kColO + c, o);
+        tmem_ld_32x32b_x32(tmem + t_lane + ocol + c, o);
         tmem_wait_ld();
+        if (my_row) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-        tmem_st_32x32b_x32(tmem + t_lane + kColO + c, o);
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(out_row + c + e) =
+                make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                            __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+        }
       }
-      tmem_wait_st();
-    }
-    if (raise) {
-      l_sum *= alpha;
-      m_ref = mx;
-    }
-    const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
-#pragma unroll
-    for (int c = 0; c < kKeys; c += 64) {
-      uint32_t pw[32];
-#pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        const float a = ex2_approx(z[c + e] - m_use), bb = ex2_approx(z[c + e + 1] - m_use);
-        l_sum += a + bb;
-        pw[e / 2] = pack_f16x2(a * vscale[c + e], bb * vscale[c + e + 1]);
-      }
-      tmem_st_32x32b_x32(tmem + t_lane + kColP + c / 2, pw);
-    }
-    tmem_wait_st();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      constexpr uint32_t idesc = idesc_f16_f32(kRows, kHeadDim, 0, 1);
-      const uint32_t va = smem_addr(st + kTileBytes);
-#pragma unroll
-      for (int ks = 0; ks < kKeys / 16; ++ks)
-        mma_f16_ts(tmem + kColO, tmem + kColP + ks * 8, smem_desc(va + ks * 256, 128, 2048), idesc,
-                   (j > 0 || ks > 0) ? 1u : 0u);
-      mma_commit(pv_bar);
+      if (my_row && p.lse_out)
+        p.lse_out[((int64_t)it.b * p.n_new + my_i) * Hq + my_h] =
+            l_sum > 0.0f ? (m_ref + __log2f(l_sum)) * kLn2 : -INFINITY;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_empty[q]);
+      ++n;
     }
   }
-  if (!mbar_wait(pv_bar, (nkt - 1) & 1)) ok_all = false;
-  tc_fence_after();
-  if (!ok_all) atomicOr(timeout, 1);
-
-  const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
-#pragma unroll
-  for (int c = 0; c < kHeadDim; c += 32) {
-    uint32_t o[32];
-    tmem_ld_32x32b_x32(tmem + t_lane + kColO + c, o);
-    tmem_wait_ld();
-    if (my_row) {
-#pragma unroll
-      for (int e = 0; e < 32; e += 4)
-        *reinterpret_cast<float4*>(out_row + c + e) =
-            make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                        __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-    }
-  }
-  if (my_row && p.lse_out)
-    p.lse_out[((int64_t)b * p.n_new + my_i) * Hq + my_h] = l_sum > 0.0f ? (m_ref + __log2f(l_sum)) * kLn2 : -INFINITY;
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *timeout && p.err) atomicOr(p.err, CAI_DEVERR_TIMEOUT);
+  if (tid == 0 && *abort_flag && p.err) atomicOr(p.err, CAI_DEVERR_TIMEOUT);
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -383,6 +507,7 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.log2_heads = 31 - __builtin_clz((unsigned)L.num_heads);
   p.window = L.window;
   p.kt_rows = (int32_t)(((int64_t)L.max_pages * L.page_size + kKeys - 1) / kKeys * kKeys);
+  p.pairs = (int32_t)(((int64_t)L.n_new * L.num_heads + kQT * kRows - 1) / (kQT * kRows));
   p.scale_log2 = L.scale_log2;
   const int64_t rows = (int64_t)L.batch * p.kt_rows;
   const int64_t a = ((rows * kHeadDim * 2 + 255) / 256) * 256;
@@ -413,8 +538,9 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int qtiles = (L.n_new * L.num_heads + kRows - 1) / kRows;
-  prefill_kernel<<<dim3(qtiles, L.batch), 128, kSmemBytes, stream>>>(p, kmap, vmap);
+  const int64_t items = (int64_t)L.batch * p.pairs;
+  const int grid = (int)(items < num_sms() ? items : num_sms());
+  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, kmap, vmap);
   return cudaGetLastError();
 }
 
