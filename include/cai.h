@@ -220,6 +220,10 @@ cai_status cai_host_cache_store(cai_host_cache* cache, const int32_t* tokens, in
 void cai_host_cache_stats(cai_host_cache* cache, int64_t* hits, int64_t* misses, int64_t* pages_cached,
                           int64_t* evictions);
 
+/* The CUDA runtime's description of the error behind the last CAI_ERR_CUDA returned on
+ * this thread ("no error" if none). */
+const char* cai_last_cuda_error(void);
+
 /* Static description of a status code. */
 const char* cai_status_string(cai_status status);
 

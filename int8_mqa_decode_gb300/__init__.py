@@ -39,7 +39,8 @@ class CaiUnavailable(RuntimeError):
 
 class CaiError(RuntimeError):
     def __init__(self, status: int, where: str):
-        super().__init__(f"{where}: {cai_status_string(status)} (status {status})")
+        detail = f": {load().cai_last_cuda_error().decode()}" if status == CAI_ERR_CUDA else ""
+        super().__init__(f"{where}: {cai_status_string(status)} (status {status}){detail}")
         self.status = status
 
 
@@ -70,6 +71,8 @@ def load():
     lib.cai_page_bytes.restype = sz
     lib.cai_status_string.argtypes = [ctypes.c_int]
     lib.cai_status_string.restype = ctypes.c_char_p
+    lib.cai_last_cuda_error.argtypes = []
+    lib.cai_last_cuda_error.restype = ctypes.c_char_p
     lib.cai_kv_append.argtypes = [pool_p, vp, vp, i32, i32, vp, i32, vp, vp, vp]
     lib.cai_kv_append.restype = ctypes.c_int
     lib.cai_mqa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]

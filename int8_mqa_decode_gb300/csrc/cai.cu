@@ -59,7 +59,19 @@ static size_t workspace_bytes_for(int32_t batch, int32_t num_q_heads, const Deco
 
 using namespace cai;
 
+namespace {
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+cai_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return CAI_OK;
+  g_last_cuda_error = e;
+  return CAI_ERR_CUDA;
+}
+}  // namespace
+
 extern "C" {
+
+const char* cai_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 
 size_t cai_page_bytes(int32_t page_size, int32_t head_dim) {
   if (page_size <= 0 || head_dim <= 0) return 0;
@@ -107,7 +119,7 @@ cai_status cai_kv_append(const cai_kv_pool* pool, const float* k_new, const floa
   p.table = block_table;
   p.start_pos = start_pos;
   p.err = err_flag;
-  return launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CAI_OK : CAI_ERR_CUDA;
+  return cuda_status(launch_append(p, static_cast<cudaStream_t>(stream)));
 }
 
 size_t cai_mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_pages_per_seq,
@@ -170,8 +182,7 @@ cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int
     p.ws_lse = reinterpret_cast<float*>(base + (size_t)round_up((int64_t)(rows * kHeadDim * sizeof(float)), 256));
   }
   p.err = err_flag;
-  return launch_decode(p, pool->page_size, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CAI_OK
-                                                                                                : CAI_ERR_CUDA;
+  return cuda_status(launch_decode(p, pool->page_size, static_cast<cudaStream_t>(stream)));
 }
 
 size_t cai_mqa_prefill_workspace_size(int32_t batch, int32_t max_pages_per_seq, int32_t page_size) {
@@ -214,7 +225,7 @@ cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int
   L.out = out;
   L.lse_out = lse_out;
   L.err = err_flag;
-  return launch_prefill(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CAI_OK : CAI_ERR_CUDA;
+  return cuda_status(launch_prefill(L, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

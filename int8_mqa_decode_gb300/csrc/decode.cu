@@ -65,6 +65,7 @@ constexpr int kSoftWarp0 = kConvWarp0 + kConvWarps;
 // Registers per thread after the split (launched with 128): 4 warps x 64 + 8 x 112 + 4 x 176
 // = 128 * (64 + 2 * 112 + 176) = 59392 <= 512 * 128 = 65536.
 constexpr int kRegsCtl = 64, kRegsConv = 112, kRegsSoft = 176;
+constexpr int kRegsLaunch = 128;  // 65536 / 512; checked on the host before the first launch
 constexpr int kNoPage = -2147483647 - 1;                 // a page the tile does not need
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0;    // Q[2]: 64 columns each (128 fp16 channels as pairs)
@@ -149,7 +150,7 @@ __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
 
 template <int P>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
-  static_assert(kRegsCtl * 128 + kRegsConv * 256 + kRegsSoft * 128 <= 128 * kThreads, "register split");
+  static_assert(kRegsCtl * 128 + kRegsConv * 256 + kRegsSoft * 128 <= kRegsLaunch * kThreads, "register split");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* raw = smem + kOffRaw;
@@ -738,7 +739,12 @@ cudaError_t launch_decode_p(const DecodeParams& p, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    // The register split inside the kernel assumes the launch register count.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<P>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidDeviceFunction;
+    e = cudaFuncSetAttribute(decode_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }

@@ -45,7 +45,17 @@ constexpr int kOffBars = kOffStage + kStages * kStageBytes;
 constexpr int kNumBars = 2 * kStages + 6 * kQT;
 constexpr int kOffMisc = kOffBars + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-constexpr int kThreads = 320;              // producer, MMA, 2 x 4 softmax warps
+// Warpgroup 0: K/V producer (warp 0), MMA issuer (warp 1), two spare warps;
+// warpgroups 1 and 2: the softmax of q-tile 0 and q-tile 1.  The block is
+// launched with 168 registers per thread (384 threads; 3 warps x 32 x 168 =
+// 16128 of a sub-partition's 16384), then warpgroup 0 shrinks to 72 and the
+// softmax groups grow to 216: 128 * (72 + 216 + 216) = 64512 = 384 * 168, so
+// the growth is covered exactly by what warpgroup 0 gives back.  The host
+// checks the launch register count before the first launch.
+constexpr int kThreads = 384;
+constexpr int kRegsCtl = 72, kRegsSoft = 216;
+constexpr int kRegsLaunch = 168;
+static_assert(kRegsCtl * 128 + kRegsSoft * 256 <= kRegsLaunch * kThreads, "register split");
 constexpr uint32_t kTmemCols = 512;        // per q-tile: S (128 columns, P over its first 64) + O (128)
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -169,7 +179,7 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
 // so that each softmax group works on one tile while the tensor core runs the
 // other group's MMAs; warps 2-5 and 6-9 run the softmax of q-tile 0 and 1 (one
 // thread per row) and write the outputs.
-__global__ void __maxnreg__(200) prefill_kernel(const PrefillParams p,
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParams p,
                                                               const __grid_constant__ CUtensorMap kmap,
                                                               const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ uint8_t smem_raw[];
@@ -213,7 +223,9 @@ __global__ void __maxnreg__(200) prefill_kernel(const PrefillParams p,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp < 4) {
+   setmaxnreg_dec<kRegsCtl>();
+   if (warp == 0) {
     // ------------------------------------------------------------ K/V producer
     if (lane == 0) {
       int g = 0;
@@ -233,7 +245,7 @@ __global__ void __maxnreg__(200) prefill_kernel(const PrefillParams p,
         }
       }
     }
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0, 0);
@@ -297,9 +309,11 @@ __global__ void __maxnreg__(200) prefill_kernel(const PrefillParams p,
         ++n;
       }
     }
+   }
   } else {
+    setmaxnreg_inc<kRegsSoft>();
     // ------------------------------------------------------------ softmax groups
-    const int q = (warp - 2) >> 2;          // q-tile of this group
+    const int q = (warp - 4) >> 2;          // q-tile of this group
     const int quarter = warp & 3;           // TMEM lane quarter
     const int r = quarter * 32 + lane;      // row within the q-tile
     const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
@@ -534,6 +548,11 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
+    // The register split inside the kernel assumes the launch register count.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, prefill_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidDeviceFunction;
     e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
