@@ -52,27 +52,31 @@ constexpr int kNumBars = 2 * NST + 2 * 2 /*k_full,v_full*/ + 2 * 2 /*s_full,p_fu
 constexpr int kOffMisc = kOffBars + 8 * kNumBars;        // tmem slot, abort flag, tile_full[2], page_ok[NST]
 constexpr int kOffRing = kOffMisc + 64;                  // [kRing] published work items
 constexpr int kRingInts = 16;                            // one ring entry: fields + first tile's page ids
-constexpr int kSmemBytes = kOffRing + kRing * kRingInts * 4 + 1024;
+constexpr int kOffXch = kOffRing + kRing * kRingInts * 4;    // [2 tiles][2 halves][64 rows] floats
+constexpr int kSmemBytes = kOffXch + 3 * 2 * 64 * 4 + 1024;  // maxima [2][2][64] + sums [2][64]
 // Warp roles, aligned to warpgroups so each group can resize its register file:
 //   warpgroup 0: producer (warp 0), MMA issuer (warp 1), scheduler (warp 2), spare (warp 3)
 //   warpgroups 1-2: converters (warps 4..11)
-//   warpgroup 3: softmax (warps 12..15, one per TMEM lane quarter)
-constexpr int kThreads = 512;
+//   warpgroups 3-4: softmax (warps 12..19: two per TMEM lane quarter, each taking
+//   half of a tile's tokens)
+constexpr int kThreads = 640;
 constexpr int kSchedWarp = 2;
 constexpr int kConvWarp0 = 4;
 constexpr int kConvWarps = 8;
 constexpr int kSoftWarp0 = kConvWarp0 + kConvWarps;
-// Registers per thread after the split (launched with 128): 4 warps x 64 + 8 x 112 + 4 x 176
-// = 128 * (64 + 2 * 112 + 176) = 59392 <= 512 * 128 = 65536.
-constexpr int kRegsCtl = 64, kRegsConv = 112, kRegsSoft = 176;
-constexpr int kRegsLaunch = 128;  // 65536 / 512; checked on the host before the first launch
+constexpr int kSoftWarps = 8;
+// Registers per thread: launched with 96 (20 warps: 5 per SM sub-partition,
+// 5 * 32 * 96 = 15360 <= 16384), then 4 warps x 56 + 8 x 96 + 8 x 112:
+// 128 * (56 + 2 * 96 + 2 * 112) = 60416 <= 640 * 96 = 61440.
+constexpr int kRegsCtl = 56, kRegsConv = 96, kRegsSoft = 112;
+constexpr int kRegsLaunch = 96;  // checked on the host before the first launch
 constexpr int kNoPage = -2147483647 - 1;                 // a page the tile does not need
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0;    // Q[2]: 64 columns each (128 fp16 channels as pairs)
 constexpr uint32_t kColS = 128;  // S[2]: 128 columns each; P (fp16 pairs) overwrites the first 64
 constexpr uint32_t kColO = 384;  // O: 128 columns
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: weights stay <= 2^8 between rescales
-constexpr int kItemReaders = 2 + kConvWarps + 4;  // producer, MMA warp, converter warps, softmax warps
+constexpr int kItemReaders = 2 + kConvWarps + kSoftWarps;  // producer, MMA, converters, softmax
 
 // K-major no-swizzle operand with 128 channels: element (t, k) at
 // (t/8)*2048 + (k/8)*128 + (t%8)*16 + (k%8)*2.
@@ -150,7 +154,7 @@ __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
 
 template <int P>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
-  static_assert(kRegsCtl * 128 + kRegsConv * 256 + kRegsSoft * 128 <= kRegsLaunch * kThreads, "register split");
+  static_assert(kRegsCtl * 128 + kRegsConv * 256 + kRegsSoft * 256 <= kRegsLaunch * kThreads, "register split");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* raw = smem + kOffRaw;
@@ -189,11 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       mbar_init(&k_full[c], kConvWarps);
       mbar_init(&v_full[c], kConvWarps);
       mbar_init(&s_full[c], 1);
-      mbar_init(&p_full[c], 4);
+      mbar_init(&p_full[c], kSoftWarps);
       mbar_init(&v_free[c], 1);
     }
     mbar_init(o_full, 1);
-    mbar_init(o_empty, 4);
+    mbar_init(o_empty, kSoftWarps);
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&item_full[r], 1);
       mbar_init(&item_empty[r], kItemReaders);
@@ -525,11 +529,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   } else {
     setmaxnreg_inc<kRegsSoft>();
     // ------------------------------------------------------------ softmax + epilogue
+    // Two warps per TMEM lane quarter: warp half hf takes tokens [64*hf, 64*hf + 64) of
+    // each tile and channels [64*hf, 64*hf + 64) of O; within a warp, thread half th takes
+    // 32 of those.  Head row h = 16*quarter + lane%16.  The two warps of a quarter agree
+    // on each row's maximum through a small shared exchange and a 64-thread barrier.
+    const int sw = warp - kSoftWarp0;
     const int quarter = warp & 3;
-    const int h = quarter * 16 + (lane & 15);  // head row
-    const int th = lane >> 4;                  // token half of each tile / channel half of O
+    const int hf = sw >> 2;
+    const int h = quarter * 16 + (lane & 15);
+    const int th = lane >> 4;
+    const int tok0 = hf * 64 + th * 32;         // first token (of the tile) this thread handles
     const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
-    const bool warp_live = quarter * 16 < Hq;  // padded rows only: skip the arithmetic
+    const bool warp_live = quarter * 16 < Hq;   // padded rows only: skip the arithmetic
+    float* xch = reinterpret_cast<float*>(smem + kOffXch);  // [2][2][64]
+    const uint32_t pair_bar = 1 + quarter;      // named barrier of the two warps of this quarter
     int g = 0, item_n = 0, k = 0;
     while (true) {
       bool done = false;
@@ -537,11 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       if (done) break;
       if (it.kind == 1) {
         // Nothing to attend (L = 0) or an invalid length: out = 0, lse = -inf.
-        if (it.invalid && tid == kSoftWarp0 * 32) set_err(p.err, CAI_DEVERR_LENGTH);
+        if (it.invalid && sw == 0 && lane == 0) set_err(p.err, CAI_DEVERR_LENGTH);
         if (h < Hq) {
-          float* dst = p.out + ((int64_t)it.b * Hq + h) * kHeadDim + th * 64;
-          for (int d = 0; d < 64; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (p.lse_out && th == 0) p.lse_out[(int64_t)it.b * Hq + h] = -INFINITY;
+          float* dst = p.out + ((int64_t)it.b * Hq + h) * kHeadDim + hf * 64 + th * 32;
+          for (int d = 0; d < 32; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (p.lse_out && th == 0 && hf == 0) p.lse_out[(int64_t)it.b * Hq + h] = -INFINITY;
         }
         continue;
       }
@@ -555,16 +568,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         tc_fence_after();
         const uint32_t scol = kColS + c * 128;
         if (warp_live) {
-          uint32_t sr[64];
-          tmem_ld_16x32bx2_x64<64>(tmem + t_lane + scol, sr);
+          uint32_t sr[32];
+          tmem_ld_16x32bx2_x32<32>(tmem + t_lane + scol + hf * 64, sr);
           tmem_wait_ld();
-          const float* ksc = scal + c * 3 * T + th * 64;
+          const float* ksc = scal + c * 3 * T + tok0;
           const float* kbias = ksc + T;
           const float* vsc = ksc + 2 * T;
           float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
           if (tile_full[c]) {
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) {
+            for (int j = 0; j < 32; j += 4) {
               const float4 a = *reinterpret_cast<const float4*>(ksc + j);
               const float z0 = __uint_as_float(sr[j]) * a.x, z1 = __uint_as_float(sr[j + 1]) * a.y;
               const float z2 = __uint_as_float(sr[j + 2]) * a.z, z3 = __uint_as_float(sr[j + 3]) * a.w;
@@ -579,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) {
+            for (int j = 0; j < 32; j += 4) {
               const float4 a = *reinterpret_cast<const float4*>(ksc + j);
               const float4 bb = *reinterpret_cast<const float4*>(kbias + j);
               const float z0 = fmaf(__uint_as_float(sr[j]), a.x, bb.x), z1 = fmaf(__uint_as_float(sr[j + 1]), a.y, bb.y);
@@ -596,19 +609,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           }
           float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          // Row maximum over the whole tile: exchange with the other warp of this quarter.
+          float* xg = xch + (g & 1) * 128;
+          if (th == 0) xg[hf * 64 + h] = mx;
+          named_barrier_sync(pair_bar, 64);
+          mx = fmaxf(mx, xg[(1 - hf) * 64 + h]);
           const bool raise = mx > m_ref + kRescaleThreshold;
           const float alpha = raise ? ex2_approx(m_ref - mx) : 1.0f;
           if (t > 0 && __any_sync(0xffffffffu, raise)) {
-            // O holds earlier tiles of this item: wait for the previous PV, then rescale.
+            // O holds earlier tiles of this item: wait for the previous PV, then rescale this warp's half.
             ok = mbar_wait_abortable(&v_free[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag);
             if (ok) {
               tc_fence_after();
-              uint32_t o[64];
-              tmem_ld_16x32bx2_x64<64>(tmem + t_lane + kColO, o);
+              uint32_t o[32];
+              tmem_ld_16x32bx2_x32<32>(tmem + t_lane + kColO + hf * 64, o);
               tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 64; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-              tmem_st_16x32bx2_x64<64>(tmem + t_lane + kColO, o);
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+              tmem_st_16x32bx2_x32<32>(tmem + t_lane + kColO + hf * 64, o);
               tmem_wait_st();
             }
           }
@@ -617,10 +635,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
             m_ref = mx;
           }
           const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
-          uint32_t pw[32];
+          uint32_t pw[16];
           float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 64; j += 4) {
+          for (int j = 0; j < 32; j += 4) {
             const float4 vs = *reinterpret_cast<const float4*>(vsc + j);
             const float e0 = ex2_approx(__uint_as_float(sr[j]) - m_use);
             const float e1 = ex2_approx(__uint_as_float(sr[j + 1]) - m_use);
@@ -634,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
             pw[j / 2 + 1] = pack_f16x2(e2 * vs.z, e3 * vs.w);
           }
           l_sum += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-          tmem_st_16x32bx2_x32<32>(tmem + t_lane + scol, pw);
+          // P (fp16 pairs) over the first 64 columns of the S buffer: tokens 2c, 2c+1 in column c.
+          tmem_st_16x32bx2_x16<16>(tmem + t_lane + scol + hf * 32, pw);
           tmem_wait_st();
         }
         tc_fence_before();
@@ -643,25 +662,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         if (!ok) break;
       }
       if (!ok) break;
-      // ---- end of item: normalise this thread's half row of O and write it.
+      // ---- end of item: normalise this thread's 32 channels of its row of O and write them.
       if (!mbar_wait_abortable(o_full, item_n & 1, abort_flag)) break;
       tc_fence_after();
       if (warp_live) {
-        const float l_row = l_sum + __shfl_xor_sync(0xffffffffu, l_sum, 16);
+        // Row sum over the four threads of the row (two lanes here, two in the other warp).
+        float l_half = l_sum + __shfl_xor_sync(0xffffffffu, l_sum, 16);
+        float* xs = xch + 256;  // [2][64]: the sums, after the two maxima buffers
+        if (th == 0) xs[hf * 64 + h] = l_half;
+        named_barrier_sync(pair_bar, 64);
+        const float l_row = l_half + xs[(1 - hf) * 64 + h];
+        named_barrier_sync(pair_bar, 64);  // both have read before the slots are reused
         const float inv = l_row > 0.0f ? 1.0f / l_row : 0.0f;
-        uint32_t o[64];
-        tmem_ld_16x32bx2_x64<64>(tmem + t_lane + kColO, o);
+        uint32_t o[32];
+        tmem_ld_16x32bx2_x32<32>(tmem + t_lane + kColO + hf * 64, o);
         tmem_wait_ld();
         if (h < Hq) {
-          float* dst = it.direct ? p.out + ((int64_t)it.b * Hq + h) * kHeadDim + th * 64
-                                 : p.ws_o + (((int64_t)it.b * p.plan.max_splits + it.split) * Hq + h) * kHeadDim +
-                                       th * 64;
+          const int d0 = hf * 64 + th * 32;
+          float* dst = it.direct ? p.out + ((int64_t)it.b * Hq + h) * kHeadDim + d0
+                                 : p.ws_o + (((int64_t)it.b * p.plan.max_splits + it.split) * Hq + h) * kHeadDim + d0;
 #pragma unroll
-          for (int j = 0; j < 64; j += 4)
+          for (int j = 0; j < 32; j += 4)
             *reinterpret_cast<float4*>(dst + j) =
                 make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
                             __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
-          if (th == 0) {
+          if (th == 0 && hf == 0) {
             const float lse2 = l_row > 0.0f ? m_ref + __log2f(l_row) : -INFINITY;
             if (it.direct) {
               if (p.lse_out) p.lse_out[(int64_t)it.b * Hq + h] = lse2 * kLn2;

@@ -230,6 +230,22 @@ __device__ __forceinline__ void tmem_st_16x32bx2_x64(uint32_t taddr, const uint3
       : "memory");
 }
 
+#define CAI_R16(a, o) CAI_R8(a, o), CAI_R8(a, o + 8)
+#define CAI_W16(a, o) CAI_W8(a, o), CAI_W8(a, o + 8)
+
+template <int kHalf>
+__device__ __forceinline__ void tmem_st_16x32bx2_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};" ::
+          "r"(taddr),
+      "n"(kHalf), CAI_W16(r, 0)
+      : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // M=128 accumulators: thread t reads lane (base + t), columns [col, col + 32).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
