@@ -147,7 +147,7 @@ cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int
   if (batch < 0 || max_pages_per_seq <= 0 || window < 0 || num_splits < 0 || num_splits > kMaxSplits ||
       !std::isfinite(softmax_scale))
     return CAI_ERR_INVALID_ARG;
-  if (num_q_heads < 1 || num_q_heads > kDecodeRows) return CAI_ERR_UNSUPPORTED;
+  if (num_q_heads < 1 || num_q_heads > kDecodeMaxHeads) return CAI_ERR_UNSUPPORTED;
   if ((int64_t)max_pages_per_seq * pool->page_size > (1ll << 30) || batch > 65535) return CAI_ERR_UNSUPPORTED;
   if (batch == 0) return CAI_OK;
   if (!q || !block_table || !ctx_len || !out) return CAI_ERR_INVALID_ARG;

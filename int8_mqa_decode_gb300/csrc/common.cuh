@@ -10,10 +10,9 @@ namespace cai {
 
 constexpr int kHeadDim = 128;
 constexpr int kMaxSplits = 64;
-constexpr int kDecodeTile = 128;       // tokens per decode tile (MMA N of S, K of PV)
+constexpr int kDecodeTile = 128;       // tokens per decode tile (MMA M of the scores, K of PV)
 constexpr int kRawTokens = 64;         // tokens per raw page stage (half a tile)
-constexpr int kDecodeRows = 64;        // MMA M for decode: query heads padded to 64
-constexpr int kDecodeStages = 5;       // raw page stages (64 tokens each) per CTA
+constexpr int kDecodeMaxHeads = 64;    // query heads per decode call at most (MMA N of the scores)
 constexpr int kWorkspaceHeader = 256;  // decode workspace: work-queue counters, kept zero between calls
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

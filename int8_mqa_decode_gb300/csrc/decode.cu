@@ -10,83 +10,121 @@
 // (hybrid attention, technique table of "Character.AI: inference
 // optimization", section 03).
 //
-// How.  A persistent kernel, one CTA per SM, walks a static list of work
-// items (sequence, split) in 128-token tiles with five warp roles connected by
-// mbarriers:
-//  * producer (warp 0): one 1-D bulk copy (TMA engine) per page into a
-//    3-stage ring; a page carries K codes, V codes and both scale rows and is
-//    read once for all query heads.  Pages wholly outside the split (the part
-//    of a local layer before its window) are never read;
-//  * converters (warps 2-5): int8 codes -> fp16 (exact) into the canonical
-//    no-swizzle tcgen05 operand layouts in shared memory (K K-major, V
-//    MN-major), the per-token scales and mask into a small ring, and the
-//    item's query (bf16 -> fp16) into tensor memory;
-//  * MMA issuer (warp 1): S = Q K^T (tcgen05.mma kind::f16, M = 64 padded
-//    heads, N = 128 tokens, K = 128, A from tensor memory) into a double-
-//    buffered S, then O += P V (P from tensor memory, V from shared memory);
-//  * softmax (warps 6-9, two threads per head): applies the per-token K scale
-//    and softmax scale in fp32, keeps a reference maximum that is raised only
-//    when a logit exceeds it by 2^8 (so O is rarely rescaled), scales P by the
-//    per-token V scale, rounds it to fp16 into the S buffer it came from, and
-//    at the end of an item writes the normalised partial output and its
-//    log-sum-exp (or the final output when the sequence has one split).
+// How.  A persistent kernel, one CTA per SM, takes work items (sequence,
+// split) from a global queue and walks each in 128-token tiles.  The scores
+// are computed transposed, S^T = K Q^T (tokens x heads), so that one thread
+// owns one token: its K and V scales and its mask are per-thread scalars and
+// the K operand goes from registers to tensor memory without a shared-memory
+// copy.  Warp roles, connected by mbarriers:
+//  * scheduler (warp 2): claims items with an atomic counter, prefetches the
+//    item's block-table lines into L2 and publishes the item, with the page
+//    ids of its first tiles, into a small ring read by every role;
+//  * producer (warp 0): per page, one 2-D tensor copy (TMA) of its K and V
+//    code rows into a 128-byte-swizzled slot (so that reading one token row
+//    per thread is free of bank conflicts) and one 1-D bulk copy of its two
+//    scale rows, into a ring of 64-token stages.  Each lane issues one page.
+//    Page ids are fetched a batch of tiles ahead, one id per lane.  Pages
+//    wholly outside the split (the part of a local layer before its window)
+//    are never read;
+//  * converters (warps 4-11): read a tile's codes and scales into registers
+//    and hand the stages back at once; then K codes -> fp16 (exact) into tensor
+//    memory (the A operand, one token per lane), V codes -> fp16 into the
+//    canonical no-swizzle MN-major operand layout in shared memory, the
+//    per-token scales and mask into a four-tile ring, and at an item's first
+//    tile the item's query (bf16 -> fp16) as the K-major B operand Q^T;
+//  * MMA issuer (warp 1): S^T = K Q^T (tcgen05.mma kind::f16, M = 128 tokens,
+//    N = heads padded to 32 or 64, K = 128, A from tensor memory) into a
+//    double-buffered S^T, then O^T += V^T P^T (M = 128 channels, N = heads,
+//    K = 128 tokens, both operands from shared memory) into one of two O^T
+//    accumulators (one per item in flight);
+//  * softmax (warps 12-15, one thread per token of the tile): applies the K
+//    scale and softmax scale, checks the logits against a per-head reference
+//    maximum shared by the four warps that is raised only when a logit exceeds
+//    it by 2^8 (one barrier-reduction per tile decides; O^T is rarely
+//    rescaled), scales P by the token's V scale and stores it, fp16, as the
+//    B operand P^T; at the end of an item it reduces the per-head sums and
+//    writes the normalised output and its log-sum-exp (or the partial ones of
+//    a split).
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tma.cuh"
 
 namespace cai {
 namespace {
 
-constexpr int T = kDecodeTile;                 // 128 tokens per MMA tile
-constexpr int RT = kRawTokens;                 // 64 tokens per raw stage
-constexpr int NST = kDecodeStages;             // raw page stages
-constexpr int kRawStageBytes = RT * 264;       // K, V and scales of 64 tokens
-constexpr int kOp16Bytes = T * kHeadDim * 2;   // one fp16 operand tile (32 KB)
-constexpr int kRing = 8;                       // work items published ahead by the producer
-constexpr int kOffRaw = 0;
-constexpr int kOffK16 = kOffRaw + NST * kRawStageBytes;  // K16[2]
-constexpr int kOffV16 = kOffK16 + 2 * kOp16Bytes;        // V16[2]
-constexpr int kOffScale = kOffV16 + 2 * kOp16Bytes;      // [2][3][T] floats: k scale, bias, v scale
-constexpr int kOffBars = kOffScale + 2 * 3 * T * 4;
-constexpr int kNumBars = 2 * NST + 2 * 2 /*k_full,v_full*/ + 2 * 2 /*s_full,p_full*/ + 2 /*v_free*/ + 2 /*o*/ +
-                         2 * kRing;
-constexpr int kOffMisc = kOffBars + 8 * kNumBars;        // tmem slot, abort flag, tile_full[2], page_ok[NST]
-constexpr int kOffRing = kOffMisc + 64;                  // [kRing] published work items
-constexpr int kRingInts = 16;                            // one ring entry: fields + first tile's page ids
-constexpr int kOffXch = kOffRing + kRing * kRingInts * 4;    // [2 tiles][2 halves][64 rows] floats
-constexpr int kSmemBytes = kOffXch + 3 * 2 * 64 * 4 + 1024;  // maxima [2][2][64] + sums [2][64]
+constexpr int T = kDecodeTile;                 // 128 tokens per tile
+constexpr int RT = 64;                         // tokens per raw stage
+constexpr int kStageKV = RT * 2 * kHeadDim;    // K and V code rows of one stage (16 KB)
+constexpr int kStageSc = RT * 8;               // their K and V scales (512 B)
+constexpr int kOp16Bytes = T * kHeadDim * 2;   // one fp16 128 x 128 operand (32 KB)
+constexpr int kRing = 8;                       // work items published ahead by the scheduler
+constexpr int kRingInts = 40;                  // ring entry: 8 item fields + 32 page ids
+constexpr int kScaleSlots = 4;                 // scale/mask ring depth (tiles)
+
+// Shared-memory layout for HN padded heads (32 or 64).
+template <int HN>
+struct Layout {
+  static constexpr int NST = HN <= 32 ? 7 : 6;                   // raw stages
+  static constexpr int kOffRawKV = 0;                            // [NST][16 KB], 1024-aligned (swizzle)
+  static constexpr int kOffV16 = kOffRawKV + NST * kStageKV;     // V16[2]
+  static constexpr int kPTBytes = HN * T * 2;
+  static constexpr int kOffPT = kOffV16 + 2 * kOp16Bytes;        // P^T[2]
+  static constexpr int kOffQT = kOffPT + 2 * kPTBytes;           // Q^T
+  static constexpr int kOffRawSc = kOffQT + HN * kHeadDim * 2;   // [NST][512 B]
+  static constexpr int kOffScal = kOffRawSc + NST * kStageSc;    // [4][3][T] floats
+  static constexpr int kOffXch = kOffScal + kScaleSlots * 3 * T * 4;  // softmax exchange, 13 x HN floats
+  static constexpr int kOffBars = kOffXch + 13 * HN * 4;
+  static constexpr int kNumBars = 2 * NST + 2 * 2 /*k_full, v_full*/ + 2 * 2 /*s_full, p_full*/ + 2 /*v_free*/ +
+                                  2 * 2 /*o_full, o_empty*/ + 2 * kRing + 2 * kScaleSlots;
+  static constexpr int kOffMisc = kOffBars + 8 * kNumBars;       // tmem slot, abort flag, page_ok[NST]
+  static constexpr int kOffRing = kOffMisc + 64;
+  static constexpr int kSmemBytes = kOffRing + kRing * kRingInts * 4 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "dynamic shared memory per CTA");
+  static_assert(8 + 4 * NST <= 64, "misc words");
+};
+
 // Warp roles, aligned to warpgroups so each group can resize its register file:
-//   warpgroup 0: producer (warp 0), MMA issuer (warp 1), scheduler (warp 2), spare (warp 3)
+//   warpgroup 0: producer (warp 0), MMA issuer (warp 1), scheduler (warp 2), idle (warp 3)
 //   warpgroups 1-2: converters (warps 4..11)
-//   warpgroups 3-4: softmax (warps 12..19: two per TMEM lane quarter, each taking
-//   half of a tile's tokens)
-constexpr int kThreads = 640;
+//   warpgroup 3: softmax (warps 12..15, one per TMEM lane quarter)
+constexpr int kThreads = 512;
 constexpr int kSchedWarp = 2;
 constexpr int kConvWarp0 = 4;
 constexpr int kConvWarps = 8;
 constexpr int kSoftWarp0 = kConvWarp0 + kConvWarps;
-constexpr int kSoftWarps = 8;
-// Registers per thread: launched with 96 (20 warps: 5 per SM sub-partition,
-// 5 * 32 * 96 = 15360 <= 16384), then 4 warps x 56 + 8 x 96 + 8 x 112:
-// 128 * (56 + 2 * 96 + 2 * 112) = 60416 <= 640 * 96 = 61440.
-constexpr int kRegsCtl = 56, kRegsConv = 96, kRegsSoft = 112;
-constexpr int kRegsLaunch = 96;  // checked on the host before the first launch
-constexpr int kNoPage = -2147483647 - 1;                 // a page the tile does not need
+constexpr int kSoftWarps = 4;
+// Registers per thread: launched with 128 (16 warps, 4 per SM sub-partition:
+// 4 * 32 * 128 = 16384), then 56 / 104 / 232 per warpgroup:
+// 128 * (56 + 2 * 104 + 232) = 63488 <= 512 * 128 = 65536, and per
+// sub-partition 32 * (56 + 2 * 104 + 232) = 15872 <= 16384.
+constexpr int kRegsCtl = 56, kRegsConv = 104, kRegsSoft = 232;
+constexpr int kRegsLaunch = 128;  // checked on the host before the first launch
+constexpr int kNoPage = -2147483647 - 1;      // a page the tile does not need
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColQ = 0;    // Q[2]: 64 columns each (128 fp16 channels as pairs)
-constexpr uint32_t kColS = 128;  // S[2]: 128 columns each; P (fp16 pairs) overwrites the first 64
-constexpr uint32_t kColO = 384;  // O: 128 columns
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: weights stay <= 2^8 between rescales
+constexpr float kRescaleThreshold = 8.0f;     // log2 units: weights stay <= 2^8 between rescales
 constexpr int kItemReaders = 2 + kConvWarps + kSoftWarps;  // producer, MMA, converters, softmax
-
-// K-major no-swizzle operand with 128 channels: element (t, k) at
-// (t/8)*2048 + (k/8)*128 + (t%8)*16 + (k%8)*2.
-__device__ __forceinline__ uint32_t kmajor_off(int t, int k8) { return (t >> 3) * 2048 + k8 * 128 + (t & 7) * 16; }
-// MN-major no-swizzle operand, T tokens along K and 128 channels along N:
-// element (t, n) at (n/8)*(T*16) + (t/8)*128 + (t%8)*16 + (n%8)*2.
-__device__ __forceinline__ uint32_t mnmajor_off(int t, int n8) { return n8 * (T * 16) + (t >> 3) * 128 + (t & 7) * 16; }
+constexpr uint32_t kSoftBar = 1;              // named barrier of the softmax warpgroup
 
 __device__ __forceinline__ void set_err(int32_t* err, int bits) {
   if (err) atomicOr(err, bits);
+}
+
+// Lane `lane` of a warp ends with the reduction over the warp of v[lane]
+// (a reduce-scatter: 31 shuffles for 32 values).  Destroys v.
+template <bool kMax>
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = up ? v[i] : v[i + o];
+      const float keep = up ? v[i + o] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return v[0];
 }
 
 // A work item: one split of one sequence.  kind 0 = tiles to process,
@@ -100,7 +138,7 @@ struct Item {
 
 // Ring entry: [0] b, [1] split, [2] start, [3] end, [4] tile0, [5] ntiles,
 // [6] flags (bit 0 direct, bit 1 invalid, bit 2 kind 1, bit 3 end of work),
-// [8 .. 8 + T/P) page ids of the item's first tile (kNoPage where not needed).
+// [8 .. 40) page ids of the item's first tiles (one id batch, see batch_page).
 __device__ __forceinline__ Item ring_item(const volatile int32_t* e, bool& done) {
   Item it;
   it.b = e[0];
@@ -121,8 +159,17 @@ __device__ __forceinline__ Item ring_item(const volatile int32_t* e, bool& done)
 template <int P>
 __device__ __forceinline__ int32_t tile_page(const DecodeParams& p, const Item& it, int t, int ps) {
   const int t0 = (it.tile0 + t) * T + ps * P;
-  if (ps >= T / P || t0 + P <= it.start || t0 >= it.end) return (int32_t)kNoPage;
+  if (t0 + P <= it.start || t0 >= it.end) return (int32_t)kNoPage;
   return p.table[(int64_t)it.b * p.max_pages + t0 / P];
+}
+
+// Id batch `batch` of an item: lane l holds page slot l % (T/P) of tile
+// batch * (32 / (T/P)) + l / (T/P).
+template <int P>
+__device__ __forceinline__ int32_t batch_page(const DecodeParams& p, const Item& it, int batch, int lane) {
+  constexpr int PPT = T / P, TPB = 32 / PPT;
+  const int t = batch * TPB + lane / PPT;
+  return t < it.ntiles ? tile_page<P>(p, it, t, lane % PPT) : (int32_t)kNoPage;
 }
 
 // kind 2 = an empty split, never published.
@@ -152,32 +199,60 @@ __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
   return it;
 }
 
-template <int P>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
-  static_assert(kRegsCtl * 128 + kRegsConv * 256 + kRegsSoft * 256 <= kRegsLaunch * kThreads, "register split");
+struct DecodeArgs {
+  DecodeParams p;
+  CUtensorMap kv_map;  // the page pool as rows of 128 bytes; box = the 2P code rows of a page
+};
+
+template <int P, int HN>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs args) {
+  using L = Layout<HN>;
+  constexpr int NST = L::NST;
+  constexpr int PPT = T / P;                   // pages per tile
+  constexpr int TPB = 32 / PPT;                // tiles per page-id batch
+  constexpr int SPS = RT / P;                  // pages per stage
+  constexpr int kRowsPerPage = page_bytes(P) / 128;
+  constexpr uint32_t kColKA = 0;               // K operand [2]: 64 columns each (fp16 pairs)
+  constexpr uint32_t kColS = 128;              // S^T [2]: HN columns each
+  constexpr uint32_t kColO = 128 + 2 * HN;     // O^T [2]: HN columns each
+  static_assert(kRegsCtl * 128 + kRegsConv * 256 + kRegsSoft * 128 <= kRegsLaunch * kThreads, "register split");
+  static_assert(page_bytes(P) % 128 == 0 && P % 16 == 0, "page rows");
+  const DecodeParams& p = args.p;
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* raw = smem + kOffRaw;
-  uint8_t* k16 = smem + kOffK16;
-  uint8_t* v16 = smem + kOffV16;
-  float* scal = reinterpret_cast<float*>(smem + kOffScale);  // [2][3][T]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* raw_full = bars;              // [NST] producer -> converters (tx bytes)
-  uint64_t* raw_empty = bars + NST;       // [NST] converters -> producer (4 warps)
-  uint64_t* k_full = bars + 2 * NST;      // [2] converters -> MMA, softmax (4 warps)
-  uint64_t* v_full = k_full + 2;          // [2] converters -> MMA (4 warps)
-  uint64_t* s_full = v_full + 2;          // [2] MMA commit after S
-  uint64_t* p_full = s_full + 2;          // [2] softmax -> MMA, converters (4 warps)
-  uint64_t* v_free = p_full + 2;          // [2] MMA commit after PV
-  uint64_t* o_full = v_free + 2;          // MMA commit after an item's last PV
-  uint64_t* o_empty = o_full + 1;         // softmax -> MMA after reading O (4 warps)
-  uint64_t* item_full = o_empty + 1;      // [kRing] producer -> readers
-  uint64_t* item_empty = item_full + kRing;  // [kRing] readers -> producer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kOffMisc + 4);
-  int32_t* tile_full = reinterpret_cast<int32_t*>(smem + kOffMisc + 8);               // [2]
-  uint32_t* page_ok = reinterpret_cast<uint32_t*>(smem + kOffMisc + 16);             // [NST]
-  volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(smem + kOffRing);      // [kRing][kRingInts]
+  uint8_t* raw_kv = smem + L::kOffRawKV;
+  uint8_t* raw_sc = smem + L::kOffRawSc;
+  uint8_t* v16 = smem + L::kOffV16;
+  uint8_t* pt = smem + L::kOffPT;
+  uint8_t* qt = smem + L::kOffQT;
+  float* scal = reinterpret_cast<float*>(smem + L::kOffScal);  // [kScaleSlots][k scale, valid, v scale][T]
+  float* xch = reinterpret_cast<float*>(smem + L::kOffXch);
+  float* wmax = xch;              // [4][HN] per-warp maxima
+  float* lpart = xch + 4 * HN;    // [4][HN] per-warp sums
+  float* mref = xch + 8 * HN;     // [HN] reference maxima (-inf: none yet)
+  float* muse = mref + HN;        // [HN] the reference as subtracted (0 when none)
+  float* aref = muse + HN;        // [HN] rescale factors of the last raise
+  float* dref = aref + HN;        // [HN] shift of the subtracted reference at the last raise
+  float* linv = dref + HN;        // [HN] 1 / row sums
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBars);
+  uint64_t* raw_full = bars;                 // [NST] producer -> converters (tx bytes)
+  uint64_t* raw_empty = bars + NST;          // [NST] converters -> producer
+  uint64_t* k_full = bars + 2 * NST;         // [2] converters -> MMA (K operand, Q^T)
+  uint64_t* v_full = k_full + 2;             // [2] converters -> MMA (V operand)
+  uint64_t* s_full = v_full + 2;             // [2] MMA commit after S^T
+  uint64_t* p_full = s_full + 2;             // [2] softmax -> MMA (P^T)
+  uint64_t* v_free = p_full + 2;             // [2] MMA commit after PV (V16 and P^T free)
+  uint64_t* o_full = v_free + 2;             // [2] MMA commit after an item's last PV
+  uint64_t* o_empty = o_full + 2;            // [2] softmax -> MMA after reading O^T
+  uint64_t* item_full = o_empty + 2;         // [kRing] scheduler -> readers
+  uint64_t* item_empty = item_full + kRing;  // [kRing] readers -> scheduler
+  uint64_t* scale_full = item_empty + kRing;        // [kScaleSlots] converters -> softmax
+  uint64_t* scale_free = scale_full + kScaleSlots;  // [kScaleSlots] softmax -> converters
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kOffMisc + 4);
+  uint32_t* page_ok = reinterpret_cast<uint32_t*>(smem + L::kOffMisc + 8);        // [NST]
+  volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(smem + L::kOffRing);  // [kRing][kRingInts]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_heads;
@@ -195,12 +270,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       mbar_init(&s_full[c], 1);
       mbar_init(&p_full[c], kSoftWarps);
       mbar_init(&v_free[c], 1);
+      mbar_init(&o_full[c], 1);
+      mbar_init(&o_empty[c], kSoftWarps);
     }
-    mbar_init(o_full, 1);
-    mbar_init(o_empty, kSoftWarps);
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&item_full[r], 1);
       mbar_init(&item_empty[r], kItemReaders);
+    }
+    for (int r = 0; r < kScaleSlots; ++r) {
+      mbar_init(&scale_full[r], kConvWarps);
+      mbar_init(&scale_free[r], kSoftWarps);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -220,244 +299,244 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       return it;
     }
     it = ring_item(ring + slot * kRingInts, done);
-    if (first_ids) *first_ids = lane < T / P ? (int32_t)ring[slot * kRingInts + 8 + lane] : (int32_t)kNoPage;
+    if (first_ids) *first_ids = (int32_t)ring[slot * kRingInts + 8 + lane];
     __syncwarp();
     if (lane == 0) mbar_arrive(&item_empty[slot]);
     return it;
   };
 
   if (warp < kConvWarp0) {
-   setmaxnreg_dec<kRegsCtl>();
-   if (warp == kSchedWarp) {
-    // ------------------------------------------------------------ scheduler
-    // Takes work items from the global queue, decodes them and publishes them,
-    // up to kRing ahead of the roles that consume them.
-    int k = 0;
-    while (true) {
-      int idx = 0;
-      if (lane == 0) idx = (int)atomicAdd(&p.queue[0], 1u);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
-      const bool done = idx >= num_items;
-      Item it = {};
-      int32_t id = (int32_t)kNoPage;
-      if (!done) {
-        it = make_item<P>(p, idx);
-        if (it.kind == 2) continue;  // an empty split: nobody needs to hear of it
-        if (it.kind == 0) {
-          id = tile_page<P>(p, it, 0, lane);
-          // Warm L2 with the item's block-table entries (32 ids per 128-byte line, one line per lane).
-          const int first = it.start / P, last = (it.end - 1) / P;
-          const int32_t* row = p.table + (int64_t)it.b * p.max_pages;
-          for (int pg = (first & ~31) + lane * 32; pg <= last; pg += 32 * 32) prefetch_l2(row + pg);
-        }
-      }
-      const int slot = k % kRing;
-      if (k >= kRing && !mbar_wait_abortable(&item_empty[slot], ((k / kRing) - 1) & 1, abort_flag)) break;
-      volatile int32_t* e = ring + slot * kRingInts;
-      if (lane < T / P) e[8 + lane] = id;
-      if (lane == 0) {
+    setmaxnreg_dec<kRegsCtl>();
+    if (warp == kSchedWarp) {
+      // ---------------------------------------------------------- scheduler
+      int k = 0;
+      while (true) {
+        int idx = 0;
+        if (lane == 0) idx = (int)atomicAdd(&p.queue[0], 1u);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        const bool done = idx >= num_items;
+        Item it = {};
+        int32_t id = (int32_t)kNoPage;
         if (!done) {
-          e[0] = it.b;
-          e[1] = it.split;
-          e[2] = it.start;
-          e[3] = it.end;
-          e[4] = it.tile0;
-          e[5] = it.ntiles;
-          e[6] = (it.direct ? 1 : 0) | (it.invalid ? 2 : 0) | (it.kind == 1 ? 4 : 0);
-        } else {
-          e[6] = 8;
+          it = make_item<P>(p, idx);
+          if (it.kind == 2) continue;  // an empty split: nobody needs to hear of it
+          if (it.kind == 0) {
+            id = batch_page<P>(p, it, 0, lane);
+            // Warm L2 with the item's block-table entries (32 ids per 128-byte line, one line per lane).
+            const int first = it.start / P, last = (it.end - 1) / P;
+            const int32_t* row = p.table + (int64_t)it.b * p.max_pages;
+            for (int pg = (first & ~31) + lane * 32; pg <= last; pg += 32 * 32) prefetch_l2(row + pg);
+          }
         }
+        const int slot = k % kRing;
+        if (k >= kRing && !mbar_wait_abortable(&item_empty[slot], ((k / kRing) - 1) & 1, abort_flag)) break;
+        volatile int32_t* e = ring + slot * kRingInts;
+        e[8 + lane] = id;
+        if (lane == 0) {
+          if (!done) {
+            e[0] = it.b;
+            e[1] = it.split;
+            e[2] = it.start;
+            e[3] = it.end;
+            e[4] = it.tile0;
+            e[5] = it.ntiles;
+            e[6] = (it.direct ? 1 : 0) | (it.invalid ? 2 : 0) | (it.kind == 1 ? 4 : 0);
+          } else {
+            e[6] = 8;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          mbar_arrive(&item_full[slot]);
+        }
+        ++k;
+        if (done) break;
       }
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();
-        mbar_arrive(&item_full[slot]);
+      // The last CTA to finish fetching leaves the queue counters at zero for the next call.
+      if (lane == 0 && atomicAdd(&p.queue[1], 1u) == gridDim.x - 1) {
+        atomicExch(&p.queue[0], 0u);
+        atomicExch(&p.queue[1], 0u);
       }
-      ++k;
-      if (done) break;
-    }
-    // The last CTA to finish fetching leaves the queue counters at zero for the next call.
-    if (lane == 0 && atomicAdd(&p.queue[1], 1u) == gridDim.x - 1) {
-      atomicExch(&p.queue[0], 0u);
-      atomicExch(&p.queue[1], 0u);
-    }
-  } else if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Page ids are fetched one tile ahead by the warp's lanes (lane i: page slot i).
-    const uint64_t policy = policy_evict_first();
-    int r = 0, k = 0;
-    while (true) {
-      bool done = false;
-      int32_t ids = kNoPage;
-      const Item it = next_item(k++, done, &ids);
-      if (done || *abort_flag) break;
-      if (it.kind != 0) continue;
+    } else if (warp == 0) {
+      // ---------------------------------------------------------- producer
+      // `ids` holds the current batch of page ids (one per lane), `ids_next` the
+      // following batch, loaded a whole batch of tiles before it is needed.
+      const uint64_t policy = policy_evict_first();
+      int r = 0, k = 0;
+      while (true) {
+        bool done = false;
+        int32_t ids = kNoPage;
+        const Item it = next_item(k++, done, &ids);
+        if (done || *abort_flag) break;
+        if (it.kind != 0) continue;
+        bool ok = true;
+        int32_t ids_next = it.ntiles > TPB ? batch_page<P>(p, it, 1, lane) : (int32_t)kNoPage;
+        for (int t = 0; t < it.ntiles && ok; ++t) {
+          if (t > 0 && t % TPB == 0) {
+            ids = ids_next;
+            ids_next = t + TPB < it.ntiles ? batch_page<P>(p, it, t / TPB + 1, lane) : (int32_t)kNoPage;
+          }
+          for (int hf = 0; hf < 2; ++hf, ++r) {
+            const int s = r % NST;
+            if (r >= NST && !mbar_wait_abortable(&raw_empty[s], ((r / NST) - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const int32_t pid = __shfl_sync(0xffffffffu, ids, (t % TPB) * PPT + hf * SPS + lane % SPS);
+            const bool live = lane < SPS && pid != kNoPage;
+            const bool in_range = pid >= 0 && pid < p.num_pages;
+            if (live && !in_range) set_err(p.err, CAI_DEVERR_PAGE);
+            const uint32_t okm = __ballot_sync(0xffffffffu, live && in_range);
+            if (lane == 0) {
+              page_ok[s] = okm;
+              mbar_arrive_expect_tx(&raw_full[s], (uint32_t)__popc(okm) * page_bytes(P));
+            }
+            __syncwarp();
+            if ((okm >> lane) & 1u) {
+              tma_load_2d_hint(raw_kv + s * kStageKV + lane * (2 * P * kHeadDim), &args.kv_map, 0,
+                               pid * kRowsPerPage, &raw_full[s], policy);
+              bulk_g2s_hint(raw_sc + s * kStageSc + lane * (8 * P),
+                            p.pages + (int64_t)pid * page_bytes(P) + 2 * P * kHeadDim, 8 * P, &raw_full[s], policy);
+            }
+          }
+        }
+        if (!ok) break;
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc_s = idesc_f16_f32(T, HN, 0, 0);
+      constexpr uint32_t idesc_o = idesc_f16_f32(kHeadDim, HN, 1, 1);
+      const uint32_t v16a = smem_addr(v16), pta = smem_addr(pt), qta = smem_addr(qt);
+      int g = 0, item_n = 0, k = 0;
+      // PV of tile gp of item `item`: O^T[item & 1] (+)= V16 P^T; `first` starts the
+      // accumulator, `last` signals the item's epilogue.
+      auto issue_pv = [&](int gp, int item, bool first, bool last) -> bool {
+        const int c = gp & 1;
+        const int ob = item & 1;
+        if (!mbar_wait_abortable(&p_full[c], (gp >> 1) & 1, abort_flag)) return false;
+        if (!mbar_wait_abortable(&v_full[c], (gp >> 1) & 1, abort_flag)) return false;
+        if (first && item >= 2 && !mbar_wait_abortable(&o_empty[ob], ((item >> 1) - 1) & 1, abort_flag))
+          return false;
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int ks = 0; ks < T / 16; ++ks)
+            mma_f16_ss(tmem + kColO + ob * HN, smem_desc(v16a + c * kOp16Bytes + ks * 256, 128, T * 16),
+                       smem_desc(pta + c * L::kPTBytes + ks * 256, 128, T * 16), idesc_o,
+                       (!first || ks > 0) ? 1u : 0u);
+          mma_commit(&v_free[c]);
+          if (last) mma_commit(&o_full[ob]);
+        }
+        __syncwarp();
+        return true;
+      };
+      // Order per tile: S^T(g), then PV(g-1); an item's last PV follows its last
+      // S^T at once, so its epilogue never waits for the next item's data.
       bool ok = true;
-      int32_t ids_n1 = (1 < it.ntiles) ? tile_page<P>(p, it, 1, lane) : (int32_t)kNoPage;
-      for (int t = 0; t < it.ntiles && ok; ++t) {
-        const int32_t ids_n2 = (t + 2 < it.ntiles) ? tile_page<P>(p, it, t + 2, lane) : (int32_t)kNoPage;
-        for (int hf = 0; hf < 2; ++hf, ++r) {
-          const int s = r % NST;
-          if (r >= NST && !mbar_wait_abortable(&raw_empty[s], ((r / NST) - 1) & 1, abort_flag)) {
+      while (ok) {
+        bool done = false;
+        const Item it = next_item(k++, done);
+        if (done) break;
+        if (it.kind != 0) continue;
+        for (int t = 0; t < it.ntiles; ++t, ++g) {
+          const int c = g & 1;
+          if (!mbar_wait_abortable(&k_full[c], (g >> 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
-          int32_t pid[RT / P];
-#pragma unroll
-          for (int ps = 0; ps < RT / P; ++ps) pid[ps] = __shfl_sync(0xffffffffu, ids, hf * (RT / P) + ps);
+          tc_fence_after();
           if (lane == 0) {
-            uint32_t okm = 0, bytes = 0;
 #pragma unroll
-            for (int ps = 0; ps < RT / P; ++ps) {
-              if (pid[ps] == kNoPage) continue;
-              if (pid[ps] < 0 || pid[ps] >= p.num_pages) {
-                set_err(p.err, CAI_DEVERR_PAGE);
-                continue;
-              }
-              okm |= 1u << ps;
-              bytes += page_bytes(P);
-            }
-            page_ok[s] = okm;
-            mbar_arrive_expect_tx(&raw_full[s], bytes);
-#pragma unroll
-            for (int ps = 0; ps < RT / P; ++ps) {
-              if (!(okm & (1u << ps))) continue;
-              bulk_g2s_hint(raw + s * kRawStageBytes + ps * page_bytes(P),
-                            p.pages + (int64_t)pid[ps] * page_bytes(P), page_bytes(P), &raw_full[s], policy);
-            }
+            for (int ks = 0; ks < kHeadDim / 16; ++ks)
+              mma_f16_ts(tmem + kColS + c * HN, tmem + kColKA + c * 64 + ks * 8, smem_desc(qta + ks * 256, 128, 2048),
+                         idesc_s, ks > 0 ? 1u : 0u);
+            mma_commit(&s_full[c]);
           }
           __syncwarp();
+          if (t > 0 && !issue_pv(g - 1, item_n, t == 1, false)) {
+            ok = false;
+            break;
+          }
+          if (t == it.ntiles - 1 && !issue_pv(g, item_n, t == 0, true)) {
+            ok = false;
+            break;
+          }
         }
-        ids = ids_n1;
-        ids_n1 = ids_n2;
+        ++item_n;
       }
-      if (!ok) break;
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc_s = idesc_f16_f32(kDecodeRows, T, 0, 0);
-    constexpr uint32_t idesc_o = idesc_f16_f32(kDecodeRows, kHeadDim, 0, 1);
-    const uint32_t k16a = smem_addr(k16), v16a = smem_addr(v16);
-    int g = 0, item_n = 0, k = 0;
-    bool have_prev = false, prev_first = false, prev_last = false;
-    int prev_item_n = 0;
-    auto issue_pv = [&](int gp) {
-      const int c = gp & 1;
-      if (!mbar_wait_abortable(&p_full[c], (gp >> 1) & 1, abort_flag)) return;
-      if (!mbar_wait_abortable(&v_full[c], (gp >> 1) & 1, abort_flag)) return;
-      if (prev_first && prev_item_n > 0 && !mbar_wait_abortable(o_empty, (prev_item_n - 1) & 1, abort_flag)) return;
-      tc_fence_after();
-      if (lane == 0) {
-#pragma unroll
-        for (int ks = 0; ks < T / 16; ++ks)
-          mma_f16_ts(tmem + kColO, tmem + kColS + c * 128 + ks * 8,
-                     smem_desc(v16a + c * kOp16Bytes + ks * 256, 128, T * 16), idesc_o,
-                     (!prev_first || ks > 0) ? 1u : 0u);
-        mma_commit(&v_free[c]);
-        if (prev_last) mma_commit(o_full);
-      }
-      __syncwarp();
-    };
-    while (true) {
-      bool done = false;
-      const Item it = next_item(k++, done);
-      if (done) break;
-      if (it.kind != 0) continue;
-      bool ok = true;
-      for (int t = 0; t < it.ntiles; ++t, ++g) {
-        const int c = g & 1;
-        if (!mbar_wait_abortable(&k_full[c], (g >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t qcol = kColQ + (item_n & 1) * 64;
-#pragma unroll
-          for (int ks = 0; ks < kHeadDim / 16; ++ks)
-            mma_f16_ts(tmem + kColS + c * 128, tmem + qcol + ks * 8,
-                       smem_desc(k16a + c * kOp16Bytes + ks * 256, 128, 2048), idesc_s, ks > 0 ? 1u : 0u);
-          mma_commit(&s_full[c]);
-        }
-        __syncwarp();
-        if (have_prev) issue_pv(g - 1);
-        have_prev = true;
-        prev_first = t == 0;
-        prev_last = t == it.ntiles - 1;
-        prev_item_n = item_n;
-      }
-      if (!ok) break;
-      ++item_n;
-    }
-    if (have_prev && !*abort_flag) issue_pv(g - 1);
-   }
   } else if (warp < kSoftWarp0) {
     setmaxnreg_dec<kRegsConv>();
     // ------------------------------------------------------------ converters
-    const int ctid = tid - kConvWarp0 * 32;  // 0 .. 32*kConvWarps-1
-    const int quarter = warp & 3;            // TMEM lanes this warp may touch
-    const bool q_warp = warp < kConvWarp0 + 4;  // one warp per lane quarter stores the query
-    constexpr int kUnits = (T * 8) / (32 * kConvWarps);  // 16-byte units per thread per operand
-    int g = 0, item_n = 0, k = 0;
-    while (true) {
+    const int ctid = tid - kConvWarp0 * 32;           // 0 .. 255
+    const int quarter = warp & 3;                     // TMEM lanes this warp may touch
+    const int hh = (warp - kConvWarp0) >> 2;          // which 64 channels of its token's K
+    const int tk = quarter * 32 + lane;               // this thread's token (K operand row)
+    const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
+    constexpr int kQUnits = HN * 16 / 256;            // 16-byte units of Q^T per thread
+    int g = 0, k = 0;
+    bool ok = true;
+    while (ok) {
       bool done = false;
       const Item it = next_item(k++, done);
       if (done) break;
       if (it.kind != 0) continue;
-      // The item's query rows for this warp, bf16 -> fp16 (loaded now, stored with the first tile).
-      const int qr = quarter * 16 + (lane & 15);
-      uint32_t qw[32];
-      if (q_warp && qr < Hq) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)it.b * Hq + qr) * kHeadDim + (lane >> 4) * 64);
+      // The item's query as Q^T (bf16 -> fp16), once the S^T of the previous
+      // item's last tile (g-1), which reads the old one, is done.
+      // Unit u: head n (8 consecutive lanes take 8 consecutive heads), channels 8*k8 .. 8*k8 + 7.
+      {
+        uint4 qv[kQUnits];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = src[v];
-          const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+        for (int i = 0; i < kQUnits; ++i) {
+          const int u = i * 256 + ctid;
+          const int n = (u & 7) | ((u >> 7) << 3), k8 = (u >> 3) & 15;
+          qv[i] = n < Hq ? __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)it.b * Hq + n) * kHeadDim + k8 * 8))
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (g >= 1) ok = mbar_wait_abortable(&s_full[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag);
+        if (!ok) break;
+#pragma unroll
+        for (int i = 0; i < kQUnits; ++i) {
+          const int u = i * 256 + ctid;
+          const int n = (u & 7) | ((u >> 7) << 3), k8 = (u >> 3) & 15;
+          const uint32_t xs[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+          uint32_t o[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            qw[v * 4 + e] = pack_f16x2(__uint_as_float(xs[e] << 16), __uint_as_float(xs[e] & 0xFFFF0000u));
+            o[e] = pack_f16x2(__uint_as_float(xs[e] << 16), __uint_as_float(xs[e] & 0xFFFF0000u));
+          *reinterpret_cast<uint4*>(qt + (n >> 3) * 2048 + k8 * 128 + (n & 7) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-      } else {
-#pragma unroll
-        for (int v = 0; v < 32; ++v) qw[v] = 0;
+        fence_proxy_async_smem();
       }
-      bool ok = true;
-      for (int t = 0; t < it.ntiles && ok; ++t, ++g) {
+      for (int t = 0; t < it.ntiles; ++t, ++g) {
         const int c = g & 1;
         const int s0 = (2 * g) % NST, s1 = (2 * g + 1) % NST;
         ok = mbar_wait_abortable(&raw_full[s0], ((2 * g) / NST) & 1, abort_flag) &&
              mbar_wait_abortable(&raw_full[s1], ((2 * g + 1) / NST) & 1, abort_flag);
-        if (ok && g >= 2) ok = mbar_wait_abortable(&s_full[c], ((g >> 1) - 1) & 1, abort_flag);  // K16[c] free
         if (!ok) break;
-        // K: 1024 16-byte units per tile; lanes rotated across chunks (conflict-free).  All loads first.
+        // Codes to registers.  Row r of a page slot holds its 16-byte chunk j at
+        // chunk position j ^ (r % 8) (128-byte swizzle; slots are 1024-aligned).
+        uint4 wk[4], wv[4];
         {
-          uint4 w[kUnits];
-          int tts[kUnits], chs[kUnits];
+          const int tr = tk & (RT - 1);
+          const uint8_t* row = raw_kv + (tk < RT ? s0 : s1) * kStageKV + (tr / P) * (2 * P * kHeadDim) +
+                               (tr % P) * kHeadDim;
 #pragma unroll
-          for (int u = 0; u < kUnits; ++u) {
-            const int unit = u * (4 * kConvWarps) + (ctid >> 3);
-            const int tt = (unit >> 3) * 8 + (ctid & 7);
-            const int ch = ((unit & 7) + (ctid & 7)) & 7;
-            const int tr = tt & (RT - 1);
-            tts[u] = tt;
-            chs[u] = ch;
-            w[u] = *reinterpret_cast<const uint4*>(raw + (tt < RT ? s0 : s1) * kRawStageBytes + (tr / P) * page_bytes(P) +
-                                                   (tr % P) * kHeadDim + ch * 16);
-          }
-          uint8_t* kd = k16 + c * kOp16Bytes;
-#pragma unroll
-          for (int u = 0; u < kUnits; ++u) {
-            uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
-            i8x4_to_f16x4(w[u].x, a0, a1);
-            i8x4_to_f16x4(w[u].y, a2, a3);
-            i8x4_to_f16x4(w[u].z, a4, a5);
-            i8x4_to_f16x4(w[u].w, a6, a7);
-            *reinterpret_cast<uint4*>(kd + kmajor_off(tts[u], 2 * chs[u])) = make_uint4(a0, a1, a2, a3);
-            *reinterpret_cast<uint4*>(kd + kmajor_off(tts[u], 2 * chs[u] + 1)) = make_uint4(a4, a5, a6, a7);
-          }
+          for (int i = 0; i < 4; ++i) wk[i] = *reinterpret_cast<const uint4*>(row + (((hh * 4 + i) ^ (tk & 7)) << 4));
         }
-        // Scales and mask of tile g into slot c: softmax of tile g-2 must be done with the slot.
-        if (g >= 2) ok = mbar_wait_abortable(&p_full[c], ((g >> 1) - 1) & 1, abort_flag);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int U = u * 256 + ctid;
+          const int tv = ((U >> 6) << 3) | (U & 7), j = (U >> 3) & 7;
+          const int tr = tv & (RT - 1);
+          const uint8_t* row = raw_kv + (tv < RT ? s0 : s1) * kStageKV + (tr / P) * (2 * P * kHeadDim) +
+                               (P + tr % P) * kHeadDim;
+          wv[u] = *reinterpret_cast<const uint4*>(row + ((j ^ (tv & 7)) << 4));
+        }
+        // Scales and mask of tile g into ring slot g % 4 (free once the softmax of tile g-4 is done).
+        const int ss = g & (kScaleSlots - 1);
+        if (g >= kScaleSlots) ok = mbar_wait_abortable(&scale_free[ss], ((g / kScaleSlots) - 1) & 1, abort_flag);
         if (!ok) break;
         if (ctid < T) {
           const int tt = ctid;
@@ -465,229 +544,223 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           const int tr = tt & (RT - 1);
           const int abs_t = (it.tile0 + t) * T + tt;
           const bool valid = abs_t >= it.start && abs_t < it.end && ((page_ok[s] >> (tr / P)) & 1u);
-          const float* sc = reinterpret_cast<const float*>(raw + s * kRawStageBytes + (tr / P) * page_bytes(P) +
-                                                           2 * P * kHeadDim);
-          float* dst = scal + c * 3 * T;
+          const float* sc = reinterpret_cast<const float*>(raw_sc + s * kStageSc + (tr / P) * (8 * P));
+          float* dst = scal + ss * 3 * T;
           dst[tt] = valid ? sc[tr % P] * p.scale_log2 : 0.0f;
-          dst[T + tt] = valid ? 0.0f : -INFINITY;
+          dst[T + tt] = valid ? 1.0f : 0.0f;
           dst[2 * T + tt] = valid ? sc[P + tr % P] : 0.0f;
-          if (tt == 0) {
-            const int tb = (it.tile0 + t) * T;
-            const uint32_t all = (1u << (RT / P)) - 1u;
-            tile_full[c] = tb >= it.start && tb + T <= it.end && page_ok[s0] == all && page_ok[s1] == all;
-          }
         }
-        if (t == 0 && q_warp) {
-          // Q[item_n & 1] was last read by the S of an item at least two tiles back: done (K16 wait above).
-          tmem_st_16x32bx2_x32<32>(tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + (item_n & 1) * 64, qw);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&scale_full[ss]);
+          mbar_arrive(&raw_empty[s0]);
+          mbar_arrive(&raw_empty[s1]);
+        }
+        // K -> tensor memory: K[c] is free once S^T of tile g-2 is done.
+        if (g >= 2) ok = mbar_wait_abortable(&s_full[c], ((g >> 1) - 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          uint32_t kw[32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t xs[4] = {wk[i].x, wk[i].y, wk[i].z, wk[i].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) i8x4_to_f16x4(xs[e], kw[(i * 4 + e) * 2], kw[(i * 4 + e) * 2 + 1]);
+          }
+          tmem_st_32x32b_x32(tmem + t_lane + kColKA + c * 64 + hh * 32, kw);
           tmem_wait_st();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&k_full[c]);
-        // V: buffer c is free once PV of tile g-2 is done.
+        // V -> V16[c], free once PV of tile g-2 is done.
         if (g >= 2) ok = mbar_wait_abortable(&v_free[c], ((g >> 1) - 1) & 1, abort_flag);
         if (!ok) break;
         {
-          uint4 w[kUnits];
-          int tts[kUnits], chs[kUnits];
-#pragma unroll
-          for (int u = 0; u < kUnits; ++u) {
-            const int unit = u * (4 * kConvWarps) + (ctid >> 3);
-            const int tt = (unit >> 3) * 8 + (ctid & 7);
-            const int ch = ((unit & 7) + (ctid & 7)) & 7;
-            const int tr = tt & (RT - 1);
-            tts[u] = tt;
-            chs[u] = ch;
-            w[u] = *reinterpret_cast<const uint4*>(raw + (tt < RT ? s0 : s1) * kRawStageBytes + (tr / P) * page_bytes(P) +
-                                                   P * kHeadDim + (tr % P) * kHeadDim + ch * 16);
-          }
           uint8_t* vd = v16 + c * kOp16Bytes;
 #pragma unroll
-          for (int u = 0; u < kUnits; ++u) {
+          for (int u = 0; u < 4; ++u) {
+            const int U = u * 256 + ctid;
+            const int tv = ((U >> 6) << 3) | (U & 7), j = (U >> 3) & 7;
             uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
-            i8x4_to_f16x4(w[u].x, a0, a1);
-            i8x4_to_f16x4(w[u].y, a2, a3);
-            i8x4_to_f16x4(w[u].z, a4, a5);
-            i8x4_to_f16x4(w[u].w, a6, a7);
-            *reinterpret_cast<uint4*>(vd + mnmajor_off(tts[u], 2 * chs[u])) = make_uint4(a0, a1, a2, a3);
-            *reinterpret_cast<uint4*>(vd + mnmajor_off(tts[u], 2 * chs[u] + 1)) = make_uint4(a4, a5, a6, a7);
+            i8x4_to_f16x4(wv[u].x, a0, a1);
+            i8x4_to_f16x4(wv[u].y, a2, a3);
+            i8x4_to_f16x4(wv[u].z, a4, a5);
+            i8x4_to_f16x4(wv[u].w, a6, a7);
+            // MN-major: channel d, token t at (d/8)*2048 + (t/8)*128 + (t%8)*16 + (d%8)*2.
+            *reinterpret_cast<uint4*>(vd + (2 * j) * 2048 + tv * 16) = make_uint4(a0, a1, a2, a3);
+            *reinterpret_cast<uint4*>(vd + (2 * j + 1) * 2048 + tv * 16) = make_uint4(a4, a5, a6, a7);
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&raw_empty[s0]);
-          mbar_arrive(&raw_empty[s1]);
-          mbar_arrive(&v_full[c]);
-        }
+        if (lane == 0) mbar_arrive(&v_full[c]);
       }
-      if (!ok) break;
-      ++item_n;
     }
   } else {
     setmaxnreg_inc<kRegsSoft>();
     // ------------------------------------------------------------ softmax + epilogue
-    // Two warps per TMEM lane quarter: warp half hf takes tokens [64*hf, 64*hf + 64) of
-    // each tile and channels [64*hf, 64*hf + 64) of O; within a warp, thread half th takes
-    // 32 of those.  Head row h = 16*quarter + lane%16.  The two warps of a quarter agree
-    // on each row's maximum through a small shared exchange and a 64-thread barrier.
-    const int sw = warp - kSoftWarp0;
-    const int quarter = warp & 3;
-    const int hf = sw >> 2;
-    const int h = quarter * 16 + (lane & 15);
-    const int th = lane >> 4;
-    const int tok0 = hf * 64 + th * 32;         // first token (of the tile) this thread handles
-    const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
-    const bool warp_live = quarter * 16 < Hq;   // padded rows only: skip the arithmetic
-    float* xch = reinterpret_cast<float*>(smem + kOffXch);  // [2][2][64]
-    const uint32_t pair_bar = 1 + quarter;      // named barrier of the two warps of this quarter
+    // Thread = token tok of each tile (TMEM lane of S^T) and channel tok of O^T.
+    const int sw = warp - kSoftWarp0;                 // lane quarter
+    const int tok = sw * 32 + lane;
+    const uint32_t t_lane = (uint32_t)(sw * 32) << 16;
     int g = 0, item_n = 0, k = 0;
-    while (true) {
+    bool ok = true;
+    while (ok) {
       bool done = false;
       const Item it = next_item(k++, done);
       if (done) break;
       if (it.kind == 1) {
         // Nothing to attend (L = 0) or an invalid length: out = 0, lse = -inf.
         if (it.invalid && sw == 0 && lane == 0) set_err(p.err, CAI_DEVERR_LENGTH);
-        if (h < Hq) {
-          float* dst = p.out + ((int64_t)it.b * Hq + h) * kHeadDim + hf * 64 + th * 32;
-          for (int d = 0; d < 32; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (p.lse_out && th == 0 && hf == 0) p.lse_out[(int64_t)it.b * Hq + h] = -INFINITY;
-        }
+        for (int h = 0; h < Hq; ++h) p.out[((int64_t)it.b * Hq + h) * kHeadDim + tok] = 0.0f;
+        if (p.lse_out && sw == 0)
+          for (int h = lane; h < Hq; h += 32) p.lse_out[(int64_t)it.b * Hq + h] = -INFINITY;
         continue;
       }
-      float m_ref = -INFINITY, l_sum = 0.0f;
-      bool ok = true;
+      float l[HN];
+#pragma unroll
+      for (int h = 0; h < HN; ++h) l[h] = 0.0f;
       for (int t = 0; t < it.ntiles; ++t, ++g) {
         const int c = g & 1;
+        const int ss = g & (kScaleSlots - 1);
         ok = mbar_wait_abortable(&s_full[c], (g >> 1) & 1, abort_flag) &&
-             mbar_wait_abortable(&k_full[c], (g >> 1) & 1, abort_flag);
+             mbar_wait_abortable(&scale_full[ss], (g / kScaleSlots) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t scol = kColS + c * 128;
-        if (warp_live) {
-          uint32_t sr[32];
-          tmem_ld_16x32bx2_x32<32>(tmem + t_lane + scol + hf * 64, sr);
-          tmem_wait_ld();
-          const float* ksc = scal + c * 3 * T + tok0;
-          const float* kbias = ksc + T;
-          const float* vsc = ksc + 2 * T;
-          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          if (tile_full[c]) {
+        float sv[HN];
+        {
+          uint32_t r[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              const float4 a = *reinterpret_cast<const float4*>(ksc + j);
-              const float z0 = __uint_as_float(sr[j]) * a.x, z1 = __uint_as_float(sr[j + 1]) * a.y;
-              const float z2 = __uint_as_float(sr[j + 2]) * a.z, z3 = __uint_as_float(sr[j + 3]) * a.w;
-              sr[j] = __float_as_uint(z0);
-              sr[j + 1] = __float_as_uint(z1);
-              sr[j + 2] = __float_as_uint(z2);
-              sr[j + 3] = __float_as_uint(z3);
-              mx4[0] = fmaxf(mx4[0], z0);
-              mx4[1] = fmaxf(mx4[1], z1);
-              mx4[2] = fmaxf(mx4[2], z2);
-              mx4[3] = fmaxf(mx4[3], z3);
-            }
-          } else {
+          for (int hb = 0; hb < HN; hb += 32) {
+            tmem_ld_32x32b_x32(tmem + t_lane + kColS + c * HN + hb, r);
+            tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              const float4 a = *reinterpret_cast<const float4*>(ksc + j);
-              const float4 bb = *reinterpret_cast<const float4*>(kbias + j);
-              const float z0 = fmaf(__uint_as_float(sr[j]), a.x, bb.x), z1 = fmaf(__uint_as_float(sr[j + 1]), a.y, bb.y);
-              const float z2 = fmaf(__uint_as_float(sr[j + 2]), a.z, bb.z), z3 = fmaf(__uint_as_float(sr[j + 3]), a.w, bb.w);
-              sr[j] = __float_as_uint(z0);
-              sr[j + 1] = __float_as_uint(z1);
-              sr[j + 2] = __float_as_uint(z2);
-              sr[j + 3] = __float_as_uint(z3);
-              mx4[0] = fmaxf(mx4[0], z0);
-              mx4[1] = fmaxf(mx4[1], z1);
-              mx4[2] = fmaxf(mx4[2], z2);
-              mx4[3] = fmaxf(mx4[3], z3);
+            for (int i = 0; i < 32; ++i) sv[hb + i] = __uint_as_float(r[i]);
+          }
+        }
+        const float* sc = scal + ss * 3 * T;
+        const float ks = sc[tok];
+        const bool valid = sc[T + tok] != 0.0f;
+        const float vs = sc[2 * T + tok];
+        // e_h = logit (log2 units) minus the head's reference.
+        float mx = -INFINITY;
+        if (valid) {
+#pragma unroll
+          for (int h = 0; h < HN; h += 4) {
+            const float4 mu = t == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(muse + h);
+            sv[h] = fmaf(sv[h], ks, -mu.x);
+            sv[h + 1] = fmaf(sv[h + 1], ks, -mu.y);
+            sv[h + 2] = fmaf(sv[h + 2], ks, -mu.z);
+            sv[h + 3] = fmaf(sv[h + 3], ks, -mu.w);
+            mx = fmaxf(mx, fmaxf(fmaxf(sv[h], sv[h + 1]), fmaxf(sv[h + 2], sv[h + 3])));
+          }
+        }
+        const bool raise = t == 0 || (valid && mx > kRescaleThreshold);
+        if (bar_red_or(kSoftBar, 32 * kSoftWarps, raise)) {
+          // Some head's reference must rise (always at an item's first tile):
+          // per-head maxima of the tile over the four warps, new references.
+#pragma unroll
+          for (int hb = 0; hb < HN; hb += 32) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = valid ? sv[hb + i] + (t == 0 ? 0.0f : muse[hb + i]) : -INFINITY;
+            wmax[sw * HN + hb + lane] = reduce_scatter32<true>(v, lane);
+          }
+          named_barrier_sync(kSoftBar, 32 * kSoftWarps);
+          if (sw == 0) {
+#pragma unroll
+            for (int hb = 0; hb < HN; hb += 32) {
+              const int h = hb + lane;
+              const float M = fmaxf(fmaxf(wmax[h], wmax[HN + h]), fmaxf(wmax[2 * HN + h], wmax[3 * HN + h]));
+              const float m_old = t == 0 ? -INFINITY : mref[h];
+              const float m_new = M > m_old + kRescaleThreshold ? M : m_old;
+              const float mu_old = t == 0 ? 0.0f : muse[h];
+              const float mu_new = m_new == -INFINITY ? 0.0f : m_new;
+              aref[h] = m_old == -INFINITY ? 0.0f : ex2_approx(m_old - m_new);
+              dref[h] = mu_old - mu_new;
+              mref[h] = m_new;
+              muse[h] = mu_new;
             }
           }
-          float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          // Row maximum over the whole tile: exchange with the other warp of this quarter.
-          float* xg = xch + (g & 1) * 128;
-          if (th == 0) xg[hf * 64 + h] = mx;
-          named_barrier_sync(pair_bar, 64);
-          mx = fmaxf(mx, xg[(1 - hf) * 64 + h]);
-          const bool raise = mx > m_ref + kRescaleThreshold;
-          const float alpha = raise ? ex2_approx(m_ref - mx) : 1.0f;
-          if (t > 0 && __any_sync(0xffffffffu, raise)) {
-            // O holds earlier tiles of this item: wait for the previous PV, then rescale this warp's half.
+          named_barrier_sync(kSoftBar, 32 * kSoftWarps);
+#pragma unroll
+          for (int h = 0; h < HN; ++h) {
+            l[h] *= aref[h];
+            sv[h] += dref[h];
+          }
+          if (t > 0) {
+            // O^T holds earlier tiles of this item: wait for the previous PV, then rescale this warp's channels.
             ok = mbar_wait_abortable(&v_free[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag);
             if (ok) {
               tc_fence_after();
               uint32_t o[32];
-              tmem_ld_16x32bx2_x32<32>(tmem + t_lane + kColO + hf * 64, o);
-              tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-              tmem_st_16x32bx2_x32<32>(tmem + t_lane + kColO + hf * 64, o);
+              for (int hb = 0; hb < HN; hb += 32) {
+                const uint32_t oc = tmem + t_lane + kColO + (item_n & 1) * HN + hb;
+                tmem_ld_32x32b_x32(oc, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * aref[hb + i]);
+                tmem_st_32x32b_x32(oc, o);
+              }
               tmem_wait_st();
             }
           }
-          if (raise) {
-            l_sum *= alpha;
-            m_ref = mx;
-          }
-          const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
-          uint32_t pw[16];
-          float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            const float4 vs = *reinterpret_cast<const float4*>(vsc + j);
-            const float e0 = ex2_approx(__uint_as_float(sr[j]) - m_use);
-            const float e1 = ex2_approx(__uint_as_float(sr[j + 1]) - m_use);
-            const float e2 = ex2_approx(__uint_as_float(sr[j + 2]) - m_use);
-            const float e3 = ex2_approx(__uint_as_float(sr[j + 3]) - m_use);
-            l4[0] += e0;
-            l4[1] += e1;
-            l4[2] += e2;
-            l4[3] += e3;
-            pw[j / 2] = pack_f16x2(e0 * vs.x, e1 * vs.y);
-            pw[j / 2 + 1] = pack_f16x2(e2 * vs.z, e3 * vs.w);
-          }
-          l_sum += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-          // P (fp16 pairs) over the first 64 columns of the S buffer: tokens 2c, 2c+1 in column c.
-          tmem_st_16x32bx2_x16<16>(tmem + t_lane + scol + hf * 32, pw);
-          tmem_wait_st();
         }
+        // P^T[c] is free once PV of tile g-2 is done.
+        if (ok && g >= 2) ok = mbar_wait_abortable(&v_free[c], ((g >> 1) - 1) & 1, abort_flag);
+        if (ok) {
+          // P^T row of this token: heads 8*h8 .. 8*h8+7 at (h8)*2048 + tok*16 (MN-major B operand).
+          uint8_t* dst = pt + c * L::kPTBytes + tok * 16;
+          if (valid) {
+#pragma unroll
+            for (int h8 = 0; h8 < HN; h8 += 8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float p0 = ex2_approx(sv[h8 + 2 * e]), p1 = ex2_approx(sv[h8 + 2 * e + 1]);
+                l[h8 + 2 * e] += p0;
+                l[h8 + 2 * e + 1] += p1;
+                w[e] = pack_f16x2(p0 * vs, p1 * vs);
+              }
+              *reinterpret_cast<uint4*>(dst + (h8 / 8) * 2048) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+#pragma unroll
+            for (int h8 = 0; h8 < HN; h8 += 8)
+              *reinterpret_cast<uint4*>(dst + (h8 / 8) * 2048) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[c]);
+        if (lane == 0) {
+          mbar_arrive(&p_full[c]);
+          mbar_arrive(&scale_free[ss]);
+        }
         if (!ok) break;
       }
       if (!ok) break;
-      // ---- end of item: normalise this thread's 32 channels of its row of O and write them.
-      if (!mbar_wait_abortable(o_full, item_n & 1, abort_flag)) break;
-      tc_fence_after();
-      if (warp_live) {
-        // Row sum over the four threads of the row (two lanes here, two in the other warp).
-        float l_half = l_sum + __shfl_xor_sync(0xffffffffu, l_sum, 16);
-        float* xs = xch + 256;  // [2][64]: the sums, after the two maxima buffers
-        if (th == 0) xs[hf * 64 + h] = l_half;
-        named_barrier_sync(pair_bar, 64);
-        const float l_row = l_half + xs[(1 - hf) * 64 + h];
-        named_barrier_sync(pair_bar, 64);  // both have read before the slots are reused
-        const float inv = l_row > 0.0f ? 1.0f / l_row : 0.0f;
-        uint32_t o[32];
-        tmem_ld_16x32bx2_x32<32>(tmem + t_lane + kColO + hf * 64, o);
-        tmem_wait_ld();
-        if (h < Hq) {
-          const int d0 = hf * 64 + th * 32;
-          float* dst = it.direct ? p.out + ((int64_t)it.b * Hq + h) * kHeadDim + d0
-                                 : p.ws_o + (((int64_t)it.b * p.plan.max_splits + it.split) * Hq + h) * kHeadDim + d0;
+      // ---- end of item: per-head sums over the 128 tokens, then normalise O^T and write it.
+      const int ob = item_n & 1;
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(dst + j) =
-                make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
-                            __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
-          if (th == 0 && hf == 0) {
-            const float lse2 = l_row > 0.0f ? m_ref + __log2f(l_row) : -INFINITY;
+      for (int hb = 0; hb < HN; hb += 32) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = l[hb + i];
+        lpart[sw * HN + hb + lane] = reduce_scatter32<false>(v, lane);
+      }
+      named_barrier_sync(kSoftBar, 32 * kSoftWarps);
+      if (sw == 0) {
+#pragma unroll
+        for (int hb = 0; hb < HN; hb += 32) {
+          const int h = hb + lane;
+          const float Ls = (lpart[h] + lpart[HN + h]) + (lpart[2 * HN + h] + lpart[3 * HN + h]);
+          linv[h] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+          if (h < Hq) {
+            const float lse2 = Ls > 0.0f ? mref[h] + __log2f(Ls) : -INFINITY;
             if (it.direct) {
               if (p.lse_out) p.lse_out[(int64_t)it.b * Hq + h] = lse2 * kLn2;
             } else {
@@ -696,9 +769,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           }
         }
       }
+      named_barrier_sync(kSoftBar, 32 * kSoftWarps);
+      if (!mbar_wait_abortable(&o_full[ob], (item_n >> 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      float* dst = it.direct ? p.out + (int64_t)it.b * Hq * kHeadDim
+                             : p.ws_o + ((int64_t)it.b * p.plan.max_splits + it.split) * Hq * kHeadDim;
+#pragma unroll
+      for (int hb = 0; hb < HN; hb += 32) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tmem + t_lane + kColO + ob * HN + hb, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (hb + i < Hq) dst[(hb + i) * kHeadDim + tok] = __uint_as_float(o[i]) * linv[hb + i];
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(o_empty);
+      if (lane == 0) mbar_arrive(&o_empty[ob]);
       ++item_n;
     }
   }
@@ -742,6 +829,24 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
   if (p.lse_out && lane == 0) p.lse_out[(int64_t)b * Hq + h] = wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
+// The page pool as a 2-D tensor of 128-byte rows (a page of P tokens is
+// page_bytes(P) / 128 consecutive rows: P K-code rows, P V-code rows, then the
+// scale rows); one box is the 2P code rows of a page, landing 128-byte
+// swizzled in shared memory.
+bool encode_pool_map(CUtensorMap* map, const void* pages, int64_t num_pages, int P) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  const int64_t rows = num_pages * (page_bytes(P) / 128);
+  if (rows <= 0 || rows > 2147483647ll) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, (cuuint32_t)(2 * P)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pages), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int num_sms() {
@@ -758,29 +863,38 @@ int num_sms() {
 
 namespace {
 
-template <int P>
-cudaError_t launch_decode_p(const DecodeParams& p, cudaStream_t stream) {
+template <int P, int HN>
+cudaError_t launch_decode_ph(const DecodeParams& p, cudaStream_t stream) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
     // The register split inside the kernel assumes the launch register count.
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<P>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<P, HN>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidDeviceFunction;
-    e = cudaFuncSetAttribute(decode_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(decode_kernel<P, HN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Layout<HN>::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
+  DecodeArgs a;
+  a.p = p;
+  if (!encode_pool_map(&a.kv_map, p.pages, p.num_pages, P)) return cudaErrorInvalidValue;
   const int64_t items = (int64_t)p.batch * p.plan.max_splits;
   const int grid = (int)(items < num_sms() ? items : num_sms());
-  decode_kernel<P><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  decode_kernel<P, HN><<<grid, kThreads, Layout<HN>::kSmemBytes, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.plan.max_splits <= 1) return e;
   const int64_t warps = (int64_t)p.batch * p.num_heads;
   combine_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(p, P);
   return cudaGetLastError();
+}
+
+template <int P>
+cudaError_t launch_decode_p(const DecodeParams& p, cudaStream_t stream) {
+  return p.num_heads <= 32 ? launch_decode_ph<P, 32>(p, stream) : launch_decode_ph<P, 64>(p, stream);
 }
 
 }  // namespace

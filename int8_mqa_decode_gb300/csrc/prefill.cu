@@ -23,11 +23,10 @@
 //     per row) applies the per-key scale, the causal/window mask and the
 //     per-key V scale, and writes P (fp16) back into tensor memory, where it is
 //     the A operand of O += P V (fp16, V from shared memory, MN-major).
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "tma.cuh"
 #include "ptx.cuh"
 
 namespace cai {
@@ -469,23 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // A [rows][128] 16-bit row-major matrix seen as (8 elements, rows, 16 chunks)
 // so that a (8, 128, 16) box lands in shared memory as [chunk][row][8].
 bool encode_rows128(CUtensorMap* map, const void* base, uint64_t rows) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[3] = {8, rows, 16};
   cuuint64_t strides[2] = {kHeadDim * 2, 16};

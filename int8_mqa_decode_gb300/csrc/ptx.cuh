@@ -99,6 +99,17 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst_smem, const void* src_gm
       : "memory");
 }
 
+// 2-D tensor copy (TMA) of one box at element coordinates (x, y), with an L2
+// eviction-priority hint; `map` is a __grid_constant__ CUtensorMap.
+__device__ __forceinline__ void tma_load_2d_hint(void* dst_smem, const void* map, int x, int y, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -244,6 +255,18 @@ __device__ __forceinline__ void tmem_st_16x32bx2_x16(uint32_t taddr, const uint3
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Named barrier over `threads` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
 }
 
 // M=128 accumulators: thread t reads lane (base + t), columns [col, col + 32).
