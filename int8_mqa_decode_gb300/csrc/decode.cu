@@ -85,36 +85,47 @@ struct Layout {
 
 // Warp roles, aligned to warpgroups so each group can resize its register file:
 //   warpgroup 0: producer (warp 0), MMA issuer (warp 1), scheduler (warp 2), idle (warp 3)
-//   warpgroups 1-2: converters (warps 4..11)
-//   warpgroup 3: softmax (warps 12..15, one per TMEM lane quarter)
-constexpr int kThreads = 512;
+//   warpgroups 1-2: converters (warps 4..11, two per TMEM lane quarter)
+//   then softmax: one warp per lane quarter for up to 32 heads (warps 12..15), two
+//   per lane quarter for 64 heads (warps 12..19, each taking half of the heads).
 constexpr int kSchedWarp = 2;
 constexpr int kConvWarp0 = 4;
 constexpr int kConvWarps = 8;
 constexpr int kSoftWarp0 = kConvWarp0 + kConvWarps;
-constexpr int kSoftWarps = 4;
-// Registers per thread: launched with 128 (16 warps, 4 per SM sub-partition:
-// 4 * 32 * 128 = 16384), then 56 / 104 / 232 per warpgroup:
-// 128 * (56 + 2 * 104 + 232) = 63488 <= 512 * 128 = 65536, and per
-// sub-partition 32 * (56 + 2 * 104 + 232) = 15872 <= 16384.
-constexpr int kRegsCtl = 56, kRegsConv = 104, kRegsSoft = 232;
-constexpr int kRegsLaunch = 128;  // checked on the host before the first launch
+template <int HN>
+struct Roles {
+  static constexpr int kSoftWarps = HN <= 32 ? 4 : 8;
+  static constexpr int kThreads = 32 * (kSoftWarp0 + kSoftWarps);
+  // Registers per thread, launched with kRegsLaunch and resized per warpgroup:
+  //  32 heads: 16 warps (4 per SM sub-partition) at 128 = 65536; then 56 / 104 / 232:
+  //            128 * (56 + 2 * 104 + 232) = 63488, per sub-partition 32 * 496 = 15872 <= 16384.
+  //  64 heads: 20 warps (5 per sub-partition) at 96 = 61440; then 48 / 88 / 128:
+  //            128 * (48 + 2 * 88 + 2 * 128) = 61440, per sub-partition 32 * 480 = 15360 <= 16384.
+  static constexpr int kRegsLaunch = HN <= 32 ? 128 : 96;  // checked on the host before the first launch
+  static constexpr int kRegsCtl = HN <= 32 ? 56 : 48;
+  static constexpr int kRegsConv = HN <= 32 ? 104 : 88;
+  static constexpr int kRegsSoft = HN <= 32 ? 232 : 128;
+  static_assert(128 * kRegsCtl + 32 * kConvWarps * kRegsConv + 32 * kSoftWarps * kRegsSoft <= kRegsLaunch * kThreads,
+                "register split");
+  static_assert(32 * (kRegsCtl + 2 * kRegsConv + (kSoftWarps / 4) * kRegsSoft) <= 16384, "sub-partition registers");
+  static_assert((kThreads / 32 + 3) / 4 * 32 * kRegsLaunch <= 16384, "launch registers per sub-partition");
+  static constexpr int kItemReaders = 2 + kConvWarps + kSoftWarps;  // producer, MMA, converters, softmax
+};
 constexpr int kNoPage = -2147483647 - 1;      // a page the tile does not need
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: weights stay <= 2^8 between rescales
-constexpr int kItemReaders = 2 + kConvWarps + kSoftWarps;  // producer, MMA, converters, softmax
 constexpr uint32_t kSoftBar = 1;              // named barrier of the softmax warpgroup
 
 __device__ __forceinline__ void set_err(int32_t* err, int bits) {
   if (err) atomicOr(err, bits);
 }
 
-// Lane `lane` of a warp ends with the reduction over the warp of v[lane]
-// (a reduce-scatter: 31 shuffles for 32 values).  Destroys v.
-template <bool kMax>
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+// Lane `lane` of a warp ends with the reduction over the warp of v[lane % N]
+// (a reduce-scatter: N - 1 shuffles, plus one when N = 16).  Destroys v.
+template <bool kMax, int N>
+__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
+  for (int o = N / 2; o >= 1; o >>= 1) {
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < o; ++i) {
@@ -124,7 +135,13 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
       v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
     }
   }
-  return v[0];
+  float r = v[0];
+#pragma unroll
+  for (int o = 16; o >= N; o >>= 1) {
+    const float x = __shfl_xor_sync(0xffffffffu, r, o);
+    r = kMax ? fmaxf(r, x) : r + x;
+  }
+  return r;
 }
 
 // A work item: one split of one sequence.  kind 0 = tiles to process,
@@ -205,8 +222,10 @@ struct DecodeArgs {
 };
 
 template <int P, int HN>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs args) {
+__global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs args) {
   using L = Layout<HN>;
+  using R = Roles<HN>;
+  constexpr int kSoftWarps = R::kSoftWarps;
   constexpr int NST = L::NST;
   constexpr int PPT = T / P;                   // pages per tile
   constexpr int TPB = 32 / PPT;                // tiles per page-id batch
@@ -215,7 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   constexpr uint32_t kColKA = 0;               // K operand [2]: 64 columns each (fp16 pairs)
   constexpr uint32_t kColS = 128;              // S^T [2]: HN columns each
   constexpr uint32_t kColO = 128 + 2 * HN;     // O^T [2]: HN columns each
-  static_assert(kRegsCtl * 128 + kRegsConv * 256 + kRegsSoft * 128 <= kRegsLaunch * kThreads, "register split");
   static_assert(page_bytes(P) % 128 == 0 && P % 16 == 0, "page rows");
   const DecodeParams& p = args.p;
 
@@ -275,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&item_full[r], 1);
-      mbar_init(&item_empty[r], kItemReaders);
+      mbar_init(&item_empty[r], R::kItemReaders);
     }
     for (int r = 0; r < kScaleSlots; ++r) {
       mbar_init(&scale_full[r], kConvWarps);
@@ -306,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   };
 
   if (warp < kConvWarp0) {
-    setmaxnreg_dec<kRegsCtl>();
+    setmaxnreg_dec<R::kRegsCtl>();
     if (warp == kSchedWarp) {
       // ---------------------------------------------------------- scheduler
       int k = 0;
@@ -407,7 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_s = idesc_f16_f32(T, HN, 0, 0);
       constexpr uint32_t idesc_o = idesc_f16_f32(kHeadDim, HN, 1, 1);
-      const uint32_t v16a = smem_addr(v16), pta = smem_addr(pt), qta = smem_addr(qt);
+      // Descriptor bases; a K step of 16 adds 256 bytes, i.e. 16 to the address field
+      // (shared addresses stay below 2^18, so the 14-bit field never carries).
+      const uint64_t dq = smem_desc(smem_addr(qt), 128, 2048);
+      const uint64_t dv = smem_desc(smem_addr(v16), 128, T * 16);
+      const uint64_t dp = smem_desc(smem_addr(pt), 128, T * 16);
       int g = 0, item_n = 0, k = 0;
       // PV of tile gp of item `item`: O^T[item & 1] (+)= V16 P^T; `first` starts the
       // accumulator, `last` signals the item's epilogue.
@@ -422,9 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         if (lane == 0) {
 #pragma unroll
           for (int ks = 0; ks < T / 16; ++ks)
-            mma_f16_ss(tmem + kColO + ob * HN, smem_desc(v16a + c * kOp16Bytes + ks * 256, 128, T * 16),
-                       smem_desc(pta + c * L::kPTBytes + ks * 256, 128, T * 16), idesc_o,
-                       (!first || ks > 0) ? 1u : 0u);
+            mma_f16_ss(tmem + kColO + ob * HN, dv + (uint64_t)(c * (kOp16Bytes >> 4) + ks * 16),
+                       dp + (uint64_t)(c * (L::kPTBytes >> 4) + ks * 16), idesc_o, (!first || ks > 0) ? 1u : 0u);
           mma_commit(&v_free[c]);
           if (last) mma_commit(&o_full[ob]);
         }
@@ -449,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           if (lane == 0) {
 #pragma unroll
             for (int ks = 0; ks < kHeadDim / 16; ++ks)
-              mma_f16_ts(tmem + kColS + c * HN, tmem + kColKA + c * 64 + ks * 8, smem_desc(qta + ks * 256, 128, 2048),
-                         idesc_s, ks > 0 ? 1u : 0u);
+              mma_f16_ts(tmem + kColS + c * HN, tmem + kColKA + c * 64 + ks * 8, dq + (uint64_t)(ks * 16), idesc_s,
+                         ks > 0 ? 1u : 0u);
             mma_commit(&s_full[c]);
           }
           __syncwarp();
@@ -467,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
     }
   } else if (warp < kSoftWarp0) {
-    setmaxnreg_dec<kRegsConv>();
+    setmaxnreg_dec<R::kRegsConv>();
     // ------------------------------------------------------------ converters
     const int ctid = tid - kConvWarp0 * 32;           // 0 .. 255
     const int quarter = warp & 3;                     // TMEM lanes this warp may touch
@@ -560,17 +581,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         if (g >= 2) ok = mbar_wait_abortable(&s_full[c], ((g >> 1) - 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        {
-          uint32_t kw[32];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t xs[4] = {wk[i].x, wk[i].y, wk[i].z, wk[i].w};
+        for (int half = 0; half < 2; ++half) {
+          uint32_t kw[16];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const uint4 w = wk[half * 2 + i];
+            const uint32_t xs[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) i8x4_to_f16x4(xs[e], kw[(i * 4 + e) * 2], kw[(i * 4 + e) * 2 + 1]);
           }
-          tmem_st_32x32b_x32(tmem + t_lane + kColKA + c * 64 + hh * 32, kw);
-          tmem_wait_st();
+          tmem_st_32x32b_x16(tmem + t_lane + kColKA + c * 64 + hh * 32 + half * 16, kw);
         }
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&k_full[c]);
@@ -599,12 +622,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
     }
   } else {
-    setmaxnreg_inc<kRegsSoft>();
+    setmaxnreg_inc<R::kRegsSoft>();
     // ------------------------------------------------------------ softmax + epilogue
-    // Thread = token tok of each tile (TMEM lane of S^T) and channel tok of O^T.
-    const int sw = warp - kSoftWarp0;                 // lane quarter
-    const int tok = sw * 32 + lane;
-    const uint32_t t_lane = (uint32_t)(sw * 32) << 16;
+    // Thread = token tok of each tile (TMEM lane of S^T) and channel tok of O^T;
+    // warp half hp takes heads [hp * HH, hp * HH + HH).
+    constexpr int HH = HN / (kSoftWarps / 4);
+    constexpr uint32_t kSoftThreads = 32 * kSoftWarps;
+    const int sw = warp - kSoftWarp0;
+    const int quarter = warp & 3;
+    const int hp = sw >> 2;
+    const int h0 = hp * HH;
+    const int tok = quarter * 32 + lane;
+    const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
     int g = 0, item_n = 0, k = 0;
     bool ok = true;
     while (ok) {
@@ -614,14 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       if (it.kind == 1) {
         // Nothing to attend (L = 0) or an invalid length: out = 0, lse = -inf.
         if (it.invalid && sw == 0 && lane == 0) set_err(p.err, CAI_DEVERR_LENGTH);
-        for (int h = 0; h < Hq; ++h) p.out[((int64_t)it.b * Hq + h) * kHeadDim + tok] = 0.0f;
-        if (p.lse_out && sw == 0)
-          for (int h = lane; h < Hq; h += 32) p.lse_out[(int64_t)it.b * Hq + h] = -INFINITY;
+        for (int h = h0; h < h0 + HH && h < Hq; ++h) p.out[((int64_t)it.b * Hq + h) * kHeadDim + tok] = 0.0f;
+        if (p.lse_out && quarter == 0 && lane < HH && h0 + lane < Hq)
+          p.lse_out[(int64_t)it.b * Hq + h0 + lane] = -INFINITY;
         continue;
       }
-      float l[HN];
+      float l[HH];
 #pragma unroll
-      for (int h = 0; h < HN; ++h) l[h] = 0.0f;
+      for (int h = 0; h < HH; ++h) l[h] = 0.0f;
       for (int t = 0; t < it.ntiles; ++t, ++g) {
         const int c = g & 1;
         const int ss = g & (kScaleSlots - 1);
@@ -629,16 +658,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
              mbar_wait_abortable(&scale_full[ss], (g / kScaleSlots) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        float sv[HN];
+        float sv[HH];
         {
-          uint32_t r[32];
+          uint32_t r[HH];
+          if constexpr (HH == 32) tmem_ld_32x32b_x32(tmem + t_lane + kColS + c * HN + h0, r);
+          else tmem_ld_32x32b_x16(tmem + t_lane + kColS + c * HN + h0, r);
+          tmem_wait_ld();
 #pragma unroll
-          for (int hb = 0; hb < HN; hb += 32) {
-            tmem_ld_32x32b_x32(tmem + t_lane + kColS + c * HN + hb, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) sv[hb + i] = __uint_as_float(r[i]);
-          }
+          for (int i = 0; i < HH; ++i) sv[i] = __uint_as_float(r[i]);
         }
         const float* sc = scal + ss * 3 * T;
         const float ks = sc[tok];
@@ -648,63 +675,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         float mx = -INFINITY;
         if (valid) {
 #pragma unroll
-          for (int h = 0; h < HN; h += 4) {
-            const float4 mu = t == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(muse + h);
+          for (int h = 0; h < HH; h += 4) {
+            const float4 mu = t == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(muse + h0 + h);
             sv[h] = fmaf(sv[h], ks, -mu.x);
             sv[h + 1] = fmaf(sv[h + 1], ks, -mu.y);
             sv[h + 2] = fmaf(sv[h + 2], ks, -mu.z);
             sv[h + 3] = fmaf(sv[h + 3], ks, -mu.w);
-            mx = fmaxf(mx, fmaxf(fmaxf(sv[h], sv[h + 1]), fmaxf(sv[h + 2], sv[h + 3])));
+            mx = fmax3(mx, fmax3(sv[h], sv[h + 1], sv[h + 2]), sv[h + 3]);
           }
         }
         const bool raise = t == 0 || (valid && mx > kRescaleThreshold);
-        if (bar_red_or(kSoftBar, 32 * kSoftWarps, raise)) {
+        if (bar_red_or(kSoftBar, kSoftThreads, raise)) {
           // Some head's reference must rise (always at an item's first tile):
-          // per-head maxima of the tile over the four warps, new references.
+          // per-head maxima of the tile over the four lane quarters, new references.
+          {
+            float v[HH];
 #pragma unroll
-          for (int hb = 0; hb < HN; hb += 32) {
-            float v[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = valid ? sv[hb + i] + (t == 0 ? 0.0f : muse[hb + i]) : -INFINITY;
-            wmax[sw * HN + hb + lane] = reduce_scatter32<true>(v, lane);
+            for (int i = 0; i < HH; ++i) v[i] = valid ? sv[i] + (t == 0 ? 0.0f : muse[h0 + i]) : -INFINITY;
+            const float wm = reduce_scatter<true, HH>(v, lane);
+            if (lane < HH) wmax[quarter * HN + h0 + lane] = wm;
           }
-          named_barrier_sync(kSoftBar, 32 * kSoftWarps);
-          if (sw == 0) {
-#pragma unroll
-            for (int hb = 0; hb < HN; hb += 32) {
-              const int h = hb + lane;
-              const float M = fmaxf(fmaxf(wmax[h], wmax[HN + h]), fmaxf(wmax[2 * HN + h], wmax[3 * HN + h]));
-              const float m_old = t == 0 ? -INFINITY : mref[h];
-              const float m_new = M > m_old + kRescaleThreshold ? M : m_old;
-              const float mu_old = t == 0 ? 0.0f : muse[h];
-              const float mu_new = m_new == -INFINITY ? 0.0f : m_new;
-              aref[h] = m_old == -INFINITY ? 0.0f : ex2_approx(m_old - m_new);
-              dref[h] = mu_old - mu_new;
-              mref[h] = m_new;
-              muse[h] = mu_new;
-            }
+          named_barrier_sync(kSoftBar, kSoftThreads);
+          if (quarter == 0 && lane < HH) {
+            const int h = h0 + lane;
+            const float M = fmaxf(fmaxf(wmax[h], wmax[HN + h]), fmaxf(wmax[2 * HN + h], wmax[3 * HN + h]));
+            const float m_old = t == 0 ? -INFINITY : mref[h];
+            const float m_new = M > m_old + kRescaleThreshold ? M : m_old;
+            const float mu_old = t == 0 ? 0.0f : muse[h];
+            const float mu_new = m_new == -INFINITY ? 0.0f : m_new;
+            aref[h] = m_old == -INFINITY ? 0.0f : ex2_approx(m_old - m_new);
+            dref[h] = mu_old - mu_new;
+            mref[h] = m_new;
+            muse[h] = mu_new;
           }
-          named_barrier_sync(kSoftBar, 32 * kSoftWarps);
+          named_barrier_sync(kSoftBar, kSoftThreads);
 #pragma unroll
-          for (int h = 0; h < HN; ++h) {
-            l[h] *= aref[h];
-            sv[h] += dref[h];
+          for (int h = 0; h < HH; ++h) {
+            l[h] *= aref[h0 + h];
+            sv[h] += dref[h0 + h];
           }
           if (t > 0) {
-            // O^T holds earlier tiles of this item: wait for the previous PV, then rescale this warp's channels.
+            // O^T holds earlier tiles of this item: wait for the previous PV, then rescale this thread's entries.
             ok = mbar_wait_abortable(&v_free[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag);
             if (ok) {
               tc_fence_after();
-              uint32_t o[32];
+              uint32_t o[HH];
+              const uint32_t oc = tmem + t_lane + kColO + (item_n & 1) * HN + h0;
+              if constexpr (HH == 32) tmem_ld_32x32b_x32(oc, o);
+              else tmem_ld_32x32b_x16(oc, o);
+              tmem_wait_ld();
 #pragma unroll
-              for (int hb = 0; hb < HN; hb += 32) {
-                const uint32_t oc = tmem + t_lane + kColO + (item_n & 1) * HN + hb;
-                tmem_ld_32x32b_x32(oc, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * aref[hb + i]);
-                tmem_st_32x32b_x32(oc, o);
-              }
+              for (int i = 0; i < HH; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * aref[h0 + i]);
+              if constexpr (HH == 32) tmem_st_32x32b_x32(oc, o);
+              else tmem_st_32x32b_x16(oc, o);
               tmem_wait_st();
             }
           }
@@ -712,11 +735,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         // P^T[c] is free once PV of tile g-2 is done.
         if (ok && g >= 2) ok = mbar_wait_abortable(&v_free[c], ((g >> 1) - 1) & 1, abort_flag);
         if (ok) {
-          // P^T row of this token: heads 8*h8 .. 8*h8+7 at (h8)*2048 + tok*16 (MN-major B operand).
-          uint8_t* dst = pt + c * L::kPTBytes + tok * 16;
+          // P^T row of this token: heads 8i .. 8i+7 at i*2048 + tok*16 (MN-major B operand).
+          uint8_t* dst = pt + c * L::kPTBytes + (h0 / 8) * 2048 + tok * 16;
           if (valid) {
 #pragma unroll
-            for (int h8 = 0; h8 < HN; h8 += 8) {
+            for (int h8 = 0; h8 < HH; h8 += 8) {
               uint32_t w[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -729,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             }
           } else {
 #pragma unroll
-            for (int h8 = 0; h8 < HN; h8 += 8)
+            for (int h8 = 0; h8 < HH; h8 += 8)
               *reinterpret_cast<uint4*>(dst + (h8 / 8) * 2048) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
@@ -745,43 +768,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       if (!ok) break;
       // ---- end of item: per-head sums over the 128 tokens, then normalise O^T and write it.
       const int ob = item_n & 1;
+      {
+        float v[HH];
 #pragma unroll
-      for (int hb = 0; hb < HN; hb += 32) {
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = l[hb + i];
-        lpart[sw * HN + hb + lane] = reduce_scatter32<false>(v, lane);
+        for (int i = 0; i < HH; ++i) v[i] = l[i];
+        const float ls = reduce_scatter<false, HH>(v, lane);
+        if (lane < HH) lpart[quarter * HN + h0 + lane] = ls;
       }
-      named_barrier_sync(kSoftBar, 32 * kSoftWarps);
-      if (sw == 0) {
-#pragma unroll
-        for (int hb = 0; hb < HN; hb += 32) {
-          const int h = hb + lane;
-          const float Ls = (lpart[h] + lpart[HN + h]) + (lpart[2 * HN + h] + lpart[3 * HN + h]);
-          linv[h] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
-          if (h < Hq) {
-            const float lse2 = Ls > 0.0f ? mref[h] + __log2f(Ls) : -INFINITY;
-            if (it.direct) {
-              if (p.lse_out) p.lse_out[(int64_t)it.b * Hq + h] = lse2 * kLn2;
-            } else {
-              p.ws_lse[((int64_t)it.b * p.plan.max_splits + it.split) * Hq + h] = lse2;
-            }
+      named_barrier_sync(kSoftBar, kSoftThreads);
+      if (quarter == 0 && lane < HH) {
+        const int h = h0 + lane;
+        const float Ls = (lpart[h] + lpart[HN + h]) + (lpart[2 * HN + h] + lpart[3 * HN + h]);
+        linv[h] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+        if (h < Hq) {
+          const float lse2 = Ls > 0.0f ? mref[h] + __log2f(Ls) : -INFINITY;
+          if (it.direct) {
+            if (p.lse_out) p.lse_out[(int64_t)it.b * Hq + h] = lse2 * kLn2;
+          } else {
+            p.ws_lse[((int64_t)it.b * p.plan.max_splits + it.split) * Hq + h] = lse2;
           }
         }
       }
-      named_barrier_sync(kSoftBar, 32 * kSoftWarps);
+      named_barrier_sync(kSoftBar, kSoftThreads);
       if (!mbar_wait_abortable(&o_full[ob], (item_n >> 1) & 1, abort_flag)) break;
       tc_fence_after();
-      float* dst = it.direct ? p.out + (int64_t)it.b * Hq * kHeadDim
-                             : p.ws_o + ((int64_t)it.b * p.plan.max_splits + it.split) * Hq * kHeadDim;
-#pragma unroll
-      for (int hb = 0; hb < HN; hb += 32) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(tmem + t_lane + kColO + ob * HN + hb, o);
+      {
+        float* dst = it.direct ? p.out + (int64_t)it.b * Hq * kHeadDim
+                               : p.ws_o + ((int64_t)it.b * p.plan.max_splits + it.split) * Hq * kHeadDim;
+        uint32_t o[HH];
+        const uint32_t oc = tmem + t_lane + kColO + ob * HN + h0;
+        if constexpr (HH == 32) tmem_ld_32x32b_x32(oc, o);
+        else tmem_ld_32x32b_x16(oc, o);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (hb + i < Hq) dst[(hb + i) * kHeadDim + tok] = __uint_as_float(o[i]) * linv[hb + i];
+        for (int i = 0; i < HH; ++i)
+          if (h0 + i < Hq) dst[(h0 + i) * kHeadDim + tok] = __uint_as_float(o[i]) * linv[h0 + i];
       }
       tc_fence_before();
       __syncwarp();
@@ -873,7 +894,7 @@ cudaError_t launch_decode_ph(const DecodeParams& p, cudaStream_t stream) {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<P, HN>);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidDeviceFunction;
+    if (fa.numRegs != Roles<HN>::kRegsLaunch) return cudaErrorInvalidDeviceFunction;
     e = cudaFuncSetAttribute(decode_kernel<P, HN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Layout<HN>::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -884,7 +905,7 @@ cudaError_t launch_decode_ph(const DecodeParams& p, cudaStream_t stream) {
   if (!encode_pool_map(&a.kv_map, p.pages, p.num_pages, P)) return cudaErrorInvalidValue;
   const int64_t items = (int64_t)p.batch * p.plan.max_splits;
   const int grid = (int)(items < num_sms() ? items : num_sms());
-  decode_kernel<P, HN><<<grid, kThreads, Layout<HN>::kSmemBytes, stream>>>(a);
+  decode_kernel<P, HN><<<grid, Roles<HN>::kThreads, Layout<HN>::kSmemBytes, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.plan.max_splits <= 1) return e;
   const int64_t warps = (int64_t)p.batch * p.num_heads;
