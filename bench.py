@@ -160,7 +160,8 @@ def measured_peaks():
 
 
 def profiled_traffic(workload_tag: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it matches the current kernel."""
+    """DRAM bytes (read + write) of one step's decode launches from the committed ncu summary, if it
+    matches the current kernel source and this workload; the same unit as roofline.achieved."""
     path = os.path.join(ROOT, "profiles", "decode_dram_traffic.txt")
     src = os.path.join(ROOT, "int8_mqa_decode_gb300", "csrc", "decode.cu")
     if not os.path.exists(path):
@@ -174,7 +175,7 @@ def profiled_traffic(workload_tag: str):
     if info.get("decode_cu_sha256") != sha or info.get("workload") != workload_tag:
         return None
     try:
-        return float(info["dram_bytes_per_decode_launch"])
+        return float(info["dram_bytes_per_step"])
     except (KeyError, ValueError):
         return None
 
