@@ -25,6 +25,7 @@ import subprocess
 import sys
 import threading
 import time
+import time
 
 import numpy as np
 
@@ -39,7 +40,7 @@ BYTES_PER_TOKEN = 2 * 128 + 8  # int8 K + int8 V + two fp32 scales
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cai", choices=["cai", "reference"])
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
@@ -93,7 +94,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []          # (wall time, csv line)
+        self.t_start = None
+        self.t_end = None
 
     def __enter__(self):
         try:
@@ -102,13 +105,25 @@ class ClockSampler:
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            # sampling must be running before the timed region opens
+            deadline = time.time() + 5.0
+            while not self.lines and time.time() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def start(self):
+        self.t_start = time.time()
+
+    def stop(self):
+        self.t_end = time.time()
+        if self.proc is not None:  # one more sample period so the last stretch is covered
+            time.sleep(0.06)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -120,9 +135,16 @@ class ClockSampler:
         return False
 
     def summary(self):
+        """Median SM clock and the throttle reasons seen during the timed region [start, stop]
+        (the nearest earlier sample when the region is shorter than one sample period)."""
+        lines = self.lines
+        if self.t_start is not None and self.t_end is not None:
+            inside = [x for x in lines if self.t_start <= x[0] <= self.t_end + 0.06]
+            before = [x for x in lines if x[0] < self.t_start]
+            lines = inside if inside else before[-1:]
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for _, line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 7:
                 continue
@@ -290,11 +312,13 @@ def run_prefill(args, rank, world):
         torch.cuda.synchronize()
         if args.ncu:
             torch.cuda.profiler.start()
+        clocks.start()
         t0.record(stream)
         for s in range(args.steps):
             step(ev[s])
         t1.record(stream)
         torch.cuda.synchronize()
+        clocks.stop()
         if args.ncu:
             torch.cuda.profiler.stop()
     ms = allreduce_max(t0.elapsed_time(t1), world)
@@ -368,11 +392,13 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
         if args.ncu:
             torch.cuda.profiler.start()
+        clocks.start()
         t_start.record(stream)
         for s in range(args.steps):
             step(ev[s])
         t_end.record(stream)
         torch.cuda.synchronize()
+        clocks.stop()
         if args.ncu:
             torch.cuda.profiler.stop()
     ms_total = t_start.elapsed_time(t_end)
