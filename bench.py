@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (testing only)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--local-ring", action="store_true",
+                    help="keep each sequence of a local-only KV buffer in a ring of pages (window recycling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ncu", action="store_true",
@@ -354,7 +356,7 @@ def run_gpu(args, rank, world):
     __graft_entry__.build()
     seed = (1000 + args.config) + 100 * rank
     w = synth.workload(args.config, seed=seed, sigma=args.sigma, batch=args.batch)
-    cache = harness.PagedCache(w)
+    cache = harness.PagedCache(w, local_ring=args.local_ring)
     cache.fill()
     nl = len(w.layer_windows)
     qs = [cache.decode_q(layer) for layer in range(nl)]
@@ -368,12 +370,13 @@ def run_gpu(args, rank, world):
     def step(record=None):
         for buf, pool in enumerate(cache.pools):
             k, v, start = step_kv[buf]
-            cai.cai_kv_append(pool, k, v, cache.table, start)
+            cai.cai_kv_append(pool, k, v, cache.tables[buf], start)
         for layer in range(nl):
             if record is not None:
                 record[2 * layer].record(stream)
-            cai.cai_mqa_decode(cache.pools, w.layer_to_buffer, layer, qs[layer], cache.table, cache.ctx_len,
-                               w.layer_windows[layer], w.softmax_scale, args.num_splits, wss[layer], outs[layer])
+            cai.cai_mqa_decode(cache.pools, w.layer_to_buffer, layer, qs[layer], cache.tables[w.layer_to_buffer[layer]],
+                               cache.ctx_len, w.layer_windows[layer], w.softmax_scale, args.num_splits, wss[layer],
+                               outs[layer])
             if record is not None:
                 record[2 * layer + 1].record(stream)
 
@@ -424,7 +427,9 @@ def run_gpu(args, rank, world):
         "config": {"workload": w.name, "global_batch": w.batch * world, "seq_len": "lognormal" if args.config == 3
                    else "uniform", "kv_tokens_per_step": toks_step, "num_splits": args.num_splits or "auto",
                    "l2": "KV read per step larger than L2 (129 MB); KV loads are L2 evict-first",
-                   "parallelism": f"replicas x{world} (independent sequences per GPU)"},
+                   "parallelism": f"replicas x{world} (independent sequences per GPU)",
+                   "kv_pool_bytes": cache.pool_bytes(),
+                   **({"local_ring_pages": [r for r in cache.ring if r]} if args.local_ring else {})},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind,
@@ -465,10 +470,11 @@ def run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world):
             dq.copy_(hq, non_blocking=True)
         for buf, pool in enumerate(cache.pools):
             dk, dv, ds = d_kv[buf]
-            cai.cai_kv_append(pool, dk, dv, cache.table, ds)
+            cai.cai_kv_append(pool, dk, dv, cache.tables[buf], ds)
         for layer in range(nl):
-            cai.cai_mqa_decode(cache.pools, w.layer_to_buffer, layer, d_q[layer], cache.table, cache.ctx_len,
-                               w.layer_windows[layer], w.softmax_scale, args.num_splits, wss[layer], outs[layer])
+            cai.cai_mqa_decode(cache.pools, w.layer_to_buffer, layer, d_q[layer], cache.tables[w.layer_to_buffer[layer]],
+                               cache.ctx_len, w.layer_windows[layer], w.softmax_scale, args.num_splits, wss[layer],
+                               outs[layer])
             h_out[layer].copy_(outs[layer], non_blocking=True)
 
     for _ in range(3):

@@ -220,6 +220,32 @@ cai_status cai_host_cache_store(cai_host_cache* cache, const int32_t* tokens, in
 void cai_host_cache_stats(cai_host_cache* cache, int64_t* hits, int64_t* misses, int64_t* pages_cached,
                           int64_t* evictions);
 
+/* ---- Local-window page recycling.
+ * A local layer attends only the last `window` positions ("Character.AI: inference
+ * optimization", section 03, hybrid attention with a 1024-token horizon), so a buffer
+ * read only by local layers needs to keep just the pages of that window.  It can hold
+ * each sequence in a ring of pages: logical page k of the sequence lives in ring slot
+ * k % ring.  The kernels read no page outside the call's own range: decode reads the
+ * pages of [ctx_len - window, ctx_len), prefill those of
+ * [max(0, prefix + 1 - window), prefix + n_new), append those it writes.  (The pages
+ * describe the horizon but not how freed memory is reused; this ring is that reuse.) */
+
+/* Ring length (pages per sequence) for a local buffer read with `window` and written at
+ * most `max_new_tokens` positions per call (1 for decode, the chunk length for prefill):
+ * ceil((window + max_new_tokens - 1) / page_size) + 1.  0 for invalid arguments
+ * (window < 1, max_new_tokens < 1, page_size < 1). */
+int32_t cai_ring_pages(int32_t window, int32_t page_size, int32_t max_new_tokens);
+
+/* Fill one host block-table row for a sequence whose positions [0, hi) are written
+ * (hi includes the tokens of the coming call): the last `ring` pages before
+ * ceil(hi / page_size) map to ring_ids[k % ring]; every other entry is -1, so that a
+ * kernel reading a freed or unwritten page sets CAI_DEVERR_PAGE instead of reading
+ * another position's data.  row: host int32 [max_pages_per_seq]; ring_ids: host int32
+ * [ring], distinct page ids of the buffer's pool.  Returns CAI_ERR_INVALID_ARG for null
+ * pointers, ring < 1, page_size < 1, hi < 0 or ceil(hi / page_size) > max_pages_per_seq. */
+cai_status cai_ring_table_row(int32_t* row, int32_t max_pages_per_seq, const int32_t* ring_ids, int32_t ring,
+                              int32_t hi, int32_t page_size);
+
 /* The CUDA runtime's description of the error behind the last CAI_ERR_CUDA returned on
  * this thread ("no error" if none). */
 const char* cai_last_cuda_error(void);

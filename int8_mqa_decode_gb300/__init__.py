@@ -13,6 +13,7 @@ import ctypes
 import os
 from typing import Optional, Sequence
 
+import numpy as np
 import torch
 
 __all__ = [
@@ -22,7 +23,7 @@ __all__ = [
     "cai_mqa_prefill_chunk",
     "CAI_DEVERR_PAGE", "CAI_DEVERR_LENGTH", "CAI_DEVERR_TIMEOUT", "HEAD_DIM", "cai_host_cache_create",
     "cai_host_cache_destroy", "cai_host_cache_match", "cai_host_cache_restore", "cai_host_cache_store",
-    "cai_host_cache_stats",
+    "cai_host_cache_stats", "cai_ring_pages", "cai_ring_table_row",
 ]
 
 HEAD_DIM = 128
@@ -101,6 +102,10 @@ def load():
     i64p = ctypes.POINTER(ctypes.c_int64)
     lib.cai_host_cache_stats.argtypes = [vp, i64p, i64p, i64p, i64p]
     lib.cai_host_cache_stats.restype = None
+    lib.cai_ring_pages.argtypes = [i32, i32, i32]
+    lib.cai_ring_pages.restype = i32
+    lib.cai_ring_table_row.argtypes = [vp, i32, vp, i32, i32, i32]
+    lib.cai_ring_table_row.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -244,7 +249,6 @@ def cai_mqa_prefill_chunk(pool: KVPool, q: torch.Tensor, block_table: torch.Tens
 # ----------------------------------------------------------------------------- cross-turn host KV cache
 
 def _i32_host(a) -> "ctypes.Array":
-    import numpy as np
     a = np.ascontiguousarray(a, dtype=np.int32)
     return a, a.ctypes.data_as(ctypes.c_void_p)
 
@@ -292,3 +296,18 @@ def cai_host_cache_stats(cache: int) -> dict:
     v = [ctypes.c_int64() for _ in range(4)]
     load().cai_host_cache_stats(cache, *[ctypes.byref(x) for x in v])
     return dict(zip(("hits", "misses", "pages_cached", "evictions"), (x.value for x in v)))
+
+
+def cai_ring_pages(window: int, page_size: int, max_new_tokens: int = 1) -> int:
+    """Pages per sequence of a local buffer's ring (0 for invalid arguments)."""
+    return int(load().cai_ring_pages(window, page_size, max_new_tokens))
+
+
+def cai_ring_table_row(ring_ids, hi: int, page_size: int, max_pages_per_seq: int) -> np.ndarray:
+    """One block-table row (host int32 [max_pages_per_seq]) mapping the live pages of a
+    sequence written up to `hi` into its ring; freed and unwritten entries are -1."""
+    ids = np.ascontiguousarray(np.asarray(ring_ids, dtype=np.int32))
+    row = np.empty(max_pages_per_seq, dtype=np.int32)
+    st = load().cai_ring_table_row(row.ctypes.data, max_pages_per_seq, ids.ctypes.data, len(ids), hi, page_size)
+    _check(st, "cai_ring_table_row")
+    return row

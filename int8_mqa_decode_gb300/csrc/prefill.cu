@@ -94,13 +94,14 @@ __global__ void __launch_bounds__(256) dequant_kernel(const PrefillParams p) {
   }
   const int len = p0 + p.n_new;
   if (t >= ((len + kKeys - 1) / kKeys) * kKeys) return;  // never read
-  if (p.window > 0) {
-    const int lo_min = max(0, p0 + 1 - p.window);
-    if (t < (lo_min / kKeys) * kKeys) return;  // before every window
-  }
+  // Keys before every window of the chunk are never attended: rows of their tile get
+  // zeros (masked later) and their pages are not read, so a local buffer may have
+  // recycled them.
+  const int lo_min = p.window > 0 ? max(0, p0 + 1 - p.window) : 0;
+  if (t < (lo_min / kKeys) * kKeys) return;  // before every window, whole tile
   uint32_t kw = 0, vw = 0;
   float ksc = 0.0f, vsc = 0.0f;
-  if (t < len) {
+  if (t < len && t >= lo_min) {
     const int P = p.page_size;
     const int32_t page = p.table[(int64_t)b * p.max_pages + t / P];
     if (page >= 0 && page < p.num_pages) {
