@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (testing only)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--mixed", action="store_true",
+                    help="continuous batching: 128 decode steps + 8 prefill chunks of 256 tokens in one launch")
     ap.add_argument("--local-ring", action="store_true",
                     help="keep each sequence of a local-only KV buffer in a ring of pages (window recycling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
@@ -343,6 +345,95 @@ def run_prefill(args, rank, world):
     }
 
 
+# ----------------------------------------------------------------------------- GPU arm: mixed batch
+
+def run_mixed(args, rank, world):
+    """Continuous batching: one varlen launch over 128 one-token decode steps (contexts
+    U[1024, 8192]) and 8 prefill chunks of 256 tokens on 4096-token prefixes, against the
+    same work as a decode launch plus a prefill launch."""
+    import torch
+    import harness
+    import int8_mqa_decode_gb300 as cai
+    import synth
+    import synth.gpu as sgpu
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    import __graft_entry__
+    __graft_entry__.build()
+    seed = 1006 + 100 * rank
+    n_dec, n_pf, chunk, Hq, P = 128, 8, 256, 32, 16
+    dec_len = synth.uniform_int(seed, 3, n_dec, 1024, 8192)
+    prefix = np.concatenate([dec_len - 1, np.full(n_pf, 4096)]).astype(np.int64)
+    n_new = np.concatenate([np.ones(n_dec), np.full(n_pf, chunk)]).astype(np.int64)
+    L = prefix + n_new
+    B = n_dec + n_pf
+    w = synth.Workload("mixed", B, Hq, P, L, [0], [0], n_new=1, seed=seed)
+    cache = harness.PagedCache(w)
+    cache.fill(upto=L)
+    off = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
+    total = int(off[-1])
+    q = torch.empty(total, Hq, 128, dtype=torch.bfloat16, device="cuda")
+    for b in range(B):
+        qb = torch.empty(1, int(n_new[b]) * Hq, 128, dtype=torch.bfloat16, device="cuda")
+        sgpu.q_rows(qb, seed, synth.STREAM_Q_PREFILL, b)
+        q[off[b]:off[b + 1]] = qb.view(int(n_new[b]), Hq, 128)
+    out = torch.empty(total, Hq, 128, device="cuda")
+    off_d = torch.from_numpy(off).cuda()
+    prefix_d = torch.from_numpy(prefix.astype(np.int32)).cuda()
+    ws = cache.prefill_workspace()
+    # the same work split: decode launch over the one-token sequences, prefill launch over the chunks
+    q_dec = q[:n_dec]
+    out_dec = torch.empty(n_dec, Hq, 128, device="cuda")
+    ctx_dec = torch.from_numpy(L[:n_dec].astype(np.int32)).cuda()
+    table_dec, table_pf = cache.table[:n_dec].contiguous(), cache.table[n_dec:].contiguous()
+    ws_dec = torch.zeros(cai.cai_mqa_decode_workspace_size(n_dec, Hq, cache.max_pages_per_seq, P, 0, 0),
+                         dtype=torch.uint8, device="cuda")
+    q_pf = q[n_dec:].view(n_pf, chunk, Hq, 128)
+    out_pf = torch.empty(n_pf, chunk, Hq, 128, device="cuda")
+    prefix_pf = prefix_d[n_dec:].contiguous()
+    ws_pf = torch.empty(cai.cai_mqa_prefill_workspace_size(n_pf, cache.max_pages_per_seq, P), dtype=torch.uint8,
+                        device="cuda")
+
+    def one_launch():
+        cai.cai_mqa_prefill_varlen(cache.pools[0], q, off_d, chunk, cache.table, prefix_d, 0, w.softmax_scale, ws, out)
+
+    def two_launches():
+        cai.cai_mqa_decode(cache.pools, [0], 0, q_dec, table_dec, ctx_dec, 0, w.softmax_scale, 0, ws_dec, out_dec)
+        cai.cai_mqa_prefill_chunk(cache.pools[0], q_pf, table_pf, prefix_pf, 0, w.softmax_scale, ws_pf, out_pf)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(smi_index(torch.cuda.current_device())) as clocks:
+            torch.cuda.synchronize()
+            clocks.start()
+            t0.record()
+            for _ in range(args.steps):
+                fn()
+            t1.record()
+            torch.cuda.synchronize()
+            clocks.stop()
+        return allreduce_max(t0.elapsed_time(t1), world) / args.steps, clocks.summary()
+
+    ms_one, clocks = timed(one_launch)
+    ms_two, _ = timed(two_launches)
+    torch.cuda.synchronize()
+    diff = float((out[:n_dec] - out_dec).abs().max())
+    pairs = float(np.sum(n_new * prefix + n_new * (n_new + 1) / 2)) * Hq  # (query row, attended key) pairs
+    return {
+        "metric": "continuous-batching step: new tokens/s (128 decode steps + 8 prefill chunks, one launch)",
+        "value": world * total / (ms_one * 1e-3), "unit": "new tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_one, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8 KV, bf16 QK / fp16 PV, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": f"mixed: {n_dec} decode (L~U[1024,8192]) + {n_pf} chunks of {chunk} on 4096, Hq={Hq}, "
+                               f"P={P}", "new_tokens": total, "kv_query_pairs": pairs},
+        "two_launch_ms_per_step": ms_two, "decode_rows_max_abs_diff_vs_decode_path": diff,
+        "tflops": 4 * 128 * pairs / (ms_one * 1e-3) / 1e12, "gpu_launches": 2 * args.steps, "clocks": clocks,
+    }
+
+
 # ----------------------------------------------------------------------------- GPU arm: decode
 
 def run_gpu(args, rank, world):
@@ -554,7 +645,10 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return
-    res = run_prefill(args, rank, world) if args.config == 4 else run_gpu(args, rank, world)
+    if args.mixed:
+        res = run_mixed(args, rank, world)
+    else:
+        res = run_prefill(args, rank, world) if args.config == 4 else run_gpu(args, rank, world)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

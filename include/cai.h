@@ -180,6 +180,27 @@ cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int
                                  size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
                                  void* stream);
 
+/* Continuous batching: the same attention for a batch whose sequences bring different
+ * numbers of new tokens in one launch -- decode steps (one token) next to prefill
+ * chunks (Red Hat page, "2. Processamento contínuo em lotes" and its figure 7:
+ * finished requests leave and new ones join as slots free up, instead of the whole
+ * batch waiting for its slowest request).  Sequence b owns new-token rows [q_offsets[b], q_offsets[b+1])
+ * of q, out and lse_out (packed), its token i sits at position prefix_len[b] + i and
+ * attends as in cai_mqa_prefill_chunk.  Its K/V must already be appended.
+ *   q           bf16 bits [total_new][num_q_heads][head_dim], 16-byte aligned
+ *   q_offsets   int32 [batch + 1] (device), non-decreasing, q_offsets[batch] <= total_new
+ *   max_new     host bound on q_offsets[b+1] - q_offsets[b] (sizes the launch)
+ *   out         fp32 [total_new][num_q_heads][head_dim]; lse_out fp32 [total_new][num_q_heads], nullable
+ * Other arguments, workspace and limits as cai_mqa_prefill_chunk.  A sequence whose
+ * offsets are out of order, beyond total_new or longer than max_new, or whose
+ * prefix_len + length exceeds the table, sets CAI_DEVERR_LENGTH; its rows (if its
+ * offsets are valid) get out = 0, lse = -inf. */
+cai_status cai_mqa_prefill_varlen(const cai_kv_pool* pool, const uint16_t* q, int32_t batch,
+                                  const int32_t* q_offsets, int32_t total_new, int32_t max_new, int32_t num_q_heads,
+                                  const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* prefix_len,
+                                  int32_t window, float softmax_scale, void* workspace, size_t workspace_bytes,
+                                  float* out, float* lse_out, int32_t* err_flag, void* stream);
+
 /* ---- Cross-turn KV cache in host memory ----------------------------------
  * "Character.AI: inference optimization", 04 Cache between turns: the KV of
  * every processed prefix and generated message is kept in host memory in an

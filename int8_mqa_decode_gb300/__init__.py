@@ -20,7 +20,7 @@ __all__ = [
     "CaiError", "CaiUnavailable", "KVPool", "library_path", "load", "cai_page_bytes", "cai_status_string",
     "cai_kv_append", "cai_mqa_decode_workspace_size", "cai_mqa_decode", "cai_mqa_decode_no_alloc",
     "cai_mqa_prefill_workspace_size",
-    "cai_mqa_prefill_chunk",
+    "cai_mqa_prefill_chunk", "cai_mqa_prefill_varlen",
     "CAI_DEVERR_PAGE", "CAI_DEVERR_LENGTH", "CAI_DEVERR_TIMEOUT", "HEAD_DIM", "cai_host_cache_create",
     "cai_host_cache_destroy", "cai_host_cache_match", "cai_host_cache_restore", "cai_host_cache_store",
     "cai_host_cache_stats", "cai_ring_pages", "cai_ring_table_row",
@@ -89,6 +89,9 @@ def load():
     lib.cai_mqa_prefill_chunk.argtypes = [pool_p, vp, i32, i32, i32, vp, i32, vp, i32, ctypes.c_float, vp, sz, vp, vp,
                                           vp, vp]
     lib.cai_mqa_prefill_chunk.restype = ctypes.c_int
+    lib.cai_mqa_prefill_varlen.argtypes = [pool_p, vp, i32, vp, i32, i32, i32, vp, i32, vp, i32, ctypes.c_float, vp,
+                                           sz, vp, vp, vp, vp]
+    lib.cai_mqa_prefill_varlen.restype = ctypes.c_int
     lib.cai_host_cache_create.argtypes = [i32, i32, i32, ctypes.c_int64]
     lib.cai_host_cache_create.restype = vp
     lib.cai_host_cache_destroy.argtypes = [vp]
@@ -244,6 +247,26 @@ def cai_mqa_prefill_chunk(pool: KVPool, q: torch.Tensor, block_table: torch.Tens
         _ptr(lse_out, "lse_out", torch.float32, (batch, n_new, hq)), _ptr(err_flag, "err_flag", torch.int32),
         _stream(stream))
     _check(st, "cai_mqa_prefill_chunk")
+
+
+def cai_mqa_prefill_varlen(pool: KVPool, q: torch.Tensor, q_offsets: torch.Tensor, max_new: int,
+                           block_table: torch.Tensor, prefix_len: torch.Tensor, window: int, softmax_scale: float,
+                           workspace: torch.Tensor, out: torch.Tensor, lse_out: Optional[torch.Tensor] = None,
+                           err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Mixed batch in one launch: sequence b's new tokens are rows q_offsets[b] .. q_offsets[b+1]
+    of the packed q bf16 [total_new][Hq][128] (decode steps are one-row sequences)."""
+    total, hq = q.shape[0], q.shape[1]
+    batch = q_offsets.shape[0] - 1
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().cai_mqa_prefill_varlen(
+        ctypes.byref(pool.struct), _ptr(q, "q", (torch.bfloat16, torch.int16), (total, hq, HEAD_DIM)), batch,
+        _ptr(q_offsets, "q_offsets", torch.int32, (batch + 1,)), total, int(max_new), hq,
+        _ptr(block_table, "block_table", torch.int32), block_table.shape[-1],
+        _ptr(prefix_len, "prefix_len", torch.int32, (batch,)), window, float(softmax_scale),
+        _ptr(workspace, "workspace"), ws_bytes, _ptr(out, "out", torch.float32, (total, hq, HEAD_DIM)),
+        _ptr(lse_out, "lse_out", torch.float32, (total, hq)), _ptr(err_flag, "err_flag", torch.int32),
+        _stream(stream))
+    _check(st, "cai_mqa_prefill_varlen")
 
 
 # ----------------------------------------------------------------------------- cross-turn host KV cache

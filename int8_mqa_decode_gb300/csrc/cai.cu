@@ -190,19 +190,23 @@ size_t cai_mqa_prefill_workspace_size(int32_t batch, int32_t max_pages_per_seq, 
   return prefill_workspace_bytes(batch, max_pages_per_seq, page_size);
 }
 
-cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int32_t batch, int32_t n_new,
-                                 int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
-                                 const int32_t* prefix_len, int32_t window, float softmax_scale, void* workspace,
-                                 size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
-                                 void* stream) {
+namespace {
+
+cai_status prefill_common(const cai_kv_pool* pool, const uint16_t* q, int32_t batch, const int32_t* q_off,
+                          int32_t n_new, int32_t total_new, int32_t num_q_heads, const int32_t* block_table,
+                          int32_t max_pages_per_seq, const int32_t* prefix_len, int32_t window, float softmax_scale,
+                          void* workspace, size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
+                          void* stream) {
   cai_status st = check_pool(pool);
   if (st != CAI_OK) return st;
-  if (batch < 0 || n_new < 0 || max_pages_per_seq <= 0 || window < 0 || !std::isfinite(softmax_scale))
+  if (batch < 0 || n_new < 0 || total_new < 0 || max_pages_per_seq <= 0 || window < 0 ||
+      !std::isfinite(softmax_scale))
     return CAI_ERR_INVALID_ARG;
   if (num_q_heads < 1 || num_q_heads > 128 || (num_q_heads & (num_q_heads - 1)) != 0) return CAI_ERR_UNSUPPORTED;
   if ((int64_t)max_pages_per_seq * pool->page_size > (1ll << 24) || batch > 65535) return CAI_ERR_UNSUPPORTED;
-  if ((int64_t)n_new * num_q_heads > (1ll << 24)) return CAI_ERR_UNSUPPORTED;
-  if (batch == 0 || n_new == 0) return CAI_OK;
+  if ((int64_t)n_new * num_q_heads > (1ll << 24) || (int64_t)total_new * num_q_heads > (1ll << 31) / kHeadDim)
+    return CAI_ERR_UNSUPPORTED;
+  if (batch == 0 || n_new == 0 || total_new == 0) return CAI_OK;
   if (!q || !block_table || !prefix_len || !out) return CAI_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out)) return CAI_ERR_INVALID_ARG;
   const size_t need = prefill_workspace_bytes(batch, max_pages_per_seq, pool->page_size);
@@ -216,8 +220,10 @@ cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int
   L.table = block_table;
   L.prefix_len = prefix_len;
   L.q = q;
+  L.q_off = q_off;
   L.batch = batch;
   L.n_new = n_new;
+  L.total_new = total_new;
   L.num_heads = num_q_heads;
   L.window = window;
   L.scale_log2 = softmax_scale * kLog2e;
@@ -226,6 +232,28 @@ cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int
   L.lse_out = lse_out;
   L.err = err_flag;
   return cuda_status(launch_prefill(L, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int32_t batch, int32_t n_new,
+                                 int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
+                                 const int32_t* prefix_len, int32_t window, float softmax_scale, void* workspace,
+                                 size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
+                                 void* stream) {
+  if ((int64_t)batch * n_new > 2147483647ll) return CAI_ERR_UNSUPPORTED;
+  return prefill_common(pool, q, batch, nullptr, n_new, batch * n_new, num_q_heads, block_table, max_pages_per_seq,
+                        prefix_len, window, softmax_scale, workspace, workspace_bytes, out, lse_out, err_flag, stream);
+}
+
+cai_status cai_mqa_prefill_varlen(const cai_kv_pool* pool, const uint16_t* q, int32_t batch,
+                                  const int32_t* q_offsets, int32_t total_new, int32_t max_new, int32_t num_q_heads,
+                                  const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* prefix_len,
+                                  int32_t window, float softmax_scale, void* workspace, size_t workspace_bytes,
+                                  float* out, float* lse_out, int32_t* err_flag, void* stream) {
+  if (batch > 0 && total_new > 0 && !q_offsets) return CAI_ERR_INVALID_ARG;
+  return prefill_common(pool, q, batch, q_offsets, max_new, total_new, num_q_heads, block_table, max_pages_per_seq,
+                        prefix_len, window, softmax_scale, workspace, workspace_bytes, out, lse_out, err_flag, stream);
 }
 
 }  // extern "C"

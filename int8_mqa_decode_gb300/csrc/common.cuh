@@ -80,7 +80,8 @@ struct PrefillLaunch {
   const int32_t* table;
   const int32_t* prefix_len;
   const uint16_t* q;
-  int32_t batch, n_new, num_heads, window;
+  const int32_t* q_off;  // [batch + 1] packed new-token offsets (device), or null for n_new per sequence
+  int32_t batch, n_new, total_new, num_heads, window;  // n_new: the most new tokens of any sequence
   float scale_log2;
   void* workspace;
   float* out;

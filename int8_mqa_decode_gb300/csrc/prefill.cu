@@ -63,8 +63,9 @@ struct PrefillParams {
   int32_t num_pages, page_size, max_pages;
   const int32_t* table;
   const int32_t* prefix_len;
-  const uint16_t* q;  // bf16 [B][n_new][Hq][128]
-  int32_t batch, n_new, num_heads, log2_heads, window, kt_rows, pairs;
+  const uint16_t* q;      // bf16 [rows of new tokens][Hq][128], sequence b's rows from q_row0(b)
+  const int32_t* q_off;   // [B + 1] packed new-token offsets, or null: sequence b has n_new rows at b * n_new
+  int32_t batch, n_new, total_new, num_heads, log2_heads, window, kt_rows, pairs;  // n_new: the most per sequence
   float scale_log2;
   uint16_t* kb;  // scratch bf16 [B][KT][128]
   uint16_t* vh;  // scratch fp16 [B][KT][128]
@@ -75,8 +76,28 @@ struct PrefillParams {
   int32_t* err;
 };
 
-__device__ __forceinline__ bool seq_ok(const PrefillParams& p, int32_t p0) {
-  return p0 >= 0 && (int64_t)p0 + p.n_new <= (int64_t)p.max_pages * p.page_size;
+// New tokens of sequence b: rows [r0, r0 + n) of q / out, or n = -1 when its offsets
+// are out of order or outside [0, total_new] (nothing of it is read or written).
+struct SeqRows {
+  int64_t r0;
+  int n;
+};
+
+__device__ __forceinline__ SeqRows seq_rows(const PrefillParams& p, int b) {
+  SeqRows s;
+  if (!p.q_off) {
+    s.r0 = (int64_t)b * p.n_new;
+    s.n = p.n_new;
+    return s;
+  }
+  const int32_t a = p.q_off[b], e = p.q_off[b + 1];
+  s.r0 = a;
+  s.n = (a >= 0 && a <= e && e <= p.total_new && e - a <= p.n_new) ? e - a : -1;
+  return s;
+}
+
+__device__ __forceinline__ bool seq_ok(const PrefillParams& p, int32_t p0, int n) {
+  return n >= 0 && p0 >= 0 && (int64_t)p0 + n <= (int64_t)p.max_pages * p.page_size;
 }
 
 // One warp per scratch row (sequence b, key t).
@@ -87,12 +108,14 @@ __global__ void __launch_bounds__(256) dequant_kernel(const PrefillParams p) {
   const int b = (int)(row / p.kt_rows);
   const int t = (int)(row - (int64_t)b * p.kt_rows);
   const int32_t p0 = p.prefix_len[b];
-  const bool ok = seq_ok(p, p0);
+  const SeqRows sr = seq_rows(p, b);
+  const bool ok = seq_ok(p, p0, sr.n);
   if (!ok) {
     if (t == 0 && lane == 0 && p.err) atomicOr(p.err, CAI_DEVERR_LENGTH);
     return;
   }
-  const int len = p0 + p.n_new;
+  if (sr.n == 0) return;  // no new tokens: nothing attends
+  const int len = p0 + sr.n;
   if (t >= ((len + kKeys - 1) / kKeys) * kKeys) return;  // never read
   // Keys before every window of the chunk are never attended: rows of their tile get
   // zeros (masked later) and their pages are not read, so a local buffer may have
@@ -143,9 +166,13 @@ __device__ __forceinline__ void tma_load_rows128(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// One work item: a pair of q-tiles (256 consecutive (token, head) rows) of one sequence.
+// One work item: a pair of q-tiles (256 consecutive (token, head) rows) of one
+// sequence.  ok = false: no MMA work; the softmax groups then write zeros to the
+// item's rows below `rows` (an invalid sequence) or nothing (rows beyond the chunk).
 struct PItem {
   int b, row0, kt0, nkt;
+  int64_t qrow0;  // first packed new-token row of the sequence
+  int rows;       // (token, head) rows of the sequence, 0 if its offsets are invalid
   bool ok;
 };
 
@@ -154,13 +181,16 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
   it.b = idx / p.pairs;
   it.row0 = (idx - it.b * p.pairs) * (kQT * kRows);
   const int32_t p0 = p.prefix_len[it.b];
-  it.ok = seq_ok(p, p0);
+  const SeqRows sr = seq_rows(p, it.b);
+  it.qrow0 = sr.r0;
+  it.rows = sr.n > 0 ? sr.n * p.num_heads : 0;
+  it.ok = seq_ok(p, p0, sr.n) && it.row0 < it.rows;
   if (!it.ok) {
     it.kt0 = it.nkt = 0;
     return it;
   }
   const int i0 = it.row0 >> p.log2_heads;
-  const int i_last = min((it.row0 + kQT * kRows - 1) >> p.log2_heads, p.n_new - 1);
+  const int i_last = min((it.row0 + kQT * kRows - 1) >> p.log2_heads, sr.n - 1);
   const int kv_hi = p0 + i_last + 1;
   const int kv_lo = p.window > 0 ? max(0, p0 + i0 + 1 - p.window) : 0;
   it.kt0 = kv_lo / kKeys;
@@ -199,7 +229,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_heads;
   const int num_items = p.batch * p.pairs;
-  const int64_t total_rows = (int64_t)p.n_new * Hq;
 
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
@@ -323,20 +352,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
       const PItem it = prefill_item(p, idx);
       const int64_t row = it.row0 + q * kRows + r;  // (token, head) row within the sequence
-      const bool my_row = row < total_rows;
+      const bool my_row = row < it.rows;
       const int my_i = (int)(row >> p.log2_heads), my_h = (int)(row & (Hq - 1));
-      float* out_row = p.out + (((int64_t)it.b * p.n_new + my_i) * Hq + my_h) * kHeadDim;
-      if (!it.ok) {  // flagged by the dequant pass; outputs defined as 0 / -inf
+      float* out_row = p.out + ((it.qrow0 + my_i) * Hq + my_h) * kHeadDim;
+      if (!it.ok) {  // invalid sequence (flagged by the dequant pass): 0 / -inf; beyond the chunk: nothing
         if (my_row) {
           for (int d = 0; d < kHeadDim; d += 4)
             *reinterpret_cast<float4*>(out_row + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (p.lse_out) p.lse_out[((int64_t)it.b * p.n_new + my_i) * Hq + my_h] = -INFINITY;
+          if (p.lse_out) p.lse_out[(it.qrow0 + my_i) * Hq + my_h] = -INFINITY;
         }
         continue;  // no MMA work for this item
       }
       // This row's query (bf16), zero beyond the chunk.
       {
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)it.b * total_rows + row) * kHeadDim);
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + (it.qrow0 * Hq + row) * kHeadDim);
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           *reinterpret_cast<uint4*>(qs + c * 2048 + r * 16) = my_row ? src[c] : make_uint4(0, 0, 0, 0);
@@ -455,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         }
       }
       if (my_row && p.lse_out)
-        p.lse_out[((int64_t)it.b * p.n_new + my_i) * Hq + my_h] =
+        p.lse_out[(it.qrow0 + my_i) * Hq + my_h] =
             l_sum > 0.0f ? (m_ref + __log2f(l_sum)) * kLn2 : -INFINITY;
       tc_fence_before();
       __syncwarp();
@@ -502,8 +531,10 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.table = L.table;
   p.prefix_len = L.prefix_len;
   p.q = L.q;
+  p.q_off = L.q_off;
   p.batch = L.batch;
   p.n_new = L.n_new;
+  p.total_new = L.total_new;
   p.num_heads = L.num_heads;
   p.log2_heads = 31 - __builtin_clz((unsigned)L.num_heads);
   p.window = L.window;

@@ -108,6 +108,32 @@ def test_decode_validation(lib):
     assert call(pools=bad, npools=1, l2p=(ctypes.c_int32 * 1)(0), nlayers=1) == 2
 
 
+def test_prefill_varlen_validation(lib):
+    pool = _pool()
+
+    def call(**kw):
+        a = dict(q=FAKE, batch=3, off=FAKE, total=40, maxn=32, hq=8, table=FAKE, maxp=64, prefix=FAKE, window=0,
+                 scale=0.088, ws=None, ws_bytes=0, out=FAKE)
+        a.update(kw)
+        return lib.cai_mqa_prefill_varlen(ctypes.byref(pool), a["q"], a["batch"], a["off"], a["total"], a["maxn"],
+                                          a["hq"], a["table"], a["maxp"], a["prefix"], a["window"], a["scale"],
+                                          a["ws"], a["ws_bytes"], a["out"], None, None, None)
+
+    assert call(off=None) == 1          # offsets are required
+    assert call(hq=6) == 2              # heads a power of two
+    assert call(hq=256) == 2
+    assert call(total=-1) == 1
+    assert call(maxn=-1) == 1
+    assert call(window=-1) == 1
+    assert call(q=FAKE + 4) == 1
+    assert call(out=None) == 1
+    assert call(batch=0) == 0           # nothing to do, nothing launched
+    assert call(total=0) == 0
+    assert call(maxn=0) == 0
+    assert call() == 3                  # every call here stops at the workspace check
+    assert call(ws=FAKE + 16, ws_bytes=1 << 30) == 3
+
+
 def test_binding_refuses_cpu_tensors(lib):
     torch = pytest.importorskip("torch")
     pool = cai.KVPool.__new__(cai.KVPool)
