@@ -180,6 +180,28 @@ cai_status cai_mqa_prefill_chunk(const cai_kv_pool* pool, const uint16_t* q, int
                                  size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
                                  void* stream);
 
+/* Grouped-query attention: num_kv_heads K/V heads, each shared by a group of
+ * G = num_q_heads / num_kv_heads query heads (query heads [j*G, (j+1)*G) read KV head
+ * j).  The pages compare Multi-Query Attention, one K/V head for all query heads,
+ * against it: MQA keeps the KV cache 8X smaller than the grouped-query attention of
+ * most open models ("Character.AI: inference optimization", section 03 and its
+ * technique table).  Each KV head lives in its own pool (same page size and page
+ * count, same block table and lengths) and is appended with cai_kv_append like an MQA
+ * buffer; with num_kv_heads = 1 this is cai_mqa_decode.
+ *   kv_pools    host array [num_kv_heads], 1 <= num_kv_heads <= 8
+ *   num_q_heads a multiple of num_kv_heads with G <= 64
+ *   q, out, lse_out, block_table, ctx_len, window, num_splits as cai_mqa_decode
+ *   workspace   device scratch of cai_gqa_decode_workspace_size() bytes, 256-byte aligned,
+ *               first 256 bytes zero before the first use (kept zero by every call) */
+size_t cai_gqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t max_pages_per_seq, int32_t page_size, int32_t window,
+                                     int32_t num_splits);
+cai_status cai_gqa_decode(const cai_kv_pool* kv_pools, int32_t num_kv_heads, const uint16_t* q, int32_t batch,
+                          int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
+                          const int32_t* ctx_len, int32_t window, float softmax_scale, int32_t num_splits,
+                          void* workspace, size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
+                          void* stream);
+
 /* Continuous batching: the same attention for a batch whose sequences bring different
  * numbers of new tokens in one launch -- decode steps (one token) next to prefill
  * chunks (Red Hat page, "2. Processamento contínuo em lotes" and its figure 7:

@@ -20,7 +20,7 @@ __all__ = [
     "CaiError", "CaiUnavailable", "KVPool", "library_path", "load", "cai_page_bytes", "cai_status_string",
     "cai_kv_append", "cai_mqa_decode_workspace_size", "cai_mqa_decode", "cai_mqa_decode_no_alloc",
     "cai_mqa_prefill_workspace_size",
-    "cai_mqa_prefill_chunk", "cai_mqa_prefill_varlen",
+    "cai_mqa_prefill_chunk", "cai_mqa_prefill_varlen", "cai_gqa_decode", "cai_gqa_decode_workspace_size",
     "CAI_DEVERR_PAGE", "CAI_DEVERR_LENGTH", "CAI_DEVERR_TIMEOUT", "HEAD_DIM", "cai_host_cache_create",
     "cai_host_cache_destroy", "cai_host_cache_match", "cai_host_cache_restore", "cai_host_cache_store",
     "cai_host_cache_stats", "cai_ring_pages", "cai_ring_table_row",
@@ -92,6 +92,11 @@ def load():
     lib.cai_mqa_prefill_varlen.argtypes = [pool_p, vp, i32, vp, i32, i32, i32, vp, i32, vp, i32, ctypes.c_float, vp,
                                            sz, vp, vp, vp, vp]
     lib.cai_mqa_prefill_varlen.restype = ctypes.c_int
+    lib.cai_gqa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.cai_gqa_decode_workspace_size.restype = sz
+    lib.cai_gqa_decode.argtypes = [pool_p, i32, vp, i32, i32, vp, i32, vp, i32, ctypes.c_float, i32, vp, sz, vp, vp,
+                                   vp, vp]
+    lib.cai_gqa_decode.restype = ctypes.c_int
     lib.cai_host_cache_create.argtypes = [i32, i32, i32, ctypes.c_int64]
     lib.cai_host_cache_create.restype = vp
     lib.cai_host_cache_destroy.argtypes = [vp]
@@ -247,6 +252,29 @@ def cai_mqa_prefill_chunk(pool: KVPool, q: torch.Tensor, block_table: torch.Tens
         _ptr(lse_out, "lse_out", torch.float32, (batch, n_new, hq)), _ptr(err_flag, "err_flag", torch.int32),
         _stream(stream))
     _check(st, "cai_mqa_prefill_chunk")
+
+
+def cai_gqa_decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, max_pages_per_seq: int,
+                                  page_size: int, window: int, num_splits: int = 0) -> int:
+    return int(load().cai_gqa_decode_workspace_size(batch, num_q_heads, num_kv_heads, max_pages_per_seq, page_size,
+                                                    window, num_splits))
+
+
+def cai_gqa_decode(kv_pools: Sequence[KVPool], q: torch.Tensor, block_table: torch.Tensor, ctx_len: torch.Tensor,
+                   window: int, softmax_scale: float, num_splits: int, workspace: torch.Tensor, out: torch.Tensor,
+                   lse_out: Optional[torch.Tensor] = None, err_flag: Optional[torch.Tensor] = None,
+                   stream=None) -> None:
+    """Grouped-query decode: query heads [j*G, (j+1)*G) read kv_pools[j], G = Hq / len(kv_pools)."""
+    batch, hq = q.shape[0], q.shape[1]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().cai_gqa_decode(
+        _pool_structs(kv_pools), len(kv_pools), _ptr(q, "q", (torch.bfloat16, torch.int16), (batch, hq, HEAD_DIM)),
+        batch, hq, _ptr(block_table, "block_table", torch.int32), block_table.shape[-1],
+        _ptr(ctx_len, "ctx_len", torch.int32, (batch,)), window, float(softmax_scale), num_splits,
+        _ptr(workspace, "workspace"), ws_bytes, _ptr(out, "out", torch.float32, (batch, hq, HEAD_DIM)),
+        _ptr(lse_out, "lse_out", torch.float32, (batch, hq)), _ptr(err_flag, "err_flag", torch.int32),
+        _stream(stream))
+    _check(st, "cai_gqa_decode")
 
 
 def cai_mqa_prefill_varlen(pool: KVPool, q: torch.Tensor, q_offsets: torch.Tensor, max_new: int,

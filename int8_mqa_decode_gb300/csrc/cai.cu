@@ -131,35 +131,44 @@ size_t cai_mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t
                              plan_decode(batch, max_pages_per_seq, page_size, window, num_splits, num_sms()));
 }
 
-cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int32_t* layer_to_pool,
-                          int32_t num_layers, int32_t layer, const uint16_t* q, int32_t batch,
-                          int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
-                          const int32_t* ctx_len, int32_t window, float softmax_scale, int32_t num_splits,
-                          void* workspace, size_t workspace_bytes, float* out, float* lse_out,
-                          int32_t* err_flag, void* stream) {
-  if (!pools || num_pools <= 0 || !layer_to_pool || num_layers <= 0 || layer < 0 || layer >= num_layers)
-    return CAI_ERR_INVALID_ARG;
-  const int32_t buf = layer_to_pool[layer];
-  if (buf < 0 || buf >= num_pools) return CAI_ERR_INVALID_ARG;
-  const cai_kv_pool* pool = &pools[buf];
-  cai_status st = check_pool(pool);
-  if (st != CAI_OK) return st;
+namespace {
+
+// Decode of one layer over num_kv_heads pools (one for MQA): query heads
+// [j*G, (j+1)*G) read pool j, G = num_q_heads / num_kv_heads; the split plan is
+// made for batch * num_kv_heads independent problems.
+cai_status decode_common(const cai_kv_pool* kv_pools, int32_t num_kv_heads, const uint16_t* q, int32_t batch,
+                         int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
+                         const int32_t* ctx_len, int32_t window, float softmax_scale, int32_t num_splits,
+                         void* workspace, size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
+                         void* stream) {
+  if (num_kv_heads < 1 || num_kv_heads > kMaxKvHeads) return CAI_ERR_UNSUPPORTED;
+  for (int j = 0; j < num_kv_heads; ++j) {
+    cai_status st = check_pool(&kv_pools[j]);
+    if (st != CAI_OK) return st;
+    if (kv_pools[j].page_size != kv_pools[0].page_size || kv_pools[j].num_pages != kv_pools[0].num_pages)
+      return CAI_ERR_INVALID_ARG;
+  }
+  const cai_kv_pool* pool = &kv_pools[0];
   if (batch < 0 || max_pages_per_seq <= 0 || window < 0 || num_splits < 0 || num_splits > kMaxSplits ||
       !std::isfinite(softmax_scale))
     return CAI_ERR_INVALID_ARG;
-  if (num_q_heads < 1 || num_q_heads > kDecodeMaxHeads) return CAI_ERR_UNSUPPORTED;
+  if (num_q_heads < 1 || num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > kDecodeMaxHeads)
+    return CAI_ERR_UNSUPPORTED;
   if ((int64_t)max_pages_per_seq * pool->page_size > (1ll << 30) || batch > 65535) return CAI_ERR_UNSUPPORTED;
   if (batch == 0) return CAI_OK;
   if (!q || !block_table || !ctx_len || !out) return CAI_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out)) return CAI_ERR_INVALID_ARG;
 
-  const DecodePlan plan = plan_decode(batch, max_pages_per_seq, pool->page_size, window, num_splits, num_sms());
+  const DecodePlan plan =
+      plan_decode(batch * num_kv_heads, max_pages_per_seq, pool->page_size, window, num_splits, num_sms());
   const size_t need = workspace_bytes_for(batch, num_q_heads, plan);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return CAI_ERR_WORKSPACE;
 
   DecodeParams p;
-  p.pages = static_cast<const uint8_t*>(pool->pages);
+  for (int j = 0; j < kMaxKvHeads; ++j)
+    p.pages[j] = j < num_kv_heads ? static_cast<const uint8_t*>(kv_pools[j].pages) : nullptr;
+  p.num_kv_heads = num_kv_heads;
   p.num_pages = pool->num_pages;
   p.table = block_table;
   p.max_pages = max_pages_per_seq;
@@ -183,6 +192,45 @@ cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int
   }
   p.err = err_flag;
   return cuda_status(launch_decode(p, pool->page_size, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int32_t* layer_to_pool,
+                          int32_t num_layers, int32_t layer, const uint16_t* q, int32_t batch,
+                          int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
+                          const int32_t* ctx_len, int32_t window, float softmax_scale, int32_t num_splits,
+                          void* workspace, size_t workspace_bytes, float* out, float* lse_out,
+                          int32_t* err_flag, void* stream) {
+  if (!pools || num_pools <= 0 || !layer_to_pool || num_layers <= 0 || layer < 0 || layer >= num_layers)
+    return CAI_ERR_INVALID_ARG;
+  const int32_t buf = layer_to_pool[layer];
+  if (buf < 0 || buf >= num_pools) return CAI_ERR_INVALID_ARG;
+  return decode_common(&pools[buf], 1, q, batch, num_q_heads, block_table, max_pages_per_seq, ctx_len, window,
+                       softmax_scale, num_splits, workspace, workspace_bytes, out, lse_out, err_flag, stream);
+}
+
+size_t cai_gqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t max_pages_per_seq, int32_t page_size, int32_t window,
+                                     int32_t num_splits) {
+  if (num_kv_heads < 1 || num_kv_heads > kMaxKvHeads || num_q_heads < 1 || num_q_heads % num_kv_heads != 0 ||
+      batch <= 0 || (int64_t)batch * num_kv_heads > 2147483647ll)
+    return 0;
+  if (max_pages_per_seq <= 0 || !page_size_ok(page_size) || window < 0 || num_splits < 0 || num_splits > kMaxSplits)
+    return 0;
+  return workspace_bytes_for(batch, num_q_heads, plan_decode(batch * num_kv_heads, max_pages_per_seq, page_size,
+                                                             window, num_splits, num_sms()));
+}
+
+cai_status cai_gqa_decode(const cai_kv_pool* kv_pools, int32_t num_kv_heads, const uint16_t* q, int32_t batch,
+                          int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
+                          const int32_t* ctx_len, int32_t window, float softmax_scale, int32_t num_splits,
+                          void* workspace, size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
+                          void* stream) {
+  if (!kv_pools) return CAI_ERR_INVALID_ARG;
+  if ((int64_t)batch * num_kv_heads > 65535) return CAI_ERR_UNSUPPORTED;
+  return decode_common(kv_pools, num_kv_heads, q, batch, num_q_heads, block_table, max_pages_per_seq, ctx_len,
+                       window, softmax_scale, num_splits, workspace, workspace_bytes, out, lse_out, err_flag, stream);
 }
 
 size_t cai_mqa_prefill_workspace_size(int32_t batch, int32_t max_pages_per_seq, int32_t page_size) {

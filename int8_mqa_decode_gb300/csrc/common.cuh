@@ -39,8 +39,11 @@ struct DecodePlan {
   int32_t max_splits;  // upper bound of splits per sequence
 };
 
+constexpr int kMaxKvHeads = 8;         // KV heads (pools) one decode call can read
+
 struct DecodeParams {
-  const uint8_t* pages;
+  const uint8_t* pages[kMaxKvHeads];  // the pool of each KV head (one for MQA), same page size and count
+  int32_t num_kv_heads;               // query heads [j*G, (j+1)*G) read KV head j, G = num_heads / num_kv_heads
   int32_t num_pages;
   const int32_t* table;
   int32_t max_pages;

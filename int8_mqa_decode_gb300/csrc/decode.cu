@@ -147,14 +147,14 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
 // A work item: one split of one sequence.  kind 0 = tiles to process,
 // 1 = nothing to attend (split 0 writes out = 0, lse = -inf).
 struct Item {
-  int b, split, start, end, tile0, ntiles;
+  int b, kvh, split, start, end, tile0, ntiles;
   bool direct;  // single split: write the final output
   int kind;
   bool invalid;
 };
 
 // Ring entry: [0] b, [1] split, [2] start, [3] end, [4] tile0, [5] ntiles,
-// [6] flags (bit 0 direct, bit 1 invalid, bit 2 kind 1, bit 3 end of work),
+// [6] flags (bit 0 direct, bit 1 invalid, bit 2 kind 1, bit 3 end of work), [7] KV head,
 // [8 .. 40) page ids of the item's first tiles (one id batch, see batch_page).
 __device__ __forceinline__ Item ring_item(const volatile int32_t* e, bool& done) {
   Item it;
@@ -165,6 +165,7 @@ __device__ __forceinline__ Item ring_item(const volatile int32_t* e, bool& done)
   it.tile0 = e[4];
   it.ntiles = e[5];
   const int f = e[6];
+  it.kvh = e[7];
   it.direct = f & 1;
   it.invalid = (f >> 1) & 1;
   it.kind = (f >> 2) & 1;
@@ -189,12 +190,16 @@ __device__ __forceinline__ int32_t batch_page(const DecodeParams& p, const Item&
   return t < it.ntiles ? tile_page<P>(p, it, t, lane % PPT) : (int32_t)kNoPage;
 }
 
+// Work item idx = (b * num_kv_heads + kv head) * max_splits + split.
 // kind 2 = an empty split, never published.
 template <int P>
 __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
   Item it;
-  it.b = idx / p.plan.max_splits;
-  it.split = idx - it.b * p.plan.max_splits;
+  const int per_b = p.num_kv_heads * p.plan.max_splits;
+  it.b = idx / per_b;
+  const int r = idx - it.b * per_b;
+  it.kvh = r / p.plan.max_splits;
+  it.split = r - it.kvh * p.plan.max_splits;
   const SeqSplits sp = seq_splits(p.ctx_len[it.b], p.window, p.max_pages * P, p.plan.chunk);
   it.invalid = !sp.valid;
   it.direct = sp.nsplit == 1;
@@ -218,7 +223,7 @@ __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
 
 struct DecodeArgs {
   DecodeParams p;
-  CUtensorMap kv_map;  // the page pool as rows of 128 bytes; box = the 2P code rows of a page
+  CUtensorMap kv_map[kMaxKvHeads];  // each KV head's pool as rows of 128 bytes; box = the 2P code rows of a page
 };
 
 template <int P, int HN>
@@ -273,8 +278,9 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(smem + L::kOffRing);  // [kRing][kRingInts]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int Hq = p.num_heads;
-  const int num_items = p.batch * p.plan.max_splits;
+  const int Hq = p.num_heads;                   // query heads per sequence (row stride of q and out)
+  const int G = Hq / p.num_kv_heads;            // query heads per KV head (the rows of one item)
+  const int num_items = p.batch * p.num_kv_heads * p.plan.max_splits;
 
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
@@ -359,6 +365,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
             e[4] = it.tile0;
             e[5] = it.ntiles;
             e[6] = (it.direct ? 1 : 0) | (it.invalid ? 2 : 0) | (it.kind == 1 ? 4 : 0);
+            e[7] = it.kvh;
           } else {
             e[6] = 8;
           }
@@ -389,6 +396,8 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         if (done || *abort_flag) break;
         if (it.kind != 0) continue;
         bool ok = true;
+        const CUtensorMap* kv_map = &args.kv_map[it.kvh];
+        const uint8_t* pages = p.pages[it.kvh];
         int32_t ids_next = it.ntiles > TPB ? batch_page<P>(p, it, 1, lane) : (int32_t)kNoPage;
         for (int t = 0; t < it.ntiles && ok; ++t) {
           if (t > 0 && t % TPB == 0) {
@@ -412,10 +421,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
             }
             __syncwarp();
             if ((okm >> lane) & 1u) {
-              tma_load_2d_hint(raw_kv + s * kStageKV + lane * (2 * P * kHeadDim), &args.kv_map, 0,
-                               pid * kRowsPerPage, &raw_full[s], policy);
-              bulk_g2s_hint(raw_sc + s * kStageSc + lane * (8 * P),
-                            p.pages + (int64_t)pid * page_bytes(P) + 2 * P * kHeadDim, 8 * P, &raw_full[s], policy);
+              tma_load_2d_hint(raw_kv + s * kStageKV + lane * (2 * P * kHeadDim), kv_map, 0, pid * kRowsPerPage,
+                               &raw_full[s], policy);
+              bulk_g2s_hint(raw_sc + s * kStageSc + lane * (8 * P), pages + (int64_t)pid * page_bytes(P) + 2 * P * kHeadDim,
+                            8 * P, &raw_full[s], policy);
             }
           }
         }
@@ -512,8 +521,9 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         for (int i = 0; i < kQUnits; ++i) {
           const int u = i * 256 + ctid;
           const int n = (u & 7) | ((u >> 7) << 3), k8 = (u >> 3) & 15;
-          qv[i] = n < Hq ? __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)it.b * Hq + n) * kHeadDim + k8 * 8))
-                         : make_uint4(0u, 0u, 0u, 0u);
+          qv[i] = n < G ? __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)it.b * Hq + it.kvh * G + n) * kHeadDim +
+                                                                k8 * 8))
+                        : make_uint4(0u, 0u, 0u, 0u);
         }
         if (g >= 1) ok = mbar_wait_abortable(&s_full[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag);
         if (!ok) break;
@@ -643,9 +653,9 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       if (it.kind == 1) {
         // Nothing to attend (L = 0) or an invalid length: out = 0, lse = -inf.
         if (it.invalid && sw == 0 && lane == 0) set_err(p.err, CAI_DEVERR_LENGTH);
-        for (int h = h0; h < h0 + HH && h < Hq; ++h) p.out[((int64_t)it.b * Hq + h) * kHeadDim + tok] = 0.0f;
-        if (p.lse_out && quarter == 0 && lane < HH && h0 + lane < Hq)
-          p.lse_out[(int64_t)it.b * Hq + h0 + lane] = -INFINITY;
+        const int64_t hb = (int64_t)it.b * Hq + it.kvh * G;  // first output head of the item
+        for (int h = h0; h < h0 + HH && h < G; ++h) p.out[(hb + h) * kHeadDim + tok] = 0.0f;
+        if (p.lse_out && quarter == 0 && lane < HH && h0 + lane < G) p.lse_out[hb + h0 + lane] = -INFINITY;
         continue;
       }
       float l[HH];
@@ -780,12 +790,12 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         const int h = h0 + lane;
         const float Ls = (lpart[h] + lpart[HN + h]) + (lpart[2 * HN + h] + lpart[3 * HN + h]);
         linv[h] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
-        if (h < Hq) {
+        if (h < G) {
           const float lse2 = Ls > 0.0f ? mref[h] + __log2f(Ls) : -INFINITY;
           if (it.direct) {
-            if (p.lse_out) p.lse_out[(int64_t)it.b * Hq + h] = lse2 * kLn2;
+            if (p.lse_out) p.lse_out[(int64_t)it.b * Hq + it.kvh * G + h] = lse2 * kLn2;
           } else {
-            p.ws_lse[((int64_t)it.b * p.plan.max_splits + it.split) * Hq + h] = lse2;
+            p.ws_lse[((int64_t)it.b * p.plan.max_splits + it.split) * Hq + it.kvh * G + h] = lse2;
           }
         }
       }
@@ -793,8 +803,8 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       if (!mbar_wait_abortable(&o_full[ob], (item_n >> 1) & 1, abort_flag)) break;
       tc_fence_after();
       {
-        float* dst = it.direct ? p.out + (int64_t)it.b * Hq * kHeadDim
-                               : p.ws_o + ((int64_t)it.b * p.plan.max_splits + it.split) * Hq * kHeadDim;
+        float* dst = it.direct ? p.out + ((int64_t)it.b * Hq + it.kvh * G) * kHeadDim
+                               : p.ws_o + (((int64_t)it.b * p.plan.max_splits + it.split) * Hq + it.kvh * G) * kHeadDim;
         uint32_t o[HH];
         const uint32_t oc = tmem + t_lane + kColO + ob * HN + h0;
         if constexpr (HH == 32) tmem_ld_32x32b_x32(oc, o);
@@ -802,7 +812,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < HH; ++i)
-          if (h0 + i < Hq) dst[(h0 + i) * kHeadDim + tok] = __uint_as_float(o[i]) * linv[h0 + i];
+          if (h0 + i < G) dst[(h0 + i) * kHeadDim + tok] = __uint_as_float(o[i]) * linv[h0 + i];
       }
       tc_fence_before();
       __syncwarp();
@@ -902,8 +912,9 @@ cudaError_t launch_decode_ph(const DecodeParams& p, cudaStream_t stream) {
   }
   DecodeArgs a;
   a.p = p;
-  if (!encode_pool_map(&a.kv_map, p.pages, p.num_pages, P)) return cudaErrorInvalidValue;
-  const int64_t items = (int64_t)p.batch * p.plan.max_splits;
+  for (int j = 0; j < p.num_kv_heads; ++j)
+    if (!encode_pool_map(&a.kv_map[j], p.pages[j], p.num_pages, P)) return cudaErrorInvalidValue;
+  const int64_t items = (int64_t)p.batch * p.num_kv_heads * p.plan.max_splits;
   const int grid = (int)(items < num_sms() ? items : num_sms());
   decode_kernel<P, HN><<<grid, Roles<HN>::kThreads, Layout<HN>::kSmemBytes, stream>>>(a);
   cudaError_t e = cudaGetLastError();
@@ -915,7 +926,7 @@ cudaError_t launch_decode_ph(const DecodeParams& p, cudaStream_t stream) {
 
 template <int P>
 cudaError_t launch_decode_p(const DecodeParams& p, cudaStream_t stream) {
-  return p.num_heads <= 32 ? launch_decode_ph<P, 32>(p, stream) : launch_decode_ph<P, 64>(p, stream);
+  return p.num_heads / p.num_kv_heads <= 32 ? launch_decode_ph<P, 32>(p, stream) : launch_decode_ph<P, 64>(p, stream);
 }
 
 }  // namespace
