@@ -9,11 +9,14 @@
 // Bit-exact by construction: no fused multiply-add touches the quotient path
 // and the build uses neither fast-math nor flush-to-zero.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace cai {
 namespace {
 
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int warp_global = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   const int rows = p.batch * p.n_new;
@@ -68,8 +71,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const int64_t warps = 2ll * p.batch * p.n_new;
   const int64_t blocks = (warps + 7) / 8;
-  append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, p);
 }
 
 }  // namespace cai

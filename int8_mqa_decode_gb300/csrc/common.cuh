@@ -2,6 +2,7 @@
 // constants and the split plan.
 #pragma once
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "cai.h"
@@ -94,6 +95,25 @@ struct PrefillLaunch {
 
 size_t prefill_workspace_bytes(int32_t batch, int32_t max_pages_per_seq, int32_t page_size);
 cudaError_t launch_prefill(const PrefillLaunch& p, cudaStream_t stream);
+
+// Launch with programmatic stream serialization: the grid may start while the
+// previous kernel in the stream finishes; every kernel launched this way calls
+// grid_dependency_wait() before it touches memory another kernel writes or reads.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Host side: the split plan for a launch (also used by the workspace query).
 DecodePlan plan_decode(int32_t batch, int32_t max_pages_per_seq, int32_t page_size, int32_t window,

@@ -312,6 +312,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Everything above touched only this CTA's own resources; from here on the kernel
+  // reads and writes memory that the previous kernels in the stream may still use.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   // Item k of this CTA as published by the scheduler warp; every reader warp
   // waits for it, copies it and releases the slot.
@@ -830,6 +834,8 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
 // One warp per (sequence, head): merge the partial outputs of the splits by
 // their log-sum-exp: out = sum_j 2^(lse_j - M) o_j / sum_j 2^(lse_j - M).
 __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int page_size) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   const int Hq = p.num_heads;
@@ -916,12 +922,11 @@ cudaError_t launch_decode_ph(const DecodeParams& p, cudaStream_t stream) {
     if (!encode_pool_map(&a.kv_map[j], p.pages[j], p.num_pages, P)) return cudaErrorInvalidValue;
   const int64_t items = (int64_t)p.batch * p.num_kv_heads * p.plan.max_splits;
   const int grid = (int)(items < num_sms() ? items : num_sms());
-  decode_kernel<P, HN><<<grid, Roles<HN>::kThreads, Layout<HN>::kSmemBytes, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(decode_kernel<P, HN>, dim3(grid), dim3(Roles<HN>::kThreads), Layout<HN>::kSmemBytes,
+                             stream, a);
   if (e != cudaSuccess || p.plan.max_splits <= 1) return e;
   const int64_t warps = (int64_t)p.batch * p.num_heads;
-  combine_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(p, P);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, stream, p, P);
 }
 
 template <int P>
