@@ -15,12 +15,14 @@ static inline bool page_size_ok(int32_t P) { return P == 16 || P == 32 || P == 6
 
 // Split plan.  The attended span of a sequence is at most `span` tokens (the
 // window, or the block-table capacity for a global layer).  Chunks are
-// multiples of the 128-token tile.  Automatic choice: about eight work items
-// per SM for the expected total work (half the capacity per sequence for a
-// global layer, the whole window for a local one), chunks of 512 to 16384
-// tokens, at most 64 splits; a local layer is not split when its batch alone
-// gives every SM a sequence (each extra split costs its partial's write and
-// read, about an eighth of a 1024-token window at 32 heads).
+// multiples of the 128-token tile.  Automatic choice: about 32 work items per
+// SM for the expected total work of a global layer (half the capacity per
+// sequence), chunks of 512 to 16384 tokens, at most 64 splits -- short items let
+// the dynamic queue even out the SMs whatever the length mix (measured on the
+// hybrid step: 8 items per SM 0.453 ms, 16 0.422, 32 0.396, 64 0.431); a local
+// layer is not split when its batch alone gives every SM a sequence (each extra
+// split costs its partial's write and read, about an eighth of a 1024-token
+// window at 32 heads; 2 and 4 splits measured slower).
 DecodePlan plan_decode(int32_t batch, int32_t max_pages_per_seq, int32_t page_size, int32_t window,
                        int32_t num_splits, int32_t sms) {
   const int64_t cap = (int64_t)max_pages_per_seq * page_size;
@@ -33,7 +35,7 @@ DecodePlan plan_decode(int32_t batch, int32_t max_pages_per_seq, int32_t page_si
     chunk = round_up(ceil_div(span, want), kDecodeTile);
   } else {
     const int64_t expected = (int64_t)batch * ((span + 1) / 2);
-    chunk = round_up(ceil_div(expected, 8ll * sms), kDecodeTile);
+    chunk = round_up(ceil_div(expected, 32ll * sms), kDecodeTile);
     if (chunk < 512) chunk = 512;
     if (chunk > 16384) chunk = 16384;
   }
