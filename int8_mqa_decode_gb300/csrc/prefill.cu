@@ -11,18 +11,23 @@
 // own keys were appended to the same pages before this call.
 //
 // How:
-//  1. dequant pass: the sequence's int8 pages are copied, exactly, into a
-//     contiguous scratch copy: K as bf16 [B][KT][128], V as fp16 [B][KT][128]
-//     and both scale rows as fp32 [B][KT].  The scales stay separate so every
-//     logit and weight is formed in fp32 exactly as in the definition.
-//  2. attention: one CTA per 128 query rows of a sequence, a row being one
-//     (new token, head) pair.  128-key tiles of K and V arrive by TMA tensor
-//     loads (cp.async.bulk.tensor) straight into the canonical no-swizzle
-//     tcgen05 operand layout; S = Q K^T runs as tcgen05.mma kind::f16 (bf16,
-//     M = N = 128, K = 128) into tensor memory; the online softmax (one thread
-//     per row) applies the per-key scale, the causal/window mask and the
-//     per-key V scale, and writes P (fp16) back into tensor memory, where it is
-//     the A operand of O += P V (fp16, V from shared memory, MN-major).
+//  1. dequant pass: the keys the chunk can see are copied into a contiguous
+//     scratch copy: K codes as bf16 [B][KT][128] (exact), the per-key K scale
+//     times softmax_scale * log2(e) as fp32 [B][KT], and V already multiplied by
+//     its per-key scale, rounded once to fp16 [B][KT][128] (relative error at
+//     most 2^-11, the same as the rounding of P).
+//  2. attention: a persistent kernel whose work items are pairs of 128-row
+//     q-tiles of one sequence, a row being one (new token, head) pair.  128-key
+//     tiles of K and V arrive by TMA tensor loads (cp.async.bulk.tensor)
+//     straight into the canonical no-swizzle tcgen05 operand layout; S = Q K^T
+//     runs as tcgen05.mma kind::f16 (bf16, M = N = 128, K = 128) into tensor
+//     memory; the online softmax (one thread per row, one warpgroup per q-tile
+//     so each works while the tensor core runs the other's MMAs) forms
+//     logit - reference with one FFMA per key (per-key K scale), applies the
+//     causal/window mask on boundary tiles only, raises the reference lazily
+//     (when a logit exceeds it by 2^8), and writes P (fp16) back into tensor
+//     memory, where it is the A operand of O += P V' (V' from shared memory,
+//     MN-major).
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -39,7 +44,7 @@ constexpr int kTileBytes = kKeys * kHeadDim * 2;  // 32 KB of 16-bit values
 constexpr int kStages = 2;
 constexpr int kOffQ = 0;                                     // Q[kQT]
 constexpr int kOffStage = kOffQ + kQT * kRows * kHeadDim * 2;
-constexpr int kStageBytes = 2 * kTileBytes + 2 * kKeys * 4;  // K, V, K scales, V scales
+constexpr int kStageBytes = 2 * kTileBytes + kKeys * 4;  // K codes, V (scaled), K scales
 constexpr int kOffBars = kOffStage + kStages * kStageBytes;
 constexpr int kNumBars = 2 * kStages + 6 * kQT;
 constexpr int kOffMisc = kOffBars + 8 * kNumBars;
@@ -68,9 +73,8 @@ struct PrefillParams {
   int32_t batch, n_new, total_new, num_heads, log2_heads, window, kt_rows, pairs;  // n_new: the most per sequence
   float scale_log2;
   uint16_t* kb;  // scratch bf16 [B][KT][128]
-  uint16_t* vh;  // scratch fp16 [B][KT][128]
+  uint16_t* vh;  // scratch fp16 [B][KT][128]: V codes times the V scale
   float* ks;     // scratch [B][KT]: K scale * softmax scale * log2(e)
-  float* vs;     // scratch [B][KT]: V scale
   float* out;
   float* lse_out;
   int32_t* err;
@@ -146,16 +150,13 @@ __global__ void __launch_bounds__(256) dequant_kernel(const PrefillParams p) {
     const float kf = (float)(int8_t)(kw >> (8 * e));
     const float vf = (float)(int8_t)(vw >> (8 * e));
     kb[e] = (uint16_t)(__float_as_uint(kf) >> 16);  // small integers: the top half is exact
-    const __half hv = __float2half_rn(vf);
+    const __half hv = __float2half_rn(vf * vsc);  // V scale applied here: P needs no per-key factor
     vh[e] = *reinterpret_cast<const uint16_t*>(&hv);
   }
   const int64_t off = row * kHeadDim + lane * 4;
   *reinterpret_cast<uint2*>(p.kb + off) = make_uint2(kb[0] | ((uint32_t)kb[1] << 16), kb[2] | ((uint32_t)kb[3] << 16));
   *reinterpret_cast<uint2*>(p.vh + off) = make_uint2(vh[0] | ((uint32_t)vh[1] << 16), vh[2] | ((uint32_t)vh[3] << 16));
-  if (lane == 0) {
-    p.ks[row] = ksc;
-    p.vs[row] = vsc;
-  }
+  if (lane == 0) p.ks[row] = ksc;
 }
 
 __device__ __forceinline__ void tma_load_rows128(void* dst, const CUtensorMap* map, int row, uint64_t* bar) {
@@ -270,7 +271,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
           tma_load_rows128(st, &kmap, (int)row, &kv_full[s]);
           tma_load_rows128(st + kTileBytes, &vmap, (int)row, &kv_full[s]);
           bulk_g2s(st + 2 * kTileBytes, p.ks + row, kKeys * 4, &kv_full[s]);
-          bulk_g2s(st + 2 * kTileBytes + kKeys * 4, p.vs + row, kKeys * 4, &kv_full[s]);
         }
       }
     }
@@ -385,8 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         if (!ok) break;
         tc_fence_after();
         const float* kscale = reinterpret_cast<const float*>(smem + kOffStage + s * kStageBytes + 2 * kTileBytes);
-        const float* vscale = kscale + kKeys;
         const int key0 = (it.kt0 + j) * kKeys;
+        // z = logit (log2 units) minus the row's reference maximum, one FFMA per key.
+        const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
         float z[kKeys];
 #pragma unroll
         for (int c = 0; c < kKeys; c += 32) {
@@ -396,10 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             const float4 a = *reinterpret_cast<const float4*>(kscale + c + e);
-            z[c + e] = __uint_as_float(rr[e]) * a.x;
-            z[c + e + 1] = __uint_as_float(rr[e + 1]) * a.y;
-            z[c + e + 2] = __uint_as_float(rr[e + 2]) * a.z;
-            z[c + e + 3] = __uint_as_float(rr[e + 3]) * a.w;
+            z[c + e] = fmaf(__uint_as_float(rr[e]), a.x, -m_use);
+            z[c + e + 1] = fmaf(__uint_as_float(rr[e + 1]), a.y, -m_use);
+            z[c + e + 2] = fmaf(__uint_as_float(rr[e + 2]), a.z, -m_use);
+            z[c + e + 3] = fmaf(__uint_as_float(rr[e + 3]), a.w, -m_use);
           }
         }
         if (!(key0 >= k_lo && key0 + kKeys - 1 <= q_pos)) {
@@ -411,15 +412,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         }
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < kKeys; c += 4) {
-          mx4[0] = fmaxf(mx4[0], z[c]);
-          mx4[1] = fmaxf(mx4[1], z[c + 1]);
-          mx4[2] = fmaxf(mx4[2], z[c + 2]);
-          mx4[3] = fmaxf(mx4[3], z[c + 3]);
+        for (int c = 0; c < kKeys; c += 8) {
+          mx4[0] = fmax3(mx4[0], z[c], z[c + 1]);
+          mx4[1] = fmax3(mx4[1], z[c + 2], z[c + 3]);
+          mx4[2] = fmax3(mx4[2], z[c + 4], z[c + 5]);
+          mx4[3] = fmax3(mx4[3], z[c + 6], z[c + 7]);
         }
         const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        const bool raise = mx > m_ref + kRescaleThreshold;
-        const float alpha = raise ? ex2_approx(m_ref - mx) : 1.0f;
+        // Raise the reference when the row has none yet, or a logit exceeds it by 2^8.
+        const bool raise = m_ref == -INFINITY ? mx > -INFINITY : mx > kRescaleThreshold;
+        const float alpha = raise ? ex2_approx(m_ref - (m_use + mx)) : 1.0f;  // 0 when there was no reference
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
           ok = mbar_wait_abortable(&pv_done[q], (g - 1) & 1, abort_flag);
           if (ok) {
@@ -438,24 +440,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         }
         if (raise) {
           l_sum *= alpha;
-          m_ref = mx;
+          m_ref = m_use + mx;
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) z[c] -= mx;
         }
-        const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < kKeys; c += 64) {
           uint32_t pw[32];
 #pragma unroll
           for (int e = 0; e < 64; e += 4) {
-            const float4 vs = *reinterpret_cast<const float4*>(vscale + c + e);
-            const float e0 = ex2_approx(z[c + e] - m_use), e1 = ex2_approx(z[c + e + 1] - m_use);
-            const float e2 = ex2_approx(z[c + e + 2] - m_use), e3 = ex2_approx(z[c + e + 3] - m_use);
+            const float e0 = ex2_approx(z[c + e]), e1 = ex2_approx(z[c + e + 1]);
+            const float e2 = ex2_approx(z[c + e + 2]), e3 = ex2_approx(z[c + e + 3]);
             l4[0] += e0;
             l4[1] += e1;
             l4[2] += e2;
             l4[3] += e3;
-            pw[e / 2] = pack_f16x2(e0 * vs.x, e1 * vs.y);
-            pw[e / 2 + 1] = pack_f16x2(e2 * vs.z, e3 * vs.w);
+            pw[e / 2] = pack_f16x2(e0, e1);
+            pw[e / 2 + 1] = pack_f16x2(e2, e3);
           }
           tmem_st_32x32b_x32(tmem + t_lane + scol + c / 2, pw);
         }
@@ -548,7 +550,6 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.kb = reinterpret_cast<uint16_t*>(ws);
   p.vh = reinterpret_cast<uint16_t*>(ws + a);
   p.ks = reinterpret_cast<float*>(ws + 2 * a);
-  p.vs = reinterpret_cast<float*>(ws + 2 * a + s);
   p.out = L.out;
   p.lse_out = L.lse_out;
   p.err = L.err;
