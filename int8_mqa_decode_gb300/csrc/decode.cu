@@ -32,11 +32,13 @@
 //    canonical no-swizzle MN-major operand layout in shared memory, the
 //    per-token scales and mask into a four-tile ring, and at an item's first
 //    tile the item's query (bf16 -> fp16) as the K-major B operand Q^T;
-//  * MMA issuer (warp 1): S^T = K Q^T (tcgen05.mma kind::f16, M = 128 tokens,
-//    N = heads padded to 32 or 64, K = 128, A from tensor memory) into a
-//    double-buffered S^T, then O^T += V^T P^T (M = 128 channels, N = heads,
-//    K = 128 tokens, both operands from shared memory) into one of two O^T
-//    accumulators (one per item in flight);
+//  * MMA issuers: warp 1 issues S^T = K Q^T (tcgen05.mma kind::f16, M = 128
+//    tokens, N = heads padded to 32 or 64, K = 128, A from tensor memory) into
+//    a double-buffered S^T; warp 3 issues O^T += V^T P^T (M = 128 channels,
+//    N = heads, K = 128 tokens, both operands from shared memory) into one of
+//    two O^T accumulators (one per item in flight).  Each launch of 8 K steps
+//    holds its issuing thread for most of its run time, so the two streams are
+//    issued by different warps;
 //  * softmax (warps 12-15, one thread per token of the tile): applies the K
 //    scale and softmax scale, checks the logits against a per-head reference
 //    maximum shared by the four warps that is raised only when a logit exceeds
@@ -84,7 +86,7 @@ struct Layout {
 };
 
 // Warp roles, aligned to warpgroups so each group can resize its register file:
-//   warpgroup 0: producer (warp 0), MMA issuer (warp 1), scheduler (warp 2), idle (warp 3)
+//   warpgroup 0: producer (warp 0), S^T issuer (warp 1), scheduler (warp 2), PV issuer (warp 3)
 //   warpgroups 1-2: converters (warps 4..11, two per TMEM lane quarter)
 //   then softmax: one warp per lane quarter for up to 32 heads (warps 12..15), two
 //   per lane quarter for 64 heads (warps 12..19, each taking half of the heads).
@@ -109,7 +111,7 @@ struct Roles {
                 "register split");
   static_assert(32 * (kRegsCtl + 2 * kRegsConv + (kSoftWarps / 4) * kRegsSoft) <= 16384, "sub-partition registers");
   static_assert((kThreads / 32 + 3) / 4 * 32 * kRegsLaunch <= 16384, "launch registers per sub-partition");
-  static constexpr int kItemReaders = 2 + kConvWarps + kSoftWarps;  // producer, MMA, converters, softmax
+  static constexpr int kItemReaders = 3 + kConvWarps + kSoftWarps;  // producer, 2 MMA, converters, softmax
 };
 constexpr int kNoPage = -2147483647 - 1;      // a page the tile does not need
 constexpr uint32_t kTmemCols = 512;
@@ -434,8 +436,11 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         }
         if (!ok) break;
       }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer
+    } else {
+      // ---------------------------------------------------------- MMA issuers
+      // Warp 1 issues S^T = K Q^T, warp 3 issues O^T += V16 P^T: each waits only for
+      // its own operands, so one warp's barrier waits overlap the other's launches,
+      // and an item's last PV goes out as soon as its P^T is ready.
       constexpr uint32_t idesc_s = idesc_f16_f32(T, HN, 0, 0);
       constexpr uint32_t idesc_o = idesc_f16_f32(kHeadDim, HN, 1, 1);
       // Descriptor bases; a K step of 16 adds 256 bytes, i.e. 16 to the address field
@@ -443,59 +448,48 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       const uint64_t dq = smem_desc(smem_addr(qt), 128, 2048);
       const uint64_t dv = smem_desc(smem_addr(v16), 128, T * 16);
       const uint64_t dp = smem_desc(smem_addr(pt), 128, T * 16);
+      const bool s_issuer = warp == 1;
       int g = 0, item_n = 0, k = 0;
-      // PV of tile gp of item `item`: O^T[item & 1] (+)= V16 P^T; `first` starts the
-      // accumulator, `last` signals the item's epilogue.
-      auto issue_pv = [&](int gp, int item, bool first, bool last) -> bool {
-        const int c = gp & 1;
-        const int ob = item & 1;
-        if (!mbar_wait_abortable(&p_full[c], (gp >> 1) & 1, abort_flag)) return false;
-        if (!mbar_wait_abortable(&v_full[c], (gp >> 1) & 1, abort_flag)) return false;
-        if (first && item >= 2 && !mbar_wait_abortable(&o_empty[ob], ((item >> 1) - 1) & 1, abort_flag))
-          return false;
-        tc_fence_after();
-        if (lane == 0) {
-#pragma unroll
-          for (int ks = 0; ks < T / 16; ++ks)
-            mma_f16_ss(tmem + kColO + ob * HN, dv + (uint64_t)(c * (kOp16Bytes >> 4) + ks * 16),
-                       dp + (uint64_t)(c * (L::kPTBytes >> 4) + ks * 16), idesc_o, (!first || ks > 0) ? 1u : 0u);
-          mma_commit(&v_free[c]);
-          if (last) mma_commit(&o_full[ob]);
-        }
-        __syncwarp();
-        return true;
-      };
-      // Order per tile: S^T(g), then PV(g-1); an item's last PV follows its last
-      // S^T at once, so its epilogue never waits for the next item's data.
       bool ok = true;
       while (ok) {
         bool done = false;
         const Item it = next_item(k++, done);
         if (done) break;
         if (it.kind != 0) continue;
+        const int ob = item_n & 1;
         for (int t = 0; t < it.ntiles; ++t, ++g) {
           const int c = g & 1;
-          if (!mbar_wait_abortable(&k_full[c], (g >> 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (lane == 0) {
+          if (s_issuer) {
+            // S^T[c] is free once the softmax of tile g-2 has read it (it then wrote P^T).
+            ok = mbar_wait_abortable(&k_full[c], (g >> 1) & 1, abort_flag) &&
+                 (g < 2 || mbar_wait_abortable(&p_full[c], ((g >> 1) - 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
 #pragma unroll
-            for (int ks = 0; ks < kHeadDim / 16; ++ks)
-              mma_f16_ts(tmem + kColS + c * HN, tmem + kColKA + c * 64 + ks * 8, dq + (uint64_t)(ks * 16), idesc_s,
-                         ks > 0 ? 1u : 0u);
-            mma_commit(&s_full[c]);
+              for (int ks = 0; ks < kHeadDim / 16; ++ks)
+                mma_f16_ts(tmem + kColS + c * HN, tmem + kColKA + c * 64 + ks * 8, dq + (uint64_t)(ks * 16), idesc_s,
+                           ks > 0 ? 1u : 0u);
+              mma_commit(&s_full[c]);
+            }
+          } else {
+            // PV of tile g into O^T[item & 1]; the item's first PV starts the
+            // accumulator once the epilogue of item - 2 has read it.
+            ok = mbar_wait_abortable(&p_full[c], (g >> 1) & 1, abort_flag) &&
+                 mbar_wait_abortable(&v_full[c], (g >> 1) & 1, abort_flag) &&
+                 (t > 0 || item_n < 2 || mbar_wait_abortable(&o_empty[ob], ((item_n >> 1) - 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+              for (int ks = 0; ks < T / 16; ++ks)
+                mma_f16_ss(tmem + kColO + ob * HN, dv + (uint64_t)(c * (kOp16Bytes >> 4) + ks * 16),
+                           dp + (uint64_t)(c * (L::kPTBytes >> 4) + ks * 16), idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+              mma_commit(&v_free[c]);
+              if (t == it.ntiles - 1) mma_commit(&o_full[ob]);
+            }
           }
           __syncwarp();
-          if (t > 0 && !issue_pv(g - 1, item_n, t == 1, false)) {
-            ok = false;
-            break;
-          }
-          if (t == it.ntiles - 1 && !issue_pv(g, item_n, t == 0, true)) {
-            ok = false;
-            break;
-          }
         }
         ++item_n;
       }
