@@ -120,8 +120,9 @@ size_t cai_mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t
  *                          call that uses it; every call leaves them zero again (after a call
  *                          that reported CAI_DEVERR_TIMEOUT, zero them before reuse).  Calls that
  *                          share a workspace must not overlap on the GPU.
- *   out                    fp32 [batch][num_q_heads][head_dim]
- *   lse_out                fp32 [batch][num_q_heads] natural-log log-sum-exp of the logits, nullable
+ *   out                    fp32 [batch][num_q_heads][head_dim], 16-byte aligned
+ *   lse_out                fp32 [batch][num_q_heads] natural-log log-sum-exp of the logits, nullable;
+ *                          any 4-byte alignment (at 16 bytes it is written by bulk copies)
  * A sequence with nothing to attend (L = 0) gets out = 0 and lse = -inf. */
 cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int32_t* layer_to_pool,
                           int32_t num_layers, int32_t layer, const uint16_t* q, int32_t batch,
@@ -170,7 +171,7 @@ size_t cai_mqa_prefill_workspace_size(int32_t batch, int32_t max_pages_per_seq, 
  *   num_q_heads a power of two from 1 to 128
  *   block_table int32 [batch][max_pages_per_seq]; prefix_len int32 [batch]
  *   workspace   device scratch of cai_mqa_prefill_workspace_size() bytes, 256-byte aligned
- *   out         fp32 [batch][n_new][num_q_heads][head_dim]
+ *   out         fp32 [batch][n_new][num_q_heads][head_dim], 16-byte aligned
  *   lse_out     fp32 [batch][n_new][num_q_heads], natural log, nullable
  * A sequence whose prefix_len + n_new exceeds the table sets CAI_DEVERR_LENGTH and
  * gets out = 0, lse = -inf. */
@@ -212,7 +213,8 @@ cai_status cai_gqa_decode(const cai_kv_pool* kv_pools, int32_t num_kv_heads, con
  *   q           bf16 bits [total_new][num_q_heads][head_dim], 16-byte aligned
  *   q_offsets   int32 [batch + 1] (device), non-decreasing, q_offsets[batch] <= total_new
  *   max_new     host bound on q_offsets[b+1] - q_offsets[b] (sizes the launch)
- *   out         fp32 [total_new][num_q_heads][head_dim]; lse_out fp32 [total_new][num_q_heads], nullable
+ *   out         fp32 [total_new][num_q_heads][head_dim], 16-byte aligned;
+ *               lse_out fp32 [total_new][num_q_heads], nullable
  * Other arguments, workspace and limits as cai_mqa_prefill_chunk.  A sequence whose
  * offsets are out of order, beyond total_new or longer than max_new, or whose
  * prefix_len + length exceeds the table, sets CAI_DEVERR_LENGTH; its rows (if its

@@ -76,6 +76,7 @@ struct Layout {
   static constexpr int kOffScal = kOffRawSc + NST * kStageSc;    // [4][3][T] floats
   static constexpr int kOffXch = kOffScal + kScaleSlots * 3 * T * 4;  // softmax exchange, 13 x HN floats
   static constexpr int kOffBars = kOffXch + 13 * HN * 4;
+  static_assert(kOffXch % 16 == 0 && kOffPT % 16 == 0, "bulk-copy sources");
   static constexpr int kNumBars = 2 * NST + 2 * 2 /*k_full, v_full*/ + 2 * 2 /*s_full, p_full*/ + 2 /*v_free*/ +
                                   2 * 2 /*o_full, o_empty*/ + 2 * kRing + 2 * kScaleSlots;
   static constexpr int kOffMisc = kOffBars + 8 * kNumBars;       // tmem slot, abort flag, page_ok[NST]
@@ -648,6 +649,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       bool done = false;
       const Item it = next_item(k++, done);
       if (done) break;
+      // The previous item's bulk copies must have read the P^T buffers and the
+      // exchange before this item writes them; every softmax thread passes the
+      // first tile's barrier-reduction after this.
+      if (sw == 0 && lane == 0) bulk_wait_read_all();
       if (it.kind == 1) {
         // Nothing to attend (L = 0) or an invalid length: out = 0, lse = -inf.
         if (it.invalid && sw == 0 && lane == 0) set_err(p.err, CAI_DEVERR_LENGTH);
@@ -784,39 +789,56 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         if (lane < HH) lpart[quarter * HN + h0 + lane] = ls;
       }
       named_barrier_sync(kSoftBar, kSoftThreads);
+      // The item's G output rows and G log-sum-exps are contiguous in memory: both go
+      // out as bulk copies from shared memory (O^T normalised into the P^T buffers,
+      // which no MMA reads before this warpgroup writes the next item's first P^T;
+      // the LSEs into the raise exchange, unused until then too).  The output is
+      // 16-byte aligned (checked on the host); an LSE array that is not, or a row
+      // of fewer than 4 LSEs, takes plain stores.
+      float* dst_o = it.direct ? p.out + ((int64_t)it.b * Hq + it.kvh * G) * kHeadDim
+                               : p.ws_o + (((int64_t)it.b * p.plan.max_splits + it.split) * Hq + it.kvh * G) * kHeadDim;
+      float* dst_lse = it.direct ? (p.lse_out ? p.lse_out + (int64_t)it.b * Hq + it.kvh * G : nullptr)
+                                 : p.ws_lse + ((int64_t)it.b * p.plan.max_splits + it.split) * Hq + it.kvh * G;
+      const bool bulk_lse = dst_lse != nullptr && (reinterpret_cast<uintptr_t>(dst_lse) & 15u) == 0 && (G & 3) == 0;
+      float* lse_stage = wmax;
       if (quarter == 0 && lane < HH) {
         const int h = h0 + lane;
         const float Ls = (lpart[h] + lpart[HN + h]) + (lpart[2 * HN + h] + lpart[3 * HN + h]);
         linv[h] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
         if (h < G) {
           const float lse2 = Ls > 0.0f ? mref[h] + __log2f(Ls) : -INFINITY;
-          if (it.direct) {
-            if (p.lse_out) p.lse_out[(int64_t)it.b * Hq + it.kvh * G + h] = lse2 * kLn2;
-          } else {
-            p.ws_lse[((int64_t)it.b * p.plan.max_splits + it.split) * Hq + it.kvh * G + h] = lse2;
-          }
+          const float lv = it.direct ? lse2 * kLn2 : lse2;  // the split merge works in log2 units
+          if (bulk_lse) lse_stage[h] = lv;
+          else if (dst_lse) dst_lse[h] = lv;
         }
       }
       named_barrier_sync(kSoftBar, kSoftThreads);
       if (!mbar_wait_abortable(&o_full[ob], (item_n >> 1) & 1, abort_flag)) break;
       tc_fence_after();
       {
-        float* dst = it.direct ? p.out + ((int64_t)it.b * Hq + it.kvh * G) * kHeadDim
-                               : p.ws_o + (((int64_t)it.b * p.plan.max_splits + it.split) * Hq + it.kvh * G) * kHeadDim;
         uint32_t o[HH];
         const uint32_t oc = tmem + t_lane + kColO + ob * HN + h0;
         if constexpr (HH == 32) tmem_ld_32x32b_x32(oc, o);
         else tmem_ld_32x32b_x16(oc, o);
         tmem_wait_ld();
+        float* stage = reinterpret_cast<float*>(pt);
 #pragma unroll
-        for (int i = 0; i < HH; ++i)
-          if (h0 + i < G) dst[(h0 + i) * kHeadDim + tok] = __uint_as_float(o[i]) * linv[h0 + i];
+        for (int i = 0; i < HH; ++i) stage[(h0 + i) * kHeadDim + tok] = __uint_as_float(o[i]) * linv[h0 + i];
       }
       tc_fence_before();
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[ob]);
+      named_barrier_sync(kSoftBar, kSoftThreads);
+      if (sw == 0 && lane == 0) {
+        bulk_s2g(dst_o, pt, (uint32_t)G * kHeadDim * 4);
+        if (bulk_lse) bulk_s2g(dst_lse, lse_stage, (uint32_t)G * 4);
+        bulk_commit();
+      }
       ++item_n;
     }
+    // The last bulk copies have landed before the CTA (and its shared memory) goes away.
+    if (sw == 0 && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();

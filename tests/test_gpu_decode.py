@@ -57,6 +57,28 @@ def run_decode(cache, layer, num_splits=0, with_lse=True):
     return out.cpu().numpy(), (lse.cpu().numpy() if with_lse else None)
 
 
+def test_decode_unaligned_lse():
+    """An LSE array off the 16-byte grid takes plain stores; an output array off it is refused."""
+    w = make_workload(3, 8, 16, [300, 1, 1000])
+    cache = build(w)
+    q = cache.decode_q(0)
+    n_o, n_l = w.batch * w.num_q_heads * 128, w.batch * w.num_q_heads
+    for splits in (0, 1, 4):
+        out = torch.full((w.batch, w.num_q_heads, 128), float("nan"), device="cuda")
+        l_buf = torch.full((n_l + 1,), float("nan"), device="cuda")
+        lse = l_buf[1:].view(w.batch, w.num_q_heads)
+        assert lse.data_ptr() % 16 == 4
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        cache.decode(0, q, out, lse, num_splits=splits, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert math.isnan(float(l_buf[0]))
+        check_layer(cache, 0, out.cpu().numpy(), lse.cpu().numpy())
+    o_buf = torch.zeros(n_o + 1, device="cuda")
+    with pytest.raises(cai.CaiError):
+        cache.decode(0, q, o_buf[1:].view(w.batch, w.num_q_heads, 128))
+
+
 def oracle_decode(w, layer, b, heads=None):
     L = int(w.ctx_len[b])
     buf = w.layer_to_buffer[layer]
