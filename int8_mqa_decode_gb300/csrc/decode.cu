@@ -147,6 +147,20 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
   return r;
 }
 
+// Lane i (< N) ends with the maximum over the warp of v[i]: one warp-wide float
+// reduction (redux.sync, sm_100 family) per element.
+template <int N>
+__device__ __forceinline__ float warp_max_scatter(const float (&v)[N], int lane) {
+  float r = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    float m;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v[i]));
+    r = lane == i ? m : r;
+  }
+  return r;
+}
+
 // A work item: one split of one sequence.  kind 0 = tiles to process,
 // 1 = nothing to attend (split 0 writes out = 0, lse = -inf).
 struct Item {
@@ -705,7 +719,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
             float v[HH];
 #pragma unroll
             for (int i = 0; i < HH; ++i) v[i] = valid ? sv[i] + (t == 0 ? 0.0f : muse[h0 + i]) : -INFINITY;
-            const float wm = reduce_scatter<true, HH>(v, lane);
+            const float wm = warp_max_scatter<HH>(v, lane);
             if (lane < HH) wmax[quarter * HN + h0 + lane] = wm;
           }
           named_barrier_sync(kSoftBar, kSoftThreads);
