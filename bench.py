@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--mixed", action="store_true",
                     help="continuous batching: 128 decode steps + 8 prefill chunks of 256 tokens in one launch")
+    ap.add_argument("--per-layer", action="store_true",
+                    help="one decode launch per layer instead of all the step's layers in one launch")
     ap.add_argument("--local-ring", action="store_true",
                     help="keep each sequence of a local-only KV buffer in a ring of pages (window recycling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
@@ -457,16 +459,25 @@ def run_gpu(args, rank, world):
     nl = len(w.layer_windows)
     qs = [cache.decode_q(layer) for layer in range(nl)]
     outs = [torch.empty(w.batch, w.num_q_heads, 128, device="cuda") for _ in range(nl)]
+    layered = nl > 1 and not args.per_layer
     wss = [cache.workspace(layer, args.num_splits) for layer in range(nl)]
+    ws_layers = cache.layers_workspace(args.num_splits) if layered else None
     step_kv = [cache.step_kv(buf) for buf in range(w.num_buffers)]
     stream = torch.cuda.current_stream()
-    n_events = nl
+    n_events = 1 if layered else nl
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n_events)] for _ in range(args.steps)]
 
     def step(record=None):
         for buf, pool in enumerate(cache.pools):
             k, v, start = step_kv[buf]
             cai.cai_kv_append(pool, k, v, cache.tables[buf], start)
+        if layered:
+            if record is not None:
+                record[0].record(stream)
+            cache.decode_layers(qs, outs, num_splits=args.num_splits, workspace=ws_layers)
+            if record is not None:
+                record[1].record(stream)
+            return
         for layer in range(nl):
             if record is not None:
                 record[2 * layer].record(stream)
@@ -476,10 +487,12 @@ def run_gpu(args, rank, world):
             if record is not None:
                 record[2 * layer + 1].record(stream)
 
-    launches_per_step = w.num_buffers + sum(
-        1 + (1 if cai.cai_mqa_decode_workspace_size(w.batch, w.num_q_heads, cache.max_pages_per_seq, w.page_size,
-                                                    w.layer_windows[layer], args.num_splits) > 0 else 0)
-        for layer in range(nl))
+    # Launches per step: the appends, the decode launch(es) and one combine per split layer.
+    splits_layers = sum(
+        1 for layer in range(nl)
+        if cai.cai_mqa_decode_workspace_size(w.batch, w.num_q_heads, cache.max_pages_per_seq, w.page_size,
+                                             w.layer_windows[layer], args.num_splits) > 256)
+    launches_per_step = w.num_buffers + (1 if layered else nl) + splits_layers
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -508,7 +521,7 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
         clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
-    decode_ms = sum(ev[s][2 * l].elapsed_time(ev[s][2 * l + 1]) for s in range(args.steps) for l in range(nl))
+    decode_ms = sum(ev[s][2 * l].elapsed_time(ev[s][2 * l + 1]) for s in range(args.steps) for l in range(n_events))
     ms_max = allreduce_max(ms_total, world)
 
     toks_step, bytes_step = step_work(w)
@@ -520,7 +533,7 @@ def run_gpu(args, rank, world):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world)
+        e2e = run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world, layered)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -536,7 +549,9 @@ def run_gpu(args, rank, world):
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "cai_mqa_decode (split-KV decode + LSE combine), 6 launches per step",
+                     "kernel": ("cai_mqa_decode_layers (all layers of the step in one launch, "
+                                f"LSE combine of {splits_layers} split layer(s))" if layered else
+                                f"cai_mqa_decode (split-KV decode + LSE combine), {nl} launch(es) per step"),
                      "algorithmic_bytes_per_step": bytes_step},
         "hbm_gbs_step": bytes_step * args.steps / (ms_max * 1e-3) / 1e9,
         "queries_per_s": world * w.batch * args.steps / (ms_max * 1e-3),
@@ -548,7 +563,7 @@ def run_gpu(args, rank, world):
     return result
 
 
-def run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world):
+def run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world, layered=False):
     """Same step through the public API with inputs in pinned host memory: every step copies its
     inputs host -> device and its outputs device -> host inside the timed region.  As a serving loop
     would, the copies run on their own streams: inputs are double-buffered and copied while the
@@ -563,6 +578,7 @@ def run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world):
     d_q = [[torch.empty_like(q) for q in qs] for _ in range(2)]
     d_kv = [[(torch.empty_like(k), torch.empty_like(v), torch.empty_like(s)) for k, v, s in step_kv] for _ in range(2)]
     d_out = [outs, [torch.empty_like(o) for o in outs]]
+    ws_layers = [cache.layers_workspace(args.num_splits) for _ in range(2)] if layered else None
     comp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]          # inputs of slot b copied
@@ -590,12 +606,18 @@ def run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world):
         for buf, pool in enumerate(cache.pools):
             dk, dv, ds = d_kv[b][buf]
             cai.cai_kv_append(pool, dk, dv, cache.tables[buf], ds)
-        for layer in range(nl):
+        if layered:
             if not first_use[b]:
-                comp.wait_event(ev_read[b][layer])
-            cai.cai_mqa_decode(cache.pools, w.layer_to_buffer, layer, d_q[b][layer],
-                               cache.tables[w.layer_to_buffer[layer]], cache.ctx_len, w.layer_windows[layer],
-                               w.softmax_scale, args.num_splits, wss[layer], d_out[b][layer])
+                for layer in range(nl):
+                    comp.wait_event(ev_read[b][layer])
+            cache.decode_layers(d_q[b], d_out[b], num_splits=args.num_splits, workspace=ws_layers[b])
+        for layer in range(nl):
+            if not layered:
+                if not first_use[b]:
+                    comp.wait_event(ev_read[b][layer])
+                cai.cai_mqa_decode(cache.pools, w.layer_to_buffer, layer, d_q[b][layer],
+                                   cache.tables[w.layer_to_buffer[layer]], cache.ctx_len, w.layer_windows[layer],
+                                   w.softmax_scale, args.num_splits, wss[layer], d_out[b][layer])
             ev_done[b][layer].record(comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_done[b][layer])

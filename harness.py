@@ -152,6 +152,21 @@ class PagedCache:
                                   w.layer_windows[0] if window is None else window, w.softmax_scale, workspace, out,
                                   lse, err)
 
+    def layers_workspace(self, num_splits: int = 0) -> torch.Tensor:
+        w = self.w
+        n = cai.cai_mqa_decode_layers_workspace_size(w.batch, w.num_q_heads, self.max_pages_per_seq, w.page_size,
+                                                     list(w.layer_windows), num_splits)
+        return torch.zeros(n, dtype=torch.uint8, device=self.device)  # the header must start at zero
+
+    def decode_layers(self, qs, outs, lses=None, num_splits: int = 0, workspace=None, err=None) -> None:
+        """Every layer of the step in one launch (qs[l], outs[l] as for decode)."""
+        w = self.w
+        if workspace is None:
+            workspace = self.layers_workspace(num_splits)
+        tables = [self.tables[w.layer_to_buffer[layer]] for layer in range(len(w.layer_windows))]
+        cai.cai_mqa_decode_layers(self.pools, w.layer_to_buffer, list(w.layer_windows), qs, tables, self.ctx_len,
+                                  w.softmax_scale, num_splits, workspace, outs, lses, err)
+
     def decode(self, layer: int, q: torch.Tensor, out: torch.Tensor, lse: torch.Tensor | None = None,
                num_splits: int = 0, workspace=None, err=None) -> None:
         w = self.w

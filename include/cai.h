@@ -131,6 +131,42 @@ cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int
                           void* workspace, size_t workspace_bytes, float* out, float* lse_out,
                           int32_t* err_flag, void* stream);
 
+/* Workspace bytes for cai_mqa_decode_layers (windows: host int32 [num_layers]); 0 if the
+ * arguments are invalid. */
+size_t cai_mqa_decode_layers_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_pages_per_seq,
+                                            int32_t page_size, int32_t num_layers, const int32_t* windows,
+                                            int32_t num_splits);
+
+/* One decode step of several layers in one launch: for every layer l the same
+ * computation as cai_mqa_decode, on the same work split, with the work items of
+ * all the layers taken from one queue (global layers first) so that the SMs even
+ * out over the whole step instead of layer by layer.  One call covers a decode
+ * step of the hybrid stack ("Character.AI: inference optimization" page,
+ * 03 Model architecture: local layers with a 1024 horizon, one global layer in
+ * six, neighbouring layers sharing one KV buffer; 02 The bottleneck: reading the
+ * attention KV dominates the I/O of a step).
+ *   pools, num_pools       host array of KV buffers
+ *   layer_to_pool          host int32 [num_layers]: buffer read by each layer (layers may share one)
+ *   num_layers             1..8
+ *   windows                host int32 [num_layers]: 0 = global, W > 0 = local (as in cai_mqa_decode)
+ *   q                      host array [num_layers] of device bf16 bits [batch][num_q_heads][head_dim],
+ *                          each 16-byte aligned
+ *   block_tables           host array [num_layers] of device int32 [batch][max_pages_per_seq]
+ *   ctx_len                int32 [batch], shared by the layers (append first)
+ *   workspace              device scratch of cai_mqa_decode_layers_workspace_size() bytes, 256-byte
+ *                          aligned, first 256 bytes zero (as for cai_mqa_decode)
+ *   out                    host array [num_layers] of device fp32 [batch][num_q_heads][head_dim],
+ *                          each 16-byte aligned
+ *   lse_out                host array [num_layers] of nullable device fp32 [batch][num_q_heads], or null
+ * All buffers must use one page size; at most 8 distinct buffers.  Errors as for
+ * cai_mqa_decode; nothing is launched when an argument is rejected. */
+cai_status cai_mqa_decode_layers(const cai_kv_pool* pools, int32_t num_pools, const int32_t* layer_to_pool,
+                                 int32_t num_layers, const int32_t* windows, const uint16_t* const* q,
+                                 int32_t batch, int32_t num_q_heads, const int32_t* const* block_tables,
+                                 int32_t max_pages_per_seq, const int32_t* ctx_len, float softmax_scale,
+                                 int32_t num_splits, void* workspace, size_t workspace_bytes, float* const* out,
+                                 float* const* lse_out, int32_t* err_flag, void* stream);
+
 /* Decode without any caller scratch.  The pages have no counterpart to this
  * entry point: it exists for callers that cannot allocate device memory at
  * the moment they decode -- a serving loop that forbids cudaMalloc after

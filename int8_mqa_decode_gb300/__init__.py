@@ -19,6 +19,7 @@ import torch
 __all__ = [
     "CaiError", "CaiUnavailable", "KVPool", "library_path", "load", "cai_page_bytes", "cai_status_string",
     "cai_kv_append", "cai_mqa_decode_workspace_size", "cai_mqa_decode", "cai_mqa_decode_no_alloc",
+    "cai_mqa_decode_layers_workspace_size", "cai_mqa_decode_layers",
     "cai_mqa_prefill_workspace_size",
     "cai_mqa_prefill_chunk", "cai_mqa_prefill_varlen", "cai_gqa_decode", "cai_gqa_decode_workspace_size",
     "CAI_DEVERR_PAGE", "CAI_DEVERR_LENGTH", "CAI_DEVERR_TIMEOUT", "HEAD_DIM", "cai_host_cache_create",
@@ -92,6 +93,11 @@ def load():
     lib.cai_mqa_prefill_varlen.argtypes = [pool_p, vp, i32, vp, i32, i32, i32, vp, i32, vp, i32, ctypes.c_float, vp,
                                            sz, vp, vp, vp, vp]
     lib.cai_mqa_prefill_varlen.restype = ctypes.c_int
+    lib.cai_mqa_decode_layers_workspace_size.argtypes = [i32, i32, i32, i32, i32, vp, i32]
+    lib.cai_mqa_decode_layers_workspace_size.restype = sz
+    lib.cai_mqa_decode_layers.argtypes = [pool_p, i32, vp, i32, vp, vp, i32, i32, vp, i32, vp, ctypes.c_float, i32,
+                                          vp, sz, vp, vp, vp, vp]
+    lib.cai_mqa_decode_layers.restype = ctypes.c_int
     lib.cai_gqa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.cai_gqa_decode_workspace_size.restype = sz
     lib.cai_gqa_decode.argtypes = [pool_p, i32, vp, i32, i32, vp, i32, vp, i32, ctypes.c_float, i32, vp, sz, vp, vp,
@@ -214,6 +220,46 @@ def cai_mqa_decode(pools: Sequence[KVPool], layer_to_pool: Sequence[int], layer:
         _ptr(lse_out, "lse_out", torch.float32, (batch, hq)), _ptr(err_flag, "err_flag", torch.int32),
         _stream(stream))
     _check(st, "cai_mqa_decode")
+
+
+def cai_mqa_decode_layers_workspace_size(batch: int, num_q_heads: int, max_pages_per_seq: int, page_size: int,
+                                         windows: Sequence[int], num_splits: int = 0) -> int:
+    w = (ctypes.c_int32 * len(windows))(*windows)
+    return int(load().cai_mqa_decode_layers_workspace_size(batch, num_q_heads, max_pages_per_seq, page_size,
+                                                            len(windows), w, num_splits))
+
+
+def cai_mqa_decode_layers(pools: Sequence[KVPool], layer_to_pool: Sequence[int], windows: Sequence[int],
+                          qs: Sequence[torch.Tensor], block_tables: Sequence[torch.Tensor], ctx_len: torch.Tensor,
+                          softmax_scale: float, num_splits: int, workspace: Optional[torch.Tensor],
+                          outs: Sequence[torch.Tensor], lse_outs: Optional[Sequence[Optional[torch.Tensor]]] = None,
+                          err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """One decode step of several layers in one launch: qs[l] bf16 [batch][Hq][128] -> outs[l] fp32."""
+    n = len(layer_to_pool)
+    if not (len(windows) == len(qs) == len(block_tables) == len(outs) == n):
+        raise ValueError("layer_to_pool, windows, qs, block_tables and outs must have one entry per layer")
+    if lse_outs is not None and len(lse_outs) != n:
+        raise ValueError("lse_outs must have one entry per layer")
+    batch, hq = qs[0].shape[0], qs[0].shape[1]
+    max_pages = block_tables[0].shape[-1]
+    for t in block_tables:
+        if t.shape[-1] != max_pages:
+            raise ValueError("block tables of one call must have the same width")
+    l2p = (ctypes.c_int32 * n)(*layer_to_pool)
+    win = (ctypes.c_int32 * n)(*windows)
+    q_ptrs = (ctypes.c_void_p * n)(*[_ptr(q, "q", (torch.bfloat16, torch.int16), (batch, hq, HEAD_DIM)) for q in qs])
+    t_ptrs = (ctypes.c_void_p * n)(*[_ptr(t, "block_table", torch.int32) for t in block_tables])
+    o_ptrs = (ctypes.c_void_p * n)(*[_ptr(o, "out", torch.float32, (batch, hq, HEAD_DIM)) for o in outs])
+    l_ptrs = None
+    if lse_outs is not None:
+        l_ptrs = (ctypes.c_void_p * n)(*[_ptr(t, "lse_out", torch.float32, (batch, hq)) for t in lse_outs])
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().cai_mqa_decode_layers(
+        _pool_array(pools), len(pools), l2p, n, win, q_ptrs, batch, hq, t_ptrs, max_pages,
+        _ptr(ctx_len, "ctx_len", torch.int32, (batch,)), float(softmax_scale), num_splits,
+        _ptr(workspace, "workspace"), ws_bytes, o_ptrs, l_ptrs, _ptr(err_flag, "err_flag", torch.int32),
+        _stream(stream))
+    _check(st, "cai_mqa_decode_layers")
 
 
 def cai_mqa_decode_no_alloc(pools: Sequence[KVPool], layer_to_pool: Sequence[int], layer: int, q: torch.Tensor,

@@ -135,65 +135,152 @@ size_t cai_mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t
 
 namespace {
 
-// Decode of one layer over num_kv_heads pools (one for MQA): query heads
-// [j*G, (j+1)*G) read pool j, G = num_q_heads / num_kv_heads; the split plan is
-// made for batch * num_kv_heads independent problems.
+// One layer of a decode launch, as the caller describes it.
+struct LayerArgs {
+  const cai_kv_pool* pools;  // num_kv_heads pools (one for MQA)
+  const uint16_t* q;
+  const int32_t* table;
+  int32_t window;
+  float* out;
+  float* lse_out;
+};
+
+// Workspace bytes of a launch over these windows: the queue header, then for every
+// layer that is split its partial outputs and log-sum-exps.
+size_t layers_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_pages_per_seq,
+                              int32_t page_size, const int32_t* windows, int32_t n, int32_t num_splits) {
+  size_t total = kWorkspaceHeader;
+  for (int l = 0; l < n; ++l) {
+    const DecodePlan plan =
+        plan_decode(batch * num_kv_heads, max_pages_per_seq, page_size, windows[l], num_splits, num_sms());
+    total += workspace_bytes_for(batch, num_q_heads, plan) - kWorkspaceHeader;
+  }
+  return total;
+}
+
+// Decode of n layers in one persistent launch.  Layer l reads its num_kv_heads
+// pools (query heads [j*G, (j+1)*G) read pool j, G = num_q_heads / num_kv_heads);
+// the layers share batch, heads, ctx_len, softmax scale and page size.  Their
+// work items go through one queue, global layers first (their items are the
+// longest), so the SMs even out over the whole step.
+cai_status decode_layers_common(const LayerArgs* layers, int32_t n, int32_t num_kv_heads, int32_t batch,
+                                int32_t num_q_heads, int32_t max_pages_per_seq, const int32_t* ctx_len,
+                                float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                int32_t* err_flag, void* stream) {
+  if (n < 1 || n > kMaxDecodeJobs) return CAI_ERR_UNSUPPORTED;
+  if (num_kv_heads < 1 || num_kv_heads > kMaxKvHeads) return CAI_ERR_UNSUPPORTED;
+  for (int l = 0; l < n; ++l) {
+    if (!layers[l].pools) return CAI_ERR_INVALID_ARG;
+    for (int j = 0; j < num_kv_heads; ++j) {
+      cai_status st = check_pool(&layers[l].pools[j]);
+      if (st != CAI_OK) return st;
+      if (layers[l].pools[j].page_size != layers[0].pools[0].page_size) return CAI_ERR_INVALID_ARG;
+    }
+  }
+  const int32_t P = layers[0].pools[0].page_size;
+  if (batch < 0 || max_pages_per_seq <= 0 || num_splits < 0 || num_splits > kMaxSplits ||
+      !std::isfinite(softmax_scale))
+    return CAI_ERR_INVALID_ARG;
+  for (int l = 0; l < n; ++l)
+    if (layers[l].window < 0) return CAI_ERR_INVALID_ARG;
+  if (num_q_heads < 1 || num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > kDecodeMaxHeads)
+    return CAI_ERR_UNSUPPORTED;
+  if ((int64_t)max_pages_per_seq * P > (1ll << 30) || batch > 65535) return CAI_ERR_UNSUPPORTED;
+  if (batch == 0) return CAI_OK;
+  if (!ctx_len) return CAI_ERR_INVALID_ARG;
+  for (int l = 0; l < n; ++l) {
+    if (!layers[l].q || !layers[l].table || !layers[l].out) return CAI_ERR_INVALID_ARG;
+    if (!aligned16(layers[l].q) || !aligned16(layers[l].out)) return CAI_ERR_INVALID_ARG;
+  }
+  int32_t windows[kMaxDecodeJobs];
+  for (int l = 0; l < n; ++l) windows[l] = layers[l].window;
+  const size_t need = layers_workspace_bytes(batch, num_q_heads, num_kv_heads, max_pages_per_seq, P, windows, n,
+                                             num_splits);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return CAI_ERR_WORKSPACE;
+
+  DecodeParams p;
+  p.num_slots = 0;
+  p.num_kv_heads = num_kv_heads;
+  p.ctx_len = ctx_len;
+  p.batch = batch;
+  p.num_heads = num_q_heads;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.num_jobs = n;
+  p.queue = static_cast<uint32_t*>(workspace);
+  p.err = err_flag;
+  // Job order: global layers first, then wider windows first (stable).
+  int order[kMaxDecodeJobs];
+  for (int l = 0; l < n; ++l) order[l] = l;
+  for (int a = 1; a < n; ++a)
+    for (int b = a; b > 0; --b) {
+      const int wa = windows[order[b]], wb = windows[order[b - 1]];
+      const bool before = (wa == 0 && wb != 0) || (wa != 0 && wb != 0 && wa > wb);
+      if (!before) break;
+      const int t = order[b];
+      order[b] = order[b - 1];
+      order[b - 1] = t;
+    }
+  uint8_t* ws = static_cast<uint8_t*>(workspace) + kWorkspaceHeader;
+  int64_t items = 0;
+  for (int k = 0; k < n; ++k) {
+    const LayerArgs& la = layers[order[k]];
+    DecodeJob& jb = p.job[k];
+    // Pool slots: layers reading the same pools share them.
+    int slot0 = -1;
+    for (int s0 = 0; s0 + num_kv_heads <= p.num_slots && slot0 < 0; s0 += num_kv_heads) {
+      bool same = true;
+      for (int j = 0; j < num_kv_heads; ++j) same = same && p.pages[s0 + j] == la.pools[j].pages;
+      if (same) slot0 = s0;
+    }
+    if (slot0 < 0) {
+      if (p.num_slots + num_kv_heads > kMaxKvHeads) return CAI_ERR_UNSUPPORTED;
+      slot0 = p.num_slots;
+      for (int j = 0; j < num_kv_heads; ++j) {
+        p.pages[slot0 + j] = static_cast<const uint8_t*>(la.pools[j].pages);
+        p.slot_pages[slot0 + j] = la.pools[j].num_pages;
+      }
+      p.num_slots += num_kv_heads;
+    }
+    jb.slot0 = slot0;
+    jb.window = la.window;
+    jb.table = la.table;
+    jb.max_pages = max_pages_per_seq;
+    jb.q = la.q;
+    jb.out = la.out;
+    jb.lse_out = la.lse_out;
+    jb.plan = plan_decode(batch * num_kv_heads, max_pages_per_seq, P, la.window, num_splits, num_sms());
+    jb.ws_o = nullptr;
+    jb.ws_lse = nullptr;
+    if (jb.plan.max_splits > 1) {
+      const size_t rows = (size_t)batch * jb.plan.max_splits * num_q_heads;
+      const size_t o_bytes = (size_t)round_up((int64_t)(rows * kHeadDim * sizeof(float)), 256);
+      jb.ws_o = reinterpret_cast<float*>(ws);
+      jb.ws_lse = reinterpret_cast<float*>(ws + o_bytes);
+      ws += workspace_bytes_for(batch, num_q_heads, jb.plan) - kWorkspaceHeader;
+    }
+    jb.item0 = (int32_t)items;
+    items += (int64_t)batch * num_kv_heads * jb.plan.max_splits;
+  }
+  if (items > 2147483647ll) return CAI_ERR_UNSUPPORTED;
+  p.num_items = (int32_t)items;
+  for (int k = n; k < kMaxDecodeJobs; ++k) p.job[k] = p.job[n - 1];
+  for (int j = p.num_slots; j < kMaxKvHeads; ++j) {
+    p.pages[j] = nullptr;
+    p.slot_pages[j] = 0;
+  }
+  return cuda_status(launch_decode(p, P, static_cast<cudaStream_t>(stream)));
+}
+
+// Decode of one layer over num_kv_heads pools (one for MQA).
 cai_status decode_common(const cai_kv_pool* kv_pools, int32_t num_kv_heads, const uint16_t* q, int32_t batch,
                          int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
                          const int32_t* ctx_len, int32_t window, float softmax_scale, int32_t num_splits,
                          void* workspace, size_t workspace_bytes, float* out, float* lse_out, int32_t* err_flag,
                          void* stream) {
-  if (num_kv_heads < 1 || num_kv_heads > kMaxKvHeads) return CAI_ERR_UNSUPPORTED;
-  for (int j = 0; j < num_kv_heads; ++j) {
-    cai_status st = check_pool(&kv_pools[j]);
-    if (st != CAI_OK) return st;
-    if (kv_pools[j].page_size != kv_pools[0].page_size || kv_pools[j].num_pages != kv_pools[0].num_pages)
-      return CAI_ERR_INVALID_ARG;
-  }
-  const cai_kv_pool* pool = &kv_pools[0];
-  if (batch < 0 || max_pages_per_seq <= 0 || window < 0 || num_splits < 0 || num_splits > kMaxSplits ||
-      !std::isfinite(softmax_scale))
-    return CAI_ERR_INVALID_ARG;
-  if (num_q_heads < 1 || num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > kDecodeMaxHeads)
-    return CAI_ERR_UNSUPPORTED;
-  if ((int64_t)max_pages_per_seq * pool->page_size > (1ll << 30) || batch > 65535) return CAI_ERR_UNSUPPORTED;
-  if (batch == 0) return CAI_OK;
-  if (!q || !block_table || !ctx_len || !out) return CAI_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(out)) return CAI_ERR_INVALID_ARG;
-
-  const DecodePlan plan =
-      plan_decode(batch * num_kv_heads, max_pages_per_seq, pool->page_size, window, num_splits, num_sms());
-  const size_t need = workspace_bytes_for(batch, num_q_heads, plan);
-  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return CAI_ERR_WORKSPACE;
-
-  DecodeParams p;
-  for (int j = 0; j < kMaxKvHeads; ++j)
-    p.pages[j] = j < num_kv_heads ? static_cast<const uint8_t*>(kv_pools[j].pages) : nullptr;
-  p.num_kv_heads = num_kv_heads;
-  p.num_pages = pool->num_pages;
-  p.table = block_table;
-  p.max_pages = max_pages_per_seq;
-  p.ctx_len = ctx_len;
-  p.q = q;
-  p.batch = batch;
-  p.num_heads = num_q_heads;
-  p.window = window;
-  p.scale_log2 = softmax_scale * kLog2e;
-  p.plan = plan;
-  p.out = out;
-  p.lse_out = lse_out;
-  p.queue = static_cast<uint32_t*>(workspace);
-  p.ws_o = nullptr;
-  p.ws_lse = nullptr;
-  if (plan.max_splits > 1) {
-    const size_t rows = (size_t)batch * plan.max_splits * num_q_heads;
-    uint8_t* base = static_cast<uint8_t*>(workspace) + kWorkspaceHeader;
-    p.ws_o = reinterpret_cast<float*>(base);
-    p.ws_lse = reinterpret_cast<float*>(base + (size_t)round_up((int64_t)(rows * kHeadDim * sizeof(float)), 256));
-  }
-  p.err = err_flag;
-  return cuda_status(launch_decode(p, pool->page_size, static_cast<cudaStream_t>(stream)));
+  const LayerArgs la = {kv_pools, q, block_table, window, out, lse_out};
+  return decode_layers_common(&la, 1, num_kv_heads, batch, num_q_heads, max_pages_per_seq, ctx_len, softmax_scale,
+                              num_splits, workspace, workspace_bytes, err_flag, stream);
 }
 
 }  // namespace
@@ -210,6 +297,37 @@ cai_status cai_mqa_decode(const cai_kv_pool* pools, int32_t num_pools, const int
   if (buf < 0 || buf >= num_pools) return CAI_ERR_INVALID_ARG;
   return decode_common(&pools[buf], 1, q, batch, num_q_heads, block_table, max_pages_per_seq, ctx_len, window,
                        softmax_scale, num_splits, workspace, workspace_bytes, out, lse_out, err_flag, stream);
+}
+
+size_t cai_mqa_decode_layers_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_pages_per_seq,
+                                            int32_t page_size, int32_t num_layers, const int32_t* windows,
+                                            int32_t num_splits) {
+  if (batch <= 0 || num_q_heads <= 0 || max_pages_per_seq <= 0 || !page_size_ok(page_size) || num_layers < 1 ||
+      num_layers > kMaxDecodeJobs || !windows || num_splits < 0 || num_splits > kMaxSplits)
+    return 0;
+  for (int l = 0; l < num_layers; ++l)
+    if (windows[l] < 0) return 0;
+  return layers_workspace_bytes(batch, num_q_heads, 1, max_pages_per_seq, page_size, windows, num_layers,
+                                num_splits);
+}
+
+cai_status cai_mqa_decode_layers(const cai_kv_pool* pools, int32_t num_pools, const int32_t* layer_to_pool,
+                                 int32_t num_layers, const int32_t* windows, const uint16_t* const* q,
+                                 int32_t batch, int32_t num_q_heads, const int32_t* const* block_tables,
+                                 int32_t max_pages_per_seq, const int32_t* ctx_len, float softmax_scale,
+                                 int32_t num_splits, void* workspace, size_t workspace_bytes, float* const* out,
+                                 float* const* lse_out, int32_t* err_flag, void* stream) {
+  if (!pools || num_pools <= 0 || !layer_to_pool || !windows || !q || !block_tables || !out)
+    return CAI_ERR_INVALID_ARG;
+  if (num_layers < 1 || num_layers > kMaxDecodeJobs) return CAI_ERR_UNSUPPORTED;
+  LayerArgs la[kMaxDecodeJobs];
+  for (int l = 0; l < num_layers; ++l) {
+    const int32_t buf = layer_to_pool[l];
+    if (buf < 0 || buf >= num_pools) return CAI_ERR_INVALID_ARG;
+    la[l] = LayerArgs{&pools[buf], q[l], block_tables[l], windows[l], out[l], lse_out ? lse_out[l] : nullptr};
+  }
+  return decode_layers_common(la, num_layers, 1, batch, num_q_heads, max_pages_per_seq, ctx_len, softmax_scale,
+                              num_splits, workspace, workspace_bytes, err_flag, stream);
 }
 
 size_t cai_gqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,

@@ -42,22 +42,35 @@ struct DecodePlan {
 
 constexpr int kMaxKvHeads = 8;         // KV heads (pools) one decode call can read
 
-struct DecodeParams {
-  const uint8_t* pages[kMaxKvHeads];  // the pool of each KV head (one for MQA), same page size and count
-  int32_t num_kv_heads;               // query heads [j*G, (j+1)*G) read KV head j, G = num_heads / num_kv_heads
-  int32_t num_pages;
-  const int32_t* table;
+constexpr int kMaxDecodeJobs = 8;  // layers decoded by one launch
+
+// One layer of a decode launch: its query, output and block table, its window and
+// split plan, and the pool slots its KV heads read (slot0 + j for KV head j).
+struct DecodeJob {
+  int32_t slot0;
+  int32_t window;
+  const int32_t* table;  // [B][max_pages]
   int32_t max_pages;
-  const int32_t* ctx_len;
-  const uint16_t* q;  // bf16 bits [B][Hq][128]
-  int32_t batch, num_heads, window;
-  float scale_log2;   // softmax_scale * log2(e)
+  const uint16_t* q;     // bf16 bits [B][Hq][128]
+  float* out;            // [B][Hq][128]
+  float* lse_out;        // [B][Hq] natural log, nullable
+  float* ws_o;           // [B][max_splits][Hq][128] partial outputs (normalised), null without splits
+  float* ws_lse;         // [B][max_splits][Hq] partial lse, log2 units
   DecodePlan plan;
-  float* out;         // [B][Hq][128]
-  float* lse_out;     // [B][Hq] natural log, nullable
-  float* ws_o;        // [B][max_splits][Hq][128] partial outputs (normalised)
-  float* ws_lse;      // [B][max_splits][Hq] partial lse, log2 units
-  uint32_t* queue;    // [2]: next work item, CTAs finished (both zero between calls)
+  int32_t item0;         // first work item of the layer; items are (b * KV heads + KV head) * max_splits + split
+};
+
+struct DecodeParams {
+  const uint8_t* pages[kMaxKvHeads];  // pool slots, one per (layer's) KV head, same page size
+  int32_t slot_pages[kMaxKvHeads];    // pages in each slot
+  int32_t num_slots;
+  int32_t num_kv_heads;               // query heads [j*G, (j+1)*G) read KV head j, G = num_heads / num_kv_heads
+  const int32_t* ctx_len;             // [B], shared by the layers
+  int32_t batch, num_heads;
+  float scale_log2;                   // softmax_scale * log2(e)
+  int32_t num_jobs, num_items;
+  DecodeJob job[kMaxDecodeJobs];
+  uint32_t* queue;                    // [2]: next work item, CTAs finished (both zero between calls)
   int32_t* err;
 };
 

@@ -161,17 +161,17 @@ __device__ __forceinline__ float warp_max_scatter(const float (&v)[N], int lane)
   return r;
 }
 
-// A work item: one split of one sequence.  kind 0 = tiles to process,
-// 1 = nothing to attend (split 0 writes out = 0, lse = -inf).
+// A work item: one split of one sequence of one layer (job).  kind 0 = tiles to
+// process, 1 = nothing to attend (split 0 writes out = 0, lse = -inf).
 struct Item {
-  int b, kvh, split, start, end, tile0, ntiles;
+  int job, b, kvh, split, start, end, tile0, ntiles;
   bool direct;  // single split: write the final output
   int kind;
   bool invalid;
 };
 
 // Ring entry: [0] b, [1] split, [2] start, [3] end, [4] tile0, [5] ntiles,
-// [6] flags (bit 0 direct, bit 1 invalid, bit 2 kind 1, bit 3 end of work), [7] KV head,
+// [6] flags (bit 0 direct, bit 1 invalid, bit 2 kind 1, bit 3 end of work, bits 4.. job), [7] KV head,
 // [8 .. 40) page ids of the item's first tiles (one id batch, see batch_page).
 __device__ __forceinline__ Item ring_item(const volatile int32_t* e, bool& done) {
   Item it;
@@ -187,6 +187,7 @@ __device__ __forceinline__ Item ring_item(const volatile int32_t* e, bool& done)
   it.invalid = (f >> 1) & 1;
   it.kind = (f >> 2) & 1;
   done = (f >> 3) & 1;
+  it.job = f >> 4;
   return it;
 }
 
@@ -195,7 +196,8 @@ template <int P>
 __device__ __forceinline__ int32_t tile_page(const DecodeParams& p, const Item& it, int t, int ps) {
   const int t0 = (it.tile0 + t) * T + ps * P;
   if (t0 + P <= it.start || t0 >= it.end) return (int32_t)kNoPage;
-  return p.table[(int64_t)it.b * p.max_pages + t0 / P];
+  const DecodeJob& jb = p.job[it.job];
+  return jb.table[(int64_t)it.b * jb.max_pages + t0 / P];
 }
 
 // Id batch `batch` of an item: lane l holds page slot l % (T/P) of tile
@@ -207,17 +209,22 @@ __device__ __forceinline__ int32_t batch_page(const DecodeParams& p, const Item&
   return t < it.ntiles ? tile_page<P>(p, it, t, lane % PPT) : (int32_t)kNoPage;
 }
 
-// Work item idx = (b * num_kv_heads + kv head) * max_splits + split.
-// kind 2 = an empty split, never published.
+// Work item idx: the job whose range holds it, then, within the job,
+// (b * num_kv_heads + kv head) * max_splits + split.  kind 2 = an empty split, never published.
 template <int P>
 __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
   Item it;
-  const int per_b = p.num_kv_heads * p.plan.max_splits;
+  int j = 0;
+  while (j + 1 < p.num_jobs && idx >= p.job[j + 1].item0) ++j;
+  const DecodeJob& jb = p.job[j];
+  it.job = j;
+  idx -= jb.item0;
+  const int per_b = p.num_kv_heads * jb.plan.max_splits;
   it.b = idx / per_b;
   const int r = idx - it.b * per_b;
-  it.kvh = r / p.plan.max_splits;
-  it.split = r - it.kvh * p.plan.max_splits;
-  const SeqSplits sp = seq_splits(p.ctx_len[it.b], p.window, p.max_pages * P, p.plan.chunk);
+  it.kvh = r / jb.plan.max_splits;
+  it.split = r - it.kvh * jb.plan.max_splits;
+  const SeqSplits sp = seq_splits(p.ctx_len[it.b], jb.window, jb.max_pages * P, jb.plan.chunk);
   it.invalid = !sp.valid;
   it.direct = sp.nsplit == 1;
   it.ntiles = 0;
@@ -231,8 +238,8 @@ __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
     return it;
   }
   it.kind = 0;
-  it.start = sp.lo + it.split * p.plan.chunk;
-  it.end = min(sp.hi, it.start + p.plan.chunk);
+  it.start = sp.lo + it.split * jb.plan.chunk;
+  it.end = min(sp.hi, it.start + jb.plan.chunk);
   it.tile0 = it.start / T;
   it.ntiles = (it.end - 1) / T - it.tile0 + 1;
   return it;
@@ -240,7 +247,7 @@ __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
 
 struct DecodeArgs {
   DecodeParams p;
-  CUtensorMap kv_map[kMaxKvHeads];  // each KV head's pool as rows of 128 bytes; box = the 2P code rows of a page
+  CUtensorMap kv_map[kMaxKvHeads];  // each pool slot as rows of 128 bytes; box = the 2P code rows of a page
 };
 
 template <int P, int HN>
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_heads;                   // query heads per sequence (row stride of q and out)
   const int G = Hq / p.num_kv_heads;            // query heads per KV head (the rows of one item)
-  const int num_items = p.batch * p.num_kv_heads * p.plan.max_splits;
+  const int num_items = p.num_items;
 
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
@@ -369,7 +376,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
             id = batch_page<P>(p, it, 0, lane);
             // Warm L2 with the item's block-table entries (32 ids per 128-byte line, one line per lane).
             const int first = it.start / P, last = (it.end - 1) / P;
-            const int32_t* row = p.table + (int64_t)it.b * p.max_pages;
+            const int32_t* row = p.job[it.job].table + (int64_t)it.b * p.job[it.job].max_pages;
             for (int pg = (first & ~31) + lane * 32; pg <= last; pg += 32 * 32) prefetch_l2(row + pg);
           }
         }
@@ -385,7 +392,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
             e[3] = it.end;
             e[4] = it.tile0;
             e[5] = it.ntiles;
-            e[6] = (it.direct ? 1 : 0) | (it.invalid ? 2 : 0) | (it.kind == 1 ? 4 : 0);
+            e[6] = (it.direct ? 1 : 0) | (it.invalid ? 2 : 0) | (it.kind == 1 ? 4 : 0) | (it.job << 4);
             e[7] = it.kvh;
           } else {
             e[6] = 8;
@@ -417,8 +424,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         if (done || *abort_flag) break;
         if (it.kind != 0) continue;
         bool ok = true;
-        const CUtensorMap* kv_map = &args.kv_map[it.kvh];
-        const uint8_t* pages = p.pages[it.kvh];
+        const int slot = p.job[it.job].slot0 + it.kvh;
+        const CUtensorMap* kv_map = &args.kv_map[slot];
+        const uint8_t* pages = p.pages[slot];
+        const int slot_pages = p.slot_pages[slot];
         int32_t ids_next = it.ntiles > TPB ? batch_page<P>(p, it, 1, lane) : (int32_t)kNoPage;
         for (int t = 0; t < it.ntiles && ok; ++t) {
           if (t > 0 && t % TPB == 0) {
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
             }
             const int32_t pid = __shfl_sync(0xffffffffu, ids, (t % TPB) * PPT + hf * SPS + lane % SPS);
             const bool live = lane < SPS && pid != kNoPage;
-            const bool in_range = pid >= 0 && pid < p.num_pages;
+            const bool in_range = pid >= 0 && pid < slot_pages;
             if (live && !in_range) set_err(p.err, CAI_DEVERR_PAGE);
             const uint32_t okm = __ballot_sync(0xffffffffu, live && in_range);
             if (lane == 0) {
@@ -534,7 +543,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         for (int i = 0; i < kQUnits; ++i) {
           const int u = i * 256 + ctid;
           const int n = (u & 7) | ((u >> 7) << 3), k8 = (u >> 3) & 15;
-          qv[i] = n < G ? __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)it.b * Hq + it.kvh * G + n) * kHeadDim +
+          qv[i] = n < G ? __ldg(reinterpret_cast<const uint4*>(p.job[it.job].q + ((int64_t)it.b * Hq + it.kvh * G + n) * kHeadDim +
                                                                 k8 * 8))
                         : make_uint4(0u, 0u, 0u, 0u);
         }
@@ -671,8 +680,9 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         // Nothing to attend (L = 0) or an invalid length: out = 0, lse = -inf.
         if (it.invalid && sw == 0 && lane == 0) set_err(p.err, CAI_DEVERR_LENGTH);
         const int64_t hb = (int64_t)it.b * Hq + it.kvh * G;  // first output head of the item
-        for (int h = h0; h < h0 + HH && h < G; ++h) p.out[(hb + h) * kHeadDim + tok] = 0.0f;
-        if (p.lse_out && quarter == 0 && lane < HH && h0 + lane < G) p.lse_out[hb + h0 + lane] = -INFINITY;
+        const DecodeJob& jb = p.job[it.job];
+        for (int h = h0; h < h0 + HH && h < G; ++h) jb.out[(hb + h) * kHeadDim + tok] = 0.0f;
+        if (jb.lse_out && quarter == 0 && lane < HH && h0 + lane < G) jb.lse_out[hb + h0 + lane] = -INFINITY;
         continue;
       }
       float l[HH];
@@ -809,10 +819,11 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       // the LSEs into the raise exchange, unused until then too).  The output is
       // 16-byte aligned (checked on the host); an LSE array that is not, or a row
       // of fewer than 4 LSEs, takes plain stores.
-      float* dst_o = it.direct ? p.out + ((int64_t)it.b * Hq + it.kvh * G) * kHeadDim
-                               : p.ws_o + (((int64_t)it.b * p.plan.max_splits + it.split) * Hq + it.kvh * G) * kHeadDim;
-      float* dst_lse = it.direct ? (p.lse_out ? p.lse_out + (int64_t)it.b * Hq + it.kvh * G : nullptr)
-                                 : p.ws_lse + ((int64_t)it.b * p.plan.max_splits + it.split) * Hq + it.kvh * G;
+      const DecodeJob& jb = p.job[it.job];
+      float* dst_o = it.direct ? jb.out + ((int64_t)it.b * Hq + it.kvh * G) * kHeadDim
+                               : jb.ws_o + (((int64_t)it.b * jb.plan.max_splits + it.split) * Hq + it.kvh * G) * kHeadDim;
+      float* dst_lse = it.direct ? (jb.lse_out ? jb.lse_out + (int64_t)it.b * Hq + it.kvh * G : nullptr)
+                                 : jb.ws_lse + ((int64_t)it.b * jb.plan.max_splits + it.split) * Hq + it.kvh * G;
       const bool bulk_lse = dst_lse != nullptr && (reinterpret_cast<uintptr_t>(dst_lse) & 15u) == 0 && (G & 3) == 0;
       float* lse_stage = wmax;
       if (quarter == 0 && lane < HH) {
@@ -863,7 +874,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
 
 // One warp per (sequence, head): merge the partial outputs of the splits by
 // their log-sum-exp: out = sum_j 2^(lse_j - M) o_j / sum_j 2^(lse_j - M).
-__global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int page_size) {
+__global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int job, int page_size) {
   grid_dependency_wait();
   grid_launch_dependents();
   const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
@@ -871,10 +882,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
   const int Hq = p.num_heads;
   if (gw >= p.batch * Hq) return;
   const int b = gw / Hq, h = gw - b * Hq;
-  const SeqSplits sp = seq_splits(p.ctx_len[b], p.window, p.max_pages * page_size, p.plan.chunk);
+  const DecodeJob& jb = p.job[job];
+  const SeqSplits sp = seq_splits(p.ctx_len[b], jb.window, jb.max_pages * page_size, jb.plan.chunk);
   if (!sp.valid || sp.nsplit <= 1) return;  // written by the decode kernel itself
-  const int S = p.plan.max_splits;
-  const float* lse = p.ws_lse + (int64_t)b * S * Hq + h;
+  const int S = jb.plan.max_splits;
+  const float* lse = jb.ws_lse + (int64_t)b * S * Hq + h;
   float M = -INFINITY;
   for (int j = 0; j < sp.nsplit; ++j) M = fmaxf(M, lse[(int64_t)j * Hq]);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -882,7 +894,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
   if (M != -INFINITY) {
     for (int j = 0; j < sp.nsplit; ++j) {
       const float w = ex2_approx(lse[(int64_t)j * Hq] - M);
-      const float4 o = reinterpret_cast<const float4*>(p.ws_o + (((int64_t)b * S + j) * Hq + h) * kHeadDim)[lane];
+      const float4 o = reinterpret_cast<const float4*>(jb.ws_o + (((int64_t)b * S + j) * Hq + h) * kHeadDim)[lane];
       acc.x = fmaf(w, o.x, acc.x);
       acc.y = fmaf(w, o.y, acc.y);
       acc.z = fmaf(w, o.z, acc.z);
@@ -891,9 +903,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
     }
   }
   const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-  reinterpret_cast<float4*>(p.out + ((int64_t)b * Hq + h) * kHeadDim)[lane] =
+  reinterpret_cast<float4*>(jb.out + ((int64_t)b * Hq + h) * kHeadDim)[lane] =
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (p.lse_out && lane == 0) p.lse_out[(int64_t)b * Hq + h] = wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
+  if (jb.lse_out && lane == 0) jb.lse_out[(int64_t)b * Hq + h] = wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
 // The page pool as a 2-D tensor of 128-byte rows (a page of P tokens is
@@ -948,15 +960,18 @@ cudaError_t launch_decode_ph(const DecodeParams& p, cudaStream_t stream) {
   }
   DecodeArgs a;
   a.p = p;
-  for (int j = 0; j < p.num_kv_heads; ++j)
-    if (!encode_pool_map(&a.kv_map[j], p.pages[j], p.num_pages, P)) return cudaErrorInvalidValue;
-  const int64_t items = (int64_t)p.batch * p.num_kv_heads * p.plan.max_splits;
+  for (int j = 0; j < p.num_slots; ++j)
+    if (!encode_pool_map(&a.kv_map[j], p.pages[j], p.slot_pages[j], P)) return cudaErrorInvalidValue;
+  const int64_t items = p.num_items;
   const int grid = (int)(items < num_sms() ? items : num_sms());
   cudaError_t e = launch_pdl(decode_kernel<P, HN>, dim3(grid), dim3(Roles<HN>::kThreads), Layout<HN>::kSmemBytes,
                              stream, a);
-  if (e != cudaSuccess || p.plan.max_splits <= 1) return e;
-  const int64_t warps = (int64_t)p.batch * p.num_heads;
-  return launch_pdl(combine_kernel, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, stream, p, P);
+  for (int j = 0; e == cudaSuccess && j < p.num_jobs; ++j) {
+    if (p.job[j].plan.max_splits <= 1) continue;
+    const int64_t warps = (int64_t)p.batch * p.num_heads;
+    e = launch_pdl(combine_kernel, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, stream, p, j, P);
+  }
+  return e;
 }
 
 template <int P>

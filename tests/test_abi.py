@@ -108,6 +108,43 @@ def test_decode_validation(lib):
     assert call(pools=bad, npools=1, l2p=(ctypes.c_int32 * 1)(0), nlayers=1) == 2
 
 
+def test_decode_layers_validation(lib):
+    pools = (cai.cai_kv_pool * 2)(_pool(), _pool())
+
+    def arr(ctype, vals):
+        return (ctype * len(vals))(*vals)
+
+    def call(n=3, **kw):
+        a = dict(pools=pools, npools=2, l2p=arr(ctypes.c_int32, [0, 0, 1][:n] + [0] * max(0, n - 3)),
+                 windows=arr(ctypes.c_int32, [1024, 1024, 0][:n] + [0] * max(0, n - 3)),
+                 q=arr(ctypes.c_void_p, [FAKE] * n), batch=2, hq=8, tables=arr(ctypes.c_void_p, [FAKE] * n),
+                 maxp=64, ctx=FAKE, scale=0.088, splits=0, ws=None, ws_bytes=0,
+                 out=arr(ctypes.c_void_p, [FAKE] * n))
+        a.update(kw)
+        return lib.cai_mqa_decode_layers(a["pools"], a["npools"], a["l2p"], n, a["windows"], a["q"], a["batch"],
+                                         a["hq"], a["tables"], a["maxp"], a["ctx"], a["scale"], a["splits"], a["ws"],
+                                         a["ws_bytes"], a["out"], None, None, None)
+
+    assert call(n=0) == 2
+    assert call(n=9) == 2
+    assert call(l2p=arr(ctypes.c_int32, [0, 0, 2])) == 1  # buffer index out of range
+    assert call(windows=arr(ctypes.c_int32, [1024, -1, 0])) == 1
+    assert call(q=arr(ctypes.c_void_p, [FAKE, FAKE + 4, FAKE])) == 1
+    assert call(out=arr(ctypes.c_void_p, [FAKE, None, FAKE])) == 1
+    assert call(tables=None) == 1
+    assert call(hq=65) == 2
+    assert call(scale=float("nan")) == 1
+    assert call(batch=0) == 0
+    assert call() == 3  # no workspace
+    assert call(ws=FAKE, ws_bytes=16) == 3
+    mixed = (cai.cai_kv_pool * 2)(_pool(), _pool(page_size=32))
+    assert call(pools=mixed) == 1  # one page size per call
+    windows = arr(ctypes.c_int32, [1024, 0])
+    one = lib.cai_mqa_decode_workspace_size(2, 8, 64, 16, 0, 0)
+    both = lib.cai_mqa_decode_layers_workspace_size(2, 8, 64, 16, 2, windows, 0)
+    assert both >= one and lib.cai_mqa_decode_layers_workspace_size(2, 8, 64, 16, 9, windows, 0) == 0
+
+
 def test_prefill_varlen_validation(lib):
     pool = _pool()
 

@@ -236,6 +236,62 @@ def test_decode_long_global_config_sampled():
         check_layer(cache, 0, out, lse, seqs=[0, int(np.argmax(w.ctx_len))])
 
 
+def run_layers(cache, num_splits=0):
+    w = cache.w
+    nl = len(w.layer_windows)
+    qs = [cache.decode_q(layer) for layer in range(nl)]
+    outs = [torch.full((w.batch, w.num_q_heads, 128), float("nan"), device="cuda") for _ in range(nl)]
+    lses = [torch.full((w.batch, w.num_q_heads), float("nan"), device="cuda") for _ in range(nl)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache.decode_layers(qs, outs, lses, num_splits=num_splits, err=err)
+    torch.cuda.synchronize()
+    return qs, outs, lses, int(err.item())
+
+
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_decode_layers_one_launch(num_splits):
+    """The six layers of the hybrid step in one launch: within tolerance of the oracle, and bit
+    for bit what the per-layer launches give (same work split, same per-item arithmetic)."""
+    w = synth.workload(3, batch=6)
+    cache = build(w)
+    qs, outs, lses, err = run_layers(cache, num_splits)
+    assert err == 0
+    for layer in range(len(w.layer_windows)):
+        ref_o = torch.empty_like(outs[layer])
+        ref_l = torch.empty_like(lses[layer])
+        cache.decode(layer, qs[layer], ref_o, ref_l, num_splits=num_splits)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[layer], ref_o) and torch.equal(lses[layer], ref_l), layer
+        check_layer(cache, layer, outs[layer].cpu().numpy(), lses[layer].cpu().numpy())
+
+
+def test_decode_layers_eight_layers_mixed_windows():
+    """Eight layers (the most one launch takes) on four shared buffers, windows from 1 token to global,
+    with an empty sequence and lengths across page and tile edges."""
+    w = make_workload(5, 8, 16, [1, 300, 1000, 2500, 0], windows=(0, 1024, 300, 16, 0, 128, 1024, 1),
+                      l2b=(0, 0, 1, 1, 2, 2, 3, 3), seed=44)
+    cache = build(w)
+    _, outs, lses, err = run_layers(cache)
+    assert err == 0
+    for layer in range(8):
+        o, l = outs[layer].cpu().numpy(), lses[layer].cpu().numpy()
+        assert not o[4].any() and np.all(np.isneginf(l[4]))
+        check_layer(cache, layer, o, l, seqs=range(4))
+
+
+def test_decode_layers_invalid_length_flag():
+    w = make_workload(3, 8, 16, [0, 40, 40], windows=(0, 1024), l2b=(0, 0), seed=45)
+    cache = build(w)
+    cache.ctx_len[2] = cache.max_pages_per_seq * 16 + 1  # beyond the table
+    _, outs, lses, err = run_layers(cache)
+    assert err == cai.CAI_DEVERR_LENGTH
+    for layer in range(2):
+        o, l = outs[layer].cpu().numpy(), lses[layer].cpu().numpy()
+        assert not o[0].any() and np.all(np.isneginf(l[0]))
+        ref, ref_l = oracle_decode(w, layer, 1)
+        assert np.abs(o[1] - ref).max() <= ATOL and np.abs(l[1] - ref_l).max() <= ATOL
+
+
 def test_decode_empty_and_invalid_lengths():
     w = make_workload(3, 8, 16, [0, 40, 40], seed=41)
     cache = build(w)

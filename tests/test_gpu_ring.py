@@ -78,6 +78,25 @@ def test_ring_hybrid_layers_share_buffers():
         check_decode(cache, layer, out, lse)
 
 
+def test_ring_layers_one_launch():
+    # The same three layers in one launch: ring tables for the local buffer, the full table for the global one.
+    L = [200, 1500, 4097, 64]
+    w = synth.Workload("ring-hybrid", len(L), 8, 16, np.asarray(L, dtype=np.int64), [512, 512, 0], [0, 0, 1],
+                       n_new=1, seed=43)
+    cache = harness.PagedCache(w, local_ring=True)
+    cache.fill()
+    cache.append_step()
+    qs = [cache.decode_q(layer) for layer in range(3)]
+    outs = [torch.full((w.batch, w.num_q_heads, 128), float("nan"), device="cuda") for _ in range(3)]
+    lses = [torch.full((w.batch, w.num_q_heads), float("nan"), device="cuda") for _ in range(3)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache.decode_layers(qs, outs, lses, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for layer in range(3):
+        check_decode(cache, layer, outs[layer].cpu().numpy(), lses[layer].cpu().numpy())
+
+
 def test_ring_prefill_window():
     W, n_new, P = 300, 64, 16
     L = np.asarray([2000, 64, 65 + W, 4001], dtype=np.int64)
