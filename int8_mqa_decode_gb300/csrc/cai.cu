@@ -12,19 +12,24 @@ static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static inline bool page_size_ok(int32_t P) { return P == 16 || P == 32 || P == 64; }
+constexpr int32_t kItemsPerSmAlone = 32;  // a global layer's split target when launched alone
+constexpr int32_t kItemsPerSmMixed = 22;  // ... when launched together with local layers
 
 // Split plan.  The attended span of a sequence is at most `span` tokens (the
 // window, or the block-table capacity for a global layer).  Chunks are
-// multiples of the 128-token tile.  Automatic choice: about 32 work items per
-// SM for the expected total work of a global layer (half the capacity per
-// sequence), chunks of 512 to 16384 tokens, at most 64 splits -- short items let
-// the dynamic queue even out the SMs whatever the length mix (measured on the
-// hybrid step: 8 items per SM 0.453 ms, 16 0.422, 32 0.396, 64 0.431); a local
-// layer is not split when its batch alone gives every SM a sequence (each extra
-// split costs its partial's write and read, about an eighth of a 1024-token
-// window at 32 heads; 2 and 4 splits measured slower).
+// multiples of the 128-token tile.  Automatic choice: about `items_per_sm` work
+// items per SM for the expected total work of a global layer (half the capacity
+// per sequence), chunks of 512 to 16384 tokens, at most 64 splits -- short items
+// let the dynamic queue even out the SMs whatever the length mix, long ones pay
+// fewer item boundaries.  Measured on the hybrid step: a global layer launched
+// alone is best at 32 items per SM (8: 0.453 ms, 16 0.422, 32 0.396, 64 0.431);
+// launched with the local layers, whose items then even out the tail, at 22
+// (8: 0.304 ms, 16 0.264, 20 0.254, 22 0.253, 24 0.254, 28 0.259, 32 0.270).  A
+// local layer is not split when its batch alone gives every SM a sequence (each
+// extra split costs its partial's write and read, about an eighth of a
+// 1024-token window at 32 heads; 2 and 4 splits measured slower).
 DecodePlan plan_decode(int32_t batch, int32_t max_pages_per_seq, int32_t page_size, int32_t window,
-                       int32_t num_splits, int32_t sms) {
+                       int32_t num_splits, int32_t sms, int32_t items_per_sm) {
   const int64_t cap = (int64_t)max_pages_per_seq * page_size;
   const int64_t span = window > 0 ? (window < cap ? window : cap) : cap;
   int64_t chunk;
@@ -35,7 +40,7 @@ DecodePlan plan_decode(int32_t batch, int32_t max_pages_per_seq, int32_t page_si
     chunk = round_up(ceil_div(span, want), kDecodeTile);
   } else {
     const int64_t expected = (int64_t)batch * ((span + 1) / 2);
-    chunk = round_up(ceil_div(expected, 32ll * sms), kDecodeTile);
+    chunk = round_up(ceil_div(expected, (int64_t)items_per_sm * sms), kDecodeTile);
     if (chunk < 512) chunk = 512;
     if (chunk > 16384) chunk = 16384;
   }
@@ -130,7 +135,8 @@ size_t cai_mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t
       num_splits < 0 || num_splits > kMaxSplits)
     return 0;
   return workspace_bytes_for(batch, num_q_heads,
-                             plan_decode(batch, max_pages_per_seq, page_size, window, num_splits, num_sms()));
+                             plan_decode(batch, max_pages_per_seq, page_size, window, num_splits, num_sms(),
+                                         kItemsPerSmAlone));
 }
 
 namespace {
@@ -147,12 +153,20 @@ struct LayerArgs {
 
 // Workspace bytes of a launch over these windows: the queue header, then for every
 // layer that is split its partial outputs and log-sum-exps.
+// Global layers launched together with local ones take longer items.
+int32_t items_per_sm_for(const int32_t* windows, int32_t n) {
+  bool local = false;
+  for (int l = 0; l < n; ++l) local = local || windows[l] > 0;
+  return n > 1 && local ? kItemsPerSmMixed : kItemsPerSmAlone;
+}
+
 size_t layers_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_pages_per_seq,
                               int32_t page_size, const int32_t* windows, int32_t n, int32_t num_splits) {
   size_t total = kWorkspaceHeader;
+  const int32_t ips = items_per_sm_for(windows, n);
   for (int l = 0; l < n; ++l) {
     const DecodePlan plan =
-        plan_decode(batch * num_kv_heads, max_pages_per_seq, page_size, windows[l], num_splits, num_sms());
+        plan_decode(batch * num_kv_heads, max_pages_per_seq, page_size, windows[l], num_splits, num_sms(), ips);
     total += workspace_bytes_for(batch, num_q_heads, plan) - kWorkspaceHeader;
   }
   return total;
@@ -249,7 +263,8 @@ cai_status decode_layers_common(const LayerArgs* layers, int32_t n, int32_t num_
     jb.q = la.q;
     jb.out = la.out;
     jb.lse_out = la.lse_out;
-    jb.plan = plan_decode(batch * num_kv_heads, max_pages_per_seq, P, la.window, num_splits, num_sms());
+    jb.plan = plan_decode(batch * num_kv_heads, max_pages_per_seq, P, la.window, num_splits, num_sms(),
+                          items_per_sm_for(windows, n));
     jb.ws_o = nullptr;
     jb.ws_lse = nullptr;
     if (jb.plan.max_splits > 1) {
@@ -339,7 +354,7 @@ size_t cai_gqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t
   if (max_pages_per_seq <= 0 || !page_size_ok(page_size) || window < 0 || num_splits < 0 || num_splits > kMaxSplits)
     return 0;
   return workspace_bytes_for(batch, num_q_heads, plan_decode(batch * num_kv_heads, max_pages_per_seq, page_size,
-                                                             window, num_splits, num_sms()));
+                                                             window, num_splits, num_sms(), kItemsPerSmAlone));
 }
 
 cai_status cai_gqa_decode(const cai_kv_pool* kv_pools, int32_t num_kv_heads, const uint16_t* q, int32_t batch,

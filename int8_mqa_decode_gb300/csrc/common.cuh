@@ -130,7 +130,7 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 
 // Host side: the split plan for a launch (also used by the workspace query).
 DecodePlan plan_decode(int32_t batch, int32_t max_pages_per_seq, int32_t page_size, int32_t window,
-                       int32_t num_splits, int32_t num_sms);
+                       int32_t num_splits, int32_t num_sms, int32_t items_per_sm);
 int num_sms();
 
 // Kernel launchers (return cudaGetLastError()).

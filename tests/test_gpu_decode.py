@@ -251,7 +251,9 @@ def run_layers(cache, num_splits=0):
 @pytest.mark.parametrize("num_splits", [0, 3])
 def test_decode_layers_one_launch(num_splits):
     """The six layers of the hybrid step in one launch: within tolerance of the oracle, and bit
-    for bit what the per-layer launches give (same work split, same per-item arithmetic)."""
+    for bit what the per-layer launches give wherever both use the same work split (a fixed split
+    count; the local layers always -- the automatic plan gives a global layer longer items when it
+    shares the launch with local layers)."""
     w = synth.workload(3, batch=6)
     cache = build(w)
     qs, outs, lses, err = run_layers(cache, num_splits)
@@ -261,7 +263,8 @@ def test_decode_layers_one_launch(num_splits):
         ref_l = torch.empty_like(lses[layer])
         cache.decode(layer, qs[layer], ref_o, ref_l, num_splits=num_splits)
         torch.cuda.synchronize()
-        assert torch.equal(outs[layer], ref_o) and torch.equal(lses[layer], ref_l), layer
+        if num_splits > 0 or w.layer_windows[layer] > 0:
+            assert torch.equal(outs[layer], ref_o) and torch.equal(lses[layer], ref_l), layer
         check_layer(cache, layer, outs[layer].cpu().numpy(), lses[layer].cpu().numpy())
 
 
