@@ -567,7 +567,7 @@ def run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world, layered=Fa
     """Same step through the public API with inputs in pinned host memory: every step copies its
     inputs host -> device and its outputs device -> host inside the timed region.  As a serving loop
     would, the copies run on their own streams: inputs are double-buffered and copied while the
-    previous step computes, and each layer's output is copied back while the next layer decodes."""
+    previous step computes, and outputs are copied back while the next work runs."""
     import torch
     import int8_mqa_decode_gb300 as cai
 
@@ -643,8 +643,8 @@ def run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world, layered=Fa
     return {"value": world * toks_step * args.steps / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps,
             "copies": "pinned host buffers; inputs double-buffered and copied on their own stream while the "
-                      "previous step computes; each layer's output copied back on a third stream while the "
-                      "next layer decodes"}
+                      "previous step computes; outputs copied back on a third stream while the next step "
+                      + ("computes" if layered else "layer decodes")}
 
 
 # ----------------------------------------------------------------------------- reference arm (the oracle)

@@ -102,12 +102,12 @@ struct Roles {
   // Registers per thread, launched with kRegsLaunch and resized per warpgroup:
   //  32 heads: 16 warps (4 per SM sub-partition) at 128 = 65536; then 56 / 104 / 232:
   //            128 * (56 + 2 * 104 + 232) = 63488, per sub-partition 32 * 496 = 15872 <= 16384.
-  //  64 heads: 20 warps (5 per sub-partition) at 96 = 61440; then 48 / 88 / 128:
-  //            128 * (48 + 2 * 88 + 2 * 128) = 61440, per sub-partition 32 * 480 = 15360 <= 16384.
+  //  64 heads: 20 warps (5 per sub-partition) at 96 = 61440; then 48 / 96 / 120:
+  //            128 * (48 + 2 * 96 + 2 * 120) = 61440, per sub-partition 32 * 480 = 15360 <= 16384.
   static constexpr int kRegsLaunch = HN <= 32 ? 128 : 96;  // checked on the host before the first launch
   static constexpr int kRegsCtl = HN <= 32 ? 56 : 48;
-  static constexpr int kRegsConv = HN <= 32 ? 104 : 88;
-  static constexpr int kRegsSoft = HN <= 32 ? 232 : 128;
+  static constexpr int kRegsConv = HN <= 32 ? 104 : 96;
+  static constexpr int kRegsSoft = HN <= 32 ? 232 : 120;
   static_assert(128 * kRegsCtl + 32 * kConvWarps * kRegsConv + 32 * kSoftWarps * kRegsSoft <= kRegsLaunch * kThreads,
                 "register split");
   static_assert(32 * (kRegsCtl + 2 * kRegsConv + (kSoftWarps / 4) * kRegsSoft) <= 16384, "sub-partition registers");
