@@ -468,9 +468,8 @@ def run_gpu(args, rank, world):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n_events)] for _ in range(args.steps)]
 
     def step(record=None):
-        for buf, pool in enumerate(cache.pools):
-            k, v, start = step_kv[buf]
-            cai.cai_kv_append(pool, k, v, cache.tables[buf], start)
+        cai.cai_kv_append_pools(cache.pools, [k for k, _, _ in step_kv], [v for _, v, _ in step_kv], cache.tables,
+                                [s for _, _, s in step_kv])
         if layered:
             if record is not None:
                 record[0].record(stream)
@@ -492,7 +491,7 @@ def run_gpu(args, rank, world):
         1 for layer in range(nl)
         if cai.cai_mqa_decode_workspace_size(w.batch, w.num_q_heads, cache.max_pages_per_seq, w.page_size,
                                              w.layer_windows[layer], args.num_splits) > 256)
-    launches_per_step = w.num_buffers + (1 if layered else nl) + splits_layers
+    launches_per_step = 1 + (1 if layered else nl) + splits_layers
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -603,9 +602,8 @@ def run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world, layered=Fa
                 dq.copy_(hq, non_blocking=True)
             ev_in[b].record(s_in)
         comp.wait_event(ev_in[b])
-        for buf, pool in enumerate(cache.pools):
-            dk, dv, ds = d_kv[b][buf]
-            cai.cai_kv_append(pool, dk, dv, cache.tables[buf], ds)
+        cai.cai_kv_append_pools(cache.pools, [dk for dk, _, _ in d_kv[b]], [dv for _, dv, _ in d_kv[b]],
+                                cache.tables, [ds for _, _, ds in d_kv[b]])
         if layered:
             if not first_use[b]:
                 for layer in range(nl):

@@ -126,10 +126,10 @@ class PagedCache:
         return q.view(w.batch, w.n_new, w.num_q_heads, 128)
 
     def append_step(self, err=None) -> None:
-        """Append the step's new tokens to every buffer."""
-        for buf, pool in enumerate(self.pools):
-            k, v, start = self.step_kv(buf)
-            cai.cai_kv_append(pool, k, v, self.tables[buf], start, err_flag=err)
+        """Append the step's new tokens to every buffer (one launch)."""
+        kv = [self.step_kv(buf) for buf in range(len(self.pools))]
+        cai.cai_kv_append_pools(self.pools, [k for k, _, _ in kv], [v for _, v, _ in kv], self.tables,
+                                [s for _, _, s in kv], err_flag=err)
 
     def workspace(self, layer: int, num_splits: int = 0) -> torch.Tensor | None:
         w = self.w

@@ -92,6 +92,21 @@ cai_status cai_kv_append(const cai_kv_pool* pool, const float* k_new, const floa
                          int32_t n_new, const int32_t* block_table, int32_t max_pages_per_seq,
                          const int32_t* start_pos, int32_t* err_flag, void* stream);
 
+/* The append of one step into several KV buffers in one launch: for every i the
+ * same as cai_kv_append(&pools[i], k_new[i], v_new[i], batch, n_new,
+ * block_tables[i], max_pages_per_seq, start_pos[i], ...) (neighbouring layers
+ * that share a buffer append once; "Character.AI: inference optimization"
+ * page, 03 Model architecture).
+ *   pools, num_pools       host array of 1..8 KV buffers
+ *   k_new, v_new           host arrays [num_pools] of device fp32 [batch][n_new][head_dim], 16-byte aligned
+ *   block_tables           host array [num_pools] of device int32 [batch][max_pages_per_seq]
+ *   start_pos              host array [num_pools] of device int32 [batch]
+ * Errors as for cai_kv_append; nothing is launched when an argument is rejected. */
+cai_status cai_kv_append_pools(const cai_kv_pool* pools, int32_t num_pools, const float* const* k_new,
+                               const float* const* v_new, int32_t batch, int32_t n_new,
+                               const int32_t* const* block_tables, int32_t max_pages_per_seq,
+                               const int32_t* const* start_pos, int32_t* err_flag, void* stream);
+
 /* Bytes of workspace cai_mqa_decode needs for these arguments: a 256-byte
  * header (the counters of the kernel's work queue) plus, when sequences are
  * split, the partial outputs.  Arguments as for cai_mqa_decode.  The automatic

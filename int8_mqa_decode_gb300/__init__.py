@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "CaiError", "CaiUnavailable", "KVPool", "library_path", "load", "cai_page_bytes", "cai_status_string",
-    "cai_kv_append", "cai_mqa_decode_workspace_size", "cai_mqa_decode", "cai_mqa_decode_no_alloc",
+    "cai_kv_append", "cai_kv_append_pools", "cai_mqa_decode_workspace_size", "cai_mqa_decode", "cai_mqa_decode_no_alloc",
     "cai_mqa_decode_layers_workspace_size", "cai_mqa_decode_layers",
     "cai_mqa_prefill_workspace_size",
     "cai_mqa_prefill_chunk", "cai_mqa_prefill_varlen", "cai_gqa_decode", "cai_gqa_decode_workspace_size",
@@ -77,6 +77,8 @@ def load():
     lib.cai_last_cuda_error.restype = ctypes.c_char_p
     lib.cai_kv_append.argtypes = [pool_p, vp, vp, i32, i32, vp, i32, vp, vp, vp]
     lib.cai_kv_append.restype = ctypes.c_int
+    lib.cai_kv_append_pools.argtypes = [pool_p, i32, vp, vp, i32, i32, vp, i32, vp, vp, vp]
+    lib.cai_kv_append_pools.restype = ctypes.c_int
     lib.cai_mqa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.cai_mqa_decode_workspace_size.restype = sz
     lib.cai_mqa_decode.argtypes = [pool_p, i32, vp, i32, i32, vp, i32, i32, vp, i32, vp, i32, ctypes.c_float, i32,
@@ -187,6 +189,28 @@ def cai_kv_append(pool: KVPool, k_new: torch.Tensor, v_new: torch.Tensor, block_
         batch, n_new, _ptr(block_table, "block_table", torch.int32), block_table.shape[-1],
         _ptr(start_pos, "start_pos", torch.int32, (batch,)), _ptr(err_flag, "err_flag", torch.int32), _stream(stream))
     _check(st, "cai_kv_append")
+
+
+def cai_kv_append_pools(pools: Sequence[KVPool], k_new: Sequence[torch.Tensor], v_new: Sequence[torch.Tensor],
+                        block_tables: Sequence[torch.Tensor], start_pos: Sequence[torch.Tensor],
+                        err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """cai_kv_append into every pool of the list in one launch (entry i of each list goes to pools[i])."""
+    n = len(pools)
+    if not (len(k_new) == len(v_new) == len(block_tables) == len(start_pos) == n):
+        raise ValueError("k_new, v_new, block_tables and start_pos must have one entry per pool")
+    batch, n_new = (k_new[0].shape[0], k_new[0].shape[1]) if k_new[0].dim() == 3 else (0, 0)
+    max_pages = block_tables[0].shape[-1]
+    for t in block_tables:
+        if t.shape[-1] != max_pages:
+            raise ValueError("block tables of one call must have the same width")
+    shape = (batch, n_new, HEAD_DIM)
+    ks = (ctypes.c_void_p * n)(*[_ptr(t, "k_new", torch.float32, shape) for t in k_new])
+    vs = (ctypes.c_void_p * n)(*[_ptr(t, "v_new", torch.float32, shape) for t in v_new])
+    ts = (ctypes.c_void_p * n)(*[_ptr(t, "block_table", torch.int32) for t in block_tables])
+    ss = (ctypes.c_void_p * n)(*[_ptr(t, "start_pos", torch.int32, (batch,)) for t in start_pos])
+    st = load().cai_kv_append_pools(_pool_array(pools), n, ks, vs, batch, n_new, ts, max_pages, ss,
+                                    _ptr(err_flag, "err_flag", torch.int32), _stream(stream))
+    _check(st, "cai_kv_append_pools")
 
 
 def cai_mqa_decode_workspace_size(batch: int, num_q_heads: int, max_pages_per_seq: int, page_size: int,

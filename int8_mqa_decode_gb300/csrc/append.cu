@@ -14,9 +14,15 @@
 namespace cai {
 namespace {
 
-__global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+// Up to kMaxKvHeads pools in one launch: blockIdx.y selects the pool.
+struct AppendArgs {
+  AppendParams pool[kMaxKvHeads];
+};
+
+__global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendArgs args) {
   grid_dependency_wait();
   grid_launch_dependents();
+  const AppendParams& p = args.pool[blockIdx.y];
   const int warp_global = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   const int rows = p.batch * p.n_new;
@@ -68,10 +74,13 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
 
 }  // namespace
 
-cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
-  const int64_t warps = 2ll * p.batch * p.n_new;
+cudaError_t launch_append(const AppendParams* ps, int n, cudaStream_t stream) {
+  if (n < 1 || n > kMaxKvHeads) return cudaErrorInvalidValue;
+  AppendArgs a;
+  for (int i = 0; i < kMaxKvHeads; ++i) a.pool[i] = ps[i < n ? i : n - 1];
+  const int64_t warps = 2ll * ps[0].batch * ps[0].n_new;  // the same rows in every pool
   const int64_t blocks = (warps + 7) / 8;
-  return launch_pdl(append_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, p);
+  return launch_pdl(append_kernel, dim3((unsigned)blocks, (unsigned)n), dim3(256), 0, stream, a);
 }
 
 }  // namespace cai

@@ -103,9 +103,11 @@ static cai_status check_pool(const cai_kv_pool* pool) {
   return CAI_OK;
 }
 
-cai_status cai_kv_append(const cai_kv_pool* pool, const float* k_new, const float* v_new, int32_t batch,
+namespace {
+
+cai_status append_params(const cai_kv_pool* pool, const float* k_new, const float* v_new, int32_t batch,
                          int32_t n_new, const int32_t* block_table, int32_t max_pages_per_seq,
-                         const int32_t* start_pos, int32_t* err_flag, void* stream) {
+                         const int32_t* start_pos, int32_t* err_flag, AppendParams& p) {
   cai_status st = check_pool(pool);
   if (st != CAI_OK) return st;
   if (batch < 0 || n_new < 0 || max_pages_per_seq <= 0) return CAI_ERR_INVALID_ARG;
@@ -114,7 +116,6 @@ cai_status cai_kv_append(const cai_kv_pool* pool, const float* k_new, const floa
   if ((int64_t)batch * n_new > (1ll << 30)) return CAI_ERR_UNSUPPORTED;
   if (!k_new || !v_new || !block_table || !start_pos) return CAI_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new)) return CAI_ERR_INVALID_ARG;
-  AppendParams p;
   p.pages = static_cast<uint8_t*>(pool->pages);
   p.num_pages = pool->num_pages;
   p.page_size = pool->page_size;
@@ -126,7 +127,35 @@ cai_status cai_kv_append(const cai_kv_pool* pool, const float* k_new, const floa
   p.table = block_table;
   p.start_pos = start_pos;
   p.err = err_flag;
-  return cuda_status(launch_append(p, static_cast<cudaStream_t>(stream)));
+  return CAI_OK;
+}
+
+}  // namespace
+
+cai_status cai_kv_append(const cai_kv_pool* pool, const float* k_new, const float* v_new, int32_t batch,
+                         int32_t n_new, const int32_t* block_table, int32_t max_pages_per_seq,
+                         const int32_t* start_pos, int32_t* err_flag, void* stream) {
+  AppendParams p;
+  cai_status st = append_params(pool, k_new, v_new, batch, n_new, block_table, max_pages_per_seq, start_pos,
+                                err_flag, p);
+  if (st != CAI_OK || batch == 0 || n_new == 0) return st;
+  return cuda_status(launch_append(&p, 1, static_cast<cudaStream_t>(stream)));
+}
+
+cai_status cai_kv_append_pools(const cai_kv_pool* pools, int32_t num_pools, const float* const* k_new,
+                               const float* const* v_new, int32_t batch, int32_t n_new,
+                               const int32_t* const* block_tables, int32_t max_pages_per_seq,
+                               const int32_t* const* start_pos, int32_t* err_flag, void* stream) {
+  if (!pools || !k_new || !v_new || !block_tables || !start_pos) return CAI_ERR_INVALID_ARG;
+  if (num_pools < 1 || num_pools > kMaxKvHeads) return CAI_ERR_UNSUPPORTED;
+  AppendParams ps[kMaxKvHeads];
+  for (int i = 0; i < num_pools; ++i) {
+    cai_status st = append_params(&pools[i], k_new[i], v_new[i], batch, n_new, block_tables[i], max_pages_per_seq,
+                                  start_pos[i], err_flag, ps[i]);
+    if (st != CAI_OK) return st;
+  }
+  if (batch == 0 || n_new == 0) return CAI_OK;
+  return cuda_status(launch_append(ps, num_pools, static_cast<cudaStream_t>(stream)));
 }
 
 size_t cai_mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_pages_per_seq,

@@ -134,7 +134,7 @@ DecodePlan plan_decode(int32_t batch, int32_t max_pages_per_seq, int32_t page_si
 int num_sms();
 
 // Kernel launchers (return cudaGetLastError()).
-cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_append(const AppendParams* ps, int n, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int page_size, cudaStream_t stream);
 
 }  // namespace cai

@@ -885,21 +885,40 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
   const DecodeJob& jb = p.job[job];
   const SeqSplits sp = seq_splits(p.ctx_len[b], jb.window, jb.max_pages * page_size, jb.plan.chunk);
   if (!sp.valid || sp.nsplit <= 1) return;  // written by the decode kernel itself
-  const int S = jb.plan.max_splits;
+  static_assert(kMaxSplits <= 64, "two splits per lane");
+  const int S = jb.plan.max_splits;        // <= 64: lane l holds splits l and l + 32
   const float* lse = jb.ws_lse + (int64_t)b * S * Hq + h;
-  float M = -INFINITY;
-  for (int j = 0; j < sp.nsplit; ++j) M = fmaxf(M, lse[(int64_t)j * Hq]);
+  const float l0 = lane < sp.nsplit ? lse[(int64_t)lane * Hq] : -INFINITY;
+  const float l1 = lane + 32 < sp.nsplit ? lse[(int64_t)(lane + 32) * Hq] : -INFINITY;
+  float M = fmaxf(l0, l1);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  // Split weights 2^(lse_j - M), lane l holding those of splits l and l + 32.
+  const float w0 = M == -INFINITY || lane >= sp.nsplit ? 0.0f : ex2_approx(l0 - M);
+  const float w1 = M == -INFINITY || lane + 32 >= sp.nsplit ? 0.0f : ex2_approx(l1 - M);
+  float wsum = w0 + w1;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.0f;
-  if (M != -INFINITY) {
-    for (int j = 0; j < sp.nsplit; ++j) {
-      const float w = ex2_approx(lse[(int64_t)j * Hq] - M);
-      const float4 o = reinterpret_cast<const float4*>(jb.ws_o + (((int64_t)b * S + j) * Hq + h) * kHeadDim)[lane];
-      acc.x = fmaf(w, o.x, acc.x);
-      acc.y = fmaf(w, o.y, acc.y);
-      acc.z = fmaf(w, o.z, acc.z);
-      acc.w = fmaf(w, o.w, acc.w);
-      wsum += w;
+  const float4* rows = reinterpret_cast<const float4*>(jb.ws_o + ((int64_t)b * S * Hq + h) * kHeadDim) + lane;
+  const int64_t stride = (int64_t)Hq * kHeadDim / 4;  // float4s from one split's row to the next
+  // Four splits at a time so that their loads overlap.
+  for (int j0 = 0; j0 < sp.nsplit; j0 += 4) {
+    float4 o[4];
+    float w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      o[u] = j < sp.nsplit ? rows[j * stride] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float wa = __shfl_sync(0xffffffffu, w0, j & 31), wb = __shfl_sync(0xffffffffu, w1, j & 31);
+      w[u] = j < sp.nsplit ? (j < 32 ? wa : wb) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc.x = fmaf(w[u], o[u].x, acc.x);
+      acc.y = fmaf(w[u], o[u].y, acc.y);
+      acc.z = fmaf(w[u], o[u].z, acc.z);
+      acc.w = fmaf(w[u], o[u].w, acc.w);
     }
   }
   const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;

@@ -78,6 +78,23 @@ def test_append_validation(lib):
     assert call(pool, n_new=0) == 0
 
 
+def test_append_pools_validation(lib):
+    pools = (cai.cai_kv_pool * 2)(_pool(), _pool())
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+
+    def call(pools=pools, n=2, k=arr, v=arr, batch=2, n_new=1, tables=arr, maxp=4, start=arr):
+        return lib.cai_kv_append_pools(pools, n, k, v, batch, n_new, tables, maxp, start, None, None)
+
+    assert call(n=0) == 2
+    assert call(n=9) == 2
+    assert call(k=None) == 1
+    assert call(v=(ctypes.c_void_p * 2)(FAKE, FAKE + 4)) == 1  # misaligned
+    assert call(start=(ctypes.c_void_p * 2)(FAKE, None)) == 1
+    assert call(maxp=0) == 1
+    assert call(pools=(cai.cai_kv_pool * 2)(_pool(), _pool(head_dim=96))) == 2
+    assert call(batch=0) == 0
+
+
 def test_decode_validation(lib):
     pools = (cai.cai_kv_pool * 2)(_pool(), _pool())
     l2p = (ctypes.c_int32 * 3)(0, 0, 1)

@@ -119,6 +119,22 @@ def test_append_bit_exact_whole_pool(P):
     assert np.array_equal(got, oracle_pool(w, cache, 0))
 
 
+def test_append_pools_one_launch_matches_per_pool():
+    """The step's appends into four buffers in one launch write the same bytes as four launches."""
+    w = synth.workload(3, batch=5)
+    a, b = build(w), build(w)
+    for pa, pb in zip(a.pools, b.pools):
+        pb.pages.copy_(pa.pages)  # the same bytes everywhere, written or not
+    kv = [a.step_kv(buf) for buf in range(w.num_buffers)]
+    for buf, pool in enumerate(a.pools):
+        k, v, start = kv[buf]
+        cai.cai_kv_append(pool, k, v, a.tables[buf], start)
+    cai.cai_kv_append_pools(b.pools, [k for k, _, _ in kv], [v for _, v, _ in kv], b.tables, [s for _, _, s in kv])
+    torch.cuda.synchronize()
+    for pa, pb in zip(a.pools, b.pools):
+        assert torch.equal(pa.pages, pb.pages)
+
+
 def test_append_chunk_across_page_boundaries_and_errors():
     P = 16
     w = make_workload(3, 8, P, [100, 37, 64], seed=12, n_new=29)
