@@ -565,63 +565,74 @@ def run_gpu(args, rank, world):
 def run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world, layered=False):
     """Same step through the public API with inputs in pinned host memory: every step copies its
     inputs host -> device and its outputs device -> host inside the timed region.  As a serving loop
-    would, the copies run on their own streams: inputs are double-buffered and copied while the
-    previous step computes, and outputs are copied back while the next work runs."""
+    would, the step's inputs sit packed in one pinned buffer and go over in one copy, on their own
+    stream, into one of two device buffers while the previous step computes; the outputs sit packed
+    in one device buffer and come back in one copy on a third stream while the next step computes."""
     import torch
     import int8_mqa_decode_gb300 as cai
 
     nl = len(w.layer_windows)
-    h_q = [q.cpu().pin_memory() for q in qs]
-    h_kv = [(k.cpu().pin_memory(), v.cpu().pin_memory(), s.cpu().pin_memory()) for k, v, s in step_kv]
-    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    d_q = [[torch.empty_like(q) for q in qs] for _ in range(2)]
-    d_kv = [[(torch.empty_like(k), torch.empty_like(v), torch.empty_like(s)) for k, v, s in step_kv] for _ in range(2)]
-    d_out = [outs, [torch.empty_like(o) for o in outs]]
+    # Packed input layout: per layer q, then per buffer k, v, start; every piece 256-byte aligned.
+    pieces = [q for q in qs] + [t for kv in step_kv for t in kv]
+    offs, total = [], 0
+    for t in pieces:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for t, o in zip(pieces, offs):
+        n = t.numel() * t.element_size()
+        h_in[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+    d_in = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
+
+    def views(buf):
+        out = []
+        for t, o in zip(pieces, offs):
+            n = t.numel() * t.element_size()
+            out.append(buf[o:o + n].view(t.dtype).view(t.shape))
+        return out[:nl], [tuple(out[nl + 3 * i: nl + 3 * i + 3]) for i in range(len(step_kv))]
+
+    d_views = [views(d_in[b]) for b in range(2)]
+    o_numel = outs[0].numel()
+    d_out = [torch.empty(nl * o_numel, dtype=outs[0].dtype, device="cuda") for _ in range(2)]
+    d_out_views = [[d_out[b][l * o_numel:(l + 1) * o_numel].view(outs[0].shape) for l in range(nl)] for b in range(2)]
+    h_out = torch.empty(nl * o_numel, dtype=outs[0].dtype).pin_memory()
     ws_layers = [cache.layers_workspace(args.num_splits) for _ in range(2)] if layered else None
     comp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]          # inputs of slot b copied
-    ev_used = [torch.cuda.Event() for _ in range(2)]        # kernels done with the inputs of slot b
-    ev_done = [[torch.cuda.Event() for _ in range(nl)] for _ in range(2)]  # output (b, layer) written
-    ev_read = [[torch.cuda.Event() for _ in range(nl)] for _ in range(2)]  # output (b, layer) copied out
-    h2d = sum(t.numel() * t.element_size() for t in h_q) + sum(
-        sum(t.numel() * t.element_size() for t in kv) for kv in h_kv)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of slot b copied
+    ev_used = [torch.cuda.Event() for _ in range(2)]  # kernels done with the inputs of slot b
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # outputs of slot b written
+    ev_read = [torch.cuda.Event() for _ in range(2)]  # outputs of slot b copied out
+    h2d = sum(t.numel() * t.element_size() for t in pieces)
+    d2h = h_out.numel() * h_out.element_size()
     first_use = [True, True]
 
     def step(i):
         b = i & 1
+        d_q, d_kv = d_views[b]
         with torch.cuda.stream(s_in):
             if not first_use[b]:
                 s_in.wait_event(ev_used[b])
-            for (hk, hv, hs), (dk, dv, ds) in zip(h_kv, d_kv[b]):
-                dk.copy_(hk, non_blocking=True)
-                dv.copy_(hv, non_blocking=True)
-                ds.copy_(hs, non_blocking=True)
-            for hq, dq in zip(h_q, d_q[b]):
-                dq.copy_(hq, non_blocking=True)
+            d_in[b].copy_(h_in, non_blocking=True)
             ev_in[b].record(s_in)
         comp.wait_event(ev_in[b])
-        cai.cai_kv_append_pools(cache.pools, [dk for dk, _, _ in d_kv[b]], [dv for _, dv, _ in d_kv[b]],
-                                cache.tables, [ds for _, _, ds in d_kv[b]])
+        cai.cai_kv_append_pools(cache.pools, [dk for dk, _, _ in d_kv], [dv for _, dv, _ in d_kv], cache.tables,
+                                [ds for _, _, ds in d_kv])
+        if not first_use[b]:
+            comp.wait_event(ev_read[b])
         if layered:
-            if not first_use[b]:
-                for layer in range(nl):
-                    comp.wait_event(ev_read[b][layer])
-            cache.decode_layers(d_q[b], d_out[b], num_splits=args.num_splits, workspace=ws_layers[b])
-        for layer in range(nl):
-            if not layered:
-                if not first_use[b]:
-                    comp.wait_event(ev_read[b][layer])
-                cai.cai_mqa_decode(cache.pools, w.layer_to_buffer, layer, d_q[b][layer],
+            cache.decode_layers(d_q, d_out_views[b], num_splits=args.num_splits, workspace=ws_layers[b])
+        else:
+            for layer in range(nl):
+                cai.cai_mqa_decode(cache.pools, w.layer_to_buffer, layer, d_q[layer],
                                    cache.tables[w.layer_to_buffer[layer]], cache.ctx_len, w.layer_windows[layer],
-                                   w.softmax_scale, args.num_splits, wss[layer], d_out[b][layer])
-            ev_done[b][layer].record(comp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_done[b][layer])
-                h_out[layer].copy_(d_out[b][layer], non_blocking=True)
-                ev_read[b][layer].record(s_out)
+                                   w.softmax_scale, args.num_splits, wss[layer], d_out_views[b][layer])
+        ev_done[b].record(comp)
         ev_used[b].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[b])
+            h_out.copy_(d_out[b], non_blocking=True)
+            ev_read[b].record(s_out)
         first_use[b] = False
 
     for i in range(3):
@@ -640,9 +651,9 @@ def run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world, layered=Fa
     ms = allreduce_max(e0.elapsed_time(e1), world)
     return {"value": world * toks_step * args.steps / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps,
-            "copies": "pinned host buffers; inputs double-buffered and copied on their own stream while the "
-                      "previous step computes; outputs copied back on a third stream while the next step "
-                      + ("computes" if layered else "layer decodes")}
+            "copies": "pinned host buffers; the step's inputs packed into one buffer and copied in one transfer on "
+                      "their own stream into one of two device buffers while the previous step computes; the "
+                      "outputs packed in one device buffer and copied back in one transfer on a third stream"}
 
 
 # ----------------------------------------------------------------------------- reference arm (the oracle)
