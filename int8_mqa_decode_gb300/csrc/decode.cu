@@ -41,7 +41,8 @@
 //    issued by different warps;
 //  * softmax (warps 12-15, one thread per token of the tile): applies the K
 //    scale and softmax scale, checks the logits against a per-head reference
-//    maximum shared by the four warps that is raised only when a logit exceeds
+//    maximum shared by the four warps (at an item's first tile, the logits of
+//    its first attended token) that is raised only when a logit exceeds
 //    it by 2^8 (one barrier-reduction per tile decides; O^T is rarely
 //    rescaled), scales P by the token's V scale and stores it, fp16, as the
 //    B operand P^T; at the end of an item it reduces the per-head sums and
@@ -117,6 +118,7 @@ struct Roles {
 constexpr int kNoPage = -2147483647 - 1;      // a page the tile does not need
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: weights stay <= 2^8 between rescales
+constexpr float kFirstRefMargin = 6.0f;       // log2 units above an item's first token (see the softmax)
 constexpr uint32_t kSoftBar = 1;              // named barrier of the softmax warpgroup
 
 __device__ __forceinline__ void set_err(int32_t* err, int bits) {
@@ -708,12 +710,28 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         const float ks = sc[tok];
         const bool valid = sc[T + tok] != 0.0f;
         const float vs = sc[2 * T + tok];
+        if (t == 0) {
+          // A new item's references: the logits of its first attended token plus a margin,
+          // shared by the thread that holds it (-inf when that token is masked: the raise
+          // below then sets them); a later logit above them by more than 2^8 raises them as
+          // usual.  The margin makes such raises, which wait for the previous PV to rescale
+          // O^T, rare: a logit 2^6 above the token's still leaves the weights <= 2^8.
+          if (tok == it.start - it.tile0 * T) {
+#pragma unroll
+            for (int h = 0; h < HH; ++h) {
+              const float z = sv[h] * ks + kFirstRefMargin;
+              mref[h0 + h] = valid ? z : -INFINITY;
+              muse[h0 + h] = valid ? z : 0.0f;
+            }
+          }
+          named_barrier_sync(kSoftBar, kSoftThreads);
+        }
         // e_h = logit (log2 units) minus the head's reference.
         float mx = -INFINITY;
         if (valid) {
 #pragma unroll
           for (int h = 0; h < HH; h += 4) {
-            const float4 mu = t == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(muse + h0 + h);
+            const float4 mu = *reinterpret_cast<const float4*>(muse + h0 + h);
             sv[h] = fmaf(sv[h], ks, -mu.x);
             sv[h + 1] = fmaf(sv[h + 1], ks, -mu.y);
             sv[h + 2] = fmaf(sv[h + 2], ks, -mu.z);
@@ -721,14 +739,14 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
             mx = fmax3(mx, fmax3(sv[h], sv[h + 1], sv[h + 2]), sv[h + 3]);
           }
         }
-        const bool raise = t == 0 || (valid && mx > kRescaleThreshold);
+        const bool raise = valid && (mx > kRescaleThreshold || mref[h0] == -INFINITY);  // or no reference yet
         if (bar_red_or(kSoftBar, kSoftThreads, raise)) {
-          // Some head's reference must rise (always at an item's first tile):
-          // per-head maxima of the tile over the four lane quarters, new references.
+          // Some head's reference must rise (or none is set yet): per-head maxima of the
+          // tile over the four lane quarters, new references.
           {
             float v[HH];
 #pragma unroll
-            for (int i = 0; i < HH; ++i) v[i] = valid ? sv[i] + (t == 0 ? 0.0f : muse[h0 + i]) : -INFINITY;
+            for (int i = 0; i < HH; ++i) v[i] = valid ? sv[i] + muse[h0 + i] : -INFINITY;
             const float wm = warp_max_scatter<HH>(v, lane);
             if (lane < HH) wmax[quarter * HN + h0 + lane] = wm;
           }
@@ -736,9 +754,9 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
           if (quarter == 0 && lane < HH) {
             const int h = h0 + lane;
             const float M = fmaxf(fmaxf(wmax[h], wmax[HN + h]), fmaxf(wmax[2 * HN + h], wmax[3 * HN + h]));
-            const float m_old = t == 0 ? -INFINITY : mref[h];
+            const float m_old = mref[h];
             const float m_new = M > m_old + kRescaleThreshold ? M : m_old;
-            const float mu_old = t == 0 ? 0.0f : muse[h];
+            const float mu_old = muse[h];
             const float mu_new = m_new == -INFINITY ? 0.0f : m_new;
             aref[h] = m_old == -INFINITY ? 0.0f : ex2_approx(m_old - m_new);
             dref[h] = mu_old - mu_new;
