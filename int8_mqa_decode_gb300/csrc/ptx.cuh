@@ -6,11 +6,6 @@
 
 namespace cai {
 
-// Bounded waits: a kernel never spins forever.  When a wait gives up the
-// kernel records CAI_DEVERR_TIMEOUT-like state through its own flag and
-// carries on without touching the data it waited for.
-constexpr uint32_t kSpinLimit = 1u << 26;
-
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -60,12 +55,6 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-// Returns false if the phase did not complete within the spin limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
@@ -229,63 +218,6 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
                      "=r"(a[o + 6]), "=r"(a[o + 7])
 #define CAI_W8(a, o) "r"(a[o + 0]), "r"(a[o + 1]), "r"(a[o + 2]), "r"(a[o + 3]), "r"(a[o + 4]), "r"(a[o + 5]), \
                      "r"(a[o + 6]), "r"(a[o + 7])
-
-// M=64 accumulators (16 TMEM lanes per sub-partition): thread t of the warp
-// reads lane (base + t%16), columns [col + (t/16)*half, col + (t/16)*half + 32).
-template <int kHalf>
-__device__ __forceinline__ void tmem_ld_16x32bx2_x32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], %33;"
-      : CAI_R8(r, 0), CAI_R8(r, 8), CAI_R8(r, 16), CAI_R8(r, 24)
-      : "r"(taddr), "n"(kHalf));
-}
-
-template <int kHalf>
-__device__ __forceinline__ void tmem_st_16x32bx2_x32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
-      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};" ::"r"(taddr),
-      "n"(kHalf), CAI_W8(r, 0), CAI_W8(r, 8), CAI_W8(r, 16), CAI_W8(r, 24)
-      : "memory");
-}
-
-#define CAI_R32(a, o) CAI_R8(a, o), CAI_R8(a, o + 8), CAI_R8(a, o + 16), CAI_R8(a, o + 24)
-#define CAI_W32(a, o) CAI_W8(a, o), CAI_W8(a, o + 8), CAI_W8(a, o + 16), CAI_W8(a, o + 24)
-
-template <int kHalf>
-__device__ __forceinline__ void tmem_ld_16x32bx2_x64(uint32_t taddr, uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x32bx2.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
-      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64], %65;"
-      : CAI_R32(r, 0), CAI_R32(r, 32)
-      : "r"(taddr), "n"(kHalf));
-}
-
-template <int kHalf>
-__device__ __forceinline__ void tmem_st_16x32bx2_x64(uint32_t taddr, const uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x32bx2.x64.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
-      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,"
-      "%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,"
-      "%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65};" ::"r"(taddr),
-      "n"(kHalf), CAI_W32(r, 0), CAI_W32(r, 32)
-      : "memory");
-}
-
-#define CAI_R16(a, o) CAI_R8(a, o), CAI_R8(a, o + 8)
-#define CAI_W16(a, o) CAI_W8(a, o), CAI_W8(a, o + 8)
-
-template <int kHalf>
-__device__ __forceinline__ void tmem_st_16x32bx2_x16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};" ::
-          "r"(taddr),
-      "n"(kHalf), CAI_W16(r, 0)
-      : "memory");
-}
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
