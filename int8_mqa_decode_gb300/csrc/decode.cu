@@ -10,8 +10,9 @@
 // (hybrid attention, technique table of "Character.AI: inference
 // optimization", section 03).
 //
-// How.  A persistent kernel, one CTA per SM, takes work items (sequence,
-// split) from a global queue and walks each in 128-token tiles.  The scores
+// How.  A persistent kernel, one CTA per SM, takes work items (layer,
+// sequence, KV head, split; up to eight layers per launch, global layers'
+// items first) from a global queue and walks each in 128-token tiles.  The scores
 // are computed transposed, S^T = K Q^T (tokens x heads), so that one thread
 // owns one token: its K and V scales and its mask are per-thread scalars and
 // the K operand goes from registers to tensor memory without a shared-memory
