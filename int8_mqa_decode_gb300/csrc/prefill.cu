@@ -545,7 +545,6 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.scale_log2 = L.scale_log2;
   const int64_t rows = (int64_t)L.batch * p.kt_rows;
   const int64_t a = ((rows * kHeadDim * 2 + 255) / 256) * 256;
-  const int64_t s = ((rows * 4 + 255) / 256) * 256;
   uint8_t* ws = static_cast<uint8_t*>(L.workspace);
   p.kb = reinterpret_cast<uint16_t*>(ws);
   p.vh = reinterpret_cast<uint16_t*>(ws + a);
