@@ -78,8 +78,9 @@ size_t cai_page_bytes(int32_t page_size, int32_t head_dim);
  * Int8 KV cache ("Character.AI: inference optimization", 05), written once per
  * new token (Red Hat page, "Por que o cache KV existe").  For each token and
  * separately for K and V: s = max_i |x_i| / 127 (fp32, IEEE division),
- * code_i = clamp(round_half_even(x_i / s), -127, 127); s = 0 and codes 0 when
- * the vector is all zeros.  Results are bit-exact.
+ * code_i = clamp(round_half_even(x_i / s), -127, 127); codes 0 when s is 0 (an
+ * all-zero vector, or max |x_i| / 127 below the smallest fp32 subnormal).
+ * Results are bit-exact.
  *   pool        host pointer to the pool description
  *   k_new,v_new fp32 [batch][n_new][head_dim], 16-byte aligned
  *   block_table int32 [batch][max_pages_per_seq]; entries for the written positions must be valid pages

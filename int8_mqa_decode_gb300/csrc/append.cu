@@ -52,9 +52,10 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
   }
   const int32_t slot = pos - (pos / P) * P;
 
+  // A zero scale (an all-zero vector, or amax / 127 underflowing to 0) gives zero codes.
   const float s = __fdiv_rn(amax, 127.0f);
   uint32_t packed = 0;
-  if (amax != 0.0f) {
+  if (s != 0.0f) {
     const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {

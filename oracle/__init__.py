@@ -10,12 +10,16 @@ What is computed, and from which passage of the pages:
 
 * ``quantize_rows``: int8 KV cache ("Character.AI: inference optimization",
   05 Quantization and cost).  Reading: symmetric per-token absmax, fp32 scale
-  s = absmax/127, code = round-half-even(x/s) clamped to [-127, 127]; absmax 0
-  gives s = 0 and zero codes.
+  s = absmax/127, code = round-half-even(x/s) clamped to [-127, 127], both
+  divisions single IEEE fp32 operations; a zero scale (absmax 0, or absmax/127
+  underflowing to 0) gives zero codes.
 * ``attend``: softmax attention of one query per head over cached keys and
   values ("Como funciona a inferencia de IA", "Por que o cache KV existe"),
   with one shared K/V head (Multi-Query Attention, technique table of section
   03), in float64.
+* ``merge_splits``: softmax attention over a union of disjoint parts of the
+  attended set, from each part's normalised output and log-sum-exp (the
+  algebra a split-KV decode relies on; the definition itself never splits).
 * ``attended_range``: global layers see every cached token; local layers see
   the last ``window`` positions, the current token included (hybrid attention
   with horizon 1024, technique table of section 03).
@@ -122,6 +126,37 @@ def attend(q: np.ndarray, k: np.ndarray, v: np.ndarray, c: float):
     lse = np.empty(Hq, dtype=np.float64)
     if _load().oracle_attend(_ptr(q), Hq, d, _ptr(k), _ptr(v), T, float(c), _ptr(out), _ptr(lse)) != 0:
         raise MemoryError("oracle_attend: out of host memory")
+    return out, lse
+
+
+def merge_splits(outs, lses):
+    """Attention over the union of disjoint parts of an attended set, from the parts.
+
+    outs float64 [S][Hq][d] (each part's softmax-weighted mean of v), lses float64
+    [S][Hq] (each part's log sum exp of the logits; -inf for an empty part).  For the
+    softmax over the union, the log-sum-exp is log sum_j exp(lse_j) and the output is
+    sum_j exp(lse_j - lse) * out_j: each part's exponentials summed over its own tokens
+    are exp(lse_j), so its normalised output enters with weight exp(lse_j) / sum.
+    Computed with the largest lse_j subtracted first.  All parts empty: out 0, lse -inf.
+    """
+    outs = np.asarray(outs, dtype=np.float64)
+    lses = np.asarray(lses, dtype=np.float64)
+    S, Hq, d = outs.shape
+    out = np.zeros((Hq, d))
+    lse = np.full(Hq, -np.inf)
+    for h in range(Hq):
+        m = max(lses[j, h] for j in range(S))
+        if m == -np.inf:
+            continue
+        wsum = 0.0
+        for j in range(S):
+            if lses[j, h] == -np.inf:
+                continue
+            wj = math.exp(lses[j, h] - m)
+            wsum += wj
+            out[h] += wj * outs[j, h]
+        out[h] /= wsum
+        lse[h] = m + math.log(wsum)
     return out, lse
 
 

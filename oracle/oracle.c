@@ -26,7 +26,9 @@
 #include <stdlib.h>
 
 /* Quantize one token's vector x[d] (fp32) to int8 codes and one fp32 scale.
- * amax == 0 gives scale 0 and all codes 0. */
+ * A scale of 0 -- amax == 0, or amax so small (below 127 times the smallest
+ * subnormal) that amax / 127 rounds to 0 -- gives all codes 0: every code then
+ * dequantizes to 0 anyway, and x / 0 has no integer value. */
 void oracle_quantize_token(const float* x, int32_t d, int8_t* codes, float* scale) {
   float amax = 0.0f;
   for (int32_t i = 0; i < d; ++i) {
@@ -36,7 +38,7 @@ void oracle_quantize_token(const float* x, int32_t d, int8_t* codes, float* scal
   float s = amax / 127.0f;
   *scale = s;
   for (int32_t i = 0; i < d; ++i) {
-    if (amax == 0.0f) {
+    if (s == 0.0f) {
       codes[i] = 0;
       continue;
     }

@@ -158,24 +158,39 @@ def test_append_chunk_across_page_boundaries_and_errors():
 
 
 def test_append_quantizer_edge_rows():
-    # Zero row, integer row with amax 127 (scale 1, exact halves -> ties to even), tiny and huge magnitudes.
+    # Zero row, integer row with amax 127 (scale 1, exact halves -> ties to even), tiny and huge
+    # magnitudes, subnormal rows whose scale underflows to 0 (codes 0) or to the smallest subnormal,
+    # and the golden rows whose codes depend on the reading of the division (x / s, ties to even).
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "quant_division.json")))
+    gold = np.array([r["x_bits"] for r in g["rows"]], dtype=np.uint32).view(np.float32)
     P = 16
-    pool = cai.KVPool(2, P)
+    pool = cai.KVPool(3, P)
     pool.pages.fill_(0)
-    x = torch.zeros(1, 4, 128, dtype=torch.float32)
+    n = 7 + len(gold)
+    assert n <= 2 * P
+    x = torch.zeros(1, n, 128, dtype=torch.float32)
     x[0, 1, 0] = 127.0
     x[0, 1, 1:10] = torch.tensor([0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 126.5, -126.5])
     x[0, 2] = torch.linspace(-1e-30, 1e-30, 128)
     x[0, 3] = torch.linspace(-3e38, 3e38, 128)
-    table = torch.tensor([[1, 0]], dtype=torch.int32, device="cuda")
+    tiny = float(np.finfo(np.float32).smallest_subnormal)
+    x[0, 4, :3] = torch.tensor([tiny, -tiny, 2 * tiny])
+    x[0, 5, :2] = torch.tensor([63 * tiny, -tiny])
+    x[0, 6, :2] = torch.tensor([64 * tiny, -tiny])
+    x[0, 7:] = torch.from_numpy(gold.copy())
+    table = torch.tensor([[1, 2]], dtype=torch.int32, device="cuda")
     cai.cai_kv_append(pool, x.cuda(), (-x).cuda().contiguous(), table, torch.zeros(1, dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
-    ref = oracle.pool_new(2, P, fill=0)
+    ref = oracle.pool_new(3, P, fill=0)
     kc, ks = oracle.quantize_rows(x[0].numpy())
     vc, vs = oracle.quantize_rows((-x[0]).numpy())
-    oracle.pool_write(ref, np.array([1, 0]), 0, kc, ks, vc, vs, P)
+    oracle.pool_write(ref, np.array([1, 2]), 0, kc, ks, vc, vs, P)
     assert np.array_equal(pool.pages.cpu().numpy(), ref)
     assert list(kc[1, 1:10]) == [0, 2, 2, 4, 0, -2, -2, 126, -126]
+    assert ks[4] == 0 and ks[5] == 0 and not kc[4].any() and not kc[5].any() and kc[6, 0] == 64
+    assert np.array_equal(kc[7:].astype(np.int64), np.array([r["codes"] for r in g["rows"]]))
 
 
 # --------------------------------------------------------------------- decode

@@ -76,6 +76,64 @@ def test_quant_bruteforce_nearest_code():
     assert np.all(np.abs(ratio - codes) <= 0.5 + 1e-5)
 
 
+def _quant_division_rows():
+    g = json.load(open(os.path.join(GOLDEN, "quant_division.json")))
+    x = np.array([r["x_bits"] for r in g["rows"]], dtype=np.uint32).view(np.float32)
+    codes = np.array([r["codes"] for r in g["rows"]], dtype=np.int64)
+    scales = np.array([r["scale_bits"] for r in g["rows"]], dtype=np.uint32).view(np.float32)
+    return g, x, codes, scales
+
+
+def test_quant_division_golden():
+    """Rows whose codes depend on the reading of the division: one IEEE fp32 division x/s
+    and round half to even (values written from the definition with exact rationals)."""
+    g, x, codes, scales = _quant_division_rows()
+    assert g["case_counts"]["reciprocal"] >= 10 and g["case_counts"]["tie"] >= 10
+    got_codes, got_scales = oracle.quantize_rows(x)
+    assert np.array_equal(got_scales.view(np.uint32), scales.view(np.uint32))
+    assert np.array_equal(got_codes.astype(np.int64), codes)
+
+
+def _planted_quantizer(x, variant):
+    """The oracle's quantizer with one plausible slip, on the CPU (numpy fp32)."""
+    x = x.astype(np.float32)
+    amax = np.abs(x).max(axis=1)
+    s = (amax / np.float32(127)).astype(np.float32)
+    if variant == "reciprocal":
+        q = x * (np.float32(1) / s)[:, None]
+    elif variant == "inverse_scale":
+        q = x * (np.float32(127) / amax)[:, None]
+    elif variant == "half_away":
+        q = x / s[:, None]
+        return np.clip(np.sign(q) * np.floor(np.abs(q) + np.float32(0.5)), -127, 127).astype(np.int64)
+    else:
+        q = x / s[:, None]
+    return np.clip(np.rint(q.astype(np.float32)), -127, 127).astype(np.int64)
+
+
+@pytest.mark.parametrize("variant", ["reciprocal", "inverse_scale", "half_away"])
+def test_quant_division_golden_rejects_slips(variant):
+    """Each slip gives other codes on the golden rows, so the golden test pins the reading."""
+    _, x, codes, _ = _quant_division_rows()
+    assert np.array_equal(_planted_quantizer(x, "plain"), codes)  # the plain numpy form agrees
+    assert not np.array_equal(_planted_quantizer(x, variant), codes)
+
+
+def test_quant_zero_scale_from_underflow():
+    """amax / 127 below the smallest subnormal rounds the scale to 0: codes 0, like a zero vector."""
+    x = np.zeros((4, 128), dtype=np.float32)
+    tiny = np.float32(np.finfo(np.float32).smallest_subnormal)
+    x[0, :4] = [tiny, -tiny, 2 * tiny, 0]            # amax/127 underflows to 0
+    x[1, :2] = [np.float32(63) * tiny, -tiny]        # 63/127 of a subnormal still rounds to 0
+    x[2, :2] = [np.float32(64) * tiny, -tiny]        # 64/127 rounds up: scale = smallest subnormal
+    x[3, :2] = [np.float32(127) * tiny, -tiny]       # scale = smallest subnormal, codes exact
+    codes, scales = oracle.quantize_rows(x)
+    assert scales[0] == 0 and not codes[0].any()
+    assert scales[1] == 0 and not codes[1].any()
+    assert scales[2] == tiny and codes[2, 0] == 64 and codes[2, 1] == -1
+    assert scales[3] == tiny and codes[3, 0] == 127 and codes[3, 1] == -1
+
+
 # ---------------------------------------------------------------------------
 # Attention (softmax over the attended tokens, one shared K/V head)
 # ---------------------------------------------------------------------------
@@ -160,6 +218,34 @@ def test_attend_token_permutation_and_head_independence():
 
 def test_attend_empty_set():
     out, lse = oracle.attend(np.ones((2, 128)), np.zeros((0, 128)), np.zeros((0, 128)), C)
+    assert not out.any() and np.all(np.isneginf(lse))
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_merge_splits_equals_unsplit(seed):
+    """Cutting the attended set at any points (empty parts included) and merging the parts by
+    their log-sum-exp gives the unsplit attention within 1e-12."""
+    T, Hq = 300, 4
+    q, k, v = _small_case(200 + seed, T, Hq)
+    k *= 3.0  # a wide logit range, so the weights of the parts differ by many orders
+    ref, ref_lse = oracle.attend(q, k, v, C)
+    rng = np.random.default_rng(seed)
+    cuts = np.sort(rng.integers(0, T + 1, size=int(rng.integers(1, 12))))
+    edges = [0, *cuts.tolist(), T, T]  # repeated edges give empty parts
+    parts = [oracle.attend(q, k[a:b], v[a:b], C) for a, b in zip(edges[:-1], edges[1:])]
+    assert any(b == a for a, b in zip(edges[:-1], edges[1:]))
+    out, lse = oracle.merge_splits([o for o, _ in parts], [l for _, l in parts])
+    assert np.abs(out - ref).max() <= 1e-12
+    assert np.abs(lse - ref_lse).max() <= 1e-12
+
+
+def test_merge_splits_single_part_and_all_empty():
+    q, k, v = _small_case(301, 20, 3)
+    o, l = oracle.attend(q, k, v, C)
+    out, lse = oracle.merge_splits([o], [l])
+    assert np.array_equal(out, o) and np.allclose(lse, l, atol=0, rtol=1e-15)
+    e_o, e_l = oracle.attend(q, k[:0], v[:0], C)
+    out, lse = oracle.merge_splits([e_o, e_o], [e_l, e_l])
     assert not out.any() and np.all(np.isneginf(lse))
 
 
