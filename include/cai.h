@@ -190,15 +190,21 @@ cai_status cai_mqa_decode_layers(const cai_kv_pool* pools, int32_t num_pools, co
  * streams), a plug-in interface that passes only input and output buffers,
  * or a framework that owns all device memory and lends none to its plug-ins.
  * It computes exactly what cai_mqa_decode computes, with the same arguments
- * minus the workspace: the split partials go to a scratch array built into
- * the library, CAI_NO_ALLOC_SCRATCH_BYTES per GPU, held by every GPU that
- * loads the library until the process exits.  A call whose plan needs more
- * (cai_mqa_decode_workspace_size() above the limit) returns
- * CAI_ERR_WORKSPACE and launches nothing: lower num_splits (1 needs none).
- * The first call on a device looks up the array's device address on that
- * device; make that first call before any stream capture.  All calls share
- * the array and it keeps the last call's contents: calls whose kernels
- * overlap on the GPU (unordered streams) race on it. */
+ * minus the workspace: the work-queue counters and the split partials live in
+ * a scratch array built into the library, CAI_NO_ALLOC_SCRATCH_BYTES per GPU,
+ * held by every GPU that loads the library until the process exits.  A call
+ * whose plan needs more (cai_mqa_decode_workspace_size() above the limit)
+ * returns CAI_ERR_WORKSPACE and launches nothing: lower num_splits (1 needs
+ * only the 256-byte counter header).  The first call on a device looks up the
+ * array's device address on that device (again after the device's primary
+ * context was replaced, e.g. by cudaDeviceReset); make that first call before
+ * any stream capture.  Each call clears the counter header with a
+ * stream-ordered memset before its launch, so a call after one that reported
+ * CAI_DEVERR_TIMEOUT starts clean.  All calls share the array and it keeps the
+ * last call's contents: calls whose kernels overlap on the GPU (unordered
+ * streams) race on it.  A device index of 64 or more returns
+ * CAI_ERR_UNSUPPORTED; a failed address lookup returns CAI_ERR_CUDA with the
+ * error in cai_last_cuda_error(). */
 #define CAI_NO_ALLOC_SCRATCH_BYTES (32u << 20)
 cai_status cai_mqa_decode_no_alloc(const cai_kv_pool* pools, int32_t num_pools, const int32_t* layer_to_pool,
                                    int32_t num_layers, int32_t layer, const uint16_t* q, int32_t batch,

@@ -64,17 +64,19 @@ static size_t workspace_bytes_for(int32_t batch, int32_t num_q_heads, const Deco
 
 }  // namespace cai
 
-using namespace cai;
-
+namespace cai {
 namespace {
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+}  // namespace
 
 cai_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return CAI_OK;
   g_last_cuda_error = e;
   return CAI_ERR_CUDA;
 }
-}  // namespace
+}  // namespace cai
+
+using namespace cai;
 
 extern "C" {
 

@@ -133,6 +133,10 @@ DecodePlan plan_decode(int32_t batch, int32_t max_pages_per_seq, int32_t page_si
                        int32_t num_splits, int32_t num_sms, int32_t items_per_sm);
 int num_sms();
 
+// CAI_OK for cudaSuccess; otherwise CAI_ERR_CUDA, with the error kept for
+// cai_last_cuda_error() on this thread.
+cai_status cuda_status(cudaError_t e);
+
 // Kernel launchers (return cudaGetLastError()).
 cudaError_t launch_append(const AppendParams* ps, int n, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int page_size, cudaStream_t stream);

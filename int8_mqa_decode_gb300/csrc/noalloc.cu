@@ -6,19 +6,27 @@
 // and stall every other stream), a plugin interface that hands over only
 // input and output buffers, or an embedding framework that owns all device
 // memory through its own allocator and gives its plug-ins no way to borrow
-// from it.  For them this variant keeps the split-KV partials in a fixed
-// scratch array compiled into the library instead of a caller workspace.
+// from it.  For them this variant keeps the decode workspace -- the work-queue
+// counters and the split-KV partials -- in a fixed scratch array compiled into
+// the library instead of a caller workspace.
 //
 // The array is a file-scope __device__ object of kStaticScratchBytes: every
 // GPU that loads the library holds it until the process exits.  Host code may
 // not use the array's name as a device address (on the host it names a
-// stand-in object), so the device address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, on the first call made on
-// that device; make that first call before any stream capture.  All calls
-// share the one array and it keeps the last call's contents: two calls whose
-// kernels overlap on the GPU (different streams, no ordering between them)
-// race on it.  Nothing in the array has to start at zero: every partial that
-// is read is written first by the same call.
+// stand-in object), so the device address is looked up with
+// cudaGetSymbolAddress, with the device current, on the first call made on
+// that device (and again on the first call after the device's primary context
+// was replaced, e.g. after cudaDeviceReset); make that first call before any
+// stream capture.  All calls share the one array and it keeps the last call's
+// contents: two calls whose kernels overlap on the GPU (different streams, no
+// ordering between them) race on it.  The queue counters in its first
+// kWorkspaceHeader bytes must be zero when the decode kernel starts; every call
+// clears them with a stream-ordered memset before its launch, so a call that
+// follows one that gave up (CAI_DEVERR_TIMEOUT) starts clean.  The partials
+// need no clearing: every partial a call reads is written first by that call.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -30,20 +38,49 @@ constexpr size_t kStaticScratchBytes = CAI_NO_ALLOC_SCRATCH_BYTES;  // 32 MiB pe
 __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchSlot {
+  CUcontext ctx;  // context the address was looked up in
+  void* addr;
+};
+ScratchSlot g_scratch[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
 
-// Device address of g_decode_scratch on the current device (null on failure).
-void* scratch_address() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_addr[dev]) {
+// The driver's cuCtxGetCurrent, looked up through the runtime (no -lcuda).
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  if (!fn) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess) return nullptr;
-    g_scratch_addr[dev] = ptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
   }
-  return g_scratch_addr[dev];
+  return fn;
+}
+
+// Device address of g_decode_scratch on the current device and context.
+cai_status scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= kMaxDevices) return CAI_ERR_UNSUPPORTED;
+  auto get_ctx = ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS) return cuda_status(cudaErrorInitializationError);
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  ScratchSlot& slot = g_scratch[dev];
+  if (!slot.addr || !ctx || slot.ctx != ctx) {
+    // No context current yet (the lookup makes the primary context current) or
+    // another one than at the last lookup: look the address up in this one.
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return cuda_status(cudaErrorInitializationError);
+    slot.ctx = ctx;
+    slot.addr = ptr;
+  }
+  *out = slot.addr;
+  return CAI_OK;
 }
 
 }  // namespace
@@ -64,13 +101,16 @@ cai_status cai_mqa_decode_no_alloc(const cai_kv_pool* pools, int32_t num_pools, 
                                                     window, num_splits);
   if (need > cai::kStaticScratchBytes) return CAI_ERR_WORKSPACE;
   void* scratch = nullptr;
-  if (need > 0) {
-    scratch = cai::scratch_address();
-    if (!scratch) return CAI_ERR_CUDA;
+  if (need > 0 && batch > 0) {
+    const cai_status st = cai::scratch_address(&scratch);
+    if (st != CAI_OK) return st;
+    // The work-queue counters start every call at zero (stream-ordered, no allocation).
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, cai::kWorkspaceHeader, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cai::cuda_status(e);
   }
   return cai_mqa_decode(pools, num_pools, layer_to_pool, num_layers, layer, q, batch, num_q_heads, block_table,
                         max_pages_per_seq, ctx_len, window, softmax_scale, num_splits, scratch,
-                        need > 0 ? cai::kStaticScratchBytes : 0, out, lse_out, err_flag, stream);
+                        scratch ? cai::kStaticScratchBytes : 0, out, lse_out, err_flag, stream);
 }
 
 }  // extern "C"

@@ -41,6 +41,16 @@ def test_no_alloc_matches_workspace_decode_twice():
         assert int(err.item()) == 0
         assert np.abs(out.cpu().numpy() - ref.cpu().numpy()).max() <= ATOL
         assert np.abs(lse.cpu().numpy() - ref_lse.cpu().numpy()).max() <= ATOL
+    # ... and what the oracle gives, sequence by sequence.
+    import oracle
+    got, got_lse = out.cpu().numpy(), lse.cpu().numpy()
+    qb_all = q.view(torch.int16).cpu().numpy().view(np.uint16)
+    for b in range(w.batch):
+        L = int(w.ctx_len[b])
+        kc, ks, vc, vs = oracle.seq_kv(w.seed, 0, b, L)
+        o_ref, l_ref = oracle.decode_seq(qb_all[b], kc, ks, vc, vs, L, w.layer_windows[0], w.softmax_scale)
+        assert np.abs(got[b] - o_ref).max() <= ATOL, b
+        assert np.abs(got_lse[b] - l_ref).max() <= ATOL, b
     # A plan that needs more scratch than the built-in array is refused before any launch.
     need = cai.cai_mqa_decode_workspace_size(64, 64, 2048, 64, 0, 64)
     assert need > 32 << 20
