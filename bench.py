@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--local-ring", action="store_true",
                     help="keep each sequence of a local-only KV buffer in a ring of pages (window recycling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--no-parity", action="store_true", help="skip the oracle check of the timed outputs")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="default run only: skip the long-context (5) and append-prefill (4) sub-records")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ncu", action="store_true",
                     help="open the CUDA profiler window around the timed steps only (for ncu --profile-from-start off)")
@@ -210,17 +213,25 @@ def profiled_traffic(workload_tag: str):
 
 # ----------------------------------------------------------------------------- CPU oracle leg
 
+PARITY_ATOL = 2e-3  # max abs error of attention outputs against the float64 oracle
+
+
+def sample_seqs(ctx_len, n_spaced):
+    """Shortest, longest and about n_spaced more sequences evenly spaced by length."""
+    order = np.argsort(ctx_len, kind="stable")
+    picks = [int(order[0]), int(order[-1])] + [int(i) for i in order[1:-1:max(1, len(order) // n_spaced)]]
+    return list(dict.fromkeys(picks))
+
+
 class CpuOracle:
     """The oracle (as it stands) on host cores over a bounded sample of the workload's sequences."""
 
-    def __init__(self, w):
+    def __init__(self, w, n_spaced: int = 14):
         import oracle
         import synth
 
         self.w = w
-        order = np.argsort(w.ctx_len)
-        picks = [int(order[0]), int(order[-1])] + [int(i) for i in order[1:-1:max(1, len(order) // 14)]]
-        self.picks = list(dict.fromkeys(picks))
+        self.picks = sample_seqs(w.ctx_len, n_spaced)
         # Inputs (codes, scales, queries) prepared untimed, like resident device inputs.
         self.items = []
         for b in self.picks:
@@ -230,8 +241,29 @@ class CpuOracle:
                 qb = synth.q_rows(w.seed, synth.stream_q(layer), b, w.num_q_heads)
                 W = w.layer_windows[layer]
                 tokens = min(L, W) if W > 0 else L
-                self.items.append((qb, kv[w.layer_to_buffer[layer]], L, W, tokens))
+                self.items.append((qb, kv[w.layer_to_buffer[layer]], L, W, tokens, b, layer))
         self.cores = os.cpu_count() or 1
+
+    def parity(self, outs):
+        """Max abs error of the GPU outputs (numpy [layer][B][Hq][128]) against the oracle on the
+        sampled sequences, all layers."""
+        import oracle
+        from concurrent.futures import ThreadPoolExecutor
+
+        w = self.w
+
+        def one(item):
+            qb, (kc, ks, vc, vs), L, W, _, b, layer = item
+            ref, _ = oracle.decode_seq(qb, kc, ks, vc, vs, L, W, w.softmax_scale)
+            return float(np.abs(outs[layer][b] - ref).max())
+
+        with ThreadPoolExecutor(self.cores) as ex:
+            worst = max(ex.map(one, self.items))
+        ok = bool(worst <= PARITY_ATOL)
+        return {"max_abs_err": worst, "n_seqs": len(self.picks), "layers": len(w.layer_windows),
+                "atol": PARITY_ATOL, "ok": ok,
+                "what": "outputs of the last timed step against the float64 oracle on the shortest, the longest and "
+                        "evenly spaced sequences"}
 
     def run(self, seconds: float):
         import oracle
@@ -240,7 +272,7 @@ class CpuOracle:
         w = self.w
 
         def one(item):
-            qb, (kc, ks, vc, vs), L, W, _ = item
+            qb, (kc, ks, vc, vs), L, W = item[:4]
             oracle.decode_seq(qb, kc, ks, vc, vs, L, W, w.softmax_scale)
 
         done_tokens, t0 = 0, time.perf_counter()
@@ -269,6 +301,26 @@ def prefill_flops(w):
             lo = max(0, hi - w.layer_windows[0]) if w.layer_windows[0] > 0 else 0
             pairs += hi - lo
     return 4 * 128 * w.num_q_heads * pairs, pairs
+
+
+def prefill_parity(w, out, seqs=None, tokens=(0, 1, 127, 128, 129, 254, 255)):
+    """Max abs error of prefill outputs (numpy [B][n_new][Hq][128]) against the oracle on sampled
+    sequences and new tokens (the first and last tokens of the chunk and those at the tile edges)."""
+    import oracle
+    import synth
+
+    seqs = sample_seqs(w.ctx_len, 2) if seqs is None else seqs
+    tokens = [t for t in tokens if t < w.n_new]
+    worst = 0.0
+    for b in seqs:
+        L = int(w.ctx_len[b])
+        kc, ks, vc, vs = oracle.seq_kv(w.seed, 0, b, L)
+        qb = synth.q_rows(w.seed, synth.STREAM_Q_PREFILL, b, w.n_new * w.num_q_heads).reshape(w.n_new, w.num_q_heads, 128)
+        ref, _ = oracle.prefill_seq(qb, kc, ks, vc, vs, L - w.n_new, w.layer_windows[0], w.softmax_scale, tokens)
+        worst = max(worst, float(np.abs(out[b][tokens] - ref).max()))
+    return {"max_abs_err": worst, "n_seqs": len(seqs), "tokens_per_seq": len(tokens), "atol": PARITY_ATOL,
+            "ok": bool(worst <= PARITY_ATOL),
+            "what": "outputs of the last timed call against the float64 oracle on sampled sequences and tokens"}
 
 
 def bf16_peak():
@@ -334,6 +386,7 @@ def run_prefill(args, rank, world):
         clocks.stop()
     ms = allreduce_max(t0.elapsed_time(t1), world)
     kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    parity = prefill_parity(w, out.cpu().numpy()) if rank == 0 and not args.no_parity else None
     flops, pairs = prefill_flops(w)
     sustained, burst, kind = bf16_peak()
     achieved = flops / (kernel_ms * 1e-3) / 1e12
@@ -349,6 +402,7 @@ def run_prefill(args, rank, world):
                      "frac": achieved / sustained, "traffic": None, "peak_kind": kind + " bf16 sustained",
                      "kernel": "cai_mqa_prefill_chunk (dequant pass + tcgen05 attention)"},
         "clocks": clocks.summary(),
+        "parity": parity,
     }
 
 
@@ -530,6 +584,13 @@ def run_gpu(args, rank, world):
     tag = f"config{args.config}-B{w.batch}-seed{seed}"
     traffic = profiled_traffic(tag)
 
+    # Parity of the benchmarked step: the outputs of its last timed pass against the oracle.
+    cpu = None
+    parity = None
+    if rank == 0 and not args.no_parity:
+        cpu = CpuOracle(w, n_spaced=14 if args.config != 5 else 2)
+        parity = cpu.parity([o.cpu().numpy() for o in outs])
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, w, cache, qs, outs, wss, step_kv, toks_step, world, layered)
@@ -556,9 +617,10 @@ def run_gpu(args, rank, world):
         "queries_per_s": world * w.batch * args.steps / (ms_max * 1e-3),
         "clocks": clocks.summary(),
         "e2e": e2e,
+        "parity": parity,
     }
     if rank == 0 and world == 1 and not args.no_cpu:
-        result["cpu_baseline"] = CpuOracle(w).run(args.cpu_seconds)
+        result["cpu_baseline"] = (cpu or CpuOracle(w)).run(args.cpu_seconds)
     return result
 
 
@@ -723,11 +785,40 @@ def main():
         res = run_mixed(args, rank, world)
     else:
         res = run_prefill(args, rank, world) if args.config == 4 else run_gpu(args, rank, world)
+        if args.config == 3 and not args.no_extra and not args.per_layer and not args.local_ring and args.batch is None:
+            res["extra"] = run_extra(args, rank, world)
+    bad = [k for k, r in [("main", res), *((res.get("extra") or {}).items())]
+           if isinstance(r, dict) and isinstance(r.get("parity"), dict) and not r["parity"]["ok"]]
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    if bad:
+        print(f"parity failed: {bad}", file=sys.stderr, flush=True)
+        sys.exit(3)
+
+
+def run_extra(args, rank, world):
+    """The long-context global decode (workload 5, batch 1024) and the append-prefill chunk (workload 4,
+    batch 16), each timed for a few steps after the headline step, with its roofline and an oracle check."""
+    import copy
+    import gc
+    import torch
+
+    extra = {}
+    for cfg in (5, 4):
+        gc.collect()
+        torch.cuda.empty_cache()
+        a = copy.copy(args)
+        a.config, a.steps, a.warmup, a.no_e2e, a.no_cpu, a.num_splits = cfg, min(args.steps, 30), 3, True, True, 0
+        r = run_prefill(a, rank, world) if cfg == 4 else run_gpu(a, rank, world)
+        keep = ("value", "unit", "ms_per_step", "roofline", "parity", "clocks", "gpu_launches", "queries_per_s")
+        extra[f"config{cfg}"] = {"workload": r["config"]["workload"], "steps": a.steps,
+                                 **{k: r[k] for k in keep if k in r}}
+    gc.collect()
+    torch.cuda.empty_cache()
+    return extra
 
 
 if __name__ == "__main__":
