@@ -58,8 +58,8 @@ typedef enum cai_status {
 
 /* One KV buffer: a pool of fixed-size pages (PagedAttention blocks).
  * Page layout (bytes), for P = page_size and d = head_dim:
- *   [0,        P*d)        K codes, int8 [P][d]
- *   [P*d,      2*P*d)      V codes, int8 [P][d]
+ *   [0,        P*d)        K codes, int8 [P][d] (token-major: slot s at s*d)
+ *   [P*d,      2*P*d)      V codes, int8 [d][P] (channel-major: channel c at c*P)
  *   [2*P*d,    2*P*d+4*P)  K scales, fp32 [P]
  *   [2*P*d+4P, 2*P*d+8*P)  V scales, fp32 [P]
  * Token at position p of a sequence lives in page block_table[p / P], slot p % P.

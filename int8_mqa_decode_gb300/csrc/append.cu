@@ -5,7 +5,9 @@
 // One warp per (sequence, new token, K|V): 32 lanes x float4 = one 128-wide
 // row read with 512-byte coalesced loads; warp-shuffle absmax; IEEE fp32
 // division for the scale and for every quotient, round-half-even, clamp to
-// [-127, 127]; one 32-bit store of four codes per lane and one fp32 scale.
+// [-127, 127]; the codes go to the token's K row (one 32-bit store per lane)
+// or to its column of the channel-major V block (four byte stores per lane),
+// and one fp32 scale.
 // Bit-exact by construction: no fused multiply-add touches the quotient path
 // and the build uses neither fast-math nor flush-to-zero.
 #include "common.cuh"
@@ -65,8 +67,16 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
     }
   }
   uint8_t* pg = p.pages + (int64_t)page * page_bytes(P);
-  uint8_t* codes = pg + (is_v ? P * kHeadDim : 0) + slot * kHeadDim;
-  reinterpret_cast<uint32_t*>(codes)[lane] = packed;
+  if (!is_v) {
+    // K codes are token-major: one 128-byte row per slot.
+    reinterpret_cast<uint32_t*>(pg + slot * kHeadDim)[lane] = packed;
+  } else {
+    // V codes are channel-major: channel c's P codes are contiguous, so this token's
+    // code of channel c is byte c * P + slot of the V block.
+    uint8_t* v = pg + P * kHeadDim + slot;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[(lane * 4 + e) * P] = (uint8_t)(packed >> (8 * e));
+  }
   if (lane == 0) {
     float* scales = reinterpret_cast<float*>(pg + 2 * P * kHeadDim) + (is_v ? P : 0);
     scales[slot] = s;

@@ -29,17 +29,19 @@
 //    are never read;
 //  * converters (warps 4-11): read a tile's codes and scales into registers
 //    and hand the stages back at once; then K codes -> fp16 (exact) into tensor
-//    memory (the A operand, one token per lane), V codes -> fp16 into the
-//    canonical no-swizzle MN-major operand layout in shared memory, the
-//    per-token scales and mask into a four-tile ring, and at an item's first
-//    tile the item's query (bf16 -> fp16) as the K-major B operand Q^T;
+//    memory as the A operand of S^T (one token per lane), V codes -> fp16 into
+//    tensor memory as the A operand V^T of PV (one channel per lane: a page
+//    keeps its V codes channel-major, so a lane's 16-byte load holds 16 tokens
+//    of its channel), the per-token scales and mask into a four-tile ring, and
+//    at an item's first tile the item's query (bf16 -> fp16) as the K-major B
+//    operand Q^T;
 //  * MMA issuers: warp 1 issues S^T = K Q^T (tcgen05.mma kind::f16, M = 128
 //    tokens, N = heads padded to 32 or 64, K = 128, A from tensor memory) into
 //    a double-buffered S^T; warp 3 issues O^T += V^T P^T (M = 128 channels,
-//    N = heads, K = 128 tokens, both operands from shared memory) into one of
-//    two O^T accumulators (one per item in flight).  Each launch of 8 K steps
-//    holds its issuing thread for most of its run time, so the two streams are
-//    issued by different warps;
+//    N = heads, K = 128 tokens, V^T from tensor memory, P^T from shared
+//    memory) into one of two O^T accumulators (one per item in flight).  Each
+//    launch of 8 K steps holds its issuing thread for most of its run time, so
+//    the two streams are issued by different warps;
 //  * softmax (warps 12-15, one thread per token of the tile): applies the K
 //    scale and softmax scale, checks the logits against a per-head reference
 //    maximum shared by the four warps (at an item's first tile, the logits of
@@ -60,7 +62,6 @@ constexpr int T = kDecodeTile;                 // 128 tokens per tile
 constexpr int RT = 64;                         // tokens per raw stage
 constexpr int kStageKV = RT * 2 * kHeadDim;    // K and V code rows of one stage (16 KB)
 constexpr int kStageSc = RT * 8;               // their K and V scales (512 B)
-constexpr int kOp16Bytes = T * kHeadDim * 2;   // one fp16 128 x 128 operand (32 KB)
 constexpr int kRing = 6;                       // work items published ahead by the scheduler (8: 2% slower
                                                // on the one-launch hybrid step, more items claimed ahead)
 constexpr int kRingInts = 40;                  // ring entry: 8 item fields + 32 page ids
@@ -69,11 +70,10 @@ constexpr int kScaleSlots = 4;                 // scale/mask ring depth (tiles)
 // Shared-memory layout for HN padded heads (32 or 64).
 template <int HN>
 struct Layout {
-  static constexpr int NST = HN <= 32 ? 7 : 6;                   // raw stages
+  static constexpr int NST = HN <= 32 ? 11 : 9;                  // raw stages
   static constexpr int kOffRawKV = 0;                            // [NST][16 KB], 1024-aligned (swizzle)
-  static constexpr int kOffV16 = kOffRawKV + NST * kStageKV;     // V16[2]
   static constexpr int kPTBytes = HN * T * 2;
-  static constexpr int kOffPT = kOffV16 + 2 * kOp16Bytes;        // P^T[2]
+  static constexpr int kOffPT = kOffRawKV + NST * kStageKV;      // P^T[2]
   static constexpr int kOffQT = kOffPT + 2 * kPTBytes;           // Q^T
   static constexpr int kOffRawSc = kOffQT + HN * kHeadDim * 2;   // [NST][512 B]
   static constexpr int kOffScal = kOffRawSc + NST * kStageSc;    // [4][3][T] floats
@@ -265,8 +265,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   constexpr int SPS = RT / P;                  // pages per stage
   constexpr int kRowsPerPage = page_bytes(P) / 128;
   constexpr uint32_t kColKA = 0;               // K operand [2]: 64 columns each (fp16 pairs)
-  constexpr uint32_t kColS = 128;              // S^T [2]: HN columns each
-  constexpr uint32_t kColO = 128 + 2 * HN;     // O^T [2]: HN columns each
+  constexpr uint32_t kColV = 128;              // V^T operand [2]: 64 columns each (fp16 token pairs)
+  constexpr uint32_t kColS = 256;              // S^T [2]: HN columns each
+  constexpr uint32_t kColO = 256 + 2 * HN;     // O^T [2]: HN columns each
+  static_assert(kColO + 2 * HN <= kTmemCols, "tensor memory columns");
   static_assert(page_bytes(P) % 128 == 0 && P % 16 == 0, "page rows");
   const DecodeParams& p = args.p;
 
@@ -274,7 +276,6 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* raw_kv = smem + L::kOffRawKV;
   uint8_t* raw_sc = smem + L::kOffRawSc;
-  uint8_t* v16 = smem + L::kOffV16;
   uint8_t* pt = smem + L::kOffPT;
   uint8_t* qt = smem + L::kOffQT;
   float* scal = reinterpret_cast<float*>(smem + L::kOffScal);  // [kScaleSlots][k scale, valid, v scale][T]
@@ -290,10 +291,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   uint64_t* raw_full = bars;                 // [NST] producer -> converters (tx bytes)
   uint64_t* raw_empty = bars + NST;          // [NST] converters -> producer
   uint64_t* k_full = bars + 2 * NST;         // [2] converters -> MMA (K operand, Q^T)
-  uint64_t* v_full = k_full + 2;             // [2] converters -> MMA (V operand)
+  uint64_t* v_full = k_full + 2;             // [2] converters -> MMA (V^T operand)
   uint64_t* s_full = v_full + 2;             // [2] MMA commit after S^T
   uint64_t* p_full = s_full + 2;             // [2] softmax -> MMA (P^T)
-  uint64_t* v_free = p_full + 2;             // [2] MMA commit after PV (V16 and P^T free)
+  uint64_t* v_free = p_full + 2;             // [2] MMA commit after PV (V^T and P^T free)
   uint64_t* o_full = v_free + 2;             // [2] MMA commit after an item's last PV
   uint64_t* o_empty = o_full + 2;            // [2] softmax -> MMA after reading O^T
   uint64_t* item_full = o_empty + 2;         // [kRing] scheduler -> readers
@@ -466,15 +467,14 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       }
     } else {
       // ---------------------------------------------------------- MMA issuers
-      // Warp 1 issues S^T = K Q^T, warp 3 issues O^T += V16 P^T: each waits only for
+      // Warp 1 issues S^T = K Q^T, warp 3 issues O^T += V^T P^T: each waits only for
       // its own operands, so one warp's barrier waits overlap the other's launches,
       // and an item's last PV goes out as soon as its P^T is ready.
       constexpr uint32_t idesc_s = idesc_f16_f32(T, HN, 0, 0);
-      constexpr uint32_t idesc_o = idesc_f16_f32(kHeadDim, HN, 1, 1);
+      constexpr uint32_t idesc_o = idesc_f16_f32(kHeadDim, HN, 0, 1);  // A = V^T from tensor memory
       // Descriptor bases; a K step of 16 adds 256 bytes, i.e. 16 to the address field
       // (shared addresses stay below 2^18, so the 14-bit field never carries).
       const uint64_t dq = smem_desc(smem_addr(qt), 128, 2048);
-      const uint64_t dv = smem_desc(smem_addr(v16), 128, T * 16);
       const uint64_t dp = smem_desc(smem_addr(pt), 128, T * 16);
       const bool s_issuer = warp == 1;
       int g = 0, item_n = 0, k = 0;
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
             if (lane == 0) {
 #pragma unroll
               for (int ks = 0; ks < T / 16; ++ks)
-                mma_f16_ss(tmem + kColO + ob * HN, dv + (uint64_t)(c * (kOp16Bytes >> 4) + ks * 16),
+                mma_f16_ts(tmem + kColO + ob * HN, tmem + kColV + c * 64 + ks * 8,
                            dp + (uint64_t)(c * (L::kPTBytes >> 4) + ks * 16), idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
               mma_commit(&v_free[c]);
               if (t == it.ntiles - 1) mma_commit(&o_full[ob]);
@@ -573,7 +573,13 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
              mbar_wait_abortable(&raw_full[s1], ((2 * g + 1) / NST) & 1, abort_flag);
         if (!ok) break;
         // Codes to registers.  Row r of a page slot holds its 16-byte chunk j at
-        // chunk position j ^ (r % 8) (128-byte swizzle; slots are 1024-aligned).
+        // chunk position j ^ (r % 8) (128-byte swizzle; slots are 1024-aligned,
+        // and a page occupies 2P rows of its stage, a multiple of 8).
+        //  K: this thread's token tk, channels hh*64 .. hh*64+63 (K rows are token-major).
+        //  V: this thread's channel tk, the 64 tokens of tile half hh (stage s0 or s1):
+        //     V rows are channel-major, so 16 consecutive tokens of one channel are one
+        //     16-byte chunk: channel c's codes start at byte c*P of the page's V block
+        //     (block rows P .. 2P-1 of the page).
         uint4 wk[4], wv[4];
         {
           const int tr = tk & (RT - 1);
@@ -582,14 +588,15 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
 #pragma unroll
           for (int i = 0; i < 4; ++i) wk[i] = *reinterpret_cast<const uint4*>(row + (((hh * 4 + i) ^ (tk & 7)) << 4));
         }
+        {
+          const uint8_t* st = raw_kv + (hh ? s1 : s0) * kStageKV;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int U = u * 256 + ctid;
-          const int tv = ((U >> 6) << 3) | (U & 7), j = (U >> 3) & 7;
-          const int tr = tv & (RT - 1);
-          const uint8_t* row = raw_kv + (tv < RT ? s0 : s1) * kStageKV + (tr / P) * (2 * P * kHeadDim) +
-                               (P + tr % P) * kHeadDim;
-          wv[u] = *reinterpret_cast<const uint4*>(row + ((j ^ (tv & 7)) << 4));
+          for (int u = 0; u < 4; ++u) {
+            const int j = (u * 16) / P, o = (u * 16) % P;       // page of the stage, first token in it
+            const int off = tk * P + o;                          // byte within the page's V block
+            const int r = P + off / 128, ch = (off % 128) / 16;  // row of the page, chunk of the row
+            wv[u] = *reinterpret_cast<const uint4*>(st + j * (2 * P * kHeadDim) + r * 128 + ((ch ^ (r & 7)) << 4));
+          }
         }
         // Scales and mask of tile g into ring slot g % 4 (free once the softmax of tile g-4 is done).
         const int ss = g & (kScaleSlots - 1);
@@ -633,26 +640,24 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&k_full[c]);
-        // V -> V16[c], free once PV of tile g-2 is done.
+        // V -> V^T[c] in tensor memory (lane = channel, column k = tokens 2k, 2k+1 of
+        // the tile; this warp writes the 32 columns of its tile half), free once PV of
+        // tile g-2 is done.
         if (g >= 2) ok = mbar_wait_abortable(&v_free[c], ((g >> 1) - 1) & 1, abort_flag);
         if (!ok) break;
+        tc_fence_after();
         {
-          uint8_t* vd = v16 + c * kOp16Bytes;
+          uint32_t vw[32];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int U = u * 256 + ctid;
-            const int tv = ((U >> 6) << 3) | (U & 7), j = (U >> 3) & 7;
-            uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
-            i8x4_to_f16x4(wv[u].x, a0, a1);
-            i8x4_to_f16x4(wv[u].y, a2, a3);
-            i8x4_to_f16x4(wv[u].z, a4, a5);
-            i8x4_to_f16x4(wv[u].w, a6, a7);
-            // MN-major: channel d, token t at (d/8)*2048 + (t/8)*128 + (t%8)*16 + (d%8)*2.
-            *reinterpret_cast<uint4*>(vd + (2 * j) * 2048 + tv * 16) = make_uint4(a0, a1, a2, a3);
-            *reinterpret_cast<uint4*>(vd + (2 * j + 1) * 2048 + tv * 16) = make_uint4(a4, a5, a6, a7);
+            const uint32_t xs[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) i8x4_to_f16x4(xs[e], vw[u * 8 + e * 2], vw[u * 8 + e * 2 + 1]);
           }
+          tmem_st_32x32b_x32(tmem + t_lane + kColV + c * 64 + hh * 32, vw);
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&v_full[c]);
       }

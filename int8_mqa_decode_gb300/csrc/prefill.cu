@@ -135,7 +135,9 @@ __global__ void __launch_bounds__(256) dequant_kernel(const PrefillParams p) {
       const int slot = t % P;
       const uint8_t* pg = p.pages + (int64_t)page * page_bytes(P);
       kw = reinterpret_cast<const uint32_t*>(pg + slot * kHeadDim)[lane];
-      vw = reinterpret_cast<const uint32_t*>(pg + P * kHeadDim + slot * kHeadDim)[lane];
+      const uint8_t* vcol = pg + P * kHeadDim + slot;  // channel-major V block: channel c at c * P
+#pragma unroll
+      for (int e = 0; e < 4; ++e) vw |= (uint32_t)vcol[(lane * 4 + e) * P] << (8 * e);
       const float* sc = reinterpret_cast<const float*>(pg + 2 * P * kHeadDim);
       ksc = sc[slot] * p.scale_log2;
       vsc = sc[P + slot];

@@ -26,9 +26,10 @@ What is computed, and from which passage of the pages:
 * ``pool_write`` / ``pool_read``: the paged layout (PagedAttention, section
   "1. PagedAttention" of the Red Hat page): fixed-size blocks anywhere in a
   pool plus a per-sequence table of block ids.  Byte layout of one page of P
-  tokens and head_dim d: K codes int8 [P][d], V codes int8 [P][d], K scales
-  fp32 [P], V scales fp32 [P]; token at position p of a sequence sits in page
-  table[p // P], slot p % P.
+  tokens and head_dim d (the pages fix none; this is the library's): K codes
+  int8 [P][d] (token-major), V codes int8 [d][P] (channel-major: the P codes
+  of channel c are contiguous), K scales fp32 [P], V scales fp32 [P]; token at
+  position p of a sequence sits in page table[p // P], slot p % P.
 * ``prefill_ranges``: new tokens appended on top of a reused prefix (prefix
   caching, section "3. Cache de prefixo"; cross-turn cache, section 04): new
   token i at absolute position p0+i attends keys 0..p0+i, all of them read
@@ -241,7 +242,7 @@ def pool_new(num_pages: int, page_size: int, head_dim: int = 128, fill: int = 0x
 def _page_views(pool: np.ndarray, page: int, P: int, d: int):
     base = page * page_bytes(P, d)
     kc = pool[base:base + P * d].view(np.int8).reshape(P, d)
-    vc = pool[base + P * d:base + 2 * P * d].view(np.int8).reshape(P, d)
+    vc = pool[base + P * d:base + 2 * P * d].view(np.int8).reshape(d, P).T  # [slot][channel] view of [d][P]
     ks = pool[base + 2 * P * d:base + 2 * P * d + 4 * P].view(np.float32)
     vs = pool[base + 2 * P * d + 4 * P:base + 2 * P * d + 8 * P].view(np.float32)
     return kc, vc, ks, vs

@@ -318,8 +318,9 @@ def test_pool_layout_byte_offsets_by_hand():
     vc = np.full((1, d), -4, dtype=np.int8)
     oracle.pool_write(pool, table, 17, kc, np.array([0.25], np.float32), vc, np.array([0.5], np.float32), P, d)
     base = 2 * 4224  # position 17 -> table[1] = page 2, slot 1
-    assert np.all(pool[base + 128:base + 256] == 3)
-    assert np.all(pool[base + 2048 + 128:base + 2048 + 256].view(np.int8) == -4)
+    assert np.all(pool[base + 128:base + 256] == 3)  # K: token-major, slot 1 = bytes 128..255
+    v_block = pool[base + 2048:base + 4096].view(np.int8).reshape(128, 16)  # V: channel-major [d][P]
+    assert np.all(v_block[:, 1] == -4) and np.count_nonzero(v_block) == 128
     assert pool[base + 4096 + 4:base + 4096 + 8].view(np.float32)[0] == 0.25
     assert pool[base + 4096 + 64 + 4:base + 4096 + 64 + 8].view(np.float32)[0] == 0.5
     float_bytes = np.count_nonzero(np.array([0.25, 0.5], np.float32).view(np.uint8))
