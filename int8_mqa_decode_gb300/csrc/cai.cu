@@ -13,7 +13,7 @@ static inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static inline bool page_size_ok(int32_t P) { return P == 16 || P == 32 || P == 64; }
 constexpr int32_t kItemsPerSmAlone = 32;  // a global layer's split target when launched alone
-constexpr int32_t kItemsPerSmMixed = 22;  // ... when launched together with local layers
+constexpr int32_t kItemsPerSmMixed = 6;   // ... when launched together with local layers
 
 // Split plan.  The attended span of a sequence is at most `span` tokens (the
 // window, or the block-table capacity for a global layer).  Chunks are
@@ -21,10 +21,12 @@ constexpr int32_t kItemsPerSmMixed = 22;  // ... when launched together with loc
 // items per SM for the expected total work of a global layer (half the capacity
 // per sequence), chunks of 512 to 16384 tokens, at most 64 splits -- short items
 // let the dynamic queue even out the SMs whatever the length mix, long ones pay
-// fewer item boundaries.  Measured on the hybrid step: a global layer launched
-// alone is best at 32 items per SM (8: 0.453 ms, 16 0.422, 32 0.396, 64 0.431);
-// launched with the local layers, whose items then even out the tail, at 22
-// (8: 0.304 ms, 16 0.264, 20 0.254, 22 0.253, 24 0.254, 28 0.259, 32 0.270).  A
+// fewer item boundaries (each costs a few thousand cycles).  A global layer
+// launched with local layers, whose whole-window items then even out the tail,
+// takes few long items: the hybrid step measured 0.235 ms at 4 items per SM,
+// 0.215 at 6, 0.217 at 8, 0.221 at 12, 0.225 at 16, 0.234 at 22, 0.251 at 32.
+// Launched alone (the long-context workload) the target matters little (8 to 32
+// within 0.3%); 32 keeps the tail short.  A
 // local layer is not split when its batch alone gives every SM a sequence (each
 // extra split costs its partial's write and read, about an eighth of a
 // 1024-token window at 32 heads; 2 and 4 splits measured slower).

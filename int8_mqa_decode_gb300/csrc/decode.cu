@@ -62,8 +62,8 @@ constexpr int T = kDecodeTile;                 // 128 tokens per tile
 constexpr int RT = 64;                         // tokens per raw stage
 constexpr int kStageKV = RT * 2 * kHeadDim;    // K and V code rows of one stage (16 KB)
 constexpr int kStageSc = RT * 8;               // their K and V scales (512 B)
-constexpr int kRing = 6;                       // work items published ahead by the scheduler (8: 2% slower
-                                               // on the one-launch hybrid step, more items claimed ahead)
+constexpr int kRing = 6;                       // ring of published work items (readers lag the producer)
+constexpr int kClaimAhead = 2;                 // items claimed but not yet started by the producer, at most
 constexpr int kRingInts = 40;                  // ring entry: 8 item fields + 32 page ids
 constexpr int kScaleSlots = 4;                 // scale/mask ring depth (tiles)
 
@@ -81,7 +81,7 @@ struct Layout {
   static constexpr int kOffBars = kOffXch + 13 * HN * 4;
   static_assert(kOffXch % 16 == 0 && kOffPT % 16 == 0, "bulk-copy sources");
   static constexpr int kNumBars = 2 * NST + 2 * 2 /*k_full, v_full*/ + 2 * 2 /*s_full, p_full*/ + 2 /*v_free*/ +
-                                  2 * 2 /*o_full, o_empty*/ + 2 * kRing + 2 * kScaleSlots;
+                                  2 * 2 /*o_full, o_empty*/ + 3 * kRing + 2 * kScaleSlots;
   static constexpr int kOffMisc = kOffBars + 8 * kNumBars;       // tmem slot, abort flag, page_ok[NST]
   static constexpr int kOffRing = kOffMisc + 64;
   static constexpr int kSmemBytes = kOffRing + kRing * kRingInts * 4 + 1024;
@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   uint64_t* item_empty = item_full + kRing;  // [kRing] readers -> scheduler
   uint64_t* scale_full = item_empty + kRing;        // [kScaleSlots] converters -> softmax
   uint64_t* scale_free = scale_full + kScaleSlots;  // [kScaleSlots] softmax -> converters
+  uint64_t* item_taken = scale_free + kScaleSlots;  // [kRing] producer -> scheduler (item started)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kOffMisc + 4);
   uint32_t* page_ok = reinterpret_cast<uint32_t*>(smem + L::kOffMisc + 8);        // [NST]
@@ -329,6 +330,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&item_full[r], 1);
       mbar_init(&item_empty[r], R::kItemReaders);
+      mbar_init(&item_taken[r], 1);
     }
     for (int r = 0; r < kScaleSlots; ++r) {
       mbar_init(&scale_full[r], kConvWarps);
@@ -358,7 +360,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
     it = ring_item(ring + slot * kRingInts, done);
     if (first_ids) *first_ids = (int32_t)ring[slot * kRingInts + 8 + lane];
     __syncwarp();
-    if (lane == 0) mbar_arrive(&item_empty[slot]);
+    if (lane == 0) {
+      mbar_arrive(&item_empty[slot]);
+      if (warp == 0) mbar_arrive(&item_taken[slot]);  // the producer starts item k
+    }
     return it;
   };
 
@@ -366,8 +371,15 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
     setmaxnreg_dec<R::kRegsCtl>();
     if (warp == kSchedWarp) {
       // ---------------------------------------------------------- scheduler
+      // An item is claimed from the global queue only once the producer has started the
+      // item kClaimAhead before it: a CTA holds few claimed items, so the queue, not
+      // early claims, decides which SM runs what (claiming up to the ring's depth let
+      // a few SMs hoard long items and finish far behind the others).
       int k = 0;
       while (true) {
+        if (k >= kClaimAhead &&
+            !mbar_wait_abortable(&item_taken[(k - kClaimAhead) % kRing], ((k - kClaimAhead) / kRing) & 1, abort_flag))
+          break;
         int idx = 0;
         if (lane == 0) idx = (int)atomicAdd(&p.queue[0], 1u);
         idx = __shfl_sync(0xffffffffu, idx, 0);
