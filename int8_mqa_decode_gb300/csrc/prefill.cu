@@ -43,10 +43,15 @@ constexpr int kKeys = 128;                 // keys per tile (MMA N of S, K of PV
 constexpr int kTileBytes = kKeys * kHeadDim * 2;  // 32 KB of 16-bit values
 constexpr int kStages = 2;
 constexpr int kOffQ = 0;                                     // Q[kQT]
-constexpr int kOffStage = kOffQ + kQT * kRows * kHeadDim * 2;
-constexpr int kStageBytes = 2 * kTileBytes + kKeys * 4;  // K codes, V (scaled), K scales
-constexpr int kOffBars = kOffStage + kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 6 * kQT;
+// K tiles and V tiles (with the tile's K scales) have separate two-slot rings: a K
+// slot is free as soon as both q-tiles' S = Q K^T have run, so the next K tile loads
+// while the softmax of this one runs; a V slot (and its scales, which the softmax
+// reads) is free after both PVs.
+constexpr int kOffK = kOffQ + kQT * kRows * kHeadDim * 2;   // K[kStages]
+constexpr int kVSlotBytes = kTileBytes + kKeys * 4;          // V (scaled), K scales
+constexpr int kOffV = kOffK + kStages * kTileBytes;          // V[kStages]
+constexpr int kOffBars = kOffV + kStages * kVSlotBytes;
+constexpr int kNumBars = 4 * kStages + 6 * kQT;
 constexpr int kOffMisc = kOffBars + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 // Warpgroup 0: K/V producer (warp 0), MMA issuer (warp 1), two spare warps;
@@ -218,9 +223,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* kv_full = bars;                    // [kStages] producer -> MMA, softmax (tx bytes)
-  uint64_t* kv_empty = bars + kStages;         // [kStages] MMA commit after both PVs of the tile
-  uint64_t* q_full = bars + 2 * kStages;       // [kQT] softmax group -> MMA (4 warps)
+  uint64_t* k_full = bars;                     // [kStages] producer -> MMA (tx bytes)
+  uint64_t* k_empty = bars + kStages;          // [kStages] MMA commit after both S of the tile
+  uint64_t* v_full = bars + 2 * kStages;       // [kStages] producer -> MMA, softmax (V and K scales)
+  uint64_t* v_empty = bars + 3 * kStages;      // [kStages] MMA commit after both PVs of the tile
+  uint64_t* q_full = bars + 4 * kStages;       // [kQT] softmax group -> MMA (4 warps)
   uint64_t* s_full = q_full + kQT;             // [kQT] MMA commit after S
   uint64_t* p_full = s_full + kQT;             // [kQT] softmax -> MMA (4 warps)
   uint64_t* pv_done = p_full + kQT;            // [kQT] MMA commit after PV
@@ -236,8 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int q = 0; q < kQT; ++q) {
       mbar_init(&q_full[q], 4);
@@ -266,13 +275,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         const int64_t seq_row0 = (int64_t)it.b * p.kt_rows;
         for (int j = 0; j < it.nkt; ++j, ++g) {
           const int s = g % kStages;
-          if (g >= kStages && !mbar_wait_abortable(&kv_empty[s], ((g / kStages) - 1) & 1, abort_flag)) break;
-          uint8_t* st = smem + kOffStage + s * kStageBytes;
           const int64_t row = seq_row0 + (int64_t)(it.kt0 + j) * kKeys;
-          mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
-          tma_load_rows128(st, &kmap, (int)row, &kv_full[s]);
-          tma_load_rows128(st + kTileBytes, &vmap, (int)row, &kv_full[s]);
-          bulk_g2s(st + 2 * kTileBytes, p.ks + row, kKeys * 4, &kv_full[s]);
+          if (g >= kStages && !mbar_wait_abortable(&k_empty[s], ((g / kStages) - 1) & 1, abort_flag)) break;
+          mbar_arrive_expect_tx(&k_full[s], kTileBytes);
+          tma_load_rows128(smem + kOffK + s * kTileBytes, &kmap, (int)row, &k_full[s]);
+          if (g >= kStages && !mbar_wait_abortable(&v_empty[s], ((g / kStages) - 1) & 1, abort_flag)) break;
+          uint8_t* vs = smem + kOffV + s * kVSlotBytes;
+          mbar_arrive_expect_tx(&v_full[s], kVSlotBytes);
+          tma_load_rows128(vs, &vmap, (int)row, &v_full[s]);
+          bulk_g2s(vs + kTileBytes, p.ks + row, kKeys * 4, &v_full[s]);
         }
       }
     }
@@ -284,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       const uint32_t qa0 = smem_addr(smem + kOffQ);
       int g = 0, n = 0;
       auto issue_s = [&](int q, int gg) {
-        const uint32_t ka = smem_addr(smem + kOffStage + (gg % kStages) * kStageBytes);
+        const uint32_t ka = smem_addr(smem + kOffK + (gg % kStages) * kTileBytes);
         const uint32_t qa = qa0 + q * kRows * kHeadDim * 2;
 #pragma unroll
         for (int ks = 0; ks < kHeadDim / 16; ++ks)
@@ -293,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         mma_commit(&s_full[q]);
       };
       auto issue_pv = [&](int q, int gg, bool first) {
-        const uint32_t va = smem_addr(smem + kOffStage + (gg % kStages) * kStageBytes + kTileBytes);
+        const uint32_t va = smem_addr(smem + kOffV + (gg % kStages) * kVSlotBytes);
 #pragma unroll
         for (int ks = 0; ks < kKeys / 16; ++ks)
           mma_f16_ts(tmem + q * 256 + 128, tmem + q * 256 + ks * 8, smem_desc(va + ks * 256, 128, 2048), idesc_o,
@@ -307,10 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         for (int j = 0; j < it.nkt && ok; ++j, ++g) {
           const int s = g % kStages;
           if (j == 0) {
-            if (!mbar_wait_abortable(&kv_full[s], (g / kStages) & 1, abort_flag)) break;
+            if (!mbar_wait_abortable(&k_full[s], (g / kStages) & 1, abort_flag)) break;
             tc_fence_after();
             issue_s(0, g);
             issue_s(1, g);
+            mma_commit(&k_empty[s]);
           }
           const bool more = j + 1 < it.nkt;
           for (int q = 0; q < kQT; ++q) {
@@ -322,17 +334,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
               ok = false;
               break;
             }
+            if (q == 0 && !mbar_wait_abortable(&v_full[s], (g / kStages) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
             issue_pv(q, g, j == 0);
-            if (q == kQT - 1) mma_commit(&kv_empty[s]);
+            if (q == kQT - 1) mma_commit(&v_empty[s]);
             if (!more) mma_commit(&o_full[q]);
             if (more) {
-              if (q == 0 && !mbar_wait_abortable(&kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag)) {
+              if (q == 0 && !mbar_wait_abortable(&k_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
               issue_s(q, g + 1);
+              if (q == kQT - 1) mma_commit(&k_empty[(g + 1) % kStages]);
             }
           }
         }
@@ -383,10 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       for (int j = 0; j < it.nkt; ++j, ++g) {
         const int s = g % kStages;
         ok = mbar_wait_abortable(&s_full[q], g & 1, abort_flag) &&
-             mbar_wait_abortable(&kv_full[s], (g / kStages) & 1, abort_flag);
+             mbar_wait_abortable(&v_full[s], (g / kStages) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const float* kscale = reinterpret_cast<const float*>(smem + kOffStage + s * kStageBytes + 2 * kTileBytes);
+        const float* kscale = reinterpret_cast<const float*>(smem + kOffV + s * kVSlotBytes + kTileBytes);
         const int key0 = (it.kt0 + j) * kKeys;
         // z = logit (log2 units) minus the row's reference maximum, one FFMA per key.
         const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
