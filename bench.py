@@ -323,6 +323,17 @@ def prefill_parity(w, out, seqs=None, tokens=(0, 1, 127, 128, 129, 254, 255)):
             "what": "outputs of the last timed call against the float64 oracle on sampled sequences and tokens"}
 
 
+def prefill_launches(w):
+    """Launches of one append + prefill step: the append, the dequant pass, the attention, and
+    the merge of the last wave's key pieces when the q-tile pairs leave a partial wave."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    pairs = w.batch * -(-w.n_new * w.num_q_heads // 256)
+    grid = min(pairs, sms)
+    rem = pairs % grid
+    return 3 + (1 if rem and grid // rem >= 2 else 0)
+
+
 def bf16_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -397,7 +408,7 @@ def run_prefill(args, rank, world):
         "dtype": "int8 KV, bf16/fp16 MMA / fp32 accumulate", "data": "synthetic",
         "config": {"workload": w.name, "global_batch": w.batch * world, "kv_query_pairs_per_head": pairs,
                    "flops_per_step": flops, "parallelism": f"replicas x{world}"},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": prefill_launches(w) * args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
                      "frac": achieved / sustained, "traffic": None, "peak_kind": kind + " bf16 sustained",
                      "kernel": "cai_mqa_prefill_chunk (dequant pass + tcgen05 attention)"},

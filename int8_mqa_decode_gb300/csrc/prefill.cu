@@ -77,6 +77,14 @@ struct PrefillParams {
   const int32_t* q_off;   // [B + 1] packed new-token offsets, or null: sequence b has n_new rows at b * n_new
   int32_t batch, n_new, total_new, num_heads, log2_heads, window, kt_rows, pairs;  // n_new: the most per sequence
   float scale_log2;
+  // Work items: items [0, full_items) are whole pairs of q-tiles; the pairs after them
+  // (the last, partial wave of a persistent grid) are cut into `pieces` key ranges each,
+  // item full_items + t being piece t % pieces of pair full_items + t / pieces.  A piece
+  // writes its normalised partial output and log2-sum-exp to piece_o / piece_lse
+  // ([t][256 rows][128] and [t][256]); combine_pieces_kernel merges them.
+  int32_t full_items, pieces, num_items;
+  float* piece_o;
+  float* piece_lse;
   uint16_t* kb;  // scratch bf16 [B][KT][128]
   uint16_t* vh;  // scratch fp16 [B][KT][128]: V codes times the V scale
   float* ks;     // scratch [B][KT]: K scale * softmax scale * log2(e)
@@ -182,12 +190,22 @@ struct PItem {
   int64_t qrow0;  // first packed new-token row of the sequence
   int rows;       // (token, head) rows of the sequence, 0 if its offsets are invalid
   bool ok;
+  int piece;      // -1: the whole key range; otherwise the piece's slot in piece_o / piece_lse
 };
 
 __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
   PItem it;
-  it.b = idx / p.pairs;
-  it.row0 = (idx - it.b * p.pairs) * (kQT * kRows);
+  int pair = idx, piece = -1;
+  if (idx >= p.full_items) {
+    const int t = idx - p.full_items;
+    pair = p.full_items + t / p.pieces;
+    piece = t % p.pieces;
+    it.piece = t;
+  } else {
+    it.piece = -1;
+  }
+  it.b = pair / p.pairs;
+  it.row0 = (pair - it.b * p.pairs) * (kQT * kRows);
   const int32_t p0 = p.prefix_len[it.b];
   const SeqRows sr = seq_rows(p, it.b);
   it.qrow0 = sr.r0;
@@ -203,6 +221,12 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
   const int kv_lo = p.window > 0 ? max(0, p0 + i0 + 1 - p.window) : 0;
   it.kt0 = kv_lo / kKeys;
   it.nkt = (kv_hi - 1) / kKeys - it.kt0 + 1;
+  if (piece >= 0) {  // key tiles [per * piece, per * (piece + 1)) of the pair's range
+    const int per = (it.nkt + p.pieces - 1) / p.pieces;
+    const int a = min(it.nkt, per * piece), e = min(it.nkt, per * (piece + 1));
+    it.kt0 += a;
+    it.nkt = e - a;
+  }
   return it;
 }
 
@@ -238,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_heads;
-  const int num_items = p.batch * p.pairs;
+  const int num_items = p.num_items;
 
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
@@ -313,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       };
       for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
         const PItem it = prefill_item(p, idx);
-        if (!it.ok) continue;  // no MMA work; the softmax groups write its zeros
+        if (!it.ok || it.nkt == 0) continue;  // no MMA work; the softmax groups write its zeros
         bool ok = mbar_wait_abortable(&q_full[0], n & 1, abort_flag) && mbar_wait_abortable(&q_full[1], n & 1, abort_flag);
         for (int j = 0; j < it.nkt && ok; ++j, ++g) {
           const int s = g % kStages;
@@ -381,6 +405,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
           if (p.lse_out) p.lse_out[(it.qrow0 + my_i) * Hq + my_h] = -INFINITY;
         }
         continue;  // no MMA work for this item
+      }
+      // A piece's partial output row (normalised) and log2-sum-exp, for the merge.
+      float* part_row = it.piece >= 0 ? p.piece_o + ((int64_t)it.piece * (kQT * kRows) + q * kRows + r) * kHeadDim
+                                       : nullptr;
+      if (it.nkt == 0) {  // a piece with no key tiles (no MMA work): weight zero in the merge
+        for (int d = 0; d < kHeadDim; d += 4)
+          *reinterpret_cast<float4*>(part_row + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.piece_lse[(int64_t)it.piece * (kQT * kRows) + q * kRows + r] = -INFINITY;
+        continue;
       }
       // This row's query (bf16), zero beyond the chunk.
       {
@@ -491,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       if (!mbar_wait_abortable(&o_full[q], n & 1, abort_flag)) break;
       tc_fence_after();
       const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
+      float* dst = part_row ? part_row : out_row;
 #pragma unroll
       for (int c = 0; c < kHeadDim; c += 32) {
         uint32_t o[32];
@@ -499,14 +533,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         if (my_row) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(out_row + c + e) =
+            *reinterpret_cast<float4*>(dst + c + e) =
                 make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
                             __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
         }
       }
-      if (my_row && p.lse_out)
-        p.lse_out[(it.qrow0 + my_i) * Hq + my_h] =
-            l_sum > 0.0f ? (m_ref + __log2f(l_sum)) * kLn2 : -INFINITY;
+      const float lse2 = l_sum > 0.0f ? m_ref + __log2f(l_sum) : -INFINITY;
+      if (part_row) {
+        if (my_row) p.piece_lse[(int64_t)it.piece * (kQT * kRows) + q * kRows + r] = lse2;
+      } else if (my_row && p.lse_out) {
+        p.lse_out[(it.qrow0 + my_i) * Hq + my_h] = lse2 * kLn2;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[q]);
@@ -517,6 +554,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   __syncthreads();
   if (tid == 0 && *abort_flag && p.err) atomicOr(p.err, CAI_DEVERR_TIMEOUT);
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// One warp per (split pair, row): merge the pair's pieces by their log-sum-exp,
+// out = sum_j 2^(lse_j - M) o_j / sum_j 2^(lse_j - M), into the row's output.
+__global__ void __launch_bounds__(256) combine_pieces_kernel(const PrefillParams p) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int split_pairs = (p.num_items - p.full_items) / p.pieces;
+  if (w >= (int64_t)split_pairs * (kQT * kRows)) return;
+  const int sp = (int)(w / (kQT * kRows)), r = (int)(w % (kQT * kRows));
+  const PItem it = prefill_item(p, p.full_items + sp * p.pieces);
+  const int64_t row = it.row0 + r;
+  if (!it.ok || row >= it.rows) return;  // invalid sequence (its rows hold zeros) or past the chunk
+  const int Hq = p.num_heads;
+  const int my_i = (int)(row >> p.log2_heads), my_h = (int)(row & (Hq - 1));
+  const int64_t t0 = (int64_t)sp * p.pieces;
+  const float lj = lane < p.pieces ? p.piece_lse[(t0 + lane) * (kQT * kRows) + r] : -INFINITY;
+  float M = lj;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float wj = (M == -INFINITY || lane >= p.pieces) ? 0.0f : ex2_approx(lj - M);
+  float wsum = wj;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < p.pieces; ++j) {
+    const float wt = __shfl_sync(0xffffffffu, wj, j);
+    const float4 o = reinterpret_cast<const float4*>(p.piece_o + ((t0 + j) * (kQT * kRows) + r) * kHeadDim)[lane];
+    acc.x = fmaf(wt, o.x, acc.x);
+    acc.y = fmaf(wt, o.y, acc.y);
+    acc.z = fmaf(wt, o.z, acc.z);
+    acc.w = fmaf(wt, o.w, acc.w);
+  }
+  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+  reinterpret_cast<float4*>(p.out + ((it.qrow0 + my_i) * Hq + my_h) * kHeadDim)[lane] =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (p.lse_out && lane == 0)
+    p.lse_out[(it.qrow0 + my_i) * Hq + my_h] = wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
 // A [rows][128] 16-bit row-major matrix seen as (8 elements, rows, 16 chunks)
@@ -535,12 +612,15 @@ bool encode_rows128(CUtensorMap* map, const void* base, uint64_t rows) {
 
 }  // namespace
 
+// Partial outputs of the split last wave: at most one piece per CTA of the grid.
+static int64_t piece_bytes() { return (int64_t)num_sms() * (kQT * kRows) * (kHeadDim + 1) * 4; }
+
 size_t prefill_workspace_bytes(int32_t batch, int32_t max_pages_per_seq, int32_t page_size) {
   const int64_t kt = ((int64_t)max_pages_per_seq * page_size + kKeys - 1) / kKeys * kKeys;
   const int64_t rows = (int64_t)batch * kt;
   const int64_t a = ((rows * kHeadDim * 2 + 255) / 256) * 256;
   const int64_t s = ((rows * 4 + 255) / 256) * 256;
-  return (size_t)(2 * a + 2 * s);
+  return (size_t)(2 * a + 2 * s + ((piece_bytes() + 255) / 256) * 256);
 }
 
 cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
@@ -568,6 +648,9 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.kb = reinterpret_cast<uint16_t*>(ws);
   p.vh = reinterpret_cast<uint16_t*>(ws + a);
   p.ks = reinterpret_cast<float*>(ws + 2 * a);
+  const int64_t sbytes = ((rows * 4 + 255) / 256) * 256;
+  p.piece_o = reinterpret_cast<float*>(ws + 2 * a + 2 * sbytes);
+  p.piece_lse = p.piece_o + (int64_t)num_sms() * (kQT * kRows) * kHeadDim;
   p.out = L.out;
   p.lse_out = L.lse_out;
   p.err = L.err;
@@ -594,10 +677,24 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int64_t items = (int64_t)L.batch * p.pairs;
-  const int grid = (int)(items < num_sms() ? items : num_sms());
+  // Work split: whole pairs in full waves of the persistent grid; the pairs of a partial
+  // last wave are cut into `pieces` key ranges so that wave ends sooner (with r pairs
+  // left over, pieces = grid / r, at most 4; the pieces of a pair are merged after).
+  const int64_t pairs_total = (int64_t)L.batch * p.pairs;
+  const int sms = num_sms();
+  const int grid = (int)(pairs_total < sms ? pairs_total : sms);
+  const int64_t rem = pairs_total % grid;
+  int pieces = rem > 0 ? (int)(grid / rem) : 1;
+  if (pieces > 4) pieces = 4;
+  if (pieces < 2) pieces = 1;
+  p.pieces = pieces;
+  p.full_items = (int32_t)(pieces > 1 ? pairs_total - rem : pairs_total);
+  p.num_items = (int32_t)(p.full_items + (pieces > 1 ? rem * pieces : 0));
   prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, kmap, vmap);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || pieces == 1) return e;
+  const int64_t warps_c = rem * (kQT * kRows);
+  return launch_pdl(combine_pieces_kernel, dim3((unsigned)((warps_c + 7) / 8)), dim3(256), 0, stream, p);
 }
 
 }  // namespace cai

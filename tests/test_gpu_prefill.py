@@ -97,3 +97,28 @@ def test_prefill_invalid_prefix_flags_and_zeroes():
     assert int(e.item()) == cai.CAI_DEVERR_LENGTH
     assert not o[1].cpu().numpy().any() and np.all(np.isneginf(l[1].cpu().numpy()))
     assert np.abs(o[0].cpu().numpy() - out[0]).max() == 0.0
+
+
+@pytest.mark.parametrize("window", [0, 700])
+def test_prefill_split_last_wave(window):
+    """More q-tile pairs than SMs with a remainder: the pairs of the partial last wave are
+    cut into key ranges and merged by their log-sum-exp.  Every token of the last sequence
+    (whose pairs are the split ones) and a sample of the others, against the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hq, n_new = 32, 256
+    pairs_per_seq = n_new * Hq // 256
+    B = sms // pairs_per_seq + 2          # a few pairs more than one wave
+    assert (B * pairs_per_seq) % sms != 0
+    prefix = [1500 + 37 * b for b in range(B)]
+    w, cache, out, lse, err = prefill_case(B, Hq, 16, prefix, n_new, window=window, seed=9)
+    assert err == 0
+    assert np.isfinite(out).all()
+    last = B - 1
+    o_ref, l_ref = oracle_prefill(w, last)
+    assert np.abs(out[last] - o_ref).max() <= ATOL
+    assert np.abs(lse[last] - l_ref).max() <= ATOL
+    tokens = [0, 1, 127, 128, 255]
+    for b in (0, B // 2, B - 2):
+        o_ref, l_ref = oracle_prefill(w, b, tokens)
+        assert np.abs(out[b][tokens] - o_ref).max() <= ATOL, b
+        assert np.abs(lse[b][tokens] - l_ref).max() <= ATOL, b
