@@ -623,8 +623,13 @@ def run_gpu(args, rank, world):
                      "kernel": ("cai_mqa_decode_layers (all layers of the step in one launch, "
                                 f"LSE combine of {splits_layers} split layer(s))" if layered else
                                 f"cai_mqa_decode (split-KV decode + LSE combine), {nl} launch(es) per step"),
-                     "algorithmic_bytes_per_step": bytes_step},
-        "hbm_gbs_step": bytes_step * args.steps / (ms_max * 1e-3) / 1e9,
+                     "timed_launches": (["decode_kernel"] if layered else ["decode_kernel"] * nl) +
+                                       ["combine_kernel"] * splits_layers,
+                     "algorithmic_bytes_per_step": bytes_step,
+                     "bytes_note": "KV pages read once per attended layer (264 B per token, 4 B per page id), q and "
+                                   "out; the append launch is outside the event pair and outside these bytes"},
+        "step_algorithmic_bytes": bytes_step + append_bytes(w),
+        "hbm_gbs_step": (bytes_step + append_bytes(w)) * args.steps / (ms_max * 1e-3) / 1e9,
         "queries_per_s": world * w.batch * args.steps / (ms_max * 1e-3),
         "clocks": clocks.summary(),
         "e2e": e2e,
