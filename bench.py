@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--mixed", action="store_true",
                     help="continuous batching: 128 decode steps + 8 prefill chunks of 256 tokens in one launch")
+    ap.add_argument("--dialogues", action="store_true",
+                    help="cross-turn host KV cache on a synthetic multi-turn trace (hit rate, restore GB/s, TTFT)")
     ap.add_argument("--per-layer", action="store_true",
                     help="one decode launch per layer instead of all the step's layers in one launch")
     ap.add_argument("--local-ring", action="store_true",
@@ -506,6 +508,129 @@ def run_mixed(args, rank, world):
     }
 
 
+# ----------------------------------------------------------------------------- GPU arm: cross-turn cache
+
+def run_dialogues(args, rank, world):
+    """Cross-turn KV cache on a synthetic multi-turn trace: D dialogues, T turns, U new tokens per
+    turn.  Turn t brings (t+1)*U tokens; with the host cache the previous turns' whole pages are
+    restored from host memory and only the rest is appended and prefilled, without it the whole
+    dialogue is appended and prefilled.  Reports the hit rate (restored / prompt tokens), the restore
+    rate and the time to first token per turn both ways (restore + append + prefill of the batch)."""
+    import torch
+    import harness
+    import int8_mqa_decode_gb300 as cai
+    import synth
+    import synth.gpu as sgpu
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    import __graft_entry__
+    __graft_entry__.build()
+    D, T, U, Hq, P = 16, 4, 512, 32, 16
+    seed = 1008 + 100 * rank
+    max_len = T * U
+    w = synth.Workload("dialogues", D, Hq, P, np.full(D, max_len), [0], [0], seed=seed)
+    dev = harness.PagedCache(w)
+    ids = [np.arange(d * 1000003, d * 1000003 + max_len, dtype=np.int32) for d in range(D)]
+    host = cai.cai_host_cache_create(P, 1, D * max_len // P + 64)
+    stream = torch.cuda.current_stream()
+    ws = dev.prefill_workspace()
+    scale = w.softmax_scale
+
+    def kv_for(p0, n):
+        k = torch.empty(D, n, 128, dtype=torch.float32, device="cuda")
+        v = torch.empty_like(k)
+        start = torch.full((D,), p0, dtype=torch.int32, device="cuda")
+        sgpu.normal_rows(k, seed, synth.stream_k(0), 0, pos=start)
+        sgpu.normal_rows(v, seed, synth.stream_v(0), 0, pos=start)
+        return k, v, start
+
+    def q_for(n):
+        q = torch.empty(D, n * Hq, 128, dtype=torch.bfloat16, device="cuda")
+        sgpu.q_rows(q, seed, synth.STREAM_Q_PREFILL, 0)
+        return q.view(D, n, Hq, 128)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    # One untimed append + prefill first, so the first timed call pays no first-launch setup.
+    k, v, start = kv_for(0, U)
+    q = q_for(U)
+    out = torch.empty(D, U, Hq, 128, device="cuda")
+    cai.cai_kv_append(dev.pools[0], k, v, dev.table, start)
+    cai.cai_mqa_prefill_chunk(dev.pools[0], q, dev.table, torch.zeros(D, dtype=torch.int32, device="cuda"), 0, scale,
+                              ws, out)
+    torch.cuda.synchronize()
+    del k, v, q, out
+    turns = []
+    restored_tokens = prompt_tokens = restored_bytes = 0
+    restore_ms_total = 0.0
+    try:
+        for t in range(T):
+            L = (t + 1) * U
+            # --- without the cache: the whole dialogue
+            k, v, start = kv_for(0, L)
+            q = q_for(L)
+            out = torch.empty(D, L, Hq, 128, device="cuda")
+            prefix = torch.zeros(D, dtype=torch.int32, device="cuda")
+            torch.cuda.synchronize()
+            a, b = ev(), ev()
+            a.record(stream)
+            cai.cai_kv_append(dev.pools[0], k, v, dev.table, start)
+            cai.cai_mqa_prefill_chunk(dev.pools[0], q, dev.table, prefix, 0, scale, ws, out)
+            b.record(stream)
+            torch.cuda.synchronize()
+            no_cache_ms = a.elapsed_time(b)
+            del k, v, q, out
+            # --- with the cache: restore the longest cached prefix, then append and prefill the rest
+            n = [cai.cai_host_cache_match(host, ids[d][:L]) for d in range(D)]
+            n0 = min(n)
+            k, v, start = kv_for(n0, L - n0)
+            q = q_for(L - n0)
+            out = torch.empty(D, L - n0, Hq, 128, device="cuda")
+            prefix = torch.full((D,), n0, dtype=torch.int32, device="cuda")
+            torch.cuda.synchronize()
+            a, r, b = ev(), ev(), ev()
+            a.record(stream)
+            if n0 > 0:  # the whole batch's cached prefixes in one call
+                cai.cai_host_cache_restore_batch(host, ids, [n0] * D, dev.pools, [dev.table_np[d] for d in range(D)],
+                                                 stream=stream)
+            r.record(stream)
+            cai.cai_kv_append(dev.pools[0], k, v, dev.table, start)
+            cai.cai_mqa_prefill_chunk(dev.pools[0], q, dev.table, prefix, 0, scale, ws, out)
+            b.record(stream)
+            torch.cuda.synchronize()
+            cache_ms = a.elapsed_time(b)
+            rest_ms = a.elapsed_time(r)
+            restored_tokens += D * n0
+            prompt_tokens += D * L
+            rb = D * (n0 // P) * cai.cai_page_bytes(P)
+            restored_bytes += rb
+            restore_ms_total += rest_ms
+            # the turn's pages go back to the host cache (after the first token, not timed)
+            for d in range(D):
+                cai.cai_host_cache_store(host, ids[d][:L], dev.pools, dev.table_np[d], stream=stream)
+            turns.append({"turn": t, "prompt_tokens": L, "restored_tokens": n0, "ttft_ms_cache": cache_ms,
+                          "ttft_ms_no_cache": no_cache_ms, "restore_ms": rest_ms,
+                          "restore_gbs": (rb / (rest_ms * 1e-3) / 1e9) if n0 else None})
+            del k, v, q, out
+        stats = cai.cai_host_cache_stats(host)
+    finally:
+        cai.cai_host_cache_destroy(host)
+    cached = [x["ttft_ms_cache"] for x in turns[1:]]
+    plain = [x["ttft_ms_no_cache"] for x in turns[1:]]
+    return {
+        "metric": "cross-turn KV cache: time to first token per turn (batch of dialogues), with / without the host cache",
+        "value": statistics.mean(plain) / statistics.mean(cached), "unit": "x speed-up (turns 2..T)",
+        "n_gpus": world, "steps": T, "warmup": 0, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 KV, bf16/fp16 MMA / fp32 accumulate", "data": "synthetic multi-turn trace",
+        "config": {"workload": f"{D} dialogues x {T} turns x {U} new tokens, Hq={Hq}, P={P}, one KV buffer",
+                   "parallelism": f"replicas x{world}"},
+        "hit_rate_tokens": restored_tokens / prompt_tokens,
+        "restore_gbs": restored_bytes / (restore_ms_total * 1e-3) / 1e9 if restore_ms_total else None,
+        "turns": turns, "host_cache_stats": stats, "gpu_launches": None,
+    }
+
+
 # ----------------------------------------------------------------------------- GPU arm: decode
 
 def run_gpu(args, rank, world):
@@ -799,6 +924,8 @@ def main():
         return
     if args.mixed:
         res = run_mixed(args, rank, world)
+    elif args.dialogues:
+        res = run_dialogues(args, rank, world)
     else:
         res = run_prefill(args, rank, world) if args.config == 4 else run_gpu(args, rank, world)
         if args.config == 3 and not args.no_extra and not args.per_layer and not args.local_ring and args.batch is None:

@@ -308,9 +308,20 @@ int32_t cai_host_cache_match(cai_host_cache* cache, const int32_t* tokens, int32
 /* Copy the cached pages of tokens[0, n_tokens) (n_tokens a multiple of page_size, all
  * cached) into pages block_table_row[0 .. n_tokens/page_size) of each of the num_buffers
  * pools.  block_table_row and pools are host arrays; pools[i].pages may be device or
- * host memory.  Device copies are asynchronous on `stream`. */
+ * host memory.  Device copies are asynchronous on `stream`: a copy kernel reads the
+ * pinned host arena directly (the arena must stay alive until they are done). */
 cai_status cai_host_cache_restore(cai_host_cache* cache, const int32_t* tokens, int32_t n_tokens,
                                   const cai_kv_pool* pools, const int32_t* block_table_row, void* stream);
+
+/* cai_host_cache_restore for several sequences at once (a scheduler resuming a batch of
+ * dialogues): sequence i copies its cached pages of tokens[i][0, n_tokens[i]) into pages
+ * block_table_rows[i][...] of each pool.  tokens, n_tokens and block_table_rows are host
+ * arrays [num_seqs]; every path is checked before anything is copied (CAI_ERR_INVALID_ARG
+ * when one is not fully cached).  The device copies of all the sequences are queued on
+ * `stream` together (one copy kernel per 1024 pages). */
+cai_status cai_host_cache_restore_batch(cai_host_cache* cache, int32_t num_seqs, const int32_t* const* tokens,
+                                        const int32_t* n_tokens, const cai_kv_pool* pools,
+                                        const int32_t* const* block_table_rows, void* stream);
 
 /* Keep the full pages of tokens[0, n_tokens) (a trailing partial page is ignored), read
  * from pages block_table_row[...] of each pool; pages already cached are not copied

@@ -24,7 +24,7 @@ __all__ = [
     "cai_mqa_prefill_chunk", "cai_mqa_prefill_varlen", "cai_gqa_decode", "cai_gqa_decode_workspace_size",
     "CAI_DEVERR_PAGE", "CAI_DEVERR_LENGTH", "CAI_DEVERR_TIMEOUT", "HEAD_DIM", "cai_host_cache_create",
     "cai_host_cache_destroy", "cai_host_cache_match", "cai_host_cache_restore", "cai_host_cache_store",
-    "cai_host_cache_stats", "cai_ring_pages", "cai_ring_table_row",
+    "cai_host_cache_stats", "cai_host_cache_restore_batch", "cai_ring_pages", "cai_ring_table_row",
 ]
 
 HEAD_DIM = 128
@@ -113,6 +113,8 @@ def load():
     lib.cai_host_cache_match.restype = i32
     lib.cai_host_cache_restore.argtypes = [vp, vp, i32, pool_p, vp, vp]
     lib.cai_host_cache_restore.restype = ctypes.c_int
+    lib.cai_host_cache_restore_batch.argtypes = [vp, i32, vp, vp, pool_p, vp, vp]
+    lib.cai_host_cache_restore_batch.restype = ctypes.c_int
     lib.cai_host_cache_store.argtypes = [vp, vp, i32, pool_p, vp, vp]
     lib.cai_host_cache_store.restype = ctypes.c_int
     i64p = ctypes.POINTER(ctypes.c_int64)
@@ -403,6 +405,20 @@ def cai_host_cache_restore(cache: int, tokens, n_tokens: int, pools, block_table
     st = load().cai_host_cache_restore(cache, ptr, n_tokens, _pool_structs(pools), tptr,
                                        _stream(stream) if torch.cuda.is_available() else None)
     _check(st, "cai_host_cache_restore")
+
+
+def cai_host_cache_restore_batch(cache: int, tokens, n_tokens, pools, block_table_rows, stream=None) -> None:
+    """cai_host_cache_restore for several sequences in one call (tokens[i], n_tokens[i], block_table_rows[i])."""
+    keeps = [_i32_host(t) for t in tokens]
+    tkeeps = [_i32_host(r) for r in block_table_rows]
+    n = len(keeps)
+    tok_ptrs = (ctypes.c_void_p * max(n, 1))(*[p for _, p in keeps])
+    row_ptrs = (ctypes.c_void_p * max(n, 1))(*[p for _, p in tkeeps])
+    counts = np.ascontiguousarray(np.asarray(n_tokens, dtype=np.int32))
+    st = load().cai_host_cache_restore_batch(cache, n, tok_ptrs, counts.ctypes.data_as(ctypes.c_void_p),
+                                             _pool_structs(pools), row_ptrs,
+                                             _stream(stream) if torch.cuda.is_available() else None)
+    _check(st, "cai_host_cache_restore_batch")
 
 
 def cai_host_cache_store(cache: int, tokens, pools, block_table_row, stream=None) -> None:

@@ -14,9 +14,12 @@
 // by comparing the page's tokens, so a hash collision can never return the
 // wrong KV.  Eviction takes the least recently used leaf (a page whose longer
 // continuations are all gone), so a cached path never has holes.  Pages live
-// in one host arena (pinned when a GPU is present, so host<->device copies
-// run at full link speed); copies are one cudaMemcpyAsync per page and
-// buffer, plain memcpy when both sides are host memory.
+// in one host arena, pinned when a GPU is present.  Copies between the arena
+// and device pools are done by a copy kernel that reads (restore) or writes
+// (store) the pinned arena directly through its device mapping, up to 1024
+// pages per launch, the page list passed as kernel parameters (one small
+// cudaMemcpyAsync per page had made a long prefix thousands of calls); plain
+// memcpy when both sides are host memory.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -59,6 +62,50 @@ bool copy_bytes(void* dst, const void* src, size_t n, cudaStream_t stream) {
   }
   return cudaMemcpyAsync(dst, src, n, cudaMemcpyDefault, stream) == cudaSuccess;
 }
+
+// Page copies of one launch: every byte of each source page to its destination page
+// (pinned host <-> device, both addresses 16-byte aligned, page_bytes a multiple of 16).
+constexpr int kCopyBatch = 1024;
+struct PageCopies {
+  const uint8_t* src[kCopyBatch];
+  uint8_t* dst[kCopyBatch];
+  int32_t n;
+  int32_t page_bytes;
+};
+
+__global__ void __launch_bounds__(256) page_copy_kernel(const __grid_constant__ PageCopies c) {
+  const int units = c.page_bytes / 16;
+  for (int i = blockIdx.x; i < c.n; i += gridDim.x) {
+    const uint4* s = reinterpret_cast<const uint4*>(c.src[i]);
+    uint4* d = reinterpret_cast<uint4*>(c.dst[i]);
+    for (int k = threadIdx.x; k < units; k += blockDim.x) d[k] = s[k];
+  }
+}
+
+// Copies the listed pages on `stream`, kCopyBatch per launch.
+class PageCopier {
+ public:
+  PageCopier(int32_t page_bytes, cudaStream_t stream) : stream_(stream) {
+    batch_.n = 0;
+    batch_.page_bytes = page_bytes;
+  }
+  bool add(const uint8_t* src, uint8_t* dst) {
+    batch_.src[batch_.n] = src;
+    batch_.dst[batch_.n] = dst;
+    return ++batch_.n < kCopyBatch || flush();
+  }
+  bool flush() {
+    if (batch_.n == 0) return true;
+    const int blocks = batch_.n < 1024 ? batch_.n : 1024;
+    page_copy_kernel<<<blocks, 256, 0, stream_>>>(batch_);
+    batch_.n = 0;
+    return cudaGetLastError() == cudaSuccess;
+  }
+
+ private:
+  PageCopies batch_;
+  cudaStream_t stream_;
+};
 
 struct Node {
   int parent = -1;
@@ -176,13 +223,14 @@ int32_t cai_host_cache_match(cai_host_cache* c, const int32_t* tokens, int32_t n
   return pages * c->page_size;
 }
 
-cai_status cai_host_cache_restore(cai_host_cache* c, const int32_t* tokens, int32_t n_tokens,
-                                  const cai_kv_pool* pools, const int32_t* block_table_row, void* stream) {
-  if (!c || !tokens || !pools || !block_table_row || n_tokens < 0 || n_tokens % c->page_size != 0)
-    return CAI_ERR_INVALID_ARG;
-  std::lock_guard<std::mutex> lock(c->mu);
-  // The whole path must be cached before anything is copied.
-  std::vector<int> path;
+namespace {
+
+// The cached path of tokens[0, n_tokens) checked against the pools and the table row;
+// CAI_OK with the path's nodes, or the status to return (nothing copied).
+cai_status restore_path(cai_host_cache* c, const int32_t* tokens, int32_t n_tokens, const cai_kv_pool* pools,
+                        const int32_t* block_table_row, std::vector<int>& path) {
+  if (!tokens || !block_table_row || n_tokens < 0 || n_tokens % c->page_size != 0) return CAI_ERR_INVALID_ARG;
+  path.clear();
   int node = 0;
   for (int32_t k = 0; k * c->page_size < n_tokens; ++k) {
     node = c->find_child(node, tokens + (size_t)k * c->page_size);
@@ -195,15 +243,58 @@ cai_status cai_host_cache_restore(cai_host_cache* c, const int32_t* tokens, int3
     for (size_t k = 0; k < path.size(); ++k)
       if (block_table_row[k] < 0 || block_table_row[k] >= p.num_pages) return CAI_ERR_INVALID_ARG;
   }
-  for (size_t k = 0; k < path.size(); ++k) {
-    for (int b = 0; b < c->num_buffers; ++b) {
+  return CAI_OK;
+}
+
+// Queue (or do) the copies of one checked path.
+bool restore_copies(cai_host_cache* c, const std::vector<int>& path, const cai_kv_pool* pools,
+                    const int32_t* block_table_row, PageCopier& copier, cudaStream_t stream) {
+  const bool kernel = c->pinned && (c->page_bytes % 16) == 0;
+  for (int b = 0; b < c->num_buffers; ++b) {
+    const bool dev = is_device(pools[b].pages);
+    for (size_t k = 0; k < path.size(); ++k) {
       uint8_t* dst = static_cast<uint8_t*>(pools[b].pages) + (size_t)block_table_row[k] * c->page_bytes;
-      if (!copy_bytes(dst, c->slot_ptr(c->nodes[path[k]].slot, b), c->page_bytes,
-                      static_cast<cudaStream_t>(stream)))
-        return CAI_ERR_CUDA;
+      const uint8_t* src = c->slot_ptr(c->nodes[path[k]].slot, b);
+      const bool ok = (kernel && dev) ? copier.add(src, dst) : copy_bytes(dst, src, c->page_bytes, stream);
+      if (!ok) return false;
     }
   }
-  return CAI_OK;
+  return true;
+}
+
+}  // namespace
+
+cai_status cai_host_cache_restore(cai_host_cache* c, const int32_t* tokens, int32_t n_tokens,
+                                  const cai_kv_pool* pools, const int32_t* block_table_row, void* stream) {
+  if (!c || !pools) return CAI_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(c->mu);
+  // The whole path must be cached before anything is copied.
+  std::vector<int> path;
+  const cai_status st = restore_path(c, tokens, n_tokens, pools, block_table_row, path);
+  if (st != CAI_OK) return st;
+  PageCopier copier((int32_t)c->page_bytes, static_cast<cudaStream_t>(stream));
+  if (!restore_copies(c, path, pools, block_table_row, copier, static_cast<cudaStream_t>(stream)))
+    return CAI_ERR_CUDA;
+  return copier.flush() ? CAI_OK : CAI_ERR_CUDA;
+}
+
+cai_status cai_host_cache_restore_batch(cai_host_cache* c, int32_t num_seqs, const int32_t* const* tokens,
+                                        const int32_t* n_tokens, const cai_kv_pool* pools,
+                                        const int32_t* const* block_table_rows, void* stream) {
+  if (!c || !pools || num_seqs < 0 || (num_seqs > 0 && (!tokens || !n_tokens || !block_table_rows)))
+    return CAI_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(c->mu);
+  // Every sequence's path is checked before anything is copied.
+  std::vector<std::vector<int>> paths(num_seqs);
+  for (int32_t i = 0; i < num_seqs; ++i) {
+    const cai_status st = restore_path(c, tokens[i], n_tokens[i], pools, block_table_rows[i], paths[i]);
+    if (st != CAI_OK) return st;
+  }
+  PageCopier copier((int32_t)c->page_bytes, static_cast<cudaStream_t>(stream));
+  for (int32_t i = 0; i < num_seqs; ++i)
+    if (!restore_copies(c, paths[i], pools, block_table_rows[i], copier, static_cast<cudaStream_t>(stream)))
+      return CAI_ERR_CUDA;
+  return copier.flush() ? CAI_OK : CAI_ERR_CUDA;
 }
 
 cai_status cai_host_cache_store(cai_host_cache* c, const int32_t* tokens, int32_t n_tokens, const cai_kv_pool* pools,
@@ -212,6 +303,8 @@ cai_status cai_host_cache_store(cai_host_cache* c, const int32_t* tokens, int32_
   std::lock_guard<std::mutex> lock(c->mu);
   int node = 0;
   bool copied = false;
+  const bool kernel = c->pinned && (c->page_bytes % 16) == 0;
+  PageCopier copier((int32_t)c->page_bytes, static_cast<cudaStream_t>(stream));
   for (int32_t k = 0; (k + 1) * c->page_size <= n_tokens; ++k) {
     const int32_t* tok = tokens + (size_t)k * c->page_size;
     int child = c->find_child(node, tok);
@@ -241,14 +334,17 @@ cai_status cai_host_cache_store(cai_host_cache* c, const int32_t* tokens, int32_
         const int32_t pid = block_table_row[k];
         if (pid < 0 || pid >= p.num_pages) return CAI_ERR_INVALID_ARG;
         const uint8_t* src = static_cast<const uint8_t*>(p.pages) + (size_t)pid * c->page_bytes;
-        if (!copy_bytes(c->slot_ptr(slot, b), src, c->page_bytes, static_cast<cudaStream_t>(stream)))
-          return CAI_ERR_CUDA;
+        const bool ok = (kernel && is_device(p.pages))
+                            ? copier.add(src, c->slot_ptr(slot, b))
+                            : copy_bytes(c->slot_ptr(slot, b), src, c->page_bytes, static_cast<cudaStream_t>(stream));
+        if (!ok) return CAI_ERR_CUDA;
         copied = true;
       }
     }
     node = child;
   }
   for (int id = node; id > 0; id = c->nodes[id].parent) c->touch(id);
+  if (!copier.flush()) return CAI_ERR_CUDA;
   if (copied && is_device(pools[0].pages) &&
       cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return CAI_ERR_CUDA;

@@ -92,3 +92,30 @@ def test_path_longer_than_capacity_is_refused():
         assert e.value.status == 3
     finally:
         cai.cai_host_cache_destroy(c)
+
+
+def test_restore_batch_equals_restores():
+    """Several sequences restored in one call land byte for byte where per-sequence restores
+    put them; a sequence that is not fully cached rejects the whole batch (nothing copied)."""
+    c = cai.cai_host_cache_create(P, 1, 64)
+    try:
+        src = [HostPool(40, seed=11)]
+        seqs = [tokens(20 + i, (3 + i) * P) for i in range(3)]
+        rows = [np.arange(10 * i, 10 * i + 8, dtype=np.int32) for i in range(3)]
+        for s, r in zip(seqs, rows):
+            cai.cai_host_cache_store(c, s, [p.struct for p in src], r)
+        one = [HostPool(40)]
+        two = [HostPool(40)]
+        dst_rows = [np.arange(30 - 10 * i, 38 - 10 * i, dtype=np.int32) for i in range(3)]
+        for s, r in zip(seqs, dst_rows):
+            cai.cai_host_cache_restore(c, s, len(s), [p.struct for p in one], r)
+        cai.cai_host_cache_restore_batch(c, seqs, [len(s) for s in seqs], [p.struct for p in two], dst_rows)
+        assert np.array_equal(one[0].buf, two[0].buf) and one[0].buf.any()
+        three = [HostPool(40)]
+        missing = tokens(99, 2 * P)
+        with pytest.raises(cai.CaiError):
+            cai.cai_host_cache_restore_batch(c, seqs + [missing], [len(s) for s in seqs] + [2 * P],
+                                             [p.struct for p in three], dst_rows + [dst_rows[0]])
+        assert not three[0].buf.any()
+    finally:
+        cai.cai_host_cache_destroy(c)
