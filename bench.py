@@ -497,12 +497,14 @@ def run_mixed(args, rank, world):
     diff = float((out[:n_dec] - out_dec).abs().max())
     pairs = float(np.sum(n_new * prefix + n_new * (n_new + 1) / 2)) * Hq  # (query row, attended key) pairs
     return {
-        "metric": "continuous-batching step: new tokens/s (128 decode steps + 8 prefill chunks, one launch)",
+        "metric": "continuous-batching step: new tokens/s (128 decode steps + 8 prefill chunks, one cai_mqa_prefill_varlen call)",
         "value": world * total / (ms_one * 1e-3), "unit": "new tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_one, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8 KV, bf16 QK / fp16 PV, fp32 accumulate", "data": "synthetic",
         "config": {"workload": f"mixed: {n_dec} decode (L~U[1024,8192]) + {n_pf} chunks of {chunk} on 4096, Hq={Hq}, "
                                f"P={P}", "new_tokens": total, "kv_query_pairs": pairs},
+        "one_call": "cai_mqa_prefill_varlen: the one-token rows through the decode kernel, the chunks through the "
+                    "prefill kernel (two launches inside the call)",
         "two_launch_ms_per_step": ms_two, "decode_rows_max_abs_diff_vs_decode_path": diff,
         "tflops": 4 * 128 * pairs / (ms_one * 1e-3) / 1e12, "gpu_launches": 2 * args.steps, "clocks": clocks,
     }

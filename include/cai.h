@@ -262,7 +262,7 @@ cai_status cai_gqa_decode(const cai_kv_pool* kv_pools, int32_t num_kv_heads, con
                           void* stream);
 
 /* Continuous batching: the same attention for a batch whose sequences bring different
- * numbers of new tokens in one launch -- decode steps (one token) next to prefill
+ * numbers of new tokens in one call -- decode steps (one token) next to prefill
  * chunks (Red Hat page, "2. Processamento contínuo em lotes" and its figure 7:
  * finished requests leave and new ones join as slots free up, instead of the whole
  * batch waiting for its slowest request).  Sequence b owns new-token rows [q_offsets[b], q_offsets[b+1])
@@ -276,7 +276,10 @@ cai_status cai_gqa_decode(const cai_kv_pool* kv_pools, int32_t num_kv_heads, con
  * Other arguments, workspace and limits as cai_mqa_prefill_chunk.  A sequence whose
  * offsets are out of order, beyond total_new or longer than max_new, or whose
  * prefix_len + length exceeds the table, sets CAI_DEVERR_LENGTH; its rows (if its
- * offsets are valid) get out = 0, lse = -inf. */
+ * offsets are valid) get out = 0, lse = -inf.  With num_q_heads <= 64 the call makes two
+ * launches on `stream` (three when some of those rows are split): the sequences with
+ * exactly one new token run through the decode kernel and the prefill kernel skips
+ * them; the results are the same either way. */
 cai_status cai_mqa_prefill_varlen(const cai_kv_pool* pool, const uint16_t* q, int32_t batch,
                                   const int32_t* q_offsets, int32_t total_new, int32_t max_new, int32_t num_q_heads,
                                   const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* prefix_len,

@@ -307,6 +307,8 @@ cai_status decode_layers_common(const LayerArgs* layers, int32_t n, int32_t num_
       jb.ws_lse = reinterpret_cast<float*>(ws + o_bytes);
       ws += workspace_bytes_for(batch, num_q_heads, jb.plan) - kWorkspaceHeader;
     }
+    jb.q_off = nullptr;
+    jb.total_rows = 0;
     jb.item0 = (int32_t)items;
     items += (int64_t)batch * num_kv_heads * jb.plan.max_splits;
   }
@@ -447,7 +449,69 @@ cai_status prefill_common(const cai_kv_pool* pool, const uint16_t* q, int32_t ba
   L.out = out;
   L.lse_out = lse_out;
   L.err = err_flag;
-  return cuda_status(launch_prefill(L, static_cast<cudaStream_t>(stream)));
+  // Continuous batching: sequences bringing one new token are decode steps; the decode
+  // kernel runs them (with this call's window and scale, split as a decode call would be) and the
+  // prefill kernel skips them, so they pay neither the prefill's 256-row q-tiles nor its
+  // dequantised copy of their keys.  Its queue counters sit at the end of the workspace.
+  L.skip_single = q_off != nullptr && num_q_heads <= kDecodeMaxHeads;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (L.skip_single) {
+    void* hdr = static_cast<uint8_t*>(workspace) + (need - kWorkspaceHeader);
+    cudaError_t e = cudaMemsetAsync(hdr, 0, kWorkspaceHeader, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    DecodeParams d;
+    d.pages[0] = static_cast<const uint8_t*>(pool->pages);
+    d.slot_pages[0] = pool->num_pages;
+    for (int j = 1; j < kMaxKvHeads; ++j) {
+      d.pages[j] = nullptr;
+      d.slot_pages[j] = 0;
+    }
+    d.num_slots = 1;
+    d.num_kv_heads = 1;
+    d.ctx_len = prefix_len;
+    d.batch = batch;
+    d.num_heads = num_q_heads;
+    d.scale_log2 = softmax_scale * kLog2e;
+    d.num_jobs = 1;
+    d.queue = static_cast<uint32_t*>(hdr);
+    d.err = err_flag;
+    DecodeJob& jb = d.job[0];
+    jb.slot0 = 0;
+    jb.window = window;
+    jb.table = block_table;
+    jb.max_pages = max_pages_per_seq;
+    jb.q = q;
+    jb.out = out;
+    jb.lse_out = lse_out;
+    // The automatic split plan, its partials in the workspace's piece region (free until
+    // the prefill kernel, later on the stream, writes its own pieces there); fewer splits
+    // when they would not fit.
+    void* region = nullptr;
+    size_t region_bytes = 0;
+    prefill_piece_region(workspace, batch, max_pages_per_seq, pool->page_size, &region, &region_bytes);
+    DecodePlan plan =
+        plan_decode(batch, max_pages_per_seq, pool->page_size, window, 0, num_sms(), kItemsPerSmAlone);
+    while (plan.max_splits > 1 && workspace_bytes_for(batch, num_q_heads, plan) - kWorkspaceHeader > region_bytes)
+      plan = plan_decode(batch, max_pages_per_seq, pool->page_size, window, plan.max_splits - 1, num_sms(),
+                         kItemsPerSmAlone);
+    jb.plan = plan;
+    jb.ws_o = nullptr;
+    jb.ws_lse = nullptr;
+    if (plan.max_splits > 1) {
+      const size_t rows = (size_t)batch * plan.max_splits * num_q_heads;
+      const size_t o_bytes = (size_t)round_up((int64_t)(rows * kHeadDim * sizeof(float)), 256);
+      jb.ws_o = static_cast<float*>(region);
+      jb.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(region) + o_bytes);
+    }
+    jb.item0 = 0;
+    jb.q_off = q_off;
+    jb.total_rows = total_new;
+    for (int k = 1; k < kMaxDecodeJobs; ++k) d.job[k] = jb;
+    d.num_items = batch * plan.max_splits;
+    e = launch_decode(d, pool->page_size, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return cuda_status(launch_prefill(L, s));
 }
 
 }  // namespace

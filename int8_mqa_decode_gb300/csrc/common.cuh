@@ -58,7 +58,16 @@ struct DecodeJob {
   float* ws_lse;         // [B][max_splits][Hq] partial lse, log2 units
   DecodePlan plan;
   int32_t item0;         // first work item of the layer; items are (b * KV heads + KV head) * max_splits + split
+  // Continuous batching: when q_off is set, sequence b is decoded only if it brings exactly
+  // one new token, q and out rows [q_off[b], q_off[b+1]) (< total_rows) of a packed batch,
+  // and ctx_len holds its prefix length (the token sits at position ctx_len[b]); other
+  // sequences are left to the prefill kernel.  Such a job is never split.
+  const int32_t* q_off;
+  int32_t total_rows;
 };
+
+// Row of sequence b in a job's q / out / lse_out.
+__host__ __device__ inline int64_t job_row(const DecodeJob& jb, int b) { return jb.q_off ? jb.q_off[b] : b; }
 
 struct DecodeParams {
   const uint8_t* pages[kMaxKvHeads];  // pool slots, one per (layer's) KV head, same page size
@@ -104,9 +113,12 @@ struct PrefillLaunch {
   float* out;
   float* lse_out;
   int32_t* err;
+  bool skip_single;      // with q_off: sequences with one new token are decoded elsewhere
 };
 
 size_t prefill_workspace_bytes(int32_t batch, int32_t max_pages_per_seq, int32_t page_size);
+void prefill_piece_region(void* workspace, int32_t batch, int32_t max_pages_per_seq, int32_t page_size,
+                          void** region, size_t* bytes);
 cudaError_t launch_prefill(const PrefillLaunch& p, cudaStream_t stream);
 
 // Launch with programmatic stream serialization: the grid may start while the

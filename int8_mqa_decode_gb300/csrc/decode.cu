@@ -228,7 +228,20 @@ __device__ __forceinline__ Item make_item(const DecodeParams& p, int idx) {
   const int r = idx - it.b * per_b;
   it.kvh = r / jb.plan.max_splits;
   it.split = r - it.kvh * jb.plan.max_splits;
-  const SeqSplits sp = seq_splits(p.ctx_len[it.b], jb.window, jb.max_pages * P, jb.plan.chunk);
+  int32_t L = p.ctx_len[it.b];
+  if (jb.q_off) {
+    const int32_t a = jb.q_off[it.b], e = jb.q_off[it.b + 1];
+    if (!(a >= 0 && e == a + 1 && e <= jb.total_rows)) {  // not a one-token row: the prefill kernel's
+      it.kind = 2;
+      it.invalid = false;
+      it.direct = false;
+      it.ntiles = 0;
+      it.start = it.end = it.tile0 = 0;
+      return it;
+    }
+    L = L + 1;  // ctx_len holds the prefix length; the new token is attended too
+  }
+  const SeqSplits sp = seq_splits(L, jb.window, jb.max_pages * P, jb.plan.chunk);
   it.invalid = !sp.valid;
   it.direct = sp.nsplit == 1;
   it.ntiles = 0;
@@ -559,7 +572,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         for (int i = 0; i < kQUnits; ++i) {
           const int u = i * 256 + ctid;
           const int n = (u & 7) | ((u >> 7) << 3), k8 = (u >> 3) & 15;
-          qv[i] = n < G ? __ldg(reinterpret_cast<const uint4*>(p.job[it.job].q + ((int64_t)it.b * Hq + it.kvh * G + n) * kHeadDim +
+          qv[i] = n < G ? __ldg(reinterpret_cast<const uint4*>(p.job[it.job].q + (job_row(p.job[it.job], it.b) * Hq + it.kvh * G + n) * kHeadDim +
                                                                 k8 * 8))
                         : make_uint4(0u, 0u, 0u, 0u);
         }
@@ -700,8 +713,8 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       if (it.kind == 1) {
         // Nothing to attend (L = 0) or an invalid length: out = 0, lse = -inf.
         if (it.invalid && sw == 0 && lane == 0) set_err(p.err, CAI_DEVERR_LENGTH);
-        const int64_t hb = (int64_t)it.b * Hq + it.kvh * G;  // first output head of the item
         const DecodeJob& jb = p.job[it.job];
+        const int64_t hb = job_row(jb, it.b) * Hq + it.kvh * G;  // first output head of the item
         for (int h = h0; h < h0 + HH && h < G; ++h) jb.out[(hb + h) * kHeadDim + tok] = 0.0f;
         if (jb.lse_out && quarter == 0 && lane < HH && h0 + lane < G) jb.lse_out[hb + h0 + lane] = -INFINITY;
         continue;
@@ -857,9 +870,9 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       // 16-byte aligned (checked on the host); an LSE array that is not, or a row
       // of fewer than 4 LSEs, takes plain stores.
       const DecodeJob& jb = p.job[it.job];
-      float* dst_o = it.direct ? jb.out + ((int64_t)it.b * Hq + it.kvh * G) * kHeadDim
+      float* dst_o = it.direct ? jb.out + (job_row(jb, it.b) * Hq + it.kvh * G) * kHeadDim
                                : jb.ws_o + (((int64_t)it.b * jb.plan.max_splits + it.split) * Hq + it.kvh * G) * kHeadDim;
-      float* dst_lse = it.direct ? (jb.lse_out ? jb.lse_out + (int64_t)it.b * Hq + it.kvh * G : nullptr)
+      float* dst_lse = it.direct ? (jb.lse_out ? jb.lse_out + job_row(jb, it.b) * Hq + it.kvh * G : nullptr)
                                  : jb.ws_lse + ((int64_t)it.b * jb.plan.max_splits + it.split) * Hq + it.kvh * G;
       const bool bulk_lse = dst_lse != nullptr && (reinterpret_cast<uintptr_t>(dst_lse) & 15u) == 0 && (G & 3) == 0;
       float* lse_stage = wmax;
@@ -920,8 +933,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
   if (gw >= p.batch * Hq) return;
   const int b = gw / Hq, h = gw - b * Hq;
   const DecodeJob& jb = p.job[job];
-  const SeqSplits sp = seq_splits(p.ctx_len[b], jb.window, jb.max_pages * page_size, jb.plan.chunk);
+  int32_t L = p.ctx_len[b];
+  if (jb.q_off) {  // a packed continuous batch: only its one-token rows were decoded
+    const int32_t a = jb.q_off[b], e = jb.q_off[b + 1];
+    if (!(a >= 0 && e == a + 1 && e <= jb.total_rows)) return;
+    L = L + 1;
+  }
+  const SeqSplits sp = seq_splits(L, jb.window, jb.max_pages * page_size, jb.plan.chunk);
   if (!sp.valid || sp.nsplit <= 1) return;  // written by the decode kernel itself
+  const int64_t orow = job_row(jb, b);
   static_assert(kMaxSplits <= 64, "two splits per lane");
   const int S = jb.plan.max_splits;        // <= 64: lane l holds splits l and l + 32
   const float* lse = jb.ws_lse + (int64_t)b * S * Hq + h;
@@ -959,9 +979,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
     }
   }
   const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-  reinterpret_cast<float4*>(jb.out + ((int64_t)b * Hq + h) * kHeadDim)[lane] =
+  reinterpret_cast<float4*>(jb.out + (orow * Hq + h) * kHeadDim)[lane] =
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (jb.lse_out && lane == 0) jb.lse_out[(int64_t)b * Hq + h] = wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
+  if (jb.lse_out && lane == 0) jb.lse_out[orow * Hq + h] = wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
 // The page pool as a 2-D tensor of 128-byte rows (a page of P tokens is

@@ -83,6 +83,7 @@ struct PrefillParams {
   // writes its normalised partial output and log2-sum-exp to piece_o / piece_lse
   // ([t][256 rows][128] and [t][256]); combine_pieces_kernel merges them.
   int32_t full_items, pieces, num_items;
+  int32_t skip_single;  // see PrefillLaunch
   float* piece_o;
   float* piece_lse;
   uint16_t* kb;  // scratch bf16 [B][KT][128]
@@ -110,6 +111,7 @@ __device__ __forceinline__ SeqRows seq_rows(const PrefillParams& p, int b) {
   const int32_t a = p.q_off[b], e = p.q_off[b + 1];
   s.r0 = a;
   s.n = (a >= 0 && a <= e && e <= p.total_new && e - a <= p.n_new) ? e - a : -1;
+  if (p.skip_single && s.n == 1) s.n = 0;  // decoded by the decode kernel in the same call
   return s;
 }
 
@@ -117,61 +119,64 @@ __device__ __forceinline__ bool seq_ok(const PrefillParams& p, int32_t p0, int n
   return n >= 0 && p0 >= 0 && (int64_t)p0 + n <= (int64_t)p.max_pages * p.page_size;
 }
 
-// One warp per scratch row (sequence b, key t).
+// One block per 128-key tile of a sequence (blockIdx.y = sequence), one warp per 16
+// rows of it; a block whose tile no query of the chunk reads returns at once.
 __global__ void __launch_bounds__(256) dequant_kernel(const PrefillParams p) {
-  const int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int b = blockIdx.y;
+  const int tile = blockIdx.x;
   const int lane = threadIdx.x & 31;
-  if (row >= (int64_t)p.batch * p.kt_rows) return;
-  const int b = (int)(row / p.kt_rows);
-  const int t = (int)(row - (int64_t)b * p.kt_rows);
   const int32_t p0 = p.prefix_len[b];
   const SeqRows sr = seq_rows(p, b);
   const bool ok = seq_ok(p, p0, sr.n);
   if (!ok) {
-    if (t == 0 && lane == 0 && p.err) atomicOr(p.err, CAI_DEVERR_LENGTH);
+    if (tile == 0 && threadIdx.x == 0 && p.err) atomicOr(p.err, CAI_DEVERR_LENGTH);
     return;
   }
-  if (sr.n == 0) return;  // no new tokens: nothing attends
+  if (sr.n == 0) return;  // no new tokens (or a one-token row decoded elsewhere): nothing attends
   const int len = p0 + sr.n;
-  if (t >= ((len + kKeys - 1) / kKeys) * kKeys) return;  // never read
+  if (tile * kKeys >= len) return;  // never read
   // Keys before every window of the chunk are never attended: rows of their tile get
   // zeros (masked later) and their pages are not read, so a local buffer may have
   // recycled them.
   const int lo_min = p.window > 0 ? max(0, p0 + 1 - p.window) : 0;
-  if (t < (lo_min / kKeys) * kKeys) return;  // before every window, whole tile
-  uint32_t kw = 0, vw = 0;
-  float ksc = 0.0f, vsc = 0.0f;
-  if (t < len && t >= lo_min) {
-    const int P = p.page_size;
-    const int32_t page = p.table[(int64_t)b * p.max_pages + t / P];
-    if (page >= 0 && page < p.num_pages) {
-      const int slot = t % P;
-      const uint8_t* pg = p.pages + (int64_t)page * page_bytes(P);
-      kw = reinterpret_cast<const uint32_t*>(pg + slot * kHeadDim)[lane];
-      const uint8_t* vcol = pg + P * kHeadDim + slot;  // channel-major V block: channel c at c * P
+  if (tile < lo_min / kKeys) return;  // before every window, whole tile
+  for (int rr = threadIdx.x >> 5; rr < kKeys; rr += blockDim.x >> 5) {
+    const int t = tile * kKeys + rr;
+    const int64_t row = (int64_t)b * p.kt_rows + t;
+    uint32_t kw = 0, vw = 0;
+    float ksc = 0.0f, vsc = 0.0f;
+    if (t < len && t >= lo_min) {
+      const int P = p.page_size;
+      const int32_t page = p.table[(int64_t)b * p.max_pages + t / P];
+      if (page >= 0 && page < p.num_pages) {
+        const int slot = t % P;
+        const uint8_t* pg = p.pages + (int64_t)page * page_bytes(P);
+        kw = reinterpret_cast<const uint32_t*>(pg + slot * kHeadDim)[lane];
+        const uint8_t* vcol = pg + P * kHeadDim + slot;  // channel-major V block: channel c at c * P
 #pragma unroll
-      for (int e = 0; e < 4; ++e) vw |= (uint32_t)vcol[(lane * 4 + e) * P] << (8 * e);
-      const float* sc = reinterpret_cast<const float*>(pg + 2 * P * kHeadDim);
-      ksc = sc[slot] * p.scale_log2;
-      vsc = sc[P + slot];
-    } else if (lane == 0 && p.err) {
-      atomicOr(p.err, CAI_DEVERR_PAGE);
+        for (int e = 0; e < 4; ++e) vw |= (uint32_t)vcol[(lane * 4 + e) * P] << (8 * e);
+        const float* sc = reinterpret_cast<const float*>(pg + 2 * P * kHeadDim);
+        ksc = sc[slot] * p.scale_log2;
+        vsc = sc[P + slot];
+      } else if (lane == 0 && p.err) {
+        atomicOr(p.err, CAI_DEVERR_PAGE);
+      }
     }
-  }
-  // int8 -> bf16 (K) and int8 -> fp16 (V): exact for |code| <= 127.
-  uint16_t kb[4], vh[4];
+    // int8 -> bf16 (K) and int8 -> fp16 (V): exact for |code| <= 127.
+    uint16_t kb[4], vh[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float kf = (float)(int8_t)(kw >> (8 * e));
-    const float vf = (float)(int8_t)(vw >> (8 * e));
-    kb[e] = (uint16_t)(__float_as_uint(kf) >> 16);  // small integers: the top half is exact
-    const __half hv = __float2half_rn(vf * vsc);  // V scale applied here: P needs no per-key factor
-    vh[e] = *reinterpret_cast<const uint16_t*>(&hv);
+    for (int e = 0; e < 4; ++e) {
+      const float kf = (float)(int8_t)(kw >> (8 * e));
+      const float vf = (float)(int8_t)(vw >> (8 * e));
+      kb[e] = (uint16_t)(__float_as_uint(kf) >> 16);  // small integers: the top half is exact
+      const __half hv = __float2half_rn(vf * vsc);  // V scale applied here: P needs no per-key factor
+      vh[e] = *reinterpret_cast<const uint16_t*>(&hv);
+    }
+    const int64_t off = row * kHeadDim + lane * 4;
+    *reinterpret_cast<uint2*>(p.kb + off) = make_uint2(kb[0] | ((uint32_t)kb[1] << 16), kb[2] | ((uint32_t)kb[3] << 16));
+    *reinterpret_cast<uint2*>(p.vh + off) = make_uint2(vh[0] | ((uint32_t)vh[1] << 16), vh[2] | ((uint32_t)vh[3] << 16));
+    if (lane == 0) p.ks[row] = ksc;
   }
-  const int64_t off = row * kHeadDim + lane * 4;
-  *reinterpret_cast<uint2*>(p.kb + off) = make_uint2(kb[0] | ((uint32_t)kb[1] << 16), kb[2] | ((uint32_t)kb[3] << 16));
-  *reinterpret_cast<uint2*>(p.vh + off) = make_uint2(vh[0] | ((uint32_t)vh[1] << 16), vh[2] | ((uint32_t)vh[3] << 16));
-  if (lane == 0) p.ks[row] = ksc;
 }
 
 __device__ __forceinline__ void tma_load_rows128(void* dst, const CUtensorMap* map, int row, uint64_t* bar) {
@@ -620,7 +625,22 @@ size_t prefill_workspace_bytes(int32_t batch, int32_t max_pages_per_seq, int32_t
   const int64_t rows = (int64_t)batch * kt;
   const int64_t a = ((rows * kHeadDim * 2 + 255) / 256) * 256;
   const int64_t s = ((rows * 4 + 255) / 256) * 256;
-  return (size_t)(2 * a + 2 * s + ((piece_bytes() + 255) / 256) * 256);
+  // ... and, last, the work-queue counters of the decode launch that takes a varlen batch's
+  // one-token rows (see cai_mqa_prefill_varlen).
+  return (size_t)(2 * a + 2 * s + ((piece_bytes() + 255) / 256) * 256 + kWorkspaceHeader);
+}
+
+// The piece region of a prefill workspace: the prefill kernel writes the last wave's
+// partial outputs there, and a varlen call's decode launch, which runs before it on the
+// same stream, may keep its split partials there.
+void prefill_piece_region(void* workspace, int32_t batch, int32_t max_pages_per_seq, int32_t page_size,
+                          void** region, size_t* bytes) {
+  const int64_t kt = ((int64_t)max_pages_per_seq * page_size + kKeys - 1) / kKeys * kKeys;
+  const int64_t rows = (int64_t)batch * kt;
+  const int64_t a = ((rows * kHeadDim * 2 + 255) / 256) * 256;
+  const int64_t s = ((rows * 4 + 255) / 256) * 256;
+  *region = static_cast<uint8_t*>(workspace) + 2 * a + 2 * s;
+  *bytes = (size_t)(((piece_bytes() + 255) / 256) * 256);
 }
 
 cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
@@ -633,6 +653,7 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.prefix_len = L.prefix_len;
   p.q = L.q;
   p.q_off = L.q_off;
+  p.skip_single = L.q_off && L.skip_single ? 1 : 0;
   p.batch = L.batch;
   p.n_new = L.n_new;
   p.total_new = L.total_new;
@@ -659,8 +680,7 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   if (!encode_rows128(&kmap, p.kb, (uint64_t)rows) || !encode_rows128(&vmap, p.vh, (uint64_t)rows))
     return cudaErrorInvalidValue;
 
-  const int64_t warps = rows;
-  dequant_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(p);
+  dequant_kernel<<<dim3((unsigned)(p.kt_rows / kKeys), (unsigned)L.batch), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
