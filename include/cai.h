@@ -363,6 +363,24 @@ int32_t cai_ring_pages(int32_t window, int32_t page_size, int32_t max_new_tokens
 cai_status cai_ring_table_row(int32_t* row, int32_t max_pages_per_seq, const int32_t* ring_ids, int32_t ring,
                               int32_t hi, int32_t page_size);
 
+/* Limit, in nanoseconds, of every bounded wait inside the decode and prefill kernels
+ * (process-wide, read at each launch; 0 restores the default of 2 s; a wait checks its
+ * clock after each suspension of up to 1 ms, so shorter limits act as about 1 ms).  A
+ * CTA whose wait runs out sets CAI_DEVERR_TIMEOUT, stops its work, waits for its own
+ * copies and tensor-core operations in flight, frees its tensor memory and returns;
+ * that launch's outputs are unspecified.  A short limit is for failure-detection
+ * tests; a serving process leaves the default. */
+void cai_set_wait_limit_ns(uint64_t ns);
+
+/* Fault injection for failure-detection tests (process-wide, read at each launch;
+ * -1, the default, turns it off).  With stage = n >= 0, every CTA of the following
+ * decode launches skips the load of its n-th K/V stage (64 tokens), and every CTA of
+ * the following prefill launches skips the load of its n-th K tile (128 keys); the
+ * waits for them run out after the wait limit and the launch reports
+ * CAI_DEVERR_TIMEOUT.  Nothing faults: the load is simply never issued.  A CTA with
+ * fewer stages than n + 1 is not affected. */
+void cai_set_fault_injection(int32_t stage);
+
 /* The CUDA runtime's description of the error behind the last CAI_ERR_CUDA returned on
  * this thread ("no error" if none). */
 const char* cai_last_cuda_error(void);

@@ -24,7 +24,7 @@ __all__ = [
     "cai_mqa_prefill_chunk", "cai_mqa_prefill_varlen", "cai_gqa_decode", "cai_gqa_decode_workspace_size",
     "CAI_DEVERR_PAGE", "CAI_DEVERR_LENGTH", "CAI_DEVERR_TIMEOUT", "HEAD_DIM", "cai_host_cache_create",
     "cai_host_cache_destroy", "cai_host_cache_match", "cai_host_cache_restore", "cai_host_cache_store",
-    "cai_host_cache_stats", "cai_host_cache_restore_batch", "cai_ring_pages", "cai_ring_table_row",
+    "cai_host_cache_stats", "cai_host_cache_restore_batch", "cai_set_wait_limit_ns", "cai_set_fault_injection", "cai_ring_pages", "cai_ring_table_row",
 ]
 
 HEAD_DIM = 128
@@ -75,6 +75,10 @@ def load():
     lib.cai_status_string.restype = ctypes.c_char_p
     lib.cai_last_cuda_error.argtypes = []
     lib.cai_last_cuda_error.restype = ctypes.c_char_p
+    lib.cai_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.cai_set_wait_limit_ns.restype = None
+    lib.cai_set_fault_injection.argtypes = [ctypes.c_int32]
+    lib.cai_set_fault_injection.restype = None
     lib.cai_kv_append.argtypes = [pool_p, vp, vp, i32, i32, vp, i32, vp, vp, vp]
     lib.cai_kv_append.restype = ctypes.c_int
     lib.cai_kv_append_pools.argtypes = [pool_p, i32, vp, vp, i32, i32, vp, i32, vp, vp, vp]
@@ -374,6 +378,16 @@ def cai_mqa_prefill_varlen(pool: KVPool, q: torch.Tensor, q_offsets: torch.Tenso
 def _i32_host(a) -> "ctypes.Array":
     a = np.ascontiguousarray(a, dtype=np.int32)
     return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def cai_set_wait_limit_ns(ns: int) -> None:
+    """Limit of the kernels' bounded waits in nanoseconds (0: the default, 2 s); for failure tests."""
+    load().cai_set_wait_limit_ns(int(ns))
+
+
+def cai_set_fault_injection(stage: int) -> None:
+    """Every CTA skips the load of its `stage`-th K/V stage (decode) or K tile (prefill); -1: off."""
+    load().cai_set_fault_injection(int(stage))
 
 
 def cai_host_cache_create(page_size: int, num_buffers: int, capacity_pages: int, head_dim: int = HEAD_DIM) -> int:

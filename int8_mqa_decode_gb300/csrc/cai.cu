@@ -1,6 +1,7 @@
 // Host side of the C ABI: argument validation, split planning and launches.
 // Everything here is plain bookkeeping; all arithmetic on the data runs in
 // the kernels.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -69,7 +70,12 @@ static size_t workspace_bytes_for(int32_t batch, int32_t num_q_heads, const Deco
 namespace cai {
 namespace {
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int32_t> g_drop_stage{-1};
 }  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+int32_t fault_drop_stage() { return g_drop_stage.load(std::memory_order_relaxed); }
 
 cai_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return CAI_OK;
@@ -83,6 +89,10 @@ using namespace cai;
 extern "C" {
 
 const char* cai_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
+
+void cai_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 2000000000ull, std::memory_order_relaxed); }
+
+void cai_set_fault_injection(int32_t stage) { g_drop_stage.store(stage < 0 ? -1 : stage, std::memory_order_relaxed); }
 
 size_t cai_page_bytes(int32_t page_size, int32_t head_dim) {
   if (page_size <= 0 || head_dim <= 0) return 0;
@@ -256,6 +266,8 @@ cai_status decode_layers_common(const LayerArgs* layers, int32_t n, int32_t num_
   p.num_jobs = n;
   p.queue = static_cast<uint32_t*>(workspace);
   p.err = err_flag;
+  p.wait_ns = wait_limit_ns();
+  p.drop_stage = fault_drop_stage();
   // Job order: global layers first, then wider windows first (stable).
   int order[kMaxDecodeJobs];
   for (int l = 0; l < n; ++l) order[l] = l;
@@ -475,6 +487,8 @@ cai_status prefill_common(const cai_kv_pool* pool, const uint16_t* q, int32_t ba
     d.num_jobs = 1;
     d.queue = static_cast<uint32_t*>(hdr);
     d.err = err_flag;
+    d.wait_ns = wait_limit_ns();
+    d.drop_stage = fault_drop_stage();
     DecodeJob& jb = d.job[0];
     jb.slot0 = 0;
     jb.window = window;

@@ -81,6 +81,8 @@ struct DecodeParams {
   DecodeJob job[kMaxDecodeJobs];
   uint32_t* queue;                    // [2]: next work item, CTAs finished (both zero between calls)
   int32_t* err;
+  uint64_t wait_ns;                   // limit of every bounded wait inside the kernel
+  int32_t drop_stage;                 // fault injection: K/V stage each CTA skips (-1: none)
 };
 
 // Attended range and split bookkeeping shared by the decode and combine kernels.
@@ -115,6 +117,11 @@ struct PrefillLaunch {
   int32_t* err;
   bool skip_single;      // with q_off: sequences with one new token are decoded elsewhere
 };
+
+// Limit of the kernels' bounded waits (cai_set_wait_limit_ns), read at every launch.
+uint64_t wait_limit_ns();
+// The stage every CTA skips (cai_set_fault_injection; -1: none), read at every launch.
+int32_t fault_drop_stage();
 
 size_t prefill_workspace_bytes(int32_t batch, int32_t max_pages_per_seq, int32_t page_size);
 void prefill_piece_region(void* workspace, int32_t batch, int32_t max_pages_per_seq, int32_t page_size,

@@ -81,12 +81,12 @@ struct Layout {
   static constexpr int kOffBars = kOffXch + 13 * HN * 4;
   static_assert(kOffXch % 16 == 0 && kOffPT % 16 == 0, "bulk-copy sources");
   static constexpr int kNumBars = 2 * NST + 2 * 2 /*k_full, v_full*/ + 2 * 2 /*s_full, p_full*/ + 2 /*v_free*/ +
-                                  2 * 2 /*o_full, o_empty*/ + 3 * kRing + 2 * kScaleSlots;
-  static constexpr int kOffMisc = kOffBars + 8 * kNumBars;       // tmem slot, abort flag, page_ok[NST]
-  static constexpr int kOffRing = kOffMisc + 64;
+                                  2 * 2 /*o_full, o_empty*/ + 3 * kRing + 2 * kScaleSlots + 1 /*drain*/;
+  static constexpr int kOffMisc = kOffBars + 8 * kNumBars;       // tmem slot, wait state (+8), page_ok[NST] (+24)
+  static constexpr int kOffRing = kOffMisc + 80;
   static constexpr int kSmemBytes = kOffRing + kRing * kRingInts * 4 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "dynamic shared memory per CTA");
-  static_assert(8 + 4 * NST <= 64, "misc words");
+  static_assert(24 + 4 * NST <= 80, "misc words");
 };
 
 // Warp roles, aligned to warpgroups so each group can resize its register file:
@@ -105,12 +105,13 @@ struct Roles {
   // Registers per thread, launched with kRegsLaunch and resized per warpgroup:
   //  32 heads: 16 warps (4 per SM sub-partition) at 128 = 65536; then 56 / 104 / 232:
   //            128 * (56 + 2 * 104 + 232) = 63488, per sub-partition 32 * 496 = 15872 <= 16384.
-  //  64 heads: 20 warps (5 per sub-partition) at 96 = 61440; then 48 / 96 / 120:
-  //            128 * (48 + 2 * 96 + 2 * 120) = 61440, per sub-partition 32 * 480 = 15360 <= 16384.
+  //  64 heads: 20 warps (5 per sub-partition) at 96 = 61440; then 48 / 80 / 136:
+  //            128 * (48 + 2 * 80 + 2 * 136) = 61440, per sub-partition 32 * 480 = 15360 <= 16384
+  //            (the softmax holds 32 heads per thread; below 136 registers it spills).
   static constexpr int kRegsLaunch = HN <= 32 ? 128 : 96;  // checked on the host before the first launch
   static constexpr int kRegsCtl = HN <= 32 ? 56 : 48;
-  static constexpr int kRegsConv = HN <= 32 ? 104 : 96;
-  static constexpr int kRegsSoft = HN <= 32 ? 232 : 120;
+  static constexpr int kRegsConv = HN <= 32 ? 104 : 80;
+  static constexpr int kRegsSoft = HN <= 32 ? 232 : 136;
   static_assert(128 * kRegsCtl + 32 * kConvWarps * kRegsConv + 32 * kSoftWarps * kRegsSoft <= kRegsLaunch * kThreads,
                 "register split");
   static_assert(32 * (kRegsCtl + 2 * kRegsConv + (kSoftWarps / 4) * kRegsSoft) <= 16384, "sub-partition registers");
@@ -315,9 +316,11 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   uint64_t* scale_full = item_empty + kRing;        // [kScaleSlots] converters -> softmax
   uint64_t* scale_free = scale_full + kScaleSlots;  // [kScaleSlots] softmax -> converters
   uint64_t* item_taken = scale_free + kScaleSlots;  // [kRing] producer -> scheduler (item started)
+  uint64_t* mma_drain = item_taken + kRing;         // MMA issuers' last commits, at exit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kOffMisc + 4);
-  uint32_t* page_ok = reinterpret_cast<uint32_t*>(smem + L::kOffMisc + 8);        // [NST]
+  volatile WaitState* const wctl = reinterpret_cast<volatile WaitState*>(smem + L::kOffMisc + 8);
+  volatile int32_t* abort_flag = &wctl->abort;
+  uint32_t* page_ok = reinterpret_cast<uint32_t*>(smem + L::kOffMisc + 24);        // [NST]
   volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(smem + L::kOffRing);  // [kRing][kRingInts]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -345,11 +348,13 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       mbar_init(&item_empty[r], R::kItemReaders);
       mbar_init(&item_taken[r], 1);
     }
+    mbar_init(mma_drain, 2);
     for (int r = 0; r < kScaleSlots; ++r) {
       mbar_init(&scale_full[r], kConvWarps);
       mbar_init(&scale_free[r], kSoftWarps);
     }
     *abort_flag = 0;
+    wctl->limit_ns = p.wait_ns;
     fence_barrier_init();
   }
   tc_fence_before();
@@ -362,24 +367,25 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   grid_launch_dependents();
 
   // Item k of this CTA as published by the scheduler warp; every reader warp
-  // waits for it, copies it and releases the slot.
-  auto next_item = [&](int k, bool& done, int32_t* first_ids = nullptr) -> Item {
+  // waits for it, copies it and releases the slot.  Waits answer per thread (no
+  // collective step right after a wait on the hot path, where one costs about 15% of
+  // the decode), so the reader's lanes agree here, once per item: the item is used
+  // only if every lane saw it published and none has given up earlier (`stop`);
+  // otherwise `done` ends the reader.  The softmax warps agree through their own
+  // barrier-reduction instead (group_vote = false: `done` is then per lane).
+  auto next_item = [&](int k, bool& done, bool stop, bool group_vote, int32_t* first_ids = nullptr) -> Item {
     const int slot = k % kRing;
-    Item it = {};
-    if (!mbar_wait_abortable(&item_full[slot], (k / kRing) & 1, abort_flag)) {
-      done = true;
-      return it;
-    }
-    it = ring_item(ring + slot * kRingInts, done);
+    const bool seen = mbar_wait_abortable(&item_full[slot], (k / kRing) & 1, wctl);
+    Item it = ring_item(ring + slot * kRingInts, done);
     if (first_ids) *first_ids = (int32_t)ring[slot * kRingInts + 8 + lane];
     __syncwarp();
-    if (lane == 0) {
+    if (lane == 0 && seen) {  // a slot is released only by a reader that saw it published
       mbar_arrive(&item_empty[slot]);
       if (warp == 0) mbar_arrive(&item_taken[slot]);  // the producer starts item k
     }
+    if (group_vote ? !__all_sync(0xffffffffu, seen && !stop) : !(seen && !stop)) done = true;
     return it;
   };
-
   if (warp < kConvWarp0) {
     setmaxnreg_dec<R::kRegsCtl>();
     if (warp == kSchedWarp) {
@@ -388,14 +394,17 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       // item kClaimAhead before it: a CTA holds few claimed items, so the queue, not
       // early claims, decides which SM runs what (claiming up to the ring's depth let
       // a few SMs hoard long items and finish far behind the others).
+      // Lane 0 decides for the warp (the claim goes through a shuffle); a lane writes
+      // its part of a ring slot only after seeing every reader release the slot.
       int k = 0;
+      bool stop = false;  // lane 0: one of its waits gave up
       while (true) {
-        if (k >= kClaimAhead &&
-            !mbar_wait_abortable(&item_taken[(k - kClaimAhead) % kRing], ((k - kClaimAhead) / kRing) & 1, abort_flag))
-          break;
-        int idx = 0;
-        if (lane == 0) idx = (int)atomicAdd(&p.queue[0], 1u);
+        const bool taken = k < kClaimAhead || mbar_wait_abortable(&item_taken[(k - kClaimAhead) % kRing],
+                                                                  ((k - kClaimAhead) / kRing) & 1, wctl);
+        int idx = -1;
+        if (lane == 0 && taken && !stop) idx = (int)atomicAdd(&p.queue[0], 1u);
         idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx < 0) break;
         const bool done = idx >= num_items;
         Item it = {};
         int32_t id = (int32_t)kNoPage;
@@ -411,10 +420,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
           }
         }
         const int slot = k % kRing;
-        if (k >= kRing && !mbar_wait_abortable(&item_empty[slot], ((k / kRing) - 1) & 1, abort_flag)) break;
+        const bool free = k < kRing || mbar_wait_abortable(&item_empty[slot], ((k / kRing) - 1) & 1, wctl);
         volatile int32_t* e = ring + slot * kRingInts;
-        e[8 + lane] = id;
-        if (lane == 0) {
+        if (free) e[8 + lane] = id;
+        if (lane == 0 && free) {
           if (!done) {
             e[0] = it.b;
             e[1] = it.split;
@@ -430,8 +439,12 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         }
         __syncwarp();
         if (lane == 0) {
-          __threadfence_block();
-          mbar_arrive(&item_full[slot]);
+          if (free) {
+            __threadfence_block();
+            mbar_arrive(&item_full[slot]);
+          } else {
+            stop = true;
+          }
         }
         ++k;
         if (done) break;
@@ -450,8 +463,8 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       while (true) {
         bool done = false;
         int32_t ids = kNoPage;
-        const Item it = next_item(k++, done, &ids);
-        if (done || *abort_flag) break;
+        const Item it = next_item(k++, done, *abort_flag != 0, true, &ids);
+        if (done) break;
         if (it.kind != 0) continue;
         bool ok = true;
         const int slot = p.job[it.job].slot0 + it.kvh;
@@ -466,15 +479,20 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
           }
           for (int hf = 0; hf < 2; ++hf, ++r) {
             const int s = r % NST;
-            if (r >= NST && !mbar_wait_abortable(&raw_empty[s], ((r / NST) - 1) & 1, abort_flag)) {
-              ok = false;
-              break;
-            }
+            // Lane 31 (never a page lane) carries into the ballot whether it saw the
+            // converters release the stage: the stage is armed only then, by every lane.
+            const bool free = r < NST || mbar_wait_abortable(&raw_empty[s], ((r / NST) - 1) & 1, wctl);
             const int32_t pid = __shfl_sync(0xffffffffu, ids, (t % TPB) * PPT + hf * SPS + lane % SPS);
             const bool live = lane < SPS && pid != kNoPage;
             const bool in_range = pid >= 0 && pid < slot_pages;
+            const uint32_t vote = __ballot_sync(0xffffffffu, lane == 31 ? free : (live && in_range));
+            if (!(vote >> 31)) {
+              ok = false;
+              break;
+            }
             if (live && !in_range) set_err(p.err, CAI_DEVERR_PAGE);
-            const uint32_t okm = __ballot_sync(0xffffffffu, live && in_range);
+            const uint32_t okm = vote & 0x7fffffffu;
+            if (r == p.drop_stage) continue;  // fault injection: this stage is never loaded
             if (lane == 0) {
               page_ok[s] = okm;
               mbar_arrive_expect_tx(&raw_full[s], (uint32_t)__popc(okm) * page_bytes(P));
@@ -490,6 +508,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         }
         if (!ok) break;
       }
+      // Every stage this producer armed has landed before the CTA goes away, whatever
+      // happened to the other roles (copies into a CTA's shared memory must not outlive it).
+      for (int i = r > NST ? r - NST : 0; i < r; ++i)
+        if (i != p.drop_stage) mbar_wait_drain(&raw_full[i % NST], (i / NST) & 1);
     } else {
       // ---------------------------------------------------------- MMA issuers
       // Warp 1 issues S^T = K Q^T, warp 3 issues O^T += V^T P^T: each waits only for
@@ -502,11 +524,14 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       const uint64_t dq = smem_desc(smem_addr(qt), 128, 2048);
       const uint64_t dp = smem_desc(smem_addr(pt), 128, T * 16);
       const bool s_issuer = warp == 1;
+      // Every lane runs the loop and waits for itself; lane 0 issues only what its own
+      // waits allow.  The lanes agree at the end of each tile (one vote, which also
+      // keeps them together while lane 0 issues).
       int g = 0, item_n = 0, k = 0;
       bool ok = true;
-      while (ok) {
+      while (true) {
         bool done = false;
-        const Item it = next_item(k++, done);
+        const Item it = next_item(k++, done, !ok, true);
         if (done) break;
         if (it.kind != 0) continue;
         const int ob = item_n & 1;
@@ -514,11 +539,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
           const int c = g & 1;
           if (s_issuer) {
             // S^T[c] is free once the softmax of tile g-2 has read it (it then wrote P^T).
-            ok = mbar_wait_abortable(&k_full[c], (g >> 1) & 1, abort_flag) &&
-                 (g < 2 || mbar_wait_abortable(&p_full[c], ((g >> 1) - 1) & 1, abort_flag));
-            if (!ok) break;
+            ok = mbar_wait_abortable(&k_full[c], (g >> 1) & 1, wctl) &&
+                 (g < 2 || mbar_wait_abortable(&p_full[c], ((g >> 1) - 1) & 1, wctl));
             tc_fence_after();
-            if (lane == 0) {
+            if (lane == 0 && ok) {
 #pragma unroll
               for (int ks = 0; ks < kHeadDim / 16; ++ks)
                 mma_f16_ts(tmem + kColS + c * HN, tmem + kColKA + c * 64 + ks * 8, dq + (uint64_t)(ks * 16), idesc_s,
@@ -528,12 +552,11 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
           } else {
             // PV of tile g into O^T[item & 1]; the item's first PV starts the
             // accumulator once the epilogue of item - 2 has read it.
-            ok = mbar_wait_abortable(&p_full[c], (g >> 1) & 1, abort_flag) &&
-                 mbar_wait_abortable(&v_full[c], (g >> 1) & 1, abort_flag) &&
-                 (t > 0 || item_n < 2 || mbar_wait_abortable(&o_empty[ob], ((item_n >> 1) - 1) & 1, abort_flag));
-            if (!ok) break;
+            ok = mbar_wait_abortable(&p_full[c], (g >> 1) & 1, wctl) &&
+                 mbar_wait_abortable(&v_full[c], (g >> 1) & 1, wctl) &&
+                 (t > 0 || item_n < 2 || mbar_wait_abortable(&o_empty[ob], ((item_n >> 1) - 1) & 1, wctl));
             tc_fence_after();
-            if (lane == 0) {
+            if (lane == 0 && ok) {
 #pragma unroll
               for (int ks = 0; ks < T / 16; ++ks)
                 mma_f16_ts(tmem + kColO + ob * HN, tmem + kColV + c * 64 + ks * 8,
@@ -542,10 +565,17 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
               if (t == it.ntiles - 1) mma_commit(&o_full[ob]);
             }
           }
-          __syncwarp();
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
         }
         ++item_n;
       }
+      // This issuer's MMAs have completed before tensor memory is freed.
+      if (lane == 0) {
+        mma_commit(mma_drain);
+        mbar_wait_drain(mma_drain, 0);
+      }
+      __syncwarp();
     }
   } else if (warp < kSoftWarp0) {
     setmaxnreg_dec<R::kRegsConv>();
@@ -556,11 +586,14 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
     const int tk = quarter * 32 + lane;               // this thread's token (K operand row)
     const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
     constexpr int kQUnits = HN * 16 / 256;            // 16-byte units of Q^T per thread
+    // A converter warp's control flow does not depend on its waits: a lane whose wait
+    // gave up carries on with the tile (its operands are then garbage) and releases
+    // nothing it did not see filled; the lanes agree on stopping at the next item.
     int g = 0, k = 0;
     bool ok = true;
-    while (ok) {
+    while (true) {
       bool done = false;
-      const Item it = next_item(k++, done);
+      const Item it = next_item(k++, done, !ok, true);
       if (done) break;
       if (it.kind != 0) continue;
       // The item's query as Q^T (bf16 -> fp16), once the S^T of the previous
@@ -576,8 +609,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
                                                                 k8 * 8))
                         : make_uint4(0u, 0u, 0u, 0u);
         }
-        if (g >= 1) ok = mbar_wait_abortable(&s_full[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag);
-        if (!ok) break;
+        if (g >= 1) ok = mbar_wait_abortable(&s_full[(g - 1) & 1], ((g - 1) >> 1) & 1, wctl) && ok;
 #pragma unroll
         for (int i = 0; i < kQUnits; ++i) {
           const int u = i * 256 + ctid;
@@ -594,9 +626,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       for (int t = 0; t < it.ntiles; ++t, ++g) {
         const int c = g & 1;
         const int s0 = (2 * g) % NST, s1 = (2 * g + 1) % NST;
-        ok = mbar_wait_abortable(&raw_full[s0], ((2 * g) / NST) & 1, abort_flag) &&
-             mbar_wait_abortable(&raw_full[s1], ((2 * g + 1) / NST) & 1, abort_flag);
-        if (!ok) break;
+        // Only a lane that saw both stages land may release them (lane 0 does).
+        const bool landed = mbar_wait_abortable(&raw_full[s0], ((2 * g) / NST) & 1, wctl) &&
+                            mbar_wait_abortable(&raw_full[s1], ((2 * g + 1) / NST) & 1, wctl);
+        ok = ok && landed;
         // Codes to registers.  Row r of a page slot holds its 16-byte chunk j at
         // chunk position j ^ (r % 8) (128-byte swizzle; slots are 1024-aligned,
         // and a page occupies 2P rows of its stage, a multiple of 8).
@@ -625,8 +658,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         }
         // Scales and mask of tile g into ring slot g % 4 (free once the softmax of tile g-4 is done).
         const int ss = g & (kScaleSlots - 1);
-        if (g >= kScaleSlots) ok = mbar_wait_abortable(&scale_free[ss], ((g / kScaleSlots) - 1) & 1, abort_flag);
-        if (!ok) break;
+        if (g >= kScaleSlots) ok = mbar_wait_abortable(&scale_free[ss], ((g / kScaleSlots) - 1) & 1, wctl) && ok;
         if (ctid < T) {
           const int tt = ctid;
           const int s = tt < RT ? s0 : s1;
@@ -642,12 +674,13 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&scale_full[ss]);
-          mbar_arrive(&raw_empty[s0]);
-          mbar_arrive(&raw_empty[s1]);
+          if (landed) {
+            mbar_arrive(&raw_empty[s0]);
+            mbar_arrive(&raw_empty[s1]);
+          }
         }
         // K -> tensor memory: K[c] is free once S^T of tile g-2 is done.
-        if (g >= 2) ok = mbar_wait_abortable(&s_full[c], ((g >> 1) - 1) & 1, abort_flag);
-        if (!ok) break;
+        if (g >= 2) ok = mbar_wait_abortable(&s_full[c], ((g >> 1) - 1) & 1, wctl) && ok;
         tc_fence_after();
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -668,8 +701,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         // V -> V^T[c] in tensor memory (lane = channel, column k = tokens 2k, 2k+1 of
         // the tile; this warp writes the 32 columns of its tile half), free once PV of
         // tile g-2 is done.
-        if (g >= 2) ok = mbar_wait_abortable(&v_free[c], ((g >> 1) - 1) & 1, abort_flag);
-        if (!ok) break;
+        if (g >= 2) ok = mbar_wait_abortable(&v_free[c], ((g >> 1) - 1) & 1, wctl) && ok;
         tc_fence_after();
         {
           uint32_t vw[32];
@@ -700,12 +732,16 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
     const int h0 = hp * HH;
     const int tok = quarter * 32 + lane;
     const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
+    // The softmax warps meet at named barriers, so they stop together.  A thread
+    // whose wait gave up carries on with the same steps (on garbage) and brings
+    // ok = false to the group's next barrier-reduction (the item's start, a raise,
+    // the item's end), which gives every thread the same answer.
     int g = 0, item_n = 0, k = 0;
     bool ok = true;
-    while (ok) {
+    while (true) {
       bool done = false;
-      const Item it = next_item(k++, done);
-      if (done) break;
+      const Item it = next_item(k++, done, false, false);
+      if (bar_red_or(kSoftBar, kSoftThreads, done)) break;
       // The previous item's bulk copies must have read the P^T buffers and the
       // exchange before this item writes them; every softmax thread passes the
       // first tile's barrier-reduction after this.
@@ -725,9 +761,8 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       for (int t = 0; t < it.ntiles; ++t, ++g) {
         const int c = g & 1;
         const int ss = g & (kScaleSlots - 1);
-        ok = mbar_wait_abortable(&s_full[c], (g >> 1) & 1, abort_flag) &&
-             mbar_wait_abortable(&scale_full[ss], (g / kScaleSlots) & 1, abort_flag);
-        if (!ok) break;
+        ok = ok && mbar_wait_abortable(&s_full[c], (g >> 1) & 1, wctl) &&
+             mbar_wait_abortable(&scale_full[ss], (g / kScaleSlots) & 1, wctl);
         tc_fence_after();
         float sv[HH];
         {
@@ -771,8 +806,13 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
             mx = fmax3(mx, fmax3(sv[h], sv[h + 1], sv[h + 2]), sv[h + 3]);
           }
         }
-        const bool raise = valid && (mx > kRescaleThreshold || mref[h0] == -INFINITY);  // or no reference yet
+        // (A thread that gave up asks for a raise, and then all stop at its second reduction.)
+        const bool raise = !ok || (valid && (mx > kRescaleThreshold || mref[h0] == -INFINITY));  // or no reference yet
         if (bar_red_or(kSoftBar, kSoftThreads, raise)) {
+          if (bar_red_or(kSoftBar, kSoftThreads, !ok)) {
+            ok = false;
+            break;
+          }
           // Some head's reference must rise (or none is set yet): per-head maxima of the
           // tile over the four lane quarters, new references.
           {
@@ -803,8 +843,8 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
           }
           if (t > 0) {
             // O^T holds earlier tiles of this item: wait for the previous PV, then rescale this thread's entries.
-            ok = mbar_wait_abortable(&v_free[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag);
-            if (ok) {
+            ok = mbar_wait_abortable(&v_free[(g - 1) & 1], ((g - 1) >> 1) & 1, wctl);
+            {
               tc_fence_after();
               uint32_t o[HH];
               const uint32_t oc = tmem + t_lane + kColO + (item_n & 1) * HN + h0;
@@ -820,7 +860,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
           }
         }
         // P^T[c] is free once PV of tile g-2 is done.
-        if (ok && g >= 2) ok = mbar_wait_abortable(&v_free[c], ((g >> 1) - 1) & 1, abort_flag);
+        if (ok && g >= 2) ok = mbar_wait_abortable(&v_free[c], ((g >> 1) - 1) & 1, wctl);
         if (ok) {
           // P^T row of this token: heads 8i .. 8i+7 at i*2048 + tok*16 (MN-major B operand).
           uint8_t* dst = pt + c * L::kPTBytes + (h0 / 8) * 2048 + tok * 16;
@@ -850,9 +890,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
           mbar_arrive(&p_full[c]);
           mbar_arrive(&scale_free[ss]);
         }
-        if (!ok) break;
       }
-      if (!ok) break;
       // ---- end of item: per-head sums over the 128 tokens, then normalise O^T and write it.
       const int ob = item_n & 1;
       {
@@ -862,7 +900,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         const float ls = reduce_scatter<false, HH>(v, lane);
         if (lane < HH) lpart[quarter * HN + h0 + lane] = ls;
       }
-      named_barrier_sync(kSoftBar, kSoftThreads);
+      if (bar_red_or(kSoftBar, kSoftThreads, !ok)) break;
       // The item's G output rows and G log-sum-exps are contiguous in memory: both go
       // out as bulk copies from shared memory (O^T normalised into the P^T buffers,
       // which no MMA reads before this warpgroup writes the next item's first P^T;
@@ -888,9 +926,9 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         }
       }
       named_barrier_sync(kSoftBar, kSoftThreads);
-      if (!mbar_wait_abortable(&o_full[ob], (item_n >> 1) & 1, abort_flag)) break;
-      tc_fence_after();
+      ok = mbar_wait_abortable(&o_full[ob], (item_n >> 1) & 1, wctl);
       {
+        tc_fence_after();
         uint32_t o[HH];
         const uint32_t oc = tmem + t_lane + kColO + ob * HN + h0;
         if constexpr (HH == 32) tmem_ld_32x32b_x32(oc, o);
@@ -904,7 +942,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[ob]);
-      named_barrier_sync(kSoftBar, kSoftThreads);
+      if (bar_red_or(kSoftBar, kSoftThreads, !ok)) break;
       if (sw == 0 && lane == 0) {
         bulk_s2g(dst_o, pt, (uint32_t)G * kHeadDim * 4);
         if (bulk_lse) bulk_s2g(dst_lse, lse_stage, (uint32_t)G * 4);

@@ -51,9 +51,9 @@ constexpr int kOffK = kOffQ + kQT * kRows * kHeadDim * 2;   // K[kStages]
 constexpr int kVSlotBytes = kTileBytes + kKeys * 4;          // V (scaled), K scales
 constexpr int kOffV = kOffK + kStages * kTileBytes;          // V[kStages]
 constexpr int kOffBars = kOffV + kStages * kVSlotBytes;
-constexpr int kNumBars = 4 * kStages + 6 * kQT;
+constexpr int kNumBars = 4 * kStages + 6 * kQT + 1;  // ... and the MMA issuer's last commit
 constexpr int kOffMisc = kOffBars + 8 * kNumBars;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr int kSmemBytes = kOffMisc + 24 + 1024;  // tmem slot, wait state (+8); alignment slack
 // Warpgroup 0: K/V producer (warp 0), MMA issuer (warp 1), two spare warps;
 // warpgroups 1 and 2: the softmax of q-tile 0 and q-tile 1.  The block is
 // launched with 168 registers per thread (384 threads; 3 warps x 32 x 168 =
@@ -83,6 +83,8 @@ struct PrefillParams {
   // writes its normalised partial output and log2-sum-exp to piece_o / piece_lse
   // ([t][256 rows][128] and [t][256]); combine_pieces_kernel merges them.
   int32_t full_items, pieces, num_items;
+  uint64_t wait_ns;  // limit of every bounded wait inside the kernel
+  int32_t drop_stage;  // fault injection: K tile each CTA skips (-1: none)
   int32_t skip_single;  // see PrefillLaunch
   float* piece_o;
   float* piece_lse;
@@ -263,7 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   uint64_t* o_full = pv_done + kQT;            // [kQT] MMA commit after an item's last PV
   uint64_t* o_empty = o_full + kQT;            // [kQT] softmax -> MMA after reading O (4 warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kOffMisc + 4);
+  volatile WaitState* const wctl = reinterpret_cast<volatile WaitState*>(smem + kOffMisc + 8);
+  volatile int32_t* abort_flag = &wctl->abort;
+  uint64_t* mma_drain = o_empty + kQT;         // the MMA issuer's last commit, at exit
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_heads;
@@ -285,7 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       mbar_init(&o_full[q], 1);
       mbar_init(&o_empty[q], 4);
     }
+    mbar_init(mma_drain, 1);
     *abort_flag = 0;
+    wctl->limit_ns = p.wait_ns;
     fence_barrier_init();
   }
   tc_fence_before();
@@ -298,23 +304,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
    if (warp == 0) {
     // ------------------------------------------------------------ K/V producer
     if (lane == 0) {
-      int g = 0;
+      int g = 0, gk = 0, gv = 0;  // tiles; tiles whose K and V loads were issued (or dropped)
       for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
         const PItem it = prefill_item(p, idx);
         const int64_t seq_row0 = (int64_t)it.b * p.kt_rows;
         for (int j = 0; j < it.nkt; ++j, ++g) {
           const int s = g % kStages;
           const int64_t row = seq_row0 + (int64_t)(it.kt0 + j) * kKeys;
-          if (g >= kStages && !mbar_wait_abortable(&k_empty[s], ((g / kStages) - 1) & 1, abort_flag)) break;
-          mbar_arrive_expect_tx(&k_full[s], kTileBytes);
-          tma_load_rows128(smem + kOffK + s * kTileBytes, &kmap, (int)row, &k_full[s]);
-          if (g >= kStages && !mbar_wait_abortable(&v_empty[s], ((g / kStages) - 1) & 1, abort_flag)) break;
+          if (g >= kStages && !mbar_wait_abortable(&k_empty[s], ((g / kStages) - 1) & 1, wctl)) break;
+          if (g != p.drop_stage) {  // (fault injection: that K tile is never loaded)
+            mbar_arrive_expect_tx(&k_full[s], kTileBytes);
+            tma_load_rows128(smem + kOffK + s * kTileBytes, &kmap, (int)row, &k_full[s]);
+          }
+          gk = g + 1;
+          if (g >= kStages && !mbar_wait_abortable(&v_empty[s], ((g / kStages) - 1) & 1, wctl)) break;
           uint8_t* vs = smem + kOffV + s * kVSlotBytes;
           mbar_arrive_expect_tx(&v_full[s], kVSlotBytes);
           tma_load_rows128(vs, &vmap, (int)row, &v_full[s]);
           bulk_g2s(vs + kTileBytes, p.ks + row, kKeys * 4, &v_full[s]);
+          gv = g + 1;
         }
       }
+      // Every slot this producer armed has landed before the CTA goes away, whatever
+      // happened to the other roles (copies into a CTA's shared memory must not outlive it).
+      for (int i = gk > kStages ? gk - kStages : 0; i < gk; ++i)
+        if (i != p.drop_stage) mbar_wait_drain(&k_full[i % kStages], (i / kStages) & 1);
+      for (int i = gv > kStages ? gv - kStages : 0; i < gv; ++i) mbar_wait_drain(&v_full[i % kStages], (i / kStages) & 1);
     }
    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -343,11 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
         const PItem it = prefill_item(p, idx);
         if (!it.ok || it.nkt == 0) continue;  // no MMA work; the softmax groups write its zeros
-        bool ok = mbar_wait_abortable(&q_full[0], n & 1, abort_flag) && mbar_wait_abortable(&q_full[1], n & 1, abort_flag);
+        bool ok = mbar_wait_abortable(&q_full[0], n & 1, wctl) && mbar_wait_abortable(&q_full[1], n & 1, wctl);
         for (int j = 0; j < it.nkt && ok; ++j, ++g) {
           const int s = g % kStages;
           if (j == 0) {
-            if (!mbar_wait_abortable(&k_full[s], (g / kStages) & 1, abort_flag)) break;
+            if (!mbar_wait_abortable(&k_full[s], (g / kStages) & 1, wctl)) break;
             tc_fence_after();
             issue_s(0, g);
             issue_s(1, g);
@@ -355,15 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
           }
           const bool more = j + 1 < it.nkt;
           for (int q = 0; q < kQT; ++q) {
-            if (!mbar_wait_abortable(&p_full[q], g & 1, abort_flag)) {
+            if (!mbar_wait_abortable(&p_full[q], g & 1, wctl)) {
               ok = false;
               break;
             }
-            if (j == 0 && n > 0 && !mbar_wait_abortable(&o_empty[q], (n - 1) & 1, abort_flag)) {
+            if (j == 0 && n > 0 && !mbar_wait_abortable(&o_empty[q], (n - 1) & 1, wctl)) {
               ok = false;
               break;
             }
-            if (q == 0 && !mbar_wait_abortable(&v_full[s], (g / kStages) & 1, abort_flag)) {
+            if (q == 0 && !mbar_wait_abortable(&v_full[s], (g / kStages) & 1, wctl)) {
               ok = false;
               break;
             }
@@ -372,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
             if (q == kQT - 1) mma_commit(&v_empty[s]);
             if (!more) mma_commit(&o_full[q]);
             if (more) {
-              if (q == 0 && !mbar_wait_abortable(&k_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag)) {
+              if (q == 0 && !mbar_wait_abortable(&k_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, wctl)) {
                 ok = false;
                 break;
               }
@@ -385,6 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         if (!ok) break;
         ++n;
       }
+      // The issued MMAs have completed before tensor memory is freed.
+      mma_commit(mma_drain);
+      mbar_wait_drain(mma_drain, 0);
     }
    }
   } else {
@@ -396,8 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
     const uint32_t scol = (uint32_t)q * 256, ocol = scol + 128;
     uint8_t* qs = smem + kOffQ + q * kRows * kHeadDim * 2;
+    // Each warp decides alone (its waits and its abort reads agree in all lanes); the
+    // warps of a group meet only at mbarriers, so one that stops early strands nobody.
     int g = 0, n = 0;
-    for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
+    for (int idx = blockIdx.x; idx < num_items && !abort_seen_warp(wctl); idx += gridDim.x) {
       const PItem it = prefill_item(p, idx);
       const int64_t row = it.row0 + q * kRows + r;  // (token, head) row within the sequence
       const bool my_row = row < it.rows;
@@ -437,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       bool ok = true;
       for (int j = 0; j < it.nkt; ++j, ++g) {
         const int s = g % kStages;
-        ok = mbar_wait_abortable(&s_full[q], g & 1, abort_flag) &&
-             mbar_wait_abortable(&v_full[s], (g / kStages) & 1, abort_flag);
+        ok = mbar_wait_warp(&s_full[q], g & 1, wctl) &&
+             mbar_wait_warp(&v_full[s], (g / kStages) & 1, wctl);
         if (!ok) break;
         tc_fence_after();
         const float* kscale = reinterpret_cast<const float*>(smem + kOffV + s * kVSlotBytes + kTileBytes);
@@ -480,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         const bool raise = m_ref == -INFINITY ? mx > -INFINITY : mx > kRescaleThreshold;
         const float alpha = raise ? ex2_approx(m_ref - (m_use + mx)) : 1.0f;  // 0 when there was no reference
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
-          ok = mbar_wait_abortable(&pv_done[q], (g - 1) & 1, abort_flag);
+          ok = mbar_wait_warp(&pv_done[q], (g - 1) & 1, wctl);
           if (ok) {
             tc_fence_after();
 #pragma unroll
@@ -526,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         if (!ok) break;
       }
       if (!ok) break;
-      if (!mbar_wait_abortable(&o_full[q], n & 1, abort_flag)) break;
+      if (!mbar_wait_warp(&o_full[q], n & 1, wctl)) break;
       tc_fence_after();
       const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
       float* dst = part_row ? part_row : out_row;
@@ -663,6 +683,8 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.kt_rows = (int32_t)(((int64_t)L.max_pages * L.page_size + kKeys - 1) / kKeys * kKeys);
   p.pairs = (int32_t)(((int64_t)L.n_new * L.num_heads + kQT * kRows - 1) / (kQT * kRows));
   p.scale_log2 = L.scale_log2;
+  p.wait_ns = wait_limit_ns();
+  p.drop_stage = fault_drop_stage();
   const int64_t rows = (int64_t)L.batch * p.kt_rows;
   const int64_t a = ((rows * kHeadDim * 2 + 255) / 256) * 256;
   uint8_t* ws = static_cast<uint8_t*>(L.workspace);

@@ -62,24 +62,67 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s by default: far beyond any legitimate wait
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // 200 ms: waits for a CTA's own copies and MMAs at exit
 
 // Wait with a time limit shared by a whole CTA: once any wait of the CTA has
-// given up (or *abort is set) every later wait returns false at once, so a
-// broken hand-off ends the kernel within seconds instead of hanging it.
+// given up (or *abort is set) every later wait that is not already satisfied
+// returns false, so a broken hand-off ends the kernel within seconds instead of
+// hanging it.  The limit is a launch parameter (cai_set_wait_limit_ns), so a test
+// can make the waits run out.
+//
+// The answer is per thread.  Giving up must never split a group of threads that
+// meets again at a collective step (a shuffle, a vote, a .sync.aligned
+// tensor-memory access, a named barrier): the threads that carried on would wait
+// there forever for those that left.  So either the threads of a warp agree right
+// away (mbar_wait_warp, abort_seen_warp), or their control flow does not depend on
+// the answer until a collective step that already exists makes it one answer; in
+// between, a thread acts on its own answer only for what it does alone (a release,
+// a store).  A thread that saw the phase complete may always act: the phase stays
+// complete until the waiting warp itself takes its next step.
 constexpr uint32_t kSuspendHintNs = 1000000;  // 1 ms: longest single suspension of a waiting thread
 
-__device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
+// A CTA's wait state, in its shared memory (8-byte aligned): read only once a wait
+// has not been satisfied by its first try, so the limit occupies no register.
+struct WaitState {
+  int32_t abort;      // set by the first wait of the CTA that gives up
+  int32_t pad;
+  uint64_t limit_ns;  // the launch's wait limit
+};
+
+// The state is read only after a suspension that the phase did not end, so a wait
+// of ordinary length touches nothing but its barrier (the limit is therefore
+// checked at suspension granularity: a limit below 1 ms acts as about 1 ms).
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t parity, volatile WaitState* w) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
+    if (w->abort) return false;
+    if (globaltimer_ns() - t0 > w->limit_ns) {
+      w->abort = 1;
       return false;
     }
   }
+}
+
+// The same wait made by all 32 lanes of a warp: true in every lane only if it held in
+// every lane.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile WaitState* w) {
+  return __all_sync(0xffffffffu, mbar_wait_abortable(bar, parity, w));
+}
+
+// The abort flag as one answer for a whole warp (lanes may read it at different times).
+__device__ __forceinline__ bool abort_seen_warp(volatile WaitState* w) { return __any_sync(0xffffffffu, w->abort != 0); }
+
+// At a CTA's exit: wait for the completion of its own asynchronous copies or MMAs
+// (which always complete), whatever the abort state, with a fixed limit.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 <= kDrainLimitNs)
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+  return false;
 }
 
 // Programmatic dependent launch: wait until the grids this one depends on have
