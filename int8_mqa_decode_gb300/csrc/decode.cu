@@ -479,31 +479,32 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
           }
           for (int hf = 0; hf < 2; ++hf, ++r) {
             const int s = r % NST;
-            // Lane 31 (never a page lane) carries into the ballot whether it saw the
-            // converters release the stage: the stage is armed only then, by every lane.
-            const bool free = r < NST || mbar_wait_abortable(&raw_empty[s], ((r / NST) - 1) & 1, wctl);
-            const int32_t pid = __shfl_sync(0xffffffffu, ids, (t % TPB) * PPT + hf * SPS + lane % SPS);
-            const bool live = lane < SPS && pid != kNoPage;
-            const bool in_range = pid >= 0 && pid < slot_pages;
-            const uint32_t vote = __ballot_sync(0xffffffffu, lane == 31 ? free : (live && in_range));
-            if (!(vote >> 31)) {
+            // The warp reaches the wait converged (nothing in this loop branches on the
+            // lane: the copies below are predicated), so its one wait instruction stream
+            // gives every lane the same answer and the lanes leave together.  (A
+            // collective step right after this wait, to agree explicitly, costs about
+            // 5% of the decode: the stage turnaround is on the critical path.)
+            if (r >= NST && !mbar_wait_abortable(&raw_empty[s], ((r / NST) - 1) & 1, wctl)) {
               ok = false;
               break;
             }
+            const int32_t pid = __shfl_sync(0xffffffffu, ids, (t % TPB) * PPT + hf * SPS + lane % SPS);
+            const bool live = lane < SPS && pid != kNoPage;
+            const bool in_range = pid >= 0 && pid < slot_pages;
             if (live && !in_range) set_err(p.err, CAI_DEVERR_PAGE);
-            const uint32_t okm = vote & 0x7fffffffu;
-            if (r == p.drop_stage) continue;  // fault injection: this stage is never loaded
+            const uint32_t okm = __ballot_sync(0xffffffffu, live && in_range);
             if (lane == 0) {
               page_ok[s] = okm;
-              mbar_arrive_expect_tx(&raw_full[s], (uint32_t)__popc(okm) * page_bytes(P));
+              // (Fault injection: the dropped stage expects 16 bytes that never come.)
+              mbar_arrive_expect_tx(&raw_full[s], (uint32_t)__popc(okm) * page_bytes(P) + (r == p.drop_stage ? 16u : 0u));
             }
             __syncwarp();
-            if ((okm >> lane) & 1u) {
-              tma_load_2d_hint(raw_kv + s * kStageKV + lane * (2 * P * kHeadDim), kv_map, 0, pid * kRowsPerPage,
-                               &raw_full[s], policy);
-              bulk_g2s_hint(raw_sc + s * kStageSc + lane * (8 * P), pages + (int64_t)pid * page_bytes(P) + 2 * P * kHeadDim,
-                            8 * P, &raw_full[s], policy);
-            }
+            const bool mine = (okm >> lane) & 1u;
+            const int32_t pg = mine ? pid : 0;
+            tma_load_2d_hint_if(mine, raw_kv + s * kStageKV + lane * (2 * P * kHeadDim), kv_map, 0, pg * kRowsPerPage,
+                                &raw_full[s], policy);
+            bulk_g2s_hint_if(mine, raw_sc + s * kStageSc + lane * (8 * P), pages + (int64_t)pg * page_bytes(P) + 2 * P * kHeadDim,
+                             8 * P, &raw_full[s], policy);
           }
         }
         if (!ok) break;

@@ -176,6 +176,26 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst_smem, const void* map
       : "memory");
 }
 
+// The same two copies, issued only where `on` holds, as predicated instructions: a
+// warp issuing them from some lanes does not branch (it stays converged).
+__device__ __forceinline__ void bulk_g2s_hint_if(bool on, void* dst_smem, const void* src_gmem, uint32_t bytes,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %5, 0;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n\t}"
+      ::"r"(smem_addr(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy), "r"((uint32_t)on)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_hint_if(bool on, void* dst_smem, const void* map, int x, int y,
+                                                    uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+      "@p cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;\n\t}" ::"r"(smem_addr(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy), "r"((uint32_t)on)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
