@@ -31,32 +31,38 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
-#include "tma.cuh"
 #include "ptx.cuh"
 
 namespace cai {
 namespace {
 
 constexpr int kRows = 128;                 // query rows per q-tile (MMA M)
-constexpr int kQT = 2;                     // q-tiles per CTA sharing each K/V tile
+constexpr int kQT = 1;                     // q-tiles per work item
 constexpr int kKeys = 128;                 // keys per tile (MMA N of S, K of PV)
 constexpr int kTileBytes = kKeys * kHeadDim * 2;  // 32 KB of 16-bit values
-constexpr int kStages = 2;
-constexpr int kOffQ = 0;                                     // Q[kQT]
-// K tiles and V tiles (with the tile's K scales) have separate two-slot rings: a K
-// slot is free as soon as both q-tiles' S = Q K^T have run, so the next K tile loads
-// while the softmax of this one runs; a V slot (and its scales, which the softmax
-// reads) is free after both PVs.
-constexpr int kOffK = kOffQ + kQT * kRows * kHeadDim * 2;   // K[kStages]
+constexpr int kStagesK = 2;                // K tile slots
+constexpr int kStagesV = 3;                // V tile slots (with the tile's K scales, which the softmax reads)
+constexpr int kSBuf = 2;                   // S buffers in tensor memory
+constexpr int kOffQ = 0;                                     // Q
+// K tiles and V tiles (with the tile's K scales) have separate rings: a K slot is
+// free as soon as S = Q K^T of its tile has run, so the next K tiles load ahead of
+// the softmax; a V slot (and its scales, which the softmax of its tile reads first)
+// is free after its PV, so the V ring is one slot deeper.
+constexpr int kOffK = kOffQ + kQT * kRows * kHeadDim * 2;   // K[kStagesK]
 constexpr int kVSlotBytes = kTileBytes + kKeys * 4;          // V (scaled), K scales
-constexpr int kOffV = kOffK + kStages * kTileBytes;          // V[kStages]
-constexpr int kOffBars = kOffV + kStages * kVSlotBytes;
-constexpr int kNumBars = 4 * kStages + 6 * kQT + 1;  // ... and the MMA issuer's last commit
+constexpr int kOffV = kOffK + kStagesK * kTileBytes;         // V[kStagesV]
+constexpr int kOffXch = kOffV + kStagesV * kVSlotBytes;      // softmax exchange: row references, row sums [2][128] each
+constexpr int kOffBars = kOffXch + 4 * kRows * 4;
+// k_full, k_empty [kStagesK]; v_full, v_empty [kStagesV]; q_full; s_full, pv_done
+// [kSBuf] (one per S buffer); p_full [2 key halves][kSBuf]; o_full, o_empty; the MMA
+// issuers' last commits.
+constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 1 + 4 * kSBuf + 2 + 1;
 constexpr int kOffMisc = kOffBars + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 24 + 1024;  // tmem slot, wait state (+8); alignment slack
-// Warpgroup 0: K/V producer (warp 0), MMA issuer (warp 1), two spare warps;
-// warpgroups 1 and 2: the softmax of q-tile 0 and q-tile 1.  The block is
-// launched with 168 registers per thread (384 threads; 3 warps x 32 x 168 =
+static_assert(kOffXch % 16 == 0 && kOffBars % 8 == 0, "shared-memory layout");
+// Warpgroup 0: K/V producer (warp 0), S issuer (warp 1), PV issuer (warp 2), a spare warp;
+// warpgroups 1 and 2: the softmax, key half 0 and key half 1 of every row.  The block
+// is launched with 168 registers per thread (384 threads; 3 warps x 32 x 168 =
 // 16128 of a sub-partition's 16384), then warpgroup 0 shrinks to 72 and the
 // softmax groups grow to 216: 128 * (72 + 216 + 216) = 64512 = 384 * 168, so
 // the growth is covered exactly by what warpgroup 0 gives back.  The host
@@ -65,7 +71,7 @@ constexpr int kThreads = 384;
 constexpr int kRegsCtl = 72, kRegsSoft = 216;
 constexpr int kRegsLaunch = 168;
 static_assert(kRegsCtl * 128 + kRegsSoft * 256 <= kRegsLaunch * kThreads, "register split");
-constexpr uint32_t kTmemCols = 512;        // per q-tile: S (128 columns, P over its first 64) + O (128)
+constexpr uint32_t kTmemCols = 512;        // S[2] (128 columns; P over half of each key half), O[2] (one per key half)
 constexpr float kRescaleThreshold = 8.0f;
 
 struct PrefillParams {
@@ -174,19 +180,14 @@ __global__ void __launch_bounds__(256) dequant_kernel(const PrefillParams p) {
       const __half hv = __float2half_rn(vf * vsc);  // V scale applied here: P needs no per-key factor
       vh[e] = *reinterpret_cast<const uint16_t*>(&hv);
     }
-    const int64_t off = row * kHeadDim + lane * 4;
+    // Stored tile by tile in the MMA operand layout (element (key r, channel d) of a
+    // 128-key tile at (d / 8) * 1024 + r * 8 + d % 8), so the attention kernel moves a
+    // tile with one contiguous 32 KB bulk copy.
+    const int64_t off = ((int64_t)b * p.kt_rows + tile * kKeys) * kHeadDim + (lane >> 1) * 1024 + rr * 8 + (lane & 1) * 4;
     *reinterpret_cast<uint2*>(p.kb + off) = make_uint2(kb[0] | ((uint32_t)kb[1] << 16), kb[2] | ((uint32_t)kb[3] << 16));
     *reinterpret_cast<uint2*>(p.vh + off) = make_uint2(vh[0] | ((uint32_t)vh[1] << 16), vh[2] | ((uint32_t)vh[3] << 16));
     if (lane == 0) p.ks[row] = ksc;
   }
-}
-
-__device__ __forceinline__ void tma_load_rows128(void* dst, const CUtensorMap* map, int row, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(0), "r"(smem_addr(bar))
-      : "memory");
 }
 
 // One work item: a pair of q-tiles (256 consecutive (token, head) rows) of one
@@ -242,54 +243,62 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
 // writes.  As a K-major operand: LBO = 2048 (next 8 k), SBO = 128 (next 8 rows).
 // As an MN-major operand (rows = K, k = N): LBO = 128, SBO = 2048.
 //
-// Persistent CTAs, one per SM, each taking pairs of q-tiles in turn.  Roles:
-// warp 0 loads K/V tiles (TMA tensor copies) into a 2-stage ring; warp 1
-// issues the MMAs in the order S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) ...
-// so that each softmax group works on one tile while the tensor core runs the
-// other group's MMAs; warps 2-5 and 6-9 run the softmax of q-tile 0 and 1 (one
-// thread per row) and write the outputs.
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParams p,
-                                                              const __grid_constant__ CUtensorMap kmap,
-                                                              const __grid_constant__ CUtensorMap vmap) {
+// Persistent CTAs, one per SM, each taking q-tiles in turn.  Roles: warp 0 loads
+// K/V tiles (TMA tensor copies) into 2-slot K and V rings; warp 1 issues
+// S(g) = Q K(g)^T into S buffer g % 2 as soon as K(g) is loaded and PV(g - 2) has
+// consumed the P that buffer held, so S of the next tile runs while the softmax
+// of this one does; warp 2 issues O += P(g) V(g); warps 4-7 and 8-11 run the
+// softmax of key half 0 and key half 1 of every row (thread = row, 64 keys per
+// tile each), the halves agreeing on the row's reference through shared memory
+// when a raise is due, and write the outputs (channel half each).
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* k_full = bars;                     // [kStages] producer -> MMA (tx bytes)
-  uint64_t* k_empty = bars + kStages;          // [kStages] MMA commit after both S of the tile
-  uint64_t* v_full = bars + 2 * kStages;       // [kStages] producer -> MMA, softmax (V and K scales)
-  uint64_t* v_empty = bars + 3 * kStages;      // [kStages] MMA commit after both PVs of the tile
-  uint64_t* q_full = bars + 4 * kStages;       // [kQT] softmax group -> MMA (4 warps)
-  uint64_t* s_full = q_full + kQT;             // [kQT] MMA commit after S
-  uint64_t* p_full = s_full + kQT;             // [kQT] softmax -> MMA (4 warps)
-  uint64_t* pv_done = p_full + kQT;            // [kQT] MMA commit after PV
-  uint64_t* o_full = pv_done + kQT;            // [kQT] MMA commit after an item's last PV
-  uint64_t* o_empty = o_full + kQT;            // [kQT] softmax -> MMA after reading O (4 warps)
+  uint64_t* k_full = bars;                     // [kStagesK] producer -> S issuer (tx bytes)
+  uint64_t* k_empty = k_full + kStagesK;       // [kStagesK] S issuer commit after S of the tile
+  uint64_t* v_full = k_empty + kStagesK;       // [kStagesV] producer -> PV issuer, softmax (V and K scales)
+  uint64_t* v_empty = v_full + kStagesV;       // [kStagesV] PV issuer commit after PV of the tile
+  uint64_t* q_full = v_empty + kStagesV;       // softmax -> S issuer (8 warps)
+  uint64_t* s_full = q_full + 1;               // [kSBuf] S issuer commit after S into buffer b
+  uint64_t* p_full = s_full + kSBuf;           // [2][kSBuf] softmax half h -> PV issuer (4 warps): P in buffer b
+  uint64_t* pv_done = p_full + 2 * kSBuf;      // [kSBuf] PV issuer commit after both PVs reading buffer b
+  uint64_t* o_full = pv_done + kSBuf;          // PV issuer commit after an item's last PVs
+  uint64_t* o_empty = o_full + 1;              // softmax -> PV issuer after reading O (8 warps)
+  uint64_t* mma_drain = o_empty + 1;           // the MMA issuers' last commits, at exit
+  float* xref = reinterpret_cast<float*>(smem + kOffXch);  // [2 halves][128 rows] half-row references
+  float* xsum = xref + 2 * kRows;                          // [2 halves][128 rows] half-row sums
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile WaitState* const wctl = reinterpret_cast<volatile WaitState*>(smem + kOffMisc + 8);
   volatile int32_t* abort_flag = &wctl->abort;
-  uint64_t* mma_drain = o_empty + kQT;         // the MMA issuer's last commit, at exit
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_heads;
   const int num_items = p.num_items;
+  constexpr uint32_t kColO = kSBuf * 128;  // O of key half h at kColO + h * 128; S buffer b at b * 128
+  constexpr uint32_t kSoftBar = 1;
+  constexpr uint32_t kSoftThreads = 256;
 
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kStagesK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kStagesV; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int q = 0; q < kQT; ++q) {
-      mbar_init(&q_full[q], 4);
-      mbar_init(&s_full[q], 1);
-      mbar_init(&p_full[q], 4);
-      mbar_init(&pv_done[q], 1);
-      mbar_init(&o_full[q], 1);
-      mbar_init(&o_empty[q], 4);
+    mbar_init(q_full, 8);
+    for (int b = 0; b < kSBuf; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&p_full[kSBuf + b], 4);
+      mbar_init(&pv_done[b], 1);
     }
-    mbar_init(mma_drain, 1);
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, 8);
+    mbar_init(mma_drain, 2);
     *abort_flag = 0;
     wctl->limit_ns = p.wait_ns;
     fence_barrier_init();
@@ -309,269 +318,274 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         const PItem it = prefill_item(p, idx);
         const int64_t seq_row0 = (int64_t)it.b * p.kt_rows;
         for (int j = 0; j < it.nkt; ++j, ++g) {
-          const int s = g % kStages;
+          const int sk = g % kStagesK, sv = g % kStagesV;
           const int64_t row = seq_row0 + (int64_t)(it.kt0 + j) * kKeys;
-          if (g >= kStages && !mbar_wait_abortable(&k_empty[s], ((g / kStages) - 1) & 1, wctl)) break;
+          if (g >= kStagesK && !mbar_wait_abortable(&k_empty[sk], ((g / kStagesK) - 1) & 1, wctl)) break;
           if (g != p.drop_stage) {  // (fault injection: that K tile is never loaded)
-            mbar_arrive_expect_tx(&k_full[s], kTileBytes);
-            tma_load_rows128(smem + kOffK + s * kTileBytes, &kmap, (int)row, &k_full[s]);
+            mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
+            bulk_g2s(smem + kOffK + sk * kTileBytes, p.kb + row * kHeadDim, kTileBytes, &k_full[sk]);
           }
           gk = g + 1;
-          if (g >= kStages && !mbar_wait_abortable(&v_empty[s], ((g / kStages) - 1) & 1, wctl)) break;
-          uint8_t* vs = smem + kOffV + s * kVSlotBytes;
-          mbar_arrive_expect_tx(&v_full[s], kVSlotBytes);
-          tma_load_rows128(vs, &vmap, (int)row, &v_full[s]);
-          bulk_g2s(vs + kTileBytes, p.ks + row, kKeys * 4, &v_full[s]);
+          if (g >= kStagesV && !mbar_wait_abortable(&v_empty[sv], ((g / kStagesV) - 1) & 1, wctl)) break;
+          uint8_t* vs = smem + kOffV + sv * kVSlotBytes;
+          mbar_arrive_expect_tx(&v_full[sv], kVSlotBytes);
+          bulk_g2s(vs, p.vh + row * kHeadDim, kTileBytes, &v_full[sv]);
+          bulk_g2s(vs + kTileBytes, p.ks + row, kKeys * 4, &v_full[sv]);
           gv = g + 1;
         }
       }
       // Every slot this producer armed has landed before the CTA goes away, whatever
       // happened to the other roles (copies into a CTA's shared memory must not outlive it).
-      for (int i = gk > kStages ? gk - kStages : 0; i < gk; ++i)
-        if (i != p.drop_stage) mbar_wait_drain(&k_full[i % kStages], (i / kStages) & 1);
-      for (int i = gv > kStages ? gv - kStages : 0; i < gv; ++i) mbar_wait_drain(&v_full[i % kStages], (i / kStages) & 1);
+      for (int i = gk > kStagesK ? gk - kStagesK : 0; i < gk; ++i)
+        if (i != p.drop_stage) mbar_wait_drain(&k_full[i % kStagesK], (i / kStagesK) & 1);
+      for (int i = gv > kStagesV ? gv - kStagesV : 0; i < gv; ++i) mbar_wait_drain(&v_full[i % kStagesV], (i / kStagesV) & 1);
     }
-   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+   } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues S = Q K^T, warp 2 issues O += P V: one thread issues a
+    // 128 x 128 x 16 MMA only about every 115 cycles (measured; the tensor core takes
+    // about 64), so the two streams go out from two threads.  Their MMAs are not
+    // ordered with each other: S(g) overwrites buffer g % 2, whose P the PVs of tile
+    // g - 2 read, so it waits for them.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0, 0);
       constexpr uint32_t idesc_o = idesc_f16_f32(kRows, kHeadDim, 0, 1);
-      const uint32_t qa0 = smem_addr(smem + kOffQ);
+      const bool s_issuer = warp == 1;
+      // Descriptor bases; a K step adds 4096 bytes (S operands) or 256 bytes (V),
+      // i.e. 256 or 16 to the address field (shared addresses stay below 2^18).
+      const uint64_t dq = smem_desc(smem_addr(smem + kOffQ), 2048, 128);
+      const uint64_t dk0 = smem_desc(smem_addr(smem + kOffK), 2048, 128);
+      const uint64_t dv0 = smem_desc(smem_addr(smem + kOffV), 128, 2048);
       int g = 0, n = 0;
-      auto issue_s = [&](int q, int gg) {
-        const uint32_t ka = smem_addr(smem + kOffK + (gg % kStages) * kTileBytes);
-        const uint32_t qa = qa0 + q * kRows * kHeadDim * 2;
-#pragma unroll
-        for (int ks = 0; ks < kHeadDim / 16; ++ks)
-          mma_f16_ss(tmem + q * 256, smem_desc(qa + ks * 4096, 2048, 128), smem_desc(ka + ks * 4096, 2048, 128),
-                     idesc_s, ks > 0);
-        mma_commit(&s_full[q]);
-      };
-      auto issue_pv = [&](int q, int gg, bool first) {
-        const uint32_t va = smem_addr(smem + kOffV + (gg % kStages) * kVSlotBytes);
-#pragma unroll
-        for (int ks = 0; ks < kKeys / 16; ++ks)
-          mma_f16_ts(tmem + q * 256 + 128, tmem + q * 256 + ks * 8, smem_desc(va + ks * 256, 128, 2048), idesc_o,
-                     (!first || ks > 0) ? 1u : 0u);
-        mma_commit(&pv_done[q]);
-      };
-      for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < num_items && ok && !*abort_flag; idx += gridDim.x) {
         const PItem it = prefill_item(p, idx);
-        if (!it.ok || it.nkt == 0) continue;  // no MMA work; the softmax groups write its zeros
-        bool ok = mbar_wait_abortable(&q_full[0], n & 1, wctl) && mbar_wait_abortable(&q_full[1], n & 1, wctl);
+        if (!it.ok || it.nkt == 0) continue;  // no MMA work; the softmax writes its zeros
+        if (s_issuer) ok = mbar_wait_abortable(q_full, n & 1, wctl);
         for (int j = 0; j < it.nkt && ok; ++j, ++g) {
-          const int s = g % kStages;
-          if (j == 0) {
-            if (!mbar_wait_abortable(&k_full[s], (g / kStages) & 1, wctl)) break;
+          const int sk = g % kStagesK, sv = g % kStagesV, b = g % kSBuf;
+          if (s_issuer) {
+            ok = mbar_wait_abortable(&k_full[sk], (g / kStagesK) & 1, wctl) &&
+                 (g < kSBuf || mbar_wait_abortable(&pv_done[b], ((g / kSBuf) - 1) & 1, wctl));
+            if (!ok) break;
             tc_fence_after();
-            issue_s(0, g);
-            issue_s(1, g);
-            mma_commit(&k_empty[s]);
-          }
-          const bool more = j + 1 < it.nkt;
-          for (int q = 0; q < kQT; ++q) {
-            if (!mbar_wait_abortable(&p_full[q], g & 1, wctl)) {
-              ok = false;
-              break;
-            }
-            if (j == 0 && n > 0 && !mbar_wait_abortable(&o_empty[q], (n - 1) & 1, wctl)) {
-              ok = false;
-              break;
-            }
-            if (q == 0 && !mbar_wait_abortable(&v_full[s], (g / kStages) & 1, wctl)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_pv(q, g, j == 0);
-            if (q == kQT - 1) mma_commit(&v_empty[s]);
-            if (!more) mma_commit(&o_full[q]);
-            if (more) {
-              if (q == 0 && !mbar_wait_abortable(&k_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, wctl)) {
-                ok = false;
-                break;
-              }
+            const uint64_t dk = dk0 + (uint64_t)(sk * (kTileBytes / 16));
+#pragma unroll
+            for (int ks = 0; ks < kHeadDim / 16; ++ks)
+              mma_f16_ss(tmem + b * 128, dq + (uint64_t)(ks * 256), dk + (uint64_t)(ks * 256), idesc_s, ks > 0);
+            mma_commit(&s_full[b]);
+            mma_commit(&k_empty[sk]);
+          } else {
+            ok = (j > 0 || n == 0 || mbar_wait_abortable(o_empty, (n - 1) & 1, wctl)) &&
+                 mbar_wait_abortable(&v_full[sv], (g / kStagesV) & 1, wctl);
+            const uint64_t dv = dv0 + (uint64_t)(sv * (kVSlotBytes / 16));
+            // Key half h: O_h += P_h V_h, P_h in the first 32 columns of the half's 64.
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+              ok = mbar_wait_abortable(&p_full[hh * kSBuf + b], (g / kSBuf) & 1, wctl);
+              if (!ok) break;
               tc_fence_after();
-              issue_s(q, g + 1);
-              if (q == kQT - 1) mma_commit(&k_empty[(g + 1) % kStages]);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                mma_f16_ts(tmem + kColO + hh * 128, tmem + b * 128 + hh * 64 + ks * 8,
+                           dv + (uint64_t)((hh * 4 + ks) * 16), idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
             }
+            if (!ok) break;
+            mma_commit(&pv_done[b]);
+            mma_commit(&v_empty[sv]);
+            if (j == it.nkt - 1) mma_commit(o_full);
           }
         }
-        if (!ok) break;
         ++n;
       }
-      // The issued MMAs have completed before tensor memory is freed.
+      // This issuer's MMAs have completed before tensor memory is freed.
       mma_commit(mma_drain);
       mbar_wait_drain(mma_drain, 0);
     }
    }
   } else {
     setmaxnreg_inc<kRegsSoft>();
-    // ------------------------------------------------------------ softmax groups
-    const int q = (warp - 4) >> 2;          // q-tile of this group
+    // ------------------------------------------------------------ softmax
+    const int h = (warp - 4) >> 2;          // key half of every tile, channel half of the output
     const int quarter = warp & 3;           // TMEM lane quarter
     const int r = quarter * 32 + lane;      // row within the q-tile
     const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
-    const uint32_t scol = (uint32_t)q * 256, ocol = scol + 128;
-    uint8_t* qs = smem + kOffQ + q * kRows * kHeadDim * 2;
-    // Each warp decides alone (its waits and its abort reads agree in all lanes); the
-    // warps of a group meet only at mbarriers, so one that stops early strands nobody.
+    uint8_t* qs = smem + kOffQ;
+    // The two key halves of a row are independent within an item (own reference, own
+    // sum, own O accumulator), so a warp meets no other warp inside the tile loop and
+    // decides alone (its waits agree in all lanes).  The 8 warps meet once per item,
+    // at its start and to merge the halves; there they stop together if any gave up.
     int g = 0, n = 0;
-    for (int idx = blockIdx.x; idx < num_items && !abort_seen_warp(wctl); idx += gridDim.x) {
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < num_items; idx += gridDim.x) {
+      if (bar_red_or(kSoftBar, kSoftThreads, !ok || *abort_flag != 0)) break;
       const PItem it = prefill_item(p, idx);
-      const int64_t row = it.row0 + q * kRows + r;  // (token, head) row within the sequence
+      const int64_t row = it.row0 + r;  // (token, head) row within the sequence
       const bool my_row = row < it.rows;
       const int my_i = (int)(row >> p.log2_heads), my_h = (int)(row & (Hq - 1));
-      float* out_row = p.out + ((it.qrow0 + my_i) * Hq + my_h) * kHeadDim;
+      float* out_row = p.out + ((it.qrow0 + my_i) * Hq + my_h) * kHeadDim + h * 64;
       if (!it.ok) {  // invalid sequence (flagged by the dequant pass): 0 / -inf; beyond the chunk: nothing
         if (my_row) {
-          for (int d = 0; d < kHeadDim; d += 4)
-            *reinterpret_cast<float4*>(out_row + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (p.lse_out) p.lse_out[(it.qrow0 + my_i) * Hq + my_h] = -INFINITY;
+          for (int d = 0; d < 64; d += 4) *reinterpret_cast<float4*>(out_row + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (h == 0 && p.lse_out) p.lse_out[(it.qrow0 + my_i) * Hq + my_h] = -INFINITY;
         }
         continue;  // no MMA work for this item
       }
       // A piece's partial output row (normalised) and log2-sum-exp, for the merge.
-      float* part_row = it.piece >= 0 ? p.piece_o + ((int64_t)it.piece * (kQT * kRows) + q * kRows + r) * kHeadDim
-                                       : nullptr;
+      float* part_row = it.piece >= 0 ? p.piece_o + ((int64_t)it.piece * kRows + r) * kHeadDim + h * 64 : nullptr;
+      float* part_lse = it.piece >= 0 ? p.piece_lse + (int64_t)it.piece * kRows + r : nullptr;
       if (it.nkt == 0) {  // a piece with no key tiles (no MMA work): weight zero in the merge
-        for (int d = 0; d < kHeadDim; d += 4)
-          *reinterpret_cast<float4*>(part_row + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-        p.piece_lse[(int64_t)it.piece * (kQT * kRows) + q * kRows + r] = -INFINITY;
+        for (int d = 0; d < 64; d += 4) *reinterpret_cast<float4*>(part_row + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (h == 0) *part_lse = -INFINITY;
         continue;
       }
-      // This row's query (bf16), zero beyond the chunk.
+      // This row's query (bf16), zero beyond the chunk: each half writes 8 of its 16 chunks.
       {
         const uint4* src = reinterpret_cast<const uint4*>(p.q + (it.qrow0 * Hq + row) * kHeadDim);
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          *reinterpret_cast<uint4*>(qs + c * 2048 + r * 16) = my_row ? src[c] : make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(qs + (h * 8 + c) * 2048 + r * 16) = my_row ? src[h * 8 + c] : make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&q_full[q]);
+      if (lane == 0) mbar_arrive(q_full);
       const int32_t p0 = p.prefix_len[it.b];
       const int q_pos = p0 + my_i;
       const int k_lo = p.window > 0 ? max(0, q_pos + 1 - p.window) : 0;
       float m_ref = -INFINITY, l_sum = 0.0f;
-      bool ok = true;
       for (int j = 0; j < it.nkt; ++j, ++g) {
-        const int s = g % kStages;
-        ok = mbar_wait_warp(&s_full[q], g & 1, wctl) &&
-             mbar_wait_warp(&v_full[s], (g / kStages) & 1, wctl);
+        const int sv = g % kStagesV, b = g % kSBuf;
+        ok = mbar_wait_warp(&s_full[b], (g / kSBuf) & 1, wctl) &&
+             mbar_wait_warp(&v_full[sv], (g / kStagesV) & 1, wctl);
         if (!ok) break;
         tc_fence_after();
-        const float* kscale = reinterpret_cast<const float*>(smem + kOffV + s * kVSlotBytes + kTileBytes);
-        const int key0 = (it.kt0 + j) * kKeys;
-        // z = logit (log2 units) minus the row's reference maximum, one FFMA per key.
+        const float* kscale = reinterpret_cast<const float*>(smem + kOffV + sv * kVSlotBytes + kTileBytes) + h * 64;
+        const int key0 = (it.kt0 + j) * kKeys + h * 64;
+        // z = logit (log2 units) minus this half-row's reference, one FFMA per key.
         const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
-        float z[kKeys];
-#pragma unroll
-        for (int c = 0; c < kKeys; c += 32) {
-          uint32_t rr[32];
-          tmem_ld_32x32b_x32(tmem + t_lane + scol + c, rr);
+        float z[64];
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(tmem + t_lane + b * 128 + h * 64, r0);
+          tmem_ld_32x32b_x32(tmem + t_lane + b * 128 + h * 64 + 32, r1);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(kscale + c + e);
-            z[c + e] = fmaf(__uint_as_float(rr[e]), a.x, -m_use);
-            z[c + e + 1] = fmaf(__uint_as_float(rr[e + 1]), a.y, -m_use);
-            z[c + e + 2] = fmaf(__uint_as_float(rr[e + 2]), a.z, -m_use);
-            z[c + e + 3] = fmaf(__uint_as_float(rr[e + 3]), a.w, -m_use);
+            const float4 a = *reinterpret_cast<const float4*>(kscale + e);
+            z[e] = fmaf(__uint_as_float(r0[e]), a.x, -m_use);
+            z[e + 1] = fmaf(__uint_as_float(r0[e + 1]), a.y, -m_use);
+            z[e + 2] = fmaf(__uint_as_float(r0[e + 2]), a.z, -m_use);
+            z[e + 3] = fmaf(__uint_as_float(r0[e + 3]), a.w, -m_use);
+            const float4 a2 = *reinterpret_cast<const float4*>(kscale + 32 + e);
+            z[32 + e] = fmaf(__uint_as_float(r1[e]), a2.x, -m_use);
+            z[32 + e + 1] = fmaf(__uint_as_float(r1[e + 1]), a2.y, -m_use);
+            z[32 + e + 2] = fmaf(__uint_as_float(r1[e + 2]), a2.z, -m_use);
+            z[32 + e + 3] = fmaf(__uint_as_float(r1[e + 3]), a2.w, -m_use);
           }
         }
-        if (!(key0 >= k_lo && key0 + kKeys - 1 <= q_pos)) {
+        if (!(key0 >= k_lo && key0 + 63 <= q_pos)) {
 #pragma unroll
-          for (int c = 0; c < kKeys; ++c) {
+          for (int c = 0; c < 64; ++c) {
             const int key = key0 + c;
             if (key < k_lo || key > q_pos) z[c] = -INFINITY;
           }
         }
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < kKeys; c += 8) {
+        for (int c = 0; c < 64; c += 8) {
           mx4[0] = fmax3(mx4[0], z[c], z[c + 1]);
           mx4[1] = fmax3(mx4[1], z[c + 2], z[c + 3]);
           mx4[2] = fmax3(mx4[2], z[c + 4], z[c + 5]);
           mx4[3] = fmax3(mx4[3], z[c + 6], z[c + 7]);
         }
         const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        // Raise the reference when the row has none yet, or a logit exceeds it by 2^8.
+        // Raise the reference when the half-row has none yet, or a logit exceeds it by 2^8.
         const bool raise = m_ref == -INFINITY ? mx > -INFINITY : mx > kRescaleThreshold;
         const float alpha = raise ? ex2_approx(m_ref - (m_use + mx)) : 1.0f;  // 0 when there was no reference
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
-          ok = mbar_wait_warp(&pv_done[q], (g - 1) & 1, wctl);
-          if (ok) {
-            tc_fence_after();
+          // O_h holds earlier tiles: wait for their PVs, then rescale this row of it.
+          ok = mbar_wait_warp(&pv_done[(g - 1) % kSBuf], ((g - 1) / kSBuf) & 1, wctl);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < kHeadDim; c += 32) {
-              uint32_t o[32];
-              tmem_ld_32x32b_x32(tmem + t_lane + ocol + c, o);
-              tmem_wait_ld();
+          for (int c = 0; c < kHeadDim; c += 32) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tmem + t_lane + kColO + h * 128 + c, o);
+            tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tmem_st_32x32b_x32(tmem + t_lane + ocol + c, o);
-            }
-            tmem_wait_st();
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st_32x32b_x32(tmem + t_lane + kColO + h * 128 + c, o);
           }
+          tmem_wait_st();
         }
         if (raise) {
           l_sum *= alpha;
           m_ref = m_use + mx;
 #pragma unroll
-          for (int c = 0; c < kKeys; ++c) z[c] -= mx;
+          for (int c = 0; c < 64; ++c) z[c] -= mx;
         }
+        // P = 2^z as fp16 into the first 32 columns of this half's 64 in buffer b (its
+        // own, already read), the A operand of this half's PV.
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pw[32];
 #pragma unroll
-        for (int c = 0; c < kKeys; c += 64) {
-          uint32_t pw[32];
-#pragma unroll
-          for (int e = 0; e < 64; e += 4) {
-            const float e0 = ex2_approx(z[c + e]), e1 = ex2_approx(z[c + e + 1]);
-            const float e2 = ex2_approx(z[c + e + 2]), e3 = ex2_approx(z[c + e + 3]);
-            l4[0] += e0;
-            l4[1] += e1;
-            l4[2] += e2;
-            l4[3] += e3;
-            pw[e / 2] = pack_f16x2(e0, e1);
-            pw[e / 2 + 1] = pack_f16x2(e2, e3);
-          }
-          tmem_st_32x32b_x32(tmem + t_lane + scol + c / 2, pw);
+        for (int e = 0; e < 64; e += 4) {
+          const float e0 = ex2_approx(z[e]), e1 = ex2_approx(z[e + 1]);
+          const float e2 = ex2_approx(z[e + 2]), e3 = ex2_approx(z[e + 3]);
+          l4[0] += e0;
+          l4[1] += e1;
+          l4[2] += e2;
+          l4[3] += e3;
+          pw[e / 2] = pack_f16x2(e0, e1);
+          pw[e / 2 + 1] = pack_f16x2(e2, e3);
         }
+        tmem_st_32x32b_x32(tmem + t_lane + b * 128 + h * 64, pw);
         l_sum += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[q]);
-        if (!ok) break;
+        if (lane == 0) mbar_arrive(&p_full[h * kSBuf + b]);
       }
-      if (!ok) break;
-      if (!mbar_wait_warp(&o_full[q], n & 1, wctl)) break;
-      tc_fence_after();
-      const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
-      float* dst = part_row ? part_row : out_row;
+      // ---- end of item: merge the halves, O = (w0 O_0 + w1 O_1) / (w0 l_0 + w1 l_1)
+      // with w_h = 2^(m_h - M), M the larger reference; this thread writes its channel half.
+      xref[h * kRows + r] = m_ref;
+      xsum[h * kRows + r] = l_sum;
+      if (bar_red_or(kSoftBar, kSoftThreads, !ok)) break;
+      const float m0 = xref[r], m1 = xref[kRows + r];
+      const float M = fmaxf(m0, m1);
+      const float w0 = m0 == -INFINITY ? 0.0f : ex2_approx(m0 - M);
+      const float w1 = m1 == -INFINITY ? 0.0f : ex2_approx(m1 - M);
+      const float Ls = w0 * xsum[r] + w1 * xsum[kRows + r];
+      ok = mbar_wait_warp(o_full, n & 1, wctl);
+      if (ok) {
+        tc_fence_after();
+        const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+        const float c0 = w0 * inv, c1 = w1 * inv;
+        float* dst = part_row ? part_row : out_row;
 #pragma unroll
-      for (int c = 0; c < kHeadDim; c += 32) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(tmem + t_lane + ocol + c, o);
-        tmem_wait_ld();
-        if (my_row) {
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t o0[32], o1[32];
+          tmem_ld_32x32b_x32(tmem + t_lane + kColO + h * 64 + c, o0);
+          tmem_ld_32x32b_x32(tmem + t_lane + kColO + 128 + h * 64 + c, o1);
+          tmem_wait_ld();
+          if (my_row) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + c + e) =
-                make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                            __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(dst + c + e) = make_float4(
+                  fmaf(c0, __uint_as_float(o0[e]), c1 * __uint_as_float(o1[e])),
+                  fmaf(c0, __uint_as_float(o0[e + 1]), c1 * __uint_as_float(o1[e + 1])),
+                  fmaf(c0, __uint_as_float(o0[e + 2]), c1 * __uint_as_float(o1[e + 2])),
+                  fmaf(c0, __uint_as_float(o0[e + 3]), c1 * __uint_as_float(o1[e + 3])));
+          }
         }
+        if (h == 0 && my_row) {
+          const float lse2 = Ls > 0.0f ? M + __log2f(Ls) : -INFINITY;
+          if (part_lse) *part_lse = lse2;
+          else if (p.lse_out) p.lse_out[(it.qrow0 + my_i) * Hq + my_h] = lse2 * kLn2;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_empty);
       }
-      const float lse2 = l_sum > 0.0f ? m_ref + __log2f(l_sum) : -INFINITY;
-      if (part_row) {
-        if (my_row) p.piece_lse[(int64_t)it.piece * (kQT * kRows) + q * kRows + r] = lse2;
-      } else if (my_row && p.lse_out) {
-        p.lse_out[(it.qrow0 + my_i) * Hq + my_h] = lse2 * kLn2;
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&o_empty[q]);
       ++n;
     }
   }
@@ -619,20 +633,6 @@ __global__ void __launch_bounds__(256) combine_pieces_kernel(const PrefillParams
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   if (p.lse_out && lane == 0)
     p.lse_out[(it.qrow0 + my_i) * Hq + my_h] = wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
-}
-
-// A [rows][128] 16-bit row-major matrix seen as (8 elements, rows, 16 chunks)
-// so that a (8, 128, 16) box lands in shared memory as [chunk][row][8].
-bool encode_rows128(CUtensorMap* map, const void* base, uint64_t rows) {
-  auto fn = tensor_map_encoder();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {8, rows, 16};
-  cuuint64_t strides[2] = {kHeadDim * 2, 16};
-  cuuint32_t box[3] = {8, (cuuint32_t)kRows, 16};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -698,10 +698,6 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.lse_out = L.lse_out;
   p.err = L.err;
 
-  CUtensorMap kmap, vmap;
-  if (!encode_rows128(&kmap, p.kb, (uint64_t)rows) || !encode_rows128(&vmap, p.vh, (uint64_t)rows))
-    return cudaErrorInvalidValue;
-
   dequant_kernel<<<dim3((unsigned)(p.kt_rows / kKeys), (unsigned)L.batch), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -732,7 +728,7 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.pieces = pieces;
   p.full_items = (int32_t)(pieces > 1 ? pairs_total - rem : pairs_total);
   p.num_items = (int32_t)(p.full_items + (pieces > 1 ? rem * pieces : 0));
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, kmap, vmap);
+  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || pieces == 1) return e;
   const int64_t warps_c = rem * (kQT * kRows);
