@@ -42,7 +42,7 @@ constexpr int kKeys = 128;                 // keys per tile (MMA N of S, K of PV
 constexpr int kTileBytes = kKeys * kHeadDim * 2;  // 32 KB of 16-bit values
 constexpr int kStagesK = 2;                // K tile slots
 constexpr int kStagesV = 3;                // V tile slots (with the tile's K scales, which the softmax reads)
-constexpr int kSBuf = 2;                   // S buffers in tensor memory
+constexpr int kPBuf = 2;                   // P buffers in tensor memory (S has one)
 constexpr int kOffQ = 0;                                     // Q
 // K tiles and V tiles (with the tile's K scales) have separate rings: a K slot is
 // free as soon as S = Q K^T of its tile has run, so the next K tiles load ahead of
@@ -53,10 +53,10 @@ constexpr int kVSlotBytes = kTileBytes + kKeys * 4;          // V (scaled), K sc
 constexpr int kOffV = kOffK + kStagesK * kTileBytes;         // V[kStagesV]
 constexpr int kOffXch = kOffV + kStagesV * kVSlotBytes;      // softmax exchange: row references, row sums [2][128] each
 constexpr int kOffBars = kOffXch + 4 * kRows * 4;
-// k_full, k_empty [kStagesK]; v_full, v_empty [kStagesV]; q_full; s_full, pv_done
-// [kSBuf] (one per S buffer); p_full [2 key halves][kSBuf]; o_full, o_empty; the MMA
-// issuers' last commits.
-constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 1 + 4 * kSBuf + 2 + 1;
+// k_full, k_empty [kStagesK]; v_full, v_empty [kStagesV]; q_full; s_full, s_read;
+// p_full [2 key halves][kPBuf]; pv_done [kPBuf] (one per P buffer); o_full, o_empty;
+// the MMA issuers' last commits.
+constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 1 + 2 + 3 * kPBuf + 2 + 1;
 constexpr int kOffMisc = kOffBars + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 24 + 1024;  // tmem slot, wait state (+8); alignment slack
 static_assert(kOffXch % 16 == 0 && kOffBars % 8 == 0, "shared-memory layout");
@@ -71,7 +71,7 @@ constexpr int kThreads = 384;
 constexpr int kRegsCtl = 72, kRegsSoft = 216;
 constexpr int kRegsLaunch = 168;
 static_assert(kRegsCtl * 128 + kRegsSoft * 256 <= kRegsLaunch * kThreads, "register split");
-constexpr uint32_t kTmemCols = 512;        // S[2] (128 columns; P over half of each key half), O[2] (one per key half)
+constexpr uint32_t kTmemCols = 512;        // S (128 columns), P[2] (64 each), O[2] (128 each, one per key half)
 constexpr float kRescaleThreshold = 8.0f;
 
 struct PrefillParams {
@@ -260,10 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   uint64_t* v_full = k_empty + kStagesK;       // [kStagesV] producer -> PV issuer, softmax (V and K scales)
   uint64_t* v_empty = v_full + kStagesV;       // [kStagesV] PV issuer commit after PV of the tile
   uint64_t* q_full = v_empty + kStagesV;       // softmax -> S issuer (8 warps)
-  uint64_t* s_full = q_full + 1;               // [kSBuf] S issuer commit after S into buffer b
-  uint64_t* p_full = s_full + kSBuf;           // [2][kSBuf] softmax half h -> PV issuer (4 warps): P in buffer b
-  uint64_t* pv_done = p_full + 2 * kSBuf;      // [kSBuf] PV issuer commit after both PVs reading buffer b
-  uint64_t* o_full = pv_done + kSBuf;          // PV issuer commit after an item's last PVs
+  uint64_t* s_full = q_full + 1;               // S issuer commit after S
+  uint64_t* s_read = s_full + 1;               // softmax -> S issuer (8 warps): S read, the next may overwrite it
+  uint64_t* p_full = s_read + 1;               // [2][kPBuf] softmax half h -> PV issuer (4 warps): P in buffer b
+  uint64_t* pv_done = p_full + 2 * kPBuf;      // [kPBuf] PV issuer commit after both PVs reading P buffer b
+  uint64_t* o_full = pv_done + kPBuf;          // PV issuer commit after an item's last PVs
   uint64_t* o_empty = o_full + 1;              // softmax -> PV issuer after reading O (8 warps)
   uint64_t* mma_drain = o_empty + 1;           // the MMA issuers' last commits, at exit
   float* xref = reinterpret_cast<float*>(smem + kOffXch);  // [2 halves][128 rows] half-row references
@@ -275,7 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_heads;
   const int num_items = p.num_items;
-  constexpr uint32_t kColO = kSBuf * 128;  // O of key half h at kColO + h * 128; S buffer b at b * 128
+  constexpr uint32_t kColP = 128;  // P buffer b at kColP + b * 64 (key half h in its 32 columns at + h * 32); S at 0
+  constexpr uint32_t kColO = 256;  // O of key half h at kColO + h * 128
   constexpr uint32_t kSoftBar = 1;
   constexpr uint32_t kSoftThreads = 256;
 
@@ -290,10 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       mbar_init(&v_empty[s], 1);
     }
     mbar_init(q_full, 8);
-    for (int b = 0; b < kSBuf; ++b) {
-      mbar_init(&s_full[b], 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_read, 8);
+    for (int b = 0; b < kPBuf; ++b) {
       mbar_init(&p_full[b], 4);
-      mbar_init(&p_full[kSBuf + b], 4);
+      mbar_init(&p_full[kPBuf + b], 4);
       mbar_init(&pv_done[b], 1);
     }
     mbar_init(o_full, 1);
@@ -320,13 +323,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         for (int j = 0; j < it.nkt; ++j, ++g) {
           const int sk = g % kStagesK, sv = g % kStagesV;
           const int64_t row = seq_row0 + (int64_t)(it.kt0 + j) * kKeys;
-          if (g >= kStagesK && !mbar_wait_abortable(&k_empty[sk], ((g / kStagesK) - 1) & 1, wctl)) break;
+          if (g >= kStagesK && !mbar_wait_polled(&k_empty[sk], ((g / kStagesK) - 1) & 1, wctl)) break;
           if (g != p.drop_stage) {  // (fault injection: that K tile is never loaded)
             mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
             bulk_g2s(smem + kOffK + sk * kTileBytes, p.kb + row * kHeadDim, kTileBytes, &k_full[sk]);
           }
           gk = g + 1;
-          if (g >= kStagesV && !mbar_wait_abortable(&v_empty[sv], ((g / kStagesV) - 1) & 1, wctl)) break;
+          if (g >= kStagesV && !mbar_wait_polled(&v_empty[sv], ((g / kStagesV) - 1) & 1, wctl)) break;
           uint8_t* vs = smem + kOffV + sv * kVSlotBytes;
           mbar_arrive_expect_tx(&v_full[sv], kVSlotBytes);
           bulk_g2s(vs, p.vh + row * kHeadDim, kTileBytes, &v_full[sv]);
@@ -344,9 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     // ------------------------------------------------------------ MMA issuers
     // Warp 1 issues S = Q K^T, warp 2 issues O += P V: one thread issues a
     // 128 x 128 x 16 MMA only about every 115 cycles (measured; the tensor core takes
-    // about 64), so the two streams go out from two threads.  Their MMAs are not
-    // ordered with each other: S(g) overwrites buffer g % 2, whose P the PVs of tile
-    // g - 2 read, so it waits for them.
+    // about 64), so the two streams go out from two threads.  S(g) overwrites S once
+    // the softmax has read S(g - 1) into registers, so it runs during that softmax's
+    // exponentials; P has buffers of its own.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0, 0);
       constexpr uint32_t idesc_o = idesc_f16_f32(kRows, kHeadDim, 0, 1);
@@ -361,32 +364,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       for (int idx = blockIdx.x; idx < num_items && ok && !*abort_flag; idx += gridDim.x) {
         const PItem it = prefill_item(p, idx);
         if (!it.ok || it.nkt == 0) continue;  // no MMA work; the softmax writes its zeros
-        if (s_issuer) ok = mbar_wait_abortable(q_full, n & 1, wctl);
+        if (s_issuer) ok = mbar_wait_polled(q_full, n & 1, wctl);
         for (int j = 0; j < it.nkt && ok; ++j, ++g) {
-          const int sk = g % kStagesK, sv = g % kStagesV, b = g % kSBuf;
+          const int sk = g % kStagesK, sv = g % kStagesV, b = g % kPBuf;
           if (s_issuer) {
-            ok = mbar_wait_abortable(&k_full[sk], (g / kStagesK) & 1, wctl) &&
-                 (g < kSBuf || mbar_wait_abortable(&pv_done[b], ((g / kSBuf) - 1) & 1, wctl));
+            ok = mbar_wait_polled(&k_full[sk], (g / kStagesK) & 1, wctl) &&
+                 (g == 0 || mbar_wait_polled(s_read, (g - 1) & 1, wctl));
             if (!ok) break;
             tc_fence_after();
             const uint64_t dk = dk0 + (uint64_t)(sk * (kTileBytes / 16));
 #pragma unroll
             for (int ks = 0; ks < kHeadDim / 16; ++ks)
-              mma_f16_ss(tmem + b * 128, dq + (uint64_t)(ks * 256), dk + (uint64_t)(ks * 256), idesc_s, ks > 0);
-            mma_commit(&s_full[b]);
+              mma_f16_ss(tmem, dq + (uint64_t)(ks * 256), dk + (uint64_t)(ks * 256), idesc_s, ks > 0);
+            mma_commit(s_full);
             mma_commit(&k_empty[sk]);
           } else {
-            ok = (j > 0 || n == 0 || mbar_wait_abortable(o_empty, (n - 1) & 1, wctl)) &&
-                 mbar_wait_abortable(&v_full[sv], (g / kStagesV) & 1, wctl);
+            ok = (j > 0 || n == 0 || mbar_wait_polled(o_empty, (n - 1) & 1, wctl)) &&
+                 mbar_wait_polled(&v_full[sv], (g / kStagesV) & 1, wctl);
             const uint64_t dv = dv0 + (uint64_t)(sv * (kVSlotBytes / 16));
-            // Key half h: O_h += P_h V_h, P_h in the first 32 columns of the half's 64.
+            // Key half h: O_h += P_h V_h, P_h in its 32 columns of P buffer b.
             for (int hh = 0; hh < 2 && ok; ++hh) {
-              ok = mbar_wait_abortable(&p_full[hh * kSBuf + b], (g / kSBuf) & 1, wctl);
+              ok = mbar_wait_polled(&p_full[hh * kPBuf + b], (g / kPBuf) & 1, wctl);
               if (!ok) break;
               tc_fence_after();
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
-                mma_f16_ts(tmem + kColO + hh * 128, tmem + b * 128 + hh * 64 + ks * 8,
+                mma_f16_ts(tmem + kColO + hh * 128, tmem + kColP + b * 64 + hh * 32 + ks * 8,
                            dv + (uint64_t)((hh * 4 + ks) * 16), idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
             }
             if (!ok) break;
@@ -453,9 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       const int k_lo = p.window > 0 ? max(0, q_pos + 1 - p.window) : 0;
       float m_ref = -INFINITY, l_sum = 0.0f;
       for (int j = 0; j < it.nkt; ++j, ++g) {
-        const int sv = g % kStagesV, b = g % kSBuf;
-        ok = mbar_wait_warp(&s_full[b], (g / kSBuf) & 1, wctl) &&
-             mbar_wait_warp(&v_full[sv], (g / kStagesV) & 1, wctl);
+        const int sv = g % kStagesV, b = g % kPBuf;
+        ok = mbar_wait_polled_warp(s_full, g & 1, wctl) &&
+             mbar_wait_polled_warp(&v_full[sv], (g / kStagesV) & 1, wctl);
         if (!ok) break;
         tc_fence_after();
         const float* kscale = reinterpret_cast<const float*>(smem + kOffV + sv * kVSlotBytes + kTileBytes) + h * 64;
@@ -465,9 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         float z[64];
         {
           uint32_t r0[32], r1[32];
-          tmem_ld_32x32b_x32(tmem + t_lane + b * 128 + h * 64, r0);
-          tmem_ld_32x32b_x32(tmem + t_lane + b * 128 + h * 64 + 32, r1);
+          tmem_ld_32x32b_x32(tmem + t_lane + h * 64, r0);
+          tmem_ld_32x32b_x32(tmem + t_lane + h * 64 + 32, r1);
           tmem_wait_ld();
+          // S is read: S of the next tile may overwrite it.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_read);
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             const float4 a = *reinterpret_cast<const float4*>(kscale + e);
@@ -503,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         const float alpha = raise ? ex2_approx(m_ref - (m_use + mx)) : 1.0f;  // 0 when there was no reference
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
           // O_h holds earlier tiles: wait for their PVs, then rescale this row of it.
-          ok = mbar_wait_warp(&pv_done[(g - 1) % kSBuf], ((g - 1) / kSBuf) & 1, wctl);
+          ok = mbar_wait_polled_warp(&pv_done[(g - 1) % kPBuf], ((g - 1) / kPBuf) & 1, wctl);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -523,8 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
 #pragma unroll
           for (int c = 0; c < 64; ++c) z[c] -= mx;
         }
-        // P = 2^z as fp16 into the first 32 columns of this half's 64 in buffer b (its
-        // own, already read), the A operand of this half's PV.
+        // P = 2^z as fp16 into this half's 32 columns of P buffer b, the A operand of
+        // this half's PV, once the PVs of tile g - 2 have read that buffer.
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pw[32];
 #pragma unroll
@@ -538,12 +545,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
           pw[e / 2] = pack_f16x2(e0, e1);
           pw[e / 2 + 1] = pack_f16x2(e2, e3);
         }
-        tmem_st_32x32b_x32(tmem + t_lane + b * 128 + h * 64, pw);
+        if (g >= kPBuf) {
+          ok = mbar_wait_polled_warp(&pv_done[b], ((g / kPBuf) - 1) & 1, wctl);
+          if (!ok) break;
+        }
+        tmem_st_32x32b_x32(tmem + t_lane + kColP + b * 64 + h * 32, pw);
         l_sum += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[h * kSBuf + b]);
+        if (lane == 0) mbar_arrive(&p_full[h * kPBuf + b]);
       }
       // ---- end of item: merge the halves, O = (w0 O_0 + w1 O_1) / (w0 l_0 + w1 l_1)
       // with w_h = 2^(m_h - M), M the larger reference; this thread writes its channel half.
@@ -555,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       const float w0 = m0 == -INFINITY ? 0.0f : ex2_approx(m0 - M);
       const float w1 = m1 == -INFINITY ? 0.0f : ex2_approx(m1 - M);
       const float Ls = w0 * xsum[r] + w1 * xsum[kRows + r];
-      ok = mbar_wait_warp(o_full, n & 1, wctl);
+      ok = mbar_wait_polled_warp(o_full, n & 1, wctl);
       if (ok) {
         tc_fence_after();
         const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
