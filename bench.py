@@ -411,8 +411,11 @@ def run_prefill(args, rank, world):
         "config": {"workload": w.name, "global_batch": w.batch * world, "kv_query_pairs_per_head": pairs,
                    "flops_per_step": flops, "parallelism": f"replicas x{world}"},
         "gpu_launches": prefill_launches(w) * args.steps,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
-                     "frac": achieved / sustained, "traffic": None, "peak_kind": kind + " bf16 sustained",
+        # The launches are timed alone (a sub-millisecond burst), so the burst peak is the
+        # denominator; the sustained figure is kept for reference.
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
+                     "frac": achieved / burst, "traffic": None, "peak_kind": kind + " bf16 burst",
+                     "peak_sustained": sustained,
                      "kernel": "cai_mqa_prefill_chunk (dequant pass + tcgen05 attention)"},
         "clocks": clocks.summary(),
         "parity": parity,

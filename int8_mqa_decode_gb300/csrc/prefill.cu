@@ -16,18 +16,17 @@
 //     times softmax_scale * log2(e) as fp32 [B][KT], and V already multiplied by
 //     its per-key scale, rounded once to fp16 [B][KT][128] (relative error at
 //     most 2^-11, the same as the rounding of P).
-//  2. attention: a persistent kernel whose work items are pairs of 128-row
-//     q-tiles of one sequence, a row being one (new token, head) pair.  128-key
-//     tiles of K and V arrive by TMA tensor loads (cp.async.bulk.tensor)
-//     straight into the canonical no-swizzle tcgen05 operand layout; S = Q K^T
-//     runs as tcgen05.mma kind::f16 (bf16, M = N = 128, K = 128) into tensor
-//     memory; the online softmax (one thread per row, one warpgroup per q-tile
-//     so each works while the tensor core runs the other's MMAs) forms
-//     logit - reference with one FFMA per key (per-key K scale), applies the
-//     causal/window mask on boundary tiles only, raises the reference lazily
-//     (when a logit exceeds it by 2^8), and writes P (fp16) back into tensor
-//     memory, where it is the A operand of O += P V' (V' from shared memory,
-//     MN-major).
+//  2. attention: a persistent kernel whose work items are 128-row q-tiles of
+//     one sequence, a row being one (new token, head) pair.  Each 128-key tile of
+//     the copy is in the tcgen05 operand layout already and arrives by one bulk
+//     copy; S = Q K^T runs as tcgen05.mma kind::f16 (bf16, M = N = 128, K = 128)
+//     into tensor memory; the online softmax (thread = row; two warps per row,
+//     each taking one half of the keys with its own reference, sum and O
+//     accumulator, merged at the end of the item) forms logit - reference with
+//     one FFMA per key (per-key K scale), applies the causal/window mask on
+//     boundary tiles only, raises the reference lazily (when a logit exceeds it
+//     by 2^8), and writes P (fp16) into tensor memory, where it is the A operand
+//     of O_h += P_h V_h (V from shared memory, MN-major).
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -81,13 +80,13 @@ struct PrefillParams {
   const int32_t* prefix_len;
   const uint16_t* q;      // bf16 [rows of new tokens][Hq][128], sequence b's rows from q_row0(b)
   const int32_t* q_off;   // [B + 1] packed new-token offsets, or null: sequence b has n_new rows at b * n_new
-  int32_t batch, n_new, total_new, num_heads, log2_heads, window, kt_rows, pairs;  // n_new: the most per sequence
+  int32_t batch, n_new, total_new, num_heads, log2_heads, window, kt_rows, qtiles;  // n_new: the most per sequence; qtiles per sequence
   float scale_log2;
-  // Work items: items [0, full_items) are whole pairs of q-tiles; the pairs after them
-  // (the last, partial wave of a persistent grid) are cut into `pieces` key ranges each,
-  // item full_items + t being piece t % pieces of pair full_items + t / pieces.  A piece
-  // writes its normalised partial output and log2-sum-exp to piece_o / piece_lse
-  // ([t][256 rows][128] and [t][256]); combine_pieces_kernel merges them.
+  // Work items: items [0, full_items) are whole q-tiles; the q-tiles after them (the
+  // last, partial wave of a persistent grid) are cut into `pieces` key ranges each,
+  // item full_items + t being piece t % pieces of q-tile full_items + t / pieces.  A
+  // piece writes its normalised partial output and log2-sum-exp to piece_o / piece_lse
+  // ([t][128 rows][128] and [t][128]); combine_pieces_kernel merges them.
   int32_t full_items, pieces, num_items;
   uint64_t wait_ns;  // limit of every bounded wait inside the kernel
   int32_t drop_stage;  // fault injection: K tile each CTA skips (-1: none)
@@ -148,49 +147,63 @@ __global__ void __launch_bounds__(256) dequant_kernel(const PrefillParams p) {
   // recycled them.
   const int lo_min = p.window > 0 ? max(0, p0 + 1 - p.window) : 0;
   if (tile < lo_min / kKeys) return;  // before every window, whole tile
-  for (int rr = threadIdx.x >> 5; rr < kKeys; rr += blockDim.x >> 5) {
+  // Warp w takes keys 16w .. 16w + 15 of the tile in two groups of 8; in each group
+  // lane l handles key r0 + (l % 8) and channel chunk 4i + l / 8 (8 channels) for
+  // i = 0..3, so that a store instruction writes four whole 128-byte lines of the
+  // tiled copy (chunk c of 8 consecutive keys is 128 contiguous bytes).
+  const int warp = threadIdx.x >> 5;
+  const int P = p.page_size;
+  for (int grp = 0; grp < 2; ++grp) {
+    const int rr = warp * 16 + grp * 8 + (lane & 7);  // key within the tile
     const int t = tile * kKeys + rr;
-    const int64_t row = (int64_t)b * p.kt_rows + t;
-    uint32_t kw = 0, vw = 0;
+    const uint8_t* pg = nullptr;
+    int slot = 0;
     float ksc = 0.0f, vsc = 0.0f;
     if (t < len && t >= lo_min) {
-      const int P = p.page_size;
       const int32_t page = p.table[(int64_t)b * p.max_pages + t / P];
       if (page >= 0 && page < p.num_pages) {
-        const int slot = t % P;
-        const uint8_t* pg = p.pages + (int64_t)page * page_bytes(P);
-        kw = reinterpret_cast<const uint32_t*>(pg + slot * kHeadDim)[lane];
-        const uint8_t* vcol = pg + P * kHeadDim + slot;  // channel-major V block: channel c at c * P
-#pragma unroll
-        for (int e = 0; e < 4; ++e) vw |= (uint32_t)vcol[(lane * 4 + e) * P] << (8 * e);
+        slot = t % P;
+        pg = p.pages + (int64_t)page * page_bytes(P);
         const float* sc = reinterpret_cast<const float*>(pg + 2 * P * kHeadDim);
         ksc = sc[slot] * p.scale_log2;
         vsc = sc[P + slot];
-      } else if (lane == 0 && p.err) {
+      } else if (lane < 8 && p.err) {
         atomicOr(p.err, CAI_DEVERR_PAGE);
       }
     }
-    // int8 -> bf16 (K) and int8 -> fp16 (V): exact for |code| <= 127.
-    uint16_t kb[4], vh[4];
+    const int64_t row = (int64_t)b * p.kt_rows + t;
+    if (lane < 8) p.ks[row] = ksc;
+    uint16_t* kt = p.kb + ((int64_t)b * p.kt_rows + tile * kKeys) * kHeadDim + rr * 8;
+    uint16_t* vt = p.vh + ((int64_t)b * p.kt_rows + tile * kKeys) * kHeadDim + rr * 8;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float kf = (float)(int8_t)(kw >> (8 * e));
-      const float vf = (float)(int8_t)(vw >> (8 * e));
-      kb[e] = (uint16_t)(__float_as_uint(kf) >> 16);  // small integers: the top half is exact
-      const __half hv = __float2half_rn(vf * vsc);  // V scale applied here: P needs no per-key factor
-      vh[e] = *reinterpret_cast<const uint16_t*>(&hv);
+    for (int i = 0; i < 4; ++i) {
+      const int c = 4 * i + (lane >> 3);  // channels 8c .. 8c + 7
+      uint2 kw = make_uint2(0u, 0u);
+      uint32_t vw[2] = {0u, 0u};
+      if (pg) {
+        kw = *reinterpret_cast<const uint2*>(pg + slot * kHeadDim + c * 8);
+        const uint8_t* vcol = pg + P * kHeadDim + slot;  // channel-major V block: channel d at d * P
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vw[e >> 2] |= (uint32_t)vcol[(c * 8 + e) * P] << (8 * (e & 3));
+      }
+      // int8 -> bf16 (K) and int8 -> fp16 (V): exact for |code| <= 127.
+      uint32_t ko[4], vo[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const uint32_t kx = e < 4 ? kw.x : kw.y, vx = vw[e >> 2];
+        const float k0 = (float)(int8_t)(kx >> (8 * (e & 3))), k1 = (float)(int8_t)(kx >> (8 * ((e & 3) + 1)));
+        ko[e / 2] = (__float_as_uint(k0) >> 16) | (__float_as_uint(k1) & 0xFFFF0000u);  // small integers: exact
+        const float v0 = (float)(int8_t)(vx >> (8 * (e & 3))), v1 = (float)(int8_t)(vx >> (8 * ((e & 3) + 1)));
+        const __half2 hv = __floats2half2_rn(v0 * vsc, v1 * vsc);  // V scale applied here: P needs no per-key factor
+        vo[e / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      *reinterpret_cast<uint4*>(kt + c * 1024) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+      *reinterpret_cast<uint4*>(vt + c * 1024) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
     }
-    // Stored tile by tile in the MMA operand layout (element (key r, channel d) of a
-    // 128-key tile at (d / 8) * 1024 + r * 8 + d % 8), so the attention kernel moves a
-    // tile with one contiguous 32 KB bulk copy.
-    const int64_t off = ((int64_t)b * p.kt_rows + tile * kKeys) * kHeadDim + (lane >> 1) * 1024 + rr * 8 + (lane & 1) * 4;
-    *reinterpret_cast<uint2*>(p.kb + off) = make_uint2(kb[0] | ((uint32_t)kb[1] << 16), kb[2] | ((uint32_t)kb[3] << 16));
-    *reinterpret_cast<uint2*>(p.vh + off) = make_uint2(vh[0] | ((uint32_t)vh[1] << 16), vh[2] | ((uint32_t)vh[3] << 16));
-    if (lane == 0) p.ks[row] = ksc;
   }
 }
 
-// One work item: a pair of q-tiles (256 consecutive (token, head) rows) of one
+// One work item: a q-tile (128 consecutive (token, head) rows) of one
 // sequence.  ok = false: no MMA work; the softmax groups then write zeros to the
 // item's rows below `rows` (an invalid sequence) or nothing (rows beyond the chunk).
 struct PItem {
@@ -203,17 +216,17 @@ struct PItem {
 
 __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
   PItem it;
-  int pair = idx, piece = -1;
+  int qt = idx, piece = -1;
   if (idx >= p.full_items) {
     const int t = idx - p.full_items;
-    pair = p.full_items + t / p.pieces;
+    qt = p.full_items + t / p.pieces;
     piece = t % p.pieces;
     it.piece = t;
   } else {
     it.piece = -1;
   }
-  it.b = pair / p.pairs;
-  it.row0 = (pair - it.b * p.pairs) * (kQT * kRows);
+  it.b = qt / p.qtiles;
+  it.row0 = (qt - it.b * p.qtiles) * (kQT * kRows);
   const int32_t p0 = p.prefix_len[it.b];
   const SeqRows sr = seq_rows(p, it.b);
   it.qrow0 = sr.r0;
@@ -229,7 +242,7 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
   const int kv_lo = p.window > 0 ? max(0, p0 + i0 + 1 - p.window) : 0;
   it.kt0 = kv_lo / kKeys;
   it.nkt = (kv_hi - 1) / kKeys - it.kt0 + 1;
-  if (piece >= 0) {  // key tiles [per * piece, per * (piece + 1)) of the pair's range
+  if (piece >= 0) {  // key tiles [per * piece, per * (piece + 1)) of the q-tile's range
     const int per = (it.nkt + p.pieces - 1) / p.pieces;
     const int a = min(it.nkt, per * piece), e = min(it.nkt, per * (piece + 1));
     it.kt0 += a;
@@ -239,18 +252,20 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
 }
 
 // Operand tiles in shared memory: element (r, k) of a 128x128 16-bit tile at
-// (k/8)*2048 + r*16 + (k%8)*2 -- the order a [16 chunks][128 rows][8] TMA box
-// writes.  As a K-major operand: LBO = 2048 (next 8 k), SBO = 128 (next 8 rows).
-// As an MN-major operand (rows = K, k = N): LBO = 128, SBO = 2048.
+// (k/8)*2048 + r*16 + (k%8)*2 -- the order in which the dequant pass writes each
+// tile of its copy, so one bulk copy lands it.  As a K-major operand: LBO = 2048
+// (next 8 k), SBO = 128 (next 8 rows).  As an MN-major operand (rows = K, k = N):
+// LBO = 128, SBO = 2048.
 //
 // Persistent CTAs, one per SM, each taking q-tiles in turn.  Roles: warp 0 loads
-// K/V tiles (TMA tensor copies) into 2-slot K and V rings; warp 1 issues
-// S(g) = Q K(g)^T into S buffer g % 2 as soon as K(g) is loaded and PV(g - 2) has
-// consumed the P that buffer held, so S of the next tile runs while the softmax
-// of this one does; warp 2 issues O += P(g) V(g); warps 4-7 and 8-11 run the
-// softmax of key half 0 and key half 1 of every row (thread = row, 64 keys per
-// tile each), the halves agreeing on the row's reference through shared memory
-// when a raise is due, and write the outputs (channel half each).
+// K/V tiles (one bulk copy each) into 2-slot K and V rings; warp 1 issues
+// S(g) = Q K(g)^T into the one S buffer as soon as K(g) is loaded and the softmax
+// has read S(g - 1) into registers, so S of the next tile runs during this tile's
+// exponentials; warp 2 issues O_h += P_h(g) V_h(g) for both key halves h, P from
+// two alternating buffers; warps 4-7 and 8-11 run the softmax of key half 0 and
+// key half 1 of every row (thread = row, 64 keys per tile each), each half with
+// its own reference, sum and accumulator, and merge the halves into the outputs at
+// the end of the item (channel half each).
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -606,15 +621,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// One warp per (split pair, row): merge the pair's pieces by their log-sum-exp,
+// One warp per (split q-tile, row): merge the q-tile's pieces by their log-sum-exp,
 // out = sum_j 2^(lse_j - M) o_j / sum_j 2^(lse_j - M), into the row's output.
 __global__ void __launch_bounds__(256) combine_pieces_kernel(const PrefillParams p) {
   grid_dependency_wait();
   grid_launch_dependents();
   const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int split_pairs = (p.num_items - p.full_items) / p.pieces;
-  if (w >= (int64_t)split_pairs * (kQT * kRows)) return;
+  const int split_tiles = (p.num_items - p.full_items) / p.pieces;
+  if (w >= (int64_t)split_tiles * (kQT * kRows)) return;
   const int sp = (int)(w / (kQT * kRows)), r = (int)(w % (kQT * kRows));
   const PItem it = prefill_item(p, p.full_items + sp * p.pieces);
   const int64_t row = it.row0 + r;
@@ -692,7 +707,7 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.log2_heads = 31 - __builtin_clz((unsigned)L.num_heads);
   p.window = L.window;
   p.kt_rows = (int32_t)(((int64_t)L.max_pages * L.page_size + kKeys - 1) / kKeys * kKeys);
-  p.pairs = (int32_t)(((int64_t)L.n_new * L.num_heads + kQT * kRows - 1) / (kQT * kRows));
+  p.qtiles = (int32_t)(((int64_t)L.n_new * L.num_heads + kQT * kRows - 1) / (kQT * kRows));
   p.scale_log2 = L.scale_log2;
   p.wait_ns = wait_limit_ns();
   p.drop_stage = fault_drop_stage();
@@ -726,18 +741,18 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  // Work split: whole pairs in full waves of the persistent grid; the pairs of a partial
-  // last wave are cut into `pieces` key ranges so that wave ends sooner (with r pairs
-  // left over, pieces = grid / r, at most 4; the pieces of a pair are merged after).
-  const int64_t pairs_total = (int64_t)L.batch * p.pairs;
+  // Work split: whole q-tiles in full waves of the persistent grid; the q-tiles of a
+  // partial last wave are cut into `pieces` key ranges so that wave ends sooner (with r
+  // q-tiles left over, pieces = grid / r, at most 4; the pieces of one are merged after).
+  const int64_t qtiles_total = (int64_t)L.batch * p.qtiles;
   const int sms = num_sms();
-  const int grid = (int)(pairs_total < sms ? pairs_total : sms);
-  const int64_t rem = pairs_total % grid;
+  const int grid = (int)(qtiles_total < sms ? qtiles_total : sms);
+  const int64_t rem = qtiles_total % grid;
   int pieces = rem > 0 ? (int)(grid / rem) : 1;
   if (pieces > 4) pieces = 4;
   if (pieces < 2) pieces = 1;
   p.pieces = pieces;
-  p.full_items = (int32_t)(pieces > 1 ? pairs_total - rem : pairs_total);
+  p.full_items = (int32_t)(pieces > 1 ? qtiles_total - rem : qtiles_total);
   p.num_items = (int32_t)(p.full_items + (pieces > 1 ? rem * pieces : 0));
   prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
   e = cudaGetLastError();
