@@ -486,11 +486,15 @@ def run_mixed(args, rank, world):
         with ClockSampler(smi_index(torch.cuda.current_device())) as clocks:
             torch.cuda.synchronize()
             clocks.start()
+            if args.ncu:
+                torch.cuda.profiler.start()
             t0.record()
             for _ in range(args.steps):
                 fn()
             t1.record()
             torch.cuda.synchronize()
+            if args.ncu:
+                torch.cuda.profiler.stop()
             clocks.stop()
         return allreduce_max(t0.elapsed_time(t1), world) / args.steps, clocks.summary()
 

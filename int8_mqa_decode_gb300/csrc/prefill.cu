@@ -29,6 +29,8 @@
 //     of O_h += P_h V_h (V from shared memory, MN-major).
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -57,7 +59,14 @@ constexpr int kOffBars = kOffXch + 4 * kRows * 4;
 // the MMA issuers' last commits.
 constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 1 + 2 + 3 * kPBuf + 2 + 1;
 constexpr int kOffMisc = kOffBars + 8 * kNumBars;
-constexpr int kSmemBytes = kOffMisc + 24 + 1024;  // tmem slot, wait state (+8); alignment slack
+// Varlen dequant: sequences whose tiles one block numbers in shared memory.
+constexpr int kMaxCompactSeqs = 8192;
+// A varlen call's item list (see PrefillParams::compact): its count, then the dense
+// q-tile number of each item, in shared memory that only such a launch asks for.
+constexpr int kMaxCompactItems = 4096;
+constexpr int kOffTable = kOffMisc + 32;  // after the tmem slot and the wait state (+8)
+constexpr int kSmemBytes = kOffTable + 1024;  // without the list; ... and alignment slack
+constexpr int kSmemBytesMax = kSmemBytes + (kMaxCompactItems + 4) * 4;
 static_assert(kOffXch % 16 == 0 && kOffBars % 8 == 0, "shared-memory layout");
 // Warpgroup 0: K/V producer (warp 0), S issuer (warp 1), PV issuer (warp 2), a spare warp;
 // warpgroups 1 and 2: the softmax, key half 0 and key half 1 of every row.  The block
@@ -91,6 +100,12 @@ struct PrefillParams {
   uint64_t wait_ns;  // limit of every bounded wait inside the kernel
   int32_t drop_stage;  // fault injection: K tile each CTA skips (-1: none)
   int32_t skip_single;  // see PrefillLaunch
+  // Varlen calls: the items are only the q-tiles that hold rows, sequence by sequence,
+  // through a list of their dense numbers that every CTA builds at its start (the dense
+  // numbering, qtiles slots per sequence for the longest one, would make the grid walk
+  // the empty slots of every short or one-token sequence); past kMaxCompactItems real
+  // q-tiles, the dense numbering.  No pieces then.
+  int32_t compact;
   float* piece_o;
   float* piece_lse;
   uint16_t* kb;  // scratch bf16 [B][KT][128]
@@ -126,11 +141,9 @@ __device__ __forceinline__ bool seq_ok(const PrefillParams& p, int32_t p0, int n
   return n >= 0 && p0 >= 0 && (int64_t)p0 + n <= (int64_t)p.max_pages * p.page_size;
 }
 
-// One block per 128-key tile of a sequence (blockIdx.y = sequence), one warp per 16
-// rows of it; a block whose tile no query of the chunk reads returns at once.
-__global__ void __launch_bounds__(256) dequant_kernel(const PrefillParams p) {
-  const int b = blockIdx.y;
-  const int tile = blockIdx.x;
+// Tile `tile` of sequence b's copy, by a block of 256 threads, one warp per 16 rows;
+// a tile that no query of the chunk reads returns at once.
+__device__ __forceinline__ void dequant_tile(const PrefillParams& p, int b, int tile) {
   const int lane = threadIdx.x & 31;
   const int32_t p0 = p.prefix_len[b];
   const SeqRows sr = seq_rows(p, b);
@@ -203,6 +216,72 @@ __global__ void __launch_bounds__(256) dequant_kernel(const PrefillParams p) {
   }
 }
 
+// Tiles of sequence b's copy that the dequant pass writes: [*lo, *lo + count).  A sequence
+// whose lengths are invalid writes none (and is flagged).
+__device__ __forceinline__ int dequant_tiles(const PrefillParams& p, int b, int* lo) {
+  const int32_t p0 = p.prefix_len[b];
+  const SeqRows sr = seq_rows(p, b);
+  *lo = 0;
+  if (!seq_ok(p, p0, sr.n)) {
+    if (p.err) atomicOr(p.err, CAI_DEVERR_LENGTH);
+    return 0;
+  }
+  if (sr.n == 0) return 0;
+  const int len = p0 + sr.n;
+  const int lo_min = p.window > 0 ? max(0, p0 + 1 - p.window) : 0;
+  *lo = lo_min / kKeys;
+  return (len + kKeys - 1) / kKeys - *lo;
+}
+
+// One block per 128-key tile of a sequence (blockIdx.y = sequence).
+__global__ void __launch_bounds__(256) dequant_kernel(const PrefillParams p) {
+  dequant_tile(p, blockIdx.y, blockIdx.x);
+}
+
+// Varlen calls: a grid-stride loop over only the tiles some query reads.  Each block
+// first numbers them (a block-wide scan of every sequence's tile count into dynamic
+// shared memory, first[b] = number of sequence b's first tile, first[batch] = total);
+// the dense grid of the chunk calls would launch a block for every tile slot of every
+// sequence, most of them idle for the one-token rows of a mixed batch.
+__global__ void __launch_bounds__(256) dequant_compact_kernel(const PrefillParams p) {
+  extern __shared__ int32_t first[];
+  __shared__ int32_t warp_sum[8];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int B = p.batch;
+  const int per = (B + 255) / 256;
+  const int b0 = min(B, t * per), b1 = min(B, b0 + per);
+  int sum = 0, lo;
+  for (int b = b0; b < b1; ++b) sum += dequant_tiles(p, b, &lo);
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_sum[w];
+  int run = before + incl - sum;
+  for (int b = b0; b < b1; ++b) {
+    first[b] = run;
+    run += dequant_tiles(p, b, &lo);
+  }
+  if (t == 255) first[B] = before + incl;
+  __syncthreads();
+  const int total = first[B];
+  for (int w = blockIdx.x; w < total; w += gridDim.x) {
+    int l = 0, h = B - 1;  // the last sequence whose first tile is <= w
+    while (l < h) {
+      const int mid = (l + h + 1) >> 1;
+      if (first[mid] <= w) l = mid;
+      else h = mid - 1;
+    }
+    dequant_tiles(p, l, &lo);
+    dequant_tile(p, l, lo + (w - first[l]));
+  }
+}
+
 // One work item: a q-tile (128 consecutive (token, head) rows) of one
 // sequence.  ok = false: no MMA work; the softmax groups then write zeros to the
 // item's rows below `rows` (an invalid sequence) or nothing (rows beyond the chunk).
@@ -214,17 +293,46 @@ struct PItem {
   int piece;      // -1: the whole key range; otherwise the piece's slot in piece_o / piece_lse
 };
 
-__device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
+// q-tiles holding rows of sequence b (0 when it has no rows in this call).
+__device__ __forceinline__ int seq_qtiles(const PrefillParams& p, int b) {
+  const SeqRows sr = seq_rows(p, b);
+  return sr.n > 0 ? (int)(((int64_t)sr.n * p.num_heads + kRows - 1) / kRows) : 0;
+}
+
+// The work split of a persistent grid over `total` q-tiles: items [0, full) are whole
+// q-tiles; the q-tiles of a partial last wave are cut into `pieces` key ranges so that
+// wave ends sooner (with r q-tiles left over, pieces = grid / r, at most 4), item
+// full + t being piece t % pieces of q-tile full + t / pieces; num items in all.  The
+// host applies it to a chunk call's q-tiles.
+struct WorkSplit {
+  int full, pieces, num;
+};
+__host__ __device__ inline WorkSplit work_split(int64_t total, int grid) {
+  const int64_t rem = grid > 0 ? total % grid : 0;
+  int pieces = rem > 0 ? (int)(grid / rem) : 1;
+  if (pieces > 4) pieces = 4;
+  if (pieces < 2) pieces = 1;
+  WorkSplit w;
+  w.pieces = pieces;
+  w.full = (int)(pieces > 1 ? total - rem : total);
+  w.num = (int)(w.full + (pieces > 1 ? rem * pieces : 0));
+  return w;
+}
+
+// list: a varlen call's q-tile numbers (entry i for q-tile i - list_first), or null.
+__device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx, const int32_t* list,
+                                              const WorkSplit& ws, int list_first = 0) {
   PItem it;
-  int qt = idx, piece = -1;
-  if (idx >= p.full_items) {
-    const int t = idx - p.full_items;
-    qt = p.full_items + t / p.pieces;
-    piece = t % p.pieces;
+  int qti = idx, piece = -1;
+  if (idx >= ws.full) {
+    const int t = idx - ws.full;
+    qti = ws.full + t / ws.pieces;
+    piece = t % ws.pieces;
     it.piece = t;
   } else {
     it.piece = -1;
   }
+  const int qt = list ? list[qti - list_first] : qti;
   it.b = qt / p.qtiles;
   it.row0 = (qt - it.b * p.qtiles) * (kQT * kRows);
   const int32_t p0 = p.prefix_len[it.b];
@@ -243,7 +351,7 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
   it.kt0 = kv_lo / kKeys;
   it.nkt = (kv_hi - 1) / kKeys - it.kt0 + 1;
   if (piece >= 0) {  // key tiles [per * piece, per * (piece + 1)) of the q-tile's range
-    const int per = (it.nkt + p.pieces - 1) / p.pieces;
+    const int per = (it.nkt + ws.pieces - 1) / ws.pieces;
     const int a = min(it.nkt, per * piece), e = min(it.nkt, per * (piece + 1));
     it.kt0 += a;
     it.nkt = e - a;
@@ -266,6 +374,9 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int idx) {
 // key half 1 of every row (thread = row, 64 keys per tile each), each half with
 // its own reference, sum and accumulator, and merge the halves into the outputs at
 // the end of the item (channel half each).
+// kCompact: a varlen call's launch (p.compact): its items go through the item list.
+// Chunk calls compile without that path (its one branch per item cost them 2%).
+template <bool kCompact>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -290,7 +401,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_heads;
-  const int num_items = p.num_items;
   constexpr uint32_t kColP = 128;  // P buffer b at kColP + b * 64 (key half h in its 32 columns at + h * 32); S at 0
   constexpr uint32_t kColO = 256;  // O of key half h at kColO + h * 128
   constexpr uint32_t kSoftBar = 1;
@@ -321,10 +431,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     wctl->limit_ns = p.wait_ns;
     fence_barrier_init();
   }
+  if (kCompact && warp == 3) {
+    // The item list: lane l sums the q-tiles of a run of sequences, a warp scan gives
+    // each run its first item, and each lane writes its run's items; the count is -1
+    // (the dense numbering) when they do not fit.
+    int32_t* hdr = reinterpret_cast<int32_t*>(smem + kOffTable);
+    int32_t* list = hdr + 4;
+    const int per = (p.batch + 31) / 32;
+    const int b0 = min(p.batch, lane * per), b1 = min(p.batch, b0 + per);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) sum += seq_qtiles(p, b);
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total <= kMaxCompactItems) {
+      int run = incl - sum;
+      for (int b = b0; b < b1; ++b) {
+        const int n = seq_qtiles(p, b);
+        for (int j = 0; j < n; ++j) list[run + j] = b * p.qtiles + j;
+        run += n;
+      }
+    }
+    if (lane == 0) *hdr = total <= kMaxCompactItems ? total : -1;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // A varlen call's item list, if it was built (above).
+  const int n_list = kCompact ? *reinterpret_cast<const int32_t*>(smem + kOffTable) : -1;
+  const int32_t* table = n_list >= 0 ? reinterpret_cast<const int32_t*>(smem + kOffTable + 16) : nullptr;
+  // A varlen call's q-tiles are whole (pieces measured no faster there): the host gives it
+  // full_items = num_items = the dense count, which no listed item reaches.
+  WorkSplit ws;
+  ws.full = p.full_items;
+  ws.pieces = p.pieces;
+  ws.num = n_list >= 0 ? n_list : p.num_items;
+  const int num_items = ws.num;
 
   if (warp < 4) {
    setmaxnreg_dec<kRegsCtl>();
@@ -333,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     if (lane == 0) {
       int g = 0, gk = 0, gv = 0;  // tiles; tiles whose K and V loads were issued (or dropped)
       for (int idx = blockIdx.x; idx < num_items && !*abort_flag; idx += gridDim.x) {
-        const PItem it = prefill_item(p, idx);
+        const PItem it = prefill_item(p, idx, table, ws);
         const int64_t seq_row0 = (int64_t)it.b * p.kt_rows;
         for (int j = 0; j < it.nkt; ++j, ++g) {
           const int sk = g % kStagesK, sv = g % kStagesV;
@@ -377,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       int g = 0, n = 0;
       bool ok = true;
       for (int idx = blockIdx.x; idx < num_items && ok && !*abort_flag; idx += gridDim.x) {
-        const PItem it = prefill_item(p, idx);
+        const PItem it = prefill_item(p, idx, table, ws);
         if (!it.ok || it.nkt == 0) continue;  // no MMA work; the softmax writes its zeros
         if (s_issuer) ok = mbar_wait_polled(q_full, n & 1, wctl);
         for (int j = 0; j < it.nkt && ok; ++j, ++g) {
@@ -436,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     bool ok = true;
     for (int idx = blockIdx.x; idx < num_items; idx += gridDim.x) {
       if (bar_red_or(kSoftBar, kSoftThreads, !ok || *abort_flag != 0)) break;
-      const PItem it = prefill_item(p, idx);
+      const PItem it = prefill_item(p, idx, table, ws);
       const int64_t row = it.row0 + r;  // (token, head) row within the sequence
       const bool my_row = row < it.rows;
       const int my_i = (int)(row >> p.log2_heads), my_h = (int)(row & (Hq - 1));
@@ -628,25 +775,29 @@ __global__ void __launch_bounds__(256) combine_pieces_kernel(const PrefillParams
   grid_launch_dependents();
   const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int split_tiles = (p.num_items - p.full_items) / p.pieces;
+  WorkSplit ws;
+  ws.full = p.full_items;
+  ws.pieces = p.pieces;
+  ws.num = p.num_items;
+  const int split_tiles = (ws.num - ws.full) / ws.pieces;
   if (w >= (int64_t)split_tiles * (kQT * kRows)) return;
   const int sp = (int)(w / (kQT * kRows)), r = (int)(w % (kQT * kRows));
-  const PItem it = prefill_item(p, p.full_items + sp * p.pieces);
+  const PItem it = prefill_item(p, ws.full + sp * ws.pieces, nullptr, ws);
   const int64_t row = it.row0 + r;
   if (!it.ok || row >= it.rows) return;  // invalid sequence (its rows hold zeros) or past the chunk
   const int Hq = p.num_heads;
   const int my_i = (int)(row >> p.log2_heads), my_h = (int)(row & (Hq - 1));
-  const int64_t t0 = (int64_t)sp * p.pieces;
-  const float lj = lane < p.pieces ? p.piece_lse[(t0 + lane) * (kQT * kRows) + r] : -INFINITY;
+  const int64_t t0 = (int64_t)sp * ws.pieces;
+  const float lj = lane < ws.pieces ? p.piece_lse[(t0 + lane) * (kQT * kRows) + r] : -INFINITY;
   float M = lj;
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float wj = (M == -INFINITY || lane >= p.pieces) ? 0.0f : ex2_approx(lj - M);
+  const float wj = (M == -INFINITY || lane >= ws.pieces) ? 0.0f : ex2_approx(lj - M);
   float wsum = wj;
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < p.pieces; ++j) {
+  for (int j = 0; j < ws.pieces; ++j) {
     const float wt = __shfl_sync(0xffffffffu, wj, j);
     const float4 o = reinterpret_cast<const float4*>(p.piece_o + ((t0 + j) * (kQT * kRows) + r) * kHeadDim)[lane];
     acc.x = fmaf(wt, o.x, acc.x);
@@ -663,8 +814,10 @@ __global__ void __launch_bounds__(256) combine_pieces_kernel(const PrefillParams
 
 }  // namespace
 
-// Partial outputs of the split last wave: at most one piece per CTA of the grid.
-static int64_t piece_bytes() { return (int64_t)num_sms() * (kQT * kRows) * (kHeadDim + 1) * 4; }
+// Partial outputs of the split last wave: at most one piece per CTA of the grid.  The
+// region is twice that: a varlen call's decode launch keeps its split partials there
+// (fewer splits when they would not fit), and half the room had cost it half its splits.
+static int64_t piece_bytes() { return (int64_t)num_sms() * 2 * (kQT * kRows) * (kHeadDim + 1) * 4; }
 
 size_t prefill_workspace_bytes(int32_t batch, int32_t max_pages_per_seq, int32_t page_size) {
   const int64_t kt = ((int64_t)max_pages_per_seq * page_size + kKeys - 1) / kKeys * kKeys;
@@ -700,6 +853,7 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.q = L.q;
   p.q_off = L.q_off;
   p.skip_single = L.q_off && L.skip_single ? 1 : 0;
+  p.compact = L.q_off ? 1 : 0;
   p.batch = L.batch;
   p.n_new = L.n_new;
   p.total_new = L.total_new;
@@ -724,7 +878,12 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   p.lse_out = L.lse_out;
   p.err = L.err;
 
-  dequant_kernel<<<dim3((unsigned)(p.kt_rows / kKeys), (unsigned)L.batch), 256, 0, stream>>>(p);
+  const int64_t dq_blocks = (int64_t)L.batch * (p.kt_rows / kKeys);
+  if (dq_blocks > 0 && L.q_off && L.batch <= kMaxCompactSeqs)
+    dequant_compact_kernel<<<dim3((unsigned)std::min<int64_t>(dq_blocks, 4 * (int64_t)num_sms())), 256,
+                             (L.batch + 1) * 4, stream>>>(p);
+  else if (dq_blocks > 0)
+    dequant_kernel<<<dim3((unsigned)(p.kt_rows / kKeys), (unsigned)L.batch), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -734,30 +893,34 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
   if (dev < 64 && !attr_set[dev]) {
     // The register split inside the kernel assumes the launch register count.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, prefill_kernel);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidDeviceFunction;
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
+    for (const void* fn : {(const void*)prefill_kernel<false>, (const void*)prefill_kernel<true>}) {
+      e = cudaFuncGetAttributes(&fa, fn);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidDeviceFunction;
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytesMax);
+      if (e != cudaSuccess) return e;
+    }
     attr_set[dev] = true;
   }
-  // Work split: whole q-tiles in full waves of the persistent grid; the q-tiles of a
-  // partial last wave are cut into `pieces` key ranges so that wave ends sooner (with r
-  // q-tiles left over, pieces = grid / r, at most 4; the pieces of one are merged after).
+  // Work split (work_split) of a chunk call's q-tiles.  A varlen call's q-tiles are
+  // counted on the device (whole, no pieces); the dense count here is the fallback when
+  // they are too many to list.
   const int64_t qtiles_total = (int64_t)L.batch * p.qtiles;
   const int sms = num_sms();
   const int grid = (int)(qtiles_total < sms ? qtiles_total : sms);
-  const int64_t rem = qtiles_total % grid;
-  int pieces = rem > 0 ? (int)(grid / rem) : 1;
-  if (pieces > 4) pieces = 4;
-  if (pieces < 2) pieces = 1;
-  p.pieces = pieces;
-  p.full_items = (int32_t)(pieces > 1 ? qtiles_total - rem : qtiles_total);
-  p.num_items = (int32_t)(p.full_items + (pieces > 1 ? rem * pieces : 0));
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  WorkSplit split = work_split(qtiles_total, grid);
+  if (p.compact) split = WorkSplit{(int)qtiles_total, 1, (int)qtiles_total};
+  p.pieces = split.pieces;
+  p.full_items = split.full;
+  p.num_items = split.num;
+  const int smem = p.compact ? kSmemBytesMax : kSmemBytes;
+  if (p.compact)
+    prefill_kernel<true><<<grid, kThreads, smem, stream>>>(p);
+  else
+    prefill_kernel<false><<<grid, kThreads, smem, stream>>>(p);
   e = cudaGetLastError();
-  if (e != cudaSuccess || pieces == 1) return e;
-  const int64_t warps_c = rem * (kQT * kRows);
+  if (e != cudaSuccess || split.pieces == 1) return e;
+  const int64_t warps_c = (int64_t)(split.num - split.full) / split.pieces * kRows;  // one warp per row
   return launch_pdl(combine_pieces_kernel, dim3((unsigned)((warps_c + 7) / 8)), dim3(256), 0, stream, p);
 }
 
