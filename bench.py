@@ -510,8 +510,8 @@ def run_mixed(args, rank, world):
         "vs_baseline": None, "dtype": "int8 KV, bf16 QK / fp16 PV, fp32 accumulate", "data": "synthetic",
         "config": {"workload": f"mixed: {n_dec} decode (L~U[1024,8192]) + {n_pf} chunks of {chunk} on 4096, Hq={Hq}, "
                                f"P={P}", "new_tokens": total, "kv_query_pairs": pairs},
-        "one_call": "cai_mqa_prefill_varlen: the one-token rows through the decode kernel, the chunks through the "
-                    "prefill kernel (two launches inside the call)",
+        "one_call": "cai_mqa_prefill_varlen: the chunks through the prefill kernel, then the one-token rows through "
+                    "the decode kernel, which starts on the SMs that the prefill's last wave leaves",
         "two_launch_ms_per_step": ms_two, "decode_rows_max_abs_diff_vs_decode_path": diff,
         "tflops": 4 * 128 * pairs / (ms_one * 1e-3) / 1e12, "gpu_launches": 2 * args.steps, "clocks": clocks,
     }

@@ -276,10 +276,12 @@ cai_status cai_gqa_decode(const cai_kv_pool* kv_pools, int32_t num_kv_heads, con
  * Other arguments, workspace and limits as cai_mqa_prefill_chunk.  A sequence whose
  * offsets are out of order, beyond total_new or longer than max_new, or whose
  * prefix_len + length exceeds the table, sets CAI_DEVERR_LENGTH; its rows (if its
- * offsets are valid) get out = 0, lse = -inf.  With num_q_heads <= 64 the call makes two
- * launches on `stream` (three when some of those rows are split): the sequences with
+ * offsets are valid) get out = 0, lse = -inf.  With num_q_heads <= 64 the sequences with
  * exactly one new token run through the decode kernel and the prefill kernel skips
- * them; the results are the same either way. */
+ * them (the results are the same either way): on `stream`, the prefill's key copy and
+ * attention launches, then the decode launch (and its split combine), which shares no
+ * memory with the prefill and starts on the SMs that the prefill's CTAs leave; it ends
+ * after the prefill, so work later in the stream finds both complete. */
 cai_status cai_mqa_prefill_varlen(const cai_kv_pool* pool, const uint16_t* q, int32_t batch,
                                   const int32_t* q_offsets, int32_t total_new, int32_t max_new, int32_t num_q_heads,
                                   const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* prefix_len,

@@ -268,6 +268,7 @@ cai_status decode_layers_common(const LayerArgs* layers, int32_t n, int32_t num_
   p.err = err_flag;
   p.wait_ns = wait_limit_ns();
   p.drop_stage = fault_drop_stage();
+  p.overlap_prev = 0;
   // Job order: global layers first, then wider windows first (stable).
   int order[kMaxDecodeJobs];
   for (int l = 0; l < n; ++l) order[l] = l;
@@ -465,12 +466,21 @@ cai_status prefill_common(const cai_kv_pool* pool, const uint16_t* q, int32_t ba
   // kernel runs them (with this call's window and scale, split as a decode call would be) and the
   // prefill kernel skips them, so they pay neither the prefill's 256-row q-tiles nor its
   // dequantised copy of their keys.  Its queue counters sit at the end of the workspace.
+  // The two kernels share no memory (the decode writes the one-token rows and its
+  // partials, the prefill the other rows and its copy of the keys), so the decode is
+  // launched after the prefill without waiting for it: its CTAs take the SMs that the
+  // prefill's last, partial wave leaves idle, and its queue hands them the items.
   L.skip_single = q_off != nullptr && num_q_heads <= kDecodeMaxHeads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (L.skip_single) {
     void* hdr = static_cast<uint8_t*>(workspace) + (need - kWorkspaceHeader);
     cudaError_t e = cudaMemsetAsync(hdr, 0, kWorkspaceHeader, s);
     if (e != cudaSuccess) return cuda_status(e);
+  }
+  cudaError_t e = launch_prefill(L, s);
+  if (e != cudaSuccess || !L.skip_single) return cuda_status(e);
+  {
+    void* hdr = static_cast<uint8_t*>(workspace) + (need - kWorkspaceHeader);
     DecodeParams d;
     d.pages[0] = static_cast<const uint8_t*>(pool->pages);
     d.slot_pages[0] = pool->num_pages;
@@ -489,6 +499,7 @@ cai_status prefill_common(const cai_kv_pool* pool, const uint16_t* q, int32_t ba
     d.err = err_flag;
     d.wait_ns = wait_limit_ns();
     d.drop_stage = fault_drop_stage();
+    d.overlap_prev = 1;
     DecodeJob& jb = d.job[0];
     jb.slot0 = 0;
     jb.window = window;
@@ -497,9 +508,9 @@ cai_status prefill_common(const cai_kv_pool* pool, const uint16_t* q, int32_t ba
     jb.q = q;
     jb.out = out;
     jb.lse_out = lse_out;
-    // The automatic split plan, its partials in the workspace's piece region (free until
-    // the prefill kernel, later on the stream, writes its own pieces there); fewer splits
-    // when they would not fit.
+    // The automatic split plan, its partials in the workspace's piece region (a varlen
+    // call's prefill cuts no q-tile into pieces, so the region is the decode's); fewer
+    // splits when they would not fit.
     void* region = nullptr;
     size_t region_bytes = 0;
     prefill_piece_region(workspace, batch, max_pages_per_seq, pool->page_size, &region, &region_bytes);
@@ -523,9 +534,8 @@ cai_status prefill_common(const cai_kv_pool* pool, const uint16_t* q, int32_t ba
     for (int k = 1; k < kMaxDecodeJobs; ++k) d.job[k] = jb;
     d.num_items = batch * plan.max_splits;
     e = launch_decode(d, pool->page_size, s);
-    if (e != cudaSuccess) return cuda_status(e);
   }
-  return cuda_status(launch_prefill(L, s));
+  return cuda_status(e);
 }
 
 }  // namespace

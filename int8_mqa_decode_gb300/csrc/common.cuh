@@ -83,6 +83,10 @@ struct DecodeParams {
   int32_t* err;
   uint64_t wait_ns;                   // limit of every bounded wait inside the kernel
   int32_t drop_stage;                 // fault injection: K/V stage each CTA skips (-1: none)
+  // 1: the kernel before this launch in the stream touches none of its memory and was
+  // itself started only after everything before it had completed, so the launch does
+  // not wait for it (it starts on SMs as that kernel's CTAs leave them).
+  int32_t overlap_prev;
 };
 
 // Attended range and split bookkeeping shared by the decode and combine kernels.

@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   const uint32_t tmem = *tmem_slot;
   // Everything above touched only this CTA's own resources; from here on the kernel
   // reads and writes memory that the previous kernels in the stream may still use.
-  grid_dependency_wait();
+  if (!p.overlap_prev) grid_dependency_wait();
   grid_launch_dependents();
 
   // Item k of this CTA as published by the scheduler warp; every reader warp
@@ -959,6 +959,9 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   __syncthreads();
   if (tid == 0 && *abort_flag) set_err(p.err, CAI_DEVERR_TIMEOUT);
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  // A launch that did not wait for the kernel before it ends only after that kernel, so
+  // that whatever follows in the stream finds both complete.
+  if (p.overlap_prev) grid_dependency_wait();
 }
 
 // One warp per (sequence, head): merge the partial outputs of the splits by

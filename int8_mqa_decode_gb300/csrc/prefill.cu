@@ -462,6 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // A varlen call's decode launch, next in the stream, shares no memory with this grid:
+  // it may start now, its CTAs taking the SMs that this grid's CTAs leave.  (Chunk calls
+  // do not trigger early: measured 3.6% slower on the append-prefill workload.)
+  if (kCompact) grid_launch_dependents();
   // A varlen call's item list, if it was built (above).
   const int n_list = kCompact ? *reinterpret_cast<const int32_t*>(smem + kOffTable) : -1;
   const int32_t* table = n_list >= 0 ? reinterpret_cast<const int32_t*>(smem + kOffTable + 16) : nullptr;
@@ -829,9 +833,9 @@ size_t prefill_workspace_bytes(int32_t batch, int32_t max_pages_per_seq, int32_t
   return (size_t)(2 * a + 2 * s + ((piece_bytes() + 255) / 256) * 256 + kWorkspaceHeader);
 }
 
-// The piece region of a prefill workspace: the prefill kernel writes the last wave's
-// partial outputs there, and a varlen call's decode launch, which runs before it on the
-// same stream, may keep its split partials there.
+// The piece region of a prefill workspace: a chunk call's prefill kernel writes the last
+// wave's partial outputs there; a varlen call's prefill writes none, and its decode launch
+// may keep its split partials there.
 void prefill_piece_region(void* workspace, int32_t batch, int32_t max_pages_per_seq, int32_t page_size,
                           void** region, size_t* bytes) {
   const int64_t kt = ((int64_t)max_pages_per_seq * page_size + kKeys - 1) / kKeys * kKeys;
