@@ -124,6 +124,53 @@ def test_prefill_gives_up_then_recovers():
         assert np.abs(got_lse[b][tokens] - l_ref).max() <= ATOL, b
 
 
+def test_varlen_gives_up_then_recovers():
+    """A continuous-batching call: its prefill launch and the decode launch that runs beside it
+    (without waiting for it) both give up; the call still ends, and the next one is right."""
+    import synth.gpu as sgpu
+    synth.gpu.build()
+    prefix = np.array([900, 3000, 500, 2000, 64])
+    n_new = np.array([1, 128, 1, 64, 1])
+    L = prefix + n_new
+    w = synth.Workload("timeout-varlen", len(prefix), 32, 16, L, [0], [0], n_new=1, seed=36)
+    cache = harness.PagedCache(w)
+    cache.fill(upto=L)
+    off = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
+    total = int(off[-1])
+    q = torch.empty(total, w.num_q_heads, 128, dtype=torch.bfloat16, device="cuda")
+    for b in range(len(prefix)):
+        qb = torch.empty(1, int(n_new[b]) * w.num_q_heads, 128, dtype=torch.bfloat16, device="cuda")
+        sgpu.q_rows(qb, w.seed, synth.STREAM_Q_PREFILL, b)
+        q[off[b]:off[b + 1]] = qb.view(int(n_new[b]), w.num_q_heads, 128)
+    off_d = torch.from_numpy(off).cuda()
+    prefix_d = torch.from_numpy(prefix.astype(np.int32)).cuda()
+    out = torch.empty(total, w.num_q_heads, 128, device="cuda")
+    lse = torch.empty(total, w.num_q_heads, device="cuda")
+    ws = cache.prefill_workspace()
+
+    def call(err):
+        cai.cai_mqa_prefill_varlen(cache.pools[0], q, off_d, int(n_new.max()), cache.table, prefix_d, 0,
+                                   w.softmax_scale, ws, out, lse, err)
+
+    assert timed_out(call, 1)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out.fill_(float("nan"))
+    lse.fill_(float("nan"))
+    call(err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got, got_lse = out.cpu().numpy(), lse.cpu().numpy()
+    for b in range(len(prefix)):
+        n = int(n_new[b])
+        kc, ks, vc, vs = oracle.seq_kv(w.seed, 0, b, int(L[b]))
+        qb = synth.q_rows(w.seed, synth.STREAM_Q_PREFILL, b, n * w.num_q_heads).reshape(n, w.num_q_heads, 128)
+        tokens = [0, n - 1] if n > 1 else [0]
+        o_ref, l_ref = oracle.prefill_seq(qb, kc, ks, vc, vs, int(prefix[b]), 0, w.softmax_scale, tokens)
+        rows = [int(off[b]) + t for t in tokens]
+        assert np.abs(got[rows] - o_ref).max() <= ATOL, b
+        assert np.abs(got_lse[rows] - l_ref).max() <= ATOL, b
+
+
 def test_defaults_are_restored():
     """After the tests above the injection is off and the default limit is back."""
     w = synth.workload(1)
