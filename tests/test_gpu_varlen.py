@@ -108,3 +108,52 @@ def test_varlen_invalid_offsets_flagged():
     assert err & cai.CAI_DEVERR_LENGTH
     assert np.all(np.isfinite(out[0:8])) and np.all(np.isfinite(lse[0:8]))
     assert np.all(np.isnan(out[8:12])) and np.all(np.isnan(lse[8:12]))
+
+
+def check_all_rows(w, off, out, lse, prefix, n_new, window=0):
+    for b in range(len(prefix)):
+        n = int(n_new[b])
+        if n == 0:
+            continue
+        o_ref, l_ref = oracle_rows(w, b, int(prefix[b]), n, window)
+        rows = slice(off[b], off[b + 1])
+        assert np.abs(out[rows] - o_ref).max() <= ATOL, b
+        assert np.abs(lse[rows] - l_ref).max() <= ATOL, b
+
+
+@pytest.mark.parametrize("Hq,P", [(64, 16), (8, 32), (128, 64)])
+def test_varlen_heads_and_page_sizes(Hq, P):
+    """64 heads (the decode kernel's two-warpgroup softmax beside the prefill), a small
+    head count with 32-token pages, and 128 heads (beyond the decode kernel: every row
+    goes through the prefill kernel) with 64-token pages."""
+    prefix = [900, 37, 2500, 400, 1]
+    n_new = [1, 20, 1, 130, 1]
+    w, cache, off, out, lse, err = mixed_case(prefix, n_new, Hq=Hq, P=P, seed=73)
+    assert err == 0
+    check_all_rows(w, off, out, lse, prefix, n_new)
+
+
+def test_varlen_many_decode_rows_few_chunks():
+    """Most of the batch is one-token rows: the decode launch beside the prefill's few
+    q-tiles takes most of the SMs."""
+    rng = np.random.default_rng(5)
+    n_dec = 300
+    prefix = np.concatenate([rng.integers(1, 3000, n_dec), [1500, 200]])
+    n_new = np.concatenate([np.ones(n_dec, np.int64), [96, 33]])
+    w, cache, off, out, lse, err = mixed_case(prefix, n_new, seed=79)
+    assert err == 0
+    sample = list(range(0, n_dec, 37)) + [n_dec - 1, n_dec, n_dec + 1]
+    for b in sample:
+        o_ref, l_ref = oracle_rows(w, b, int(prefix[b]), int(n_new[b]), 0)
+        rows = slice(off[b], off[b + 1])
+        assert np.abs(out[rows] - o_ref).max() <= ATOL, b
+        assert np.abs(lse[rows] - l_ref).max() <= ATOL, b
+
+
+def test_varlen_only_decode_rows():
+    """No chunk at all: the prefill launch has no q-tile and the decode launch does everything."""
+    prefix = [10, 1000, 5000, 129]
+    n_new = [1, 1, 1, 1]
+    w, cache, off, out, lse, err = mixed_case(prefix, n_new, seed=83)
+    assert err == 0
+    check_all_rows(w, off, out, lse, prefix, n_new)
