@@ -215,6 +215,7 @@ def profiled_traffic(workload_tag: str):
 
 # ----------------------------------------------------------------------------- CPU oracle leg
 
+L2_BYTES = 129 * 1024 * 1024  # GB300 L2
 PARITY_ATOL = 2e-3  # max abs error of attention outputs against the float64 oracle
 
 
@@ -374,30 +375,36 @@ def run_prefill(args, rank, world):
         if rec is not None:
             rec[1].record(stream)
 
+    # The step's KV pages (and the copy the dequant pass writes) fit in L2: L2 is flushed
+    # between timed steps by a write of twice its size, outside each step's event pair.
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     barrier(world)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(smi_index(torch.cuda.current_device())) as clocks:
         torch.cuda.synchronize()
         if args.ncu:
             torch.cuda.profiler.start()
         clocks.start()
-        # Pass 1, the step throughput, without events between launches; pass 2, the same
-        # steps with an event pair around the prefill call, for the kernel's duration.
-        t0.record(stream)
+        # Pass 1, the step (append + prefill call), one event pair per step; pass 2, the same
+        # steps with an event pair around the prefill call, for the kernels' duration.
         for s in range(args.steps):
+            flush_buf.fill_(s & 255)
+            step_ev[s][0].record(stream)
             step()
-        t1.record(stream)
+            step_ev[s][1].record(stream)
         torch.cuda.synchronize()
         if args.ncu:
             torch.cuda.profiler.stop()
         for s in range(args.steps):
+            flush_buf.fill_(s & 255)
             step(ev[s])
         torch.cuda.synchronize()
         clocks.stop()
-    ms = allreduce_max(t0.elapsed_time(t1), world)
+    ms = allreduce_max(sum(a.elapsed_time(b) for a, b in step_ev), world)
     kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     parity = prefill_parity(w, out.cpu().numpy()) if rank == 0 and not args.no_parity else None
     flops, pairs = prefill_flops(w)
@@ -409,7 +416,8 @@ def run_prefill(args, rank, world):
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 KV, bf16/fp16 MMA / fp32 accumulate", "data": "synthetic",
         "config": {"workload": w.name, "global_batch": w.batch * world, "kv_query_pairs_per_head": pairs,
-                   "flops_per_step": flops, "parallelism": f"replicas x{world}"},
+                   "flops_per_step": flops, "parallelism": f"replicas x{world}",
+                   "l2": "L2 flushed between timed steps (a write of twice its size, outside each step's event pair)"},
         "gpu_launches": prefill_launches(w) * args.steps,
         # The launches are timed alone (a sub-millisecond burst), so the burst peak is the
         # denominator; the sustained figure is kept for reference.
@@ -692,6 +700,15 @@ def run_gpu(args, rank, world):
                                              w.layer_windows[layer], args.num_splits) > 256)
     launches_per_step = 1 + (1 if layered else nl) + splits_layers
 
+    # A step whose KV fits in L2 twice over would read it back from L2 in the next step:
+    # such workloads (the tiny and the local-layer ones) flush L2 between timed steps by
+    # writing a buffer of twice its size, outside each step's own event pair.
+    _, kv_bytes_step = step_work(w)
+    flush_buf = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+                 if kv_bytes_step < 2 * L2_BYTES else None)
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] if flush_buf is not None else None
+
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -704,10 +721,16 @@ def run_gpu(args, rank, world):
             torch.cuda.profiler.start()
         clocks.start()
         # Pass 1, the step throughput: no events between the launches (an event between two
-        # launches chained by programmatic dependent launch holds the second one back).
+        # launches chained by programmatic dependent launch holds the second one back); with
+        # an L2 flush between steps, one event pair per step and the flush outside it.
         t_start.record(stream)
         for s in range(args.steps):
+            if flush_buf is not None:
+                flush_buf.fill_(s & 255)
+                step_ev[s][0].record(stream)
             step()
+            if flush_buf is not None:
+                step_ev[s][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         if args.ncu:
@@ -715,10 +738,13 @@ def run_gpu(args, rank, world):
         # Pass 2, the same steps with an event pair around every decode launch: the kernel's
         # average launch duration for the roofline.
         for s in range(args.steps):
+            if flush_buf is not None:
+                flush_buf.fill_(s & 255)
             step(ev[s])
         torch.cuda.synchronize()
         clocks.stop()
-    ms_total = t_start.elapsed_time(t_end)
+    ms_total = (t_start.elapsed_time(t_end) if flush_buf is None
+                else sum(a.elapsed_time(b) for a, b in step_ev))
     decode_ms = sum(ev[s][2 * l].elapsed_time(ev[s][2 * l + 1]) for s in range(args.steps) for l in range(n_events))
     ms_max = allreduce_max(ms_total, world)
 
@@ -747,7 +773,9 @@ def run_gpu(args, rank, world):
         "data": "synthetic (seeded Irwin-Hall normals, lengths and permuted block tables)",
         "config": {"workload": w.name, "global_batch": w.batch * world, "seq_len": "lognormal" if args.config == 3
                    else "uniform", "kv_tokens_per_step": toks_step, "num_splits": args.num_splits or "auto",
-                   "l2": "KV read per step larger than L2 (129 MB); KV loads are L2 evict-first",
+                   "l2": ("KV read per step larger than L2 (129 MB); KV loads are L2 evict-first"
+                          if flush_buf is None else
+                          "L2 flushed between timed steps (a write of twice its size, outside each step's event pair)"),
                    "parallelism": f"replicas x{world} (independent sequences per GPU)",
                    "kv_pool_bytes": cache.pool_bytes(),
                    **({"local_ring_pages": [r for r in cache.ring if r]} if args.local_ring else {})},
