@@ -366,3 +366,29 @@ def test_decode_step_appends_then_attends():
     for layer in (0, 5):
         out, lse = run_decode(cache, layer, 0)
         check_layer(cache, layer, out, lse)
+
+
+@pytest.mark.parametrize("q_scale", [8.0, 32.0])
+def test_decode_sharp_logits_raise_the_reference(q_scale):
+    """Queries scaled by a power of two (exact in bf16) spread the logits over tens of log2
+    units, so the shared per-head references rise many times inside an item (rescaling the
+    accumulated output), and most weights underflow: a global and a local layer in one launch,
+    one of them split, against the oracle."""
+    w = make_workload(3, 32, 16, [3000, 700, 9000], windows=(0, 1024), l2b=(0, 0), seed=91)
+    cache = build(w)
+    qs = [cache.decode_q(layer).mul_(q_scale) for layer in range(2)]
+    outs = [torch.full((3, 32, 128), float("nan"), device="cuda") for _ in range(2)]
+    lses = [torch.full((3, 32), float("nan"), device="cuda") for _ in range(2)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache.decode_layers(qs, outs, lses, num_splits=3, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for layer in range(2):
+        q_bits = qs[layer].view(torch.int16).cpu().numpy().view(np.uint16)
+        got, got_lse = outs[layer].cpu().numpy(), lses[layer].cpu().numpy()
+        for b in range(3):
+            L = int(w.ctx_len[b])
+            kc, ks, vc, vs = oracle.seq_kv(w.seed, 0, b, L)
+            o_ref, l_ref = oracle.decode_seq(q_bits[b], kc, ks, vc, vs, L, w.layer_windows[layer], w.softmax_scale)
+            assert np.abs(got[b] - o_ref).max() <= ATOL, (layer, b)
+            assert np.abs(got_lse[b] - l_ref).max() <= ATOL, (layer, b)

@@ -122,3 +122,30 @@ def test_prefill_split_last_wave(window):
         o_ref, l_ref = oracle_prefill(w, b, tokens)
         assert np.abs(out[b][tokens] - o_ref).max() <= ATOL, b
         assert np.abs(lse[b][tokens] - l_ref).max() <= ATOL, b
+
+
+@pytest.mark.parametrize("q_scale", [8.0, 32.0])
+def test_prefill_sharp_logits_raise_the_reference(q_scale):
+    """Queries scaled by a power of two (exact in bf16): the half-row references rise many
+    times along the keys and most weights underflow; sampled tokens against the oracle."""
+    prefix, n_new = np.array([2500, 700]), 64
+    w = synth.Workload("sharp-prefill", 2, 32, 16, prefix + n_new, [0], [0], n_new=n_new, seed=93)
+    cache = harness.PagedCache(w)
+    cache.fill()
+    cache.append_step()
+    q = cache.prefill_q().mul_(q_scale)
+    out = torch.full((2, n_new, 32, 128), float("nan"), device="cuda")
+    lse = torch.full((2, n_new, 32), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache.prefill(q, out, lse, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got, got_lse = out.cpu().numpy(), lse.cpu().numpy()
+    q_bits = q.view(torch.int16).cpu().numpy().view(np.uint16)
+    tokens = [0, 1, 31, 62, 63]
+    for b in range(2):
+        L = int(w.ctx_len[b])
+        kc, ks, vc, vs = oracle.seq_kv(w.seed, 0, b, L)
+        o_ref, l_ref = oracle.prefill_seq(q_bits[b], kc, ks, vc, vs, L - n_new, 0, w.softmax_scale, tokens)
+        assert np.abs(got[b][tokens] - o_ref).max() <= ATOL, b
+        assert np.abs(got_lse[b][tokens] - l_ref).max() <= ATOL, b
