@@ -141,6 +141,28 @@ __device__ __forceinline__ bool seq_ok(const PrefillParams& p, int32_t p0, int n
   return n >= 0 && p0 >= 0 && (int64_t)p0 + n <= (int64_t)p.max_pages * p.page_size;
 }
 
+// 8 x 8 bytes across the 8 lanes q = lane % 8 of an aligned group: lane q enters with
+// row q (bytes 0..3 in a, 4..7 in b) and leaves with column q (rows 0..3 in a, 4..7 in
+// b).  Three exchanges: 4-byte blocks with lane q ^ 4, 2-byte blocks with q ^ 2, bytes
+// with q ^ 1.
+__device__ __forceinline__ void transpose8x8_bytes(uint32_t& a, uint32_t& b, int q) {
+  {
+    const uint32_t r = __shfl_xor_sync(0xffffffffu, (q & 4) ? a : b, 4);
+    if (q & 4) a = r;
+    else b = r;
+  }
+  {
+    const uint32_t ra = __shfl_xor_sync(0xffffffffu, a, 2), rb = __shfl_xor_sync(0xffffffffu, b, 2);
+    a = (q & 2) ? __byte_perm(ra, a, 0x7632) : __byte_perm(a, ra, 0x5410);
+    b = (q & 2) ? __byte_perm(rb, b, 0x7632) : __byte_perm(b, rb, 0x5410);
+  }
+  {
+    const uint32_t ra = __shfl_xor_sync(0xffffffffu, a, 1), rb = __shfl_xor_sync(0xffffffffu, b, 1);
+    a = (q & 1) ? __byte_perm(a, ra, 0x3715) : __byte_perm(a, ra, 0x6240);
+    b = (q & 1) ? __byte_perm(b, rb, 0x3715) : __byte_perm(b, rb, 0x6240);
+  }
+}
+
 // Tile `tile` of sequence b's copy, by a block of 256 threads, one warp per 16 rows;
 // a tile that no query of the chunk reads returns at once.
 __device__ __forceinline__ void dequant_tile(const PrefillParams& p, int b, int tile) {
@@ -184,6 +206,14 @@ __device__ __forceinline__ void dequant_tile(const PrefillParams& p, int b, int 
         atomicOr(p.err, CAI_DEVERR_PAGE);
       }
     }
+    // The page of the group's 8 keys (one page: 8 divides P), for the V loads, if any of
+    // them is attended.
+    const int t0 = tile * kKeys + warp * 16 + grp * 8;
+    const uint8_t* pg8 = nullptr;
+    if (t0 < len && t0 + 8 > lo_min) {
+      const int32_t page = p.table[(int64_t)b * p.max_pages + t0 / P];
+      if (page >= 0 && page < p.num_pages) pg8 = p.pages + (int64_t)page * page_bytes(P) + P * kHeadDim + t0 % P;
+    }
     const int64_t row = (int64_t)b * p.kt_rows + t;
     if (lane < 8) p.ks[row] = ksc;
     uint16_t* kt = p.kb + ((int64_t)b * p.kt_rows + tile * kKeys) * kHeadDim + rr * 8;
@@ -192,13 +222,18 @@ __device__ __forceinline__ void dequant_tile(const PrefillParams& p, int b, int 
     for (int i = 0; i < 4; ++i) {
       const int c = 4 * i + (lane >> 3);  // channels 8c .. 8c + 7
       uint2 kw = make_uint2(0u, 0u);
+      if (pg) kw = *reinterpret_cast<const uint2*>(pg + slot * kHeadDim + c * 8);
+      // V is channel-major in the page (channel d's P codes at d * P): lane q of the 8
+      // lanes of chunk c loads channel 8c + q of the group's 8 keys (8 contiguous bytes),
+      // and the transpose leaves each lane the 8 channels of its own key.
       uint32_t vw[2] = {0u, 0u};
-      if (pg) {
-        kw = *reinterpret_cast<const uint2*>(pg + slot * kHeadDim + c * 8);
-        const uint8_t* vcol = pg + P * kHeadDim + slot;  // channel-major V block: channel d at d * P
-#pragma unroll
-        for (int e = 0; e < 8; ++e) vw[e >> 2] |= (uint32_t)vcol[(c * 8 + e) * P] << (8 * (e & 3));
+      if (pg8) {
+        const uint2 v8 = *reinterpret_cast<const uint2*>(pg8 + (c * 8 + (lane & 7)) * P);
+        vw[0] = v8.x;
+        vw[1] = v8.y;
       }
+      transpose8x8_bytes(vw[0], vw[1], lane & 7);
+      if (!pg) vw[0] = vw[1] = 0u;
       // int8 -> bf16 (K) and int8 -> fp16 (V): exact for |code| <= 127.
       uint32_t ko[4], vo[4];
 #pragma unroll
