@@ -676,18 +676,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(s_read);
+          // Chunk calls: packed fp32 pairs, two FFMAs per instruction (in the varlen
+          // instantiation the pairs cost register spills, so it keeps scalar FFMAs).
+          const uint64_t nm2 = f2(-m_use, -m_use);
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             const float4 a = *reinterpret_cast<const float4*>(kscale + e);
-            z[e] = fmaf(__uint_as_float(r0[e]), a.x, -m_use);
-            z[e + 1] = fmaf(__uint_as_float(r0[e + 1]), a.y, -m_use);
-            z[e + 2] = fmaf(__uint_as_float(r0[e + 2]), a.z, -m_use);
-            z[e + 3] = fmaf(__uint_as_float(r0[e + 3]), a.w, -m_use);
             const float4 a2 = *reinterpret_cast<const float4*>(kscale + 32 + e);
-            z[32 + e] = fmaf(__uint_as_float(r1[e]), a2.x, -m_use);
-            z[32 + e + 1] = fmaf(__uint_as_float(r1[e + 1]), a2.y, -m_use);
-            z[32 + e + 2] = fmaf(__uint_as_float(r1[e + 2]), a2.z, -m_use);
-            z[32 + e + 3] = fmaf(__uint_as_float(r1[e + 3]), a2.w, -m_use);
+            if constexpr (!kCompact) {
+              f2_split(f2_fma(f2(__uint_as_float(r0[e]), __uint_as_float(r0[e + 1])), f2(a.x, a.y), nm2), z[e],
+                       z[e + 1]);
+              f2_split(f2_fma(f2(__uint_as_float(r0[e + 2]), __uint_as_float(r0[e + 3])), f2(a.z, a.w), nm2),
+                       z[e + 2], z[e + 3]);
+              f2_split(f2_fma(f2(__uint_as_float(r1[e]), __uint_as_float(r1[e + 1])), f2(a2.x, a2.y), nm2),
+                       z[32 + e], z[32 + e + 1]);
+              f2_split(f2_fma(f2(__uint_as_float(r1[e + 2]), __uint_as_float(r1[e + 3])), f2(a2.z, a2.w), nm2),
+                       z[32 + e + 2], z[32 + e + 3]);
+            } else {
+              z[e] = fmaf(__uint_as_float(r0[e]), a.x, -m_use);
+              z[e + 1] = fmaf(__uint_as_float(r0[e + 1]), a.y, -m_use);
+              z[e + 2] = fmaf(__uint_as_float(r0[e + 2]), a.z, -m_use);
+              z[e + 3] = fmaf(__uint_as_float(r0[e + 3]), a.w, -m_use);
+              z[32 + e] = fmaf(__uint_as_float(r1[e]), a2.x, -m_use);
+              z[32 + e + 1] = fmaf(__uint_as_float(r1[e + 1]), a2.y, -m_use);
+              z[32 + e + 2] = fmaf(__uint_as_float(r1[e + 2]), a2.z, -m_use);
+              z[32 + e + 3] = fmaf(__uint_as_float(r1[e + 3]), a2.w, -m_use);
+            }
           }
         }
         if (!(key0 >= k_lo && key0 + 63 <= q_pos)) {
@@ -733,18 +747,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         }
         // P = 2^z as fp16 into this half's 32 columns of P buffer b, the A operand of
         // this half's PV, once the PVs of tile g - 2 have read that buffer.
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four running sums (chunk calls: as two fp32 pairs)
+        uint64_t l01 = 0ull, l23 = 0ull;
         uint32_t pw[32];
 #pragma unroll
         for (int e = 0; e < 64; e += 4) {
           const float e0 = ex2_approx(z[e]), e1 = ex2_approx(z[e + 1]);
           const float e2 = ex2_approx(z[e + 2]), e3 = ex2_approx(z[e + 3]);
-          l4[0] += e0;
-          l4[1] += e1;
-          l4[2] += e2;
-          l4[3] += e3;
+          if constexpr (!kCompact) {
+            l01 = f2_add(l01, f2(e0, e1));
+            l23 = f2_add(l23, f2(e2, e3));
+          } else {
+            l4[0] += e0;
+            l4[1] += e1;
+            l4[2] += e2;
+            l4[3] += e3;
+          }
           pw[e / 2] = pack_f16x2(e0, e1);
           pw[e / 2 + 1] = pack_f16x2(e2, e3);
+        }
+        if constexpr (!kCompact) {
+          f2_split(l01, l4[0], l4[1]);
+          f2_split(l23, l4[2], l4[3]);
         }
         if (g >= kPBuf) {
           ok = mbar_wait_polled_warp(&pv_done[b], ((g / kPBuf) - 1) & 1, wctl);
