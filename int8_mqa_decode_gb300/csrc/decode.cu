@@ -76,8 +76,8 @@ struct Layout {
   static constexpr int kOffPT = kOffRawKV + NST * kStageKV;      // P^T[2]
   static constexpr int kOffQT = kOffPT + 2 * kPTBytes;           // Q^T
   static constexpr int kOffRawSc = kOffQT + HN * kHeadDim * 2;   // [NST][512 B]
-  static constexpr int kOffScal = kOffRawSc + NST * kStageSc;    // [4][3][T] floats
-  static constexpr int kOffXch = kOffScal + kScaleSlots * 3 * T * 4;  // softmax exchange, 13 x HN floats
+  static constexpr int kOffScal = kOffRawSc + NST * kStageSc;    // [4][T] float4s
+  static constexpr int kOffXch = kOffScal + kScaleSlots * T * 16;  // softmax exchange, 13 x HN floats
   static constexpr int kOffBars = kOffXch + 13 * HN * 4;
   static_assert(kOffXch % 16 == 0 && kOffPT % 16 == 0, "bulk-copy sources");
   static constexpr int kNumBars = 2 * NST + 2 * 2 /*k_full, v_full*/ + 2 * 2 /*s_full, p_full*/ + 2 /*v_free*/ +
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
   uint8_t* raw_sc = smem + L::kOffRawSc;
   uint8_t* pt = smem + L::kOffPT;
   uint8_t* qt = smem + L::kOffQT;
-  float* scal = reinterpret_cast<float*>(smem + L::kOffScal);  // [kScaleSlots][k scale, valid, v scale][T]
+  float4* scal = reinterpret_cast<float4*>(smem + L::kOffScal);  // [kScaleSlots][T] (k scale, valid, v scale, 0)
   float* xch = reinterpret_cast<float*>(smem + L::kOffXch);
   float* wmax = xch;              // [4][HN] per-warp maxima
   float* lpart = xch + 4 * HN;    // [4][HN] per-warp sums
@@ -667,10 +667,8 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
           const int abs_t = (it.tile0 + t) * T + tt;
           const bool valid = abs_t >= it.start && abs_t < it.end && ((page_ok[s] >> (tr / P)) & 1u);
           const float* sc = reinterpret_cast<const float*>(raw_sc + s * kStageSc + (tr / P) * (8 * P));
-          float* dst = scal + ss * 3 * T;
-          dst[tt] = valid ? sc[tr % P] * p.scale_log2 : 0.0f;
-          dst[T + tt] = valid ? 1.0f : 0.0f;
-          dst[2 * T + tt] = valid ? sc[P + tr % P] : 0.0f;
+          scal[ss * T + tt] = valid ? make_float4(sc[tr % P] * p.scale_log2, 1.0f, sc[P + tr % P], 0.0f)
+                                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
         __syncwarp();
         if (lane == 0) {
@@ -774,10 +772,10 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
 #pragma unroll
           for (int i = 0; i < HH; ++i) sv[i] = __uint_as_float(r[i]);
         }
-        const float* sc = scal + ss * 3 * T;
-        const float ks = sc[tok];
-        const bool valid = sc[T + tok] != 0.0f;
-        const float vs = sc[2 * T + tok];
+        const float4 sc = scal[ss * T + tok];
+        const float ks = sc.x;
+        const bool valid = sc.y != 0.0f;
+        const float vs = sc.z;
         if (t == 0) {
           // A new item's references: the logits of its first attended token plus a margin,
           // shared by the thread that holds it (-inf when that token is masked: the raise
