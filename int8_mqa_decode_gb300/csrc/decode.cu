@@ -795,21 +795,13 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
         // e_h = logit (log2 units) minus the head's reference.
         float mx = -INFINITY;
         if (valid) {
-          // (Packed fp32 pairs at 32 heads; at 64 heads, where the softmax runs at 136
-          // registers, the pairs cost it spills, so it keeps scalar FFMAs.)
+          // Packed fp32 pairs: two FFMAs per instruction.
           const uint64_t ks2 = f2(ks, ks);
 #pragma unroll
           for (int h = 0; h < HH; h += 4) {
             const float4 mu = *reinterpret_cast<const float4*>(muse + h0 + h);
-            if constexpr (kSoftWarps == 4) {
-              f2_split(f2_fma(f2(sv[h], sv[h + 1]), ks2, f2(-mu.x, -mu.y)), sv[h], sv[h + 1]);
-              f2_split(f2_fma(f2(sv[h + 2], sv[h + 3]), ks2, f2(-mu.z, -mu.w)), sv[h + 2], sv[h + 3]);
-            } else {
-              sv[h] = fmaf(sv[h], ks, -mu.x);
-              sv[h + 1] = fmaf(sv[h + 1], ks, -mu.y);
-              sv[h + 2] = fmaf(sv[h + 2], ks, -mu.z);
-              sv[h + 3] = fmaf(sv[h + 3], ks, -mu.w);
-            }
+            f2_split(f2_fma(f2(sv[h], sv[h + 1]), ks2, f2(-mu.x, -mu.y)), sv[h], sv[h + 1]);
+            f2_split(f2_fma(f2(sv[h + 2], sv[h + 3]), ks2, f2(-mu.z, -mu.w)), sv[h + 2], sv[h + 3]);
             mx = fmax3(mx, fmax3(sv[h], sv[h + 1], sv[h + 2]), sv[h + 3]);
           }
         }
@@ -878,18 +870,11 @@ __global__ void __launch_bounds__(Roles<HN>::kThreads, 1) decode_kernel(const __
               uint32_t w[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float p0 = ex2_approx(sv[h8 + 2 * e]), p1 = ex2_approx(sv[h8 + 2 * e + 1]);
-                if constexpr (kSoftWarps == 4) {
-                  const uint64_t pp = f2(p0, p1);
-                  f2_split(f2_add(f2(l[h8 + 2 * e], l[h8 + 2 * e + 1]), pp), l[h8 + 2 * e], l[h8 + 2 * e + 1]);
-                  float q0, q1;
-                  f2_split(f2_mul(pp, vs2), q0, q1);
-                  w[e] = pack_f16x2(q0, q1);
-                } else {
-                  l[h8 + 2 * e] += p0;
-                  l[h8 + 2 * e + 1] += p1;
-                  w[e] = pack_f16x2(p0 * vs, p1 * vs);
-                }
+                const uint64_t pp = f2(ex2_approx(sv[h8 + 2 * e]), ex2_approx(sv[h8 + 2 * e + 1]));
+                f2_split(f2_add(f2(l[h8 + 2 * e], l[h8 + 2 * e + 1]), pp), l[h8 + 2 * e], l[h8 + 2 * e + 1]);
+                float q0, q1;
+                f2_split(f2_mul(pp, vs2), q0, q1);
+                w[e] = pack_f16x2(q0, q1);
               }
               *reinterpret_cast<uint4*>(dst + (h8 / 8) * 2048) = make_uint4(w[0], w[1], w[2], w[3]);
             }
