@@ -14,7 +14,7 @@ static inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static inline bool page_size_ok(int32_t P) { return P == 16 || P == 32 || P == 64; }
 constexpr int32_t kItemsPerSmAlone = 32;  // a global layer's split target when launched alone
-constexpr int32_t kItemsPerSmMixed = 6;   // ... when launched together with local layers
+constexpr int32_t kItemsPerSmMixed = 5;   // ... when launched together with local layers
 
 // Split plan.  The attended span of a sequence is at most `span` tokens (the
 // window, or the block-table capacity for a global layer).  Chunks are
