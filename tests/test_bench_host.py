@@ -31,6 +31,14 @@ def test_step_work_sums_layers():
     assert toks == int((5 * np.minimum(L, 1024) + L).sum())
 
 
+def test_l2_flush_only_for_workloads_that_fit_twice_in_l2():
+    # The decode bench flushes L2 between timed steps exactly when a step's KV bytes are
+    # below twice the L2: the tiny and the local-layer workloads, not the hybrid step or
+    # the long-context one (which read more than the L2 holds every step).
+    flushed = {n: bench.step_work(synth.workload(n))[1] < 2 * bench.L2_BYTES for n in (1, 2, 3, 5)}
+    assert flushed == {1: True, 2: True, 3: False, 5: False}
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
